@@ -1,0 +1,197 @@
+"""ctypes wrapper around the C oracle (oracle/oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py``.  The product package never imports it.
+
+Arrays are numpy: bf16 data is carried as uint16 bit patterns, the pool as
+uint8 bytes, outputs as float64.
+"""
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+_lib_path = None  # override used by the mutation tests (a planted-mistake build)
+
+
+class Geom(C.Structure):
+    _fields_ = [
+        ("num_q_heads", C.c_int32),
+        ("num_kv_heads", C.c_int32),
+        ("head_dim", C.c_int32),
+        ("n_layers", C.c_int32),
+        ("num_slots", C.c_int32),
+        ("max_blocks_per_seq", C.c_int32),
+        ("num_blocks", C.c_int64),
+    ]
+
+
+OK = 0
+BAD_ARG = -1
+BAD_BLOCK = -2
+
+_P = C.c_void_p
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _lib_path or _build.build()
+        L = C.CDLL(path)
+        L.orc_write_kv.restype = C.c_int64
+        L.orc_write_kv.argtypes = [C.POINTER(Geom), _P, _P, C.c_int32, C.c_int64, _P, _P, _P, _P]
+        L.orc_gather_kv.restype = C.c_int
+        L.orc_gather_kv.argtypes = [C.POINTER(Geom), _P, _P, C.c_int32, C.c_int32, C.c_int32, _P, _P]
+        L.orc_softmax_row.restype = None
+        L.orc_softmax_row.argtypes = [_P, C.c_int32, _P, _P, _P]
+        L.orc_partial.restype = None
+        L.orc_partial.argtypes = [_P, _P, C.c_int32, C.c_int32, _P, _P, _P]
+        L.orc_merge.restype = None
+        L.orc_merge.argtypes = [C.c_int32, _P, _P, _P, C.c_int32, _P, _P, _P, _P, _P]
+        L.orc_prefill.restype = C.c_int
+        L.orc_prefill.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P,
+                                  C.c_float, _P, _P, C.c_int32]
+        L.orc_prefill_rows.restype = C.c_int
+        L.orc_prefill_rows.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P,
+                                       C.c_float, C.c_int64, _P, _P, _P, _P, C.c_int32]
+        L.orc_decode.restype = C.c_int
+        L.orc_decode.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P,
+                                 C.c_float, _P, _P, C.c_int32]
+        L.orc_default_threads.restype = C.c_int32
+        L.orc_default_threads.argtypes = []
+        _lib = L
+    return _lib
+
+
+class use_library:
+    """Context manager: run the wrapper against another build of oracle.c."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        global _lib, _lib_path
+        self.saved = (_lib, _lib_path)
+        _lib, _lib_path = None, self.path
+        return self
+
+    def __exit__(self, *exc):
+        global _lib, _lib_path
+        _lib, _lib_path = self.saved
+        return False
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def geom(num_q_heads, num_kv_heads, head_dim, n_layers, num_slots, max_blocks_per_seq, num_blocks):
+    return Geom(num_q_heads, num_kv_heads, head_dim, n_layers, num_slots, max_blocks_per_seq,
+                num_blocks)
+
+
+def default_threads():
+    return int(lib().orc_default_threads())
+
+
+def write_kv(g, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new):
+    """Scatter rows into ``pool`` (uint8, modified in place); returns skipped-row count."""
+    assert pool.dtype == np.uint8 and pool.flags.c_contiguous
+    bt = _c(block_table, np.int32)
+    ts, tp = _c(tok_slot, np.int32), _c(tok_pos, np.int32)
+    k, v = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    n = ts.shape[0]
+    r = lib().orc_write_kv(C.byref(g), _ptr(pool), _ptr(bt), layer, n, _ptr(ts), _ptr(tp),
+                           _ptr(k), _ptr(v))
+    return int(r)
+
+
+def gather_kv(g, pool, block_table, layer, slot, n):
+    K = np.zeros((n, g.num_kv_heads, g.head_dim), np.float64)
+    V = np.zeros_like(K)
+    bt = _c(block_table, np.int32)
+    st = lib().orc_gather_kv(C.byref(g), _ptr(pool), _ptr(bt), layer, slot, n, _ptr(K), _ptr(V))
+    return st, K, V
+
+
+def softmax_row(s):
+    s = _c(s, np.float64)
+    w = np.zeros_like(s)
+    m, l = C.c_double(), C.c_double()
+    lib().orc_softmax_row(_ptr(s), s.shape[0], _ptr(w), C.byref(m), C.byref(l))
+    return w, m.value, l.value
+
+
+def partial(s, v):
+    s = _c(s, np.float64)
+    v = _c(v, np.float64).reshape(s.shape[0], -1)
+    acc = np.zeros(v.shape[1], np.float64)
+    m, l = C.c_double(), C.c_double()
+    lib().orc_partial(_ptr(s), _ptr(v), s.shape[0], v.shape[1], C.byref(m), C.byref(l), _ptr(acc))
+    return m.value, l.value, acc
+
+
+def merge(ms, ls, accs):
+    ms, ls = _c(ms, np.float64), _c(ls, np.float64)
+    accs = _c(accs, np.float64).reshape(ms.shape[0], -1)
+    dv = accs.shape[1]
+    acc_out = np.zeros(dv, np.float64)
+    o = np.zeros(dv, np.float64)
+    m, l, L = C.c_double(), C.c_double(), C.c_double()
+    lib().orc_merge(ms.shape[0], _ptr(ms), _ptr(ls), _ptr(accs), dv, C.byref(m), C.byref(l),
+                    _ptr(acc_out), _ptr(o), C.byref(L))
+    return m.value, l.value, acc_out, o, L.value
+
+
+def prefill(g, q, pool, block_table, layer, cu_seqlens, slots, scale, nthreads=0):
+    """Returns (status, O[T][Hq][d] float64, L[T][Hq] float64)."""
+    cu = _c(cu_seqlens, np.int32)
+    sl = _c(slots, np.int32)
+    T = int(cu[-1])
+    q = _c(q, np.uint16)
+    o = np.zeros((T, g.num_q_heads, g.head_dim), np.float64)
+    lse = np.zeros((T, g.num_q_heads), np.float64)
+    st = lib().orc_prefill(C.byref(g), _ptr(q), _ptr(pool), _ptr(_c(block_table, np.int32)), layer,
+                           cu.shape[0] - 1, _ptr(cu), _ptr(sl), C.c_float(scale), _ptr(o), _ptr(lse),
+                           nthreads)
+    return int(st), o, lse
+
+
+def prefill_rows(g, q, pool, block_table, layer, cu_seqlens, slots, scale, rows, heads,
+                 nthreads=0):
+    """Oracle at sampled (packed row, q head) pairs: (status, O[n][d], L[n])."""
+    cu = _c(cu_seqlens, np.int32)
+    sl = _c(slots, np.int32)
+    rows = _c(rows, np.int64)
+    heads = _c(heads, np.int32)
+    q = _c(q, np.uint16)
+    n = rows.shape[0]
+    o = np.zeros((n, g.head_dim), np.float64)
+    lse = np.zeros(n, np.float64)
+    st = lib().orc_prefill_rows(C.byref(g), _ptr(q), _ptr(pool), _ptr(_c(block_table, np.int32)),
+                                layer, cu.shape[0] - 1, _ptr(cu), _ptr(sl), C.c_float(scale), n,
+                                _ptr(rows), _ptr(heads), _ptr(o), _ptr(lse), nthreads)
+    return int(st), o, lse
+
+
+def decode(g, q, pool, block_table, layer, seq_lens, slots, scale, nthreads=0):
+    """Returns (status, O[B][Hq][d] float64, L[B][Hq] float64)."""
+    lens = _c(seq_lens, np.int32)
+    sl = _c(slots, np.int32)
+    B = lens.shape[0]
+    q = _c(q, np.uint16)
+    o = np.zeros((B, g.num_q_heads, g.head_dim), np.float64)
+    lse = np.zeros((B, g.num_q_heads), np.float64)
+    st = lib().orc_decode(C.byref(g), _ptr(q), _ptr(pool), _ptr(_c(block_table, np.int32)), layer, B,
+                          _ptr(lens), _ptr(sl), C.c_float(scale), _ptr(o), _ptr(lse), nthreads)
+    return int(st), o, lse
+
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "liboracle.so")

@@ -1,0 +1,504 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for causal grouped-query attention over a
+ * paged KV cache.  TEST INFRASTRUCTURE ONLY (tests, the smoke check and the
+ * timed CPU baseline call it; the product library never does).
+ *
+ * It is the plain definition written out, with no tiling, fusion or
+ * reordering beyond what the definition states:
+ *   1. gather K/V of a sequence from its pages through the block table into
+ *      contiguous fp64 arrays;
+ *   2. scores s_j = scale * <q, k_j> for every key j, with keys j > i masked to
+ *      -inf for query row i (causal);
+ *   3. two-pass softmax: m = max_j s_j, l = sum_j e^(s_j - m),
+ *      O = sum_j e^(s_j - m) v_j / l, L = m + ln l.
+ * Citations name the web page and section; see oracle.h for the page list.
+ * Readings taken where the pages are silent or garbled:
+ *   - masked scores are exactly -inf (weight 0), not a finite sentinel;
+ *   - L uses the natural log of the *scaled* scores (the FA2 worked example
+ *     gives L = 3 + ln 1.553 = 3.440);
+ *   - the GQA map is consecutive: kv head = q head / (Hq / Hkv);
+ *   - KV_DIM = Hkv * head_dim in general (the pages fix 8 x 64 = 512).
+ */
+#define _DEFAULT_SOURCE
+#include "oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* "BLOCK_SIZE = 16 tokens" [TV6 "블록 하나가 담는 것"]. */
+#define TOKENS_PER_BLOCK 16
+
+/* ---------------------------------------------------------------- layout */
+
+/* KV_DIM: elements of one token's K (or V) row = kv heads x head dim
+ * [TV6 "블록 하나가 담는 것": KV_DIM = 8 x 64 = 512]. */
+static int64_t kv_dim(const orc_geom* g) { return (int64_t)g->num_kv_heads * g->head_dim; }
+
+/* V_OFFSET = BLOCK_SIZE * KV_DIM * sizeof(bf16); BLOCK_BYTES = 2 * V_OFFSET
+ * [TV6 "블록 하나가 담는 것": 16384 and 32768 bytes for KV_DIM 512]. */
+static int64_t v_offset(const orc_geom* g) { return (int64_t)TOKENS_PER_BLOCK * kv_dim(g) * 2; }
+static int64_t block_bytes(const orc_geom* g) { return 2 * v_offset(g); }
+
+/* bf16 is the upper 16 bits of an IEEE binary32; the conversion is exact. */
+static double bf16_to_double(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static int geom_ok(const orc_geom* g) {
+    if (!g) return 0;
+    if (g->num_q_heads <= 0 || g->num_kv_heads <= 0 || g->head_dim <= 0) return 0;
+    if (g->num_q_heads % g->num_kv_heads != 0) return 0;
+    if (g->n_layers <= 0 || g->num_slots <= 0 || g->max_blocks_per_seq <= 0) return 0;
+    if (g->num_blocks <= 0) return 0;
+    return 1;
+}
+
+/* Physical block holding token `pos` of (slot, layer), or -1 when the slot,
+ * layer, position or table entry is out of range.  The flat table index is
+ * slot * N_LAYERS * MAX_BLOCKS_PER_SEQ + layer * MAX_BLOCKS_PER_SEQ + block_idx
+ * [TV6 "block table: slot·레이어·논리 블록 세 항목의 배열"]; -1 marks an
+ * unassigned entry. */
+static int64_t block_of(const orc_geom* g, const int32_t* block_table, int32_t slot,
+                        int32_t layer, int64_t pos) {
+    if (slot < 0 || slot >= g->num_slots) return -1;
+    if (layer < 0 || layer >= g->n_layers) return -1;
+    if (pos < 0) return -1;
+    int64_t logical_block = pos / TOKENS_PER_BLOCK;
+    if (logical_block >= g->max_blocks_per_seq) return -1;
+    int64_t idx = (int64_t)slot * g->n_layers * g->max_blocks_per_seq +
+                  (int64_t)layer * g->max_blocks_per_seq + logical_block;
+    int32_t physical_block = block_table[idx];
+    if (physical_block < 0 || physical_block >= g->num_blocks) return -1;
+    return physical_block;
+}
+
+/* ----------------------------------------------------------- write_kv */
+
+/* New token's K at kv_cache + block*BLOCK_BYTES + token_in_block*KV_DIM*2 and
+ * V at the same address + V_OFFSET [TV6 "블록 하나가 담는 것", decode
+ * write; TV3 "Distributing K/V into paged blocks" for the prefill chunks]. */
+int64_t orc_write_kv(const orc_geom* g, uint8_t* pool, const int32_t* block_table,
+                     int32_t layer, int64_t n_tokens, const int32_t* tok_slot,
+                     const int32_t* tok_pos, const uint16_t* k_new, const uint16_t* v_new) {
+    if (!geom_ok(g) || n_tokens < 0) return ORC_BAD_ARG;
+    if (n_tokens == 0) return 0;
+    if (!pool || !block_table || !tok_slot || !tok_pos || !k_new || !v_new) return ORC_BAD_ARG;
+    const int64_t row_bytes = kv_dim(g) * 2;
+    int64_t skipped = 0;
+    for (int64_t t = 0; t < n_tokens; ++t) {
+        int64_t blk = block_of(g, block_table, tok_slot[t], layer, tok_pos[t]);
+        if (blk < 0) {
+            ++skipped;
+            continue;
+        }
+        int64_t token_in_block = tok_pos[t] % TOKENS_PER_BLOCK;
+        uint8_t* k_dst = pool + blk * block_bytes(g) + token_in_block * row_bytes;
+        uint8_t* v_dst = k_dst + v_offset(g);
+        memcpy(k_dst, (const uint8_t*)k_new + t * row_bytes, (size_t)row_bytes);
+        memcpy(v_dst, (const uint8_t*)v_new + t * row_bytes, (size_t)row_bytes);
+    }
+    return skipped;
+}
+
+/* -------------------------------------------------------------- gather */
+
+/* Element (token, kv head, dim) of K lives at
+ * block*BLOCK_BYTES + token*KV_DIM*2 + kv_head*HEAD_DIM*2 + dim*2, and of V at
+ * the same address + V_OFFSET; a block holds min(n - 16*lb, 16) valid tokens
+ * [TV6 "논리 블록 → 물리 블록 → 바이트 주소"]. */
+int orc_gather_kv(const orc_geom* g, const uint8_t* pool, const int32_t* block_table,
+                  int32_t layer, int32_t slot, int32_t n, double* K, double* V) {
+    if (!geom_ok(g) || n < 0 || !pool || !block_table || (n > 0 && (!K || !V)))
+        return ORC_BAD_ARG;
+    const int32_t hkv = g->num_kv_heads, d = g->head_dim;
+    for (int32_t t = 0; t < n; ++t) {
+        int64_t blk = block_of(g, block_table, slot, layer, t);
+        if (blk < 0) return ORC_BAD_BLOCK;
+        int64_t token_in_block = t % TOKENS_PER_BLOCK;
+        for (int32_t h = 0; h < hkv; ++h) {
+            for (int32_t k = 0; k < d; ++k) {
+                int64_t addr = blk * block_bytes(g) + token_in_block * kv_dim(g) * 2 +
+                               (int64_t)h * d * 2 + (int64_t)k * 2;
+                uint16_t kb, vb;
+                memcpy(&kb, pool + addr, 2);
+                memcpy(&vb, pool + addr + v_offset(g), 2);
+                K[((int64_t)t * hkv + h) * d + k] = bf16_to_double(kb);
+                V[((int64_t)t * hkv + h) * d + k] = bf16_to_double(vb);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------- softmax */
+
+/* Plain two-pass softmax of one row: m = max s, l = sum e^(s - m),
+ * w = e^(s - m) / l.  Masked entries are -inf and get weight exactly 0. */
+void orc_softmax_row(const double* s, int32_t n, double* w, double* m_out, double* l_out) {
+    double m = -INFINITY;
+    for (int32_t j = 0; j < n; ++j)
+        if (s[j] > m) m = s[j];
+    double l = 0.0;
+    if (m == -INFINITY) {
+        if (w)
+            for (int32_t j = 0; j < n; ++j) w[j] = 0.0;
+        *m_out = m;
+        *l_out = 0.0;
+        return;
+    }
+    for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m);
+    if (w)
+        for (int32_t j = 0; j < n; ++j) w[j] = exp(s[j] - m) / l;
+    *m_out = m;
+    *l_out = l;
+}
+
+/* Un-normalised output and statistics of one key subset: keep O~ and l,
+ * divide once at the end [FA2 "단계별 설명 (순전파의 두 가지 손질)"]. */
+void orc_partial(const double* s, const double* v, int32_t n, int32_t dv, double* m,
+                 double* l, double* acc) {
+    orc_softmax_row(s, n, NULL, m, l);
+    for (int32_t k = 0; k < dv; ++k) acc[k] = 0.0;
+    if (*m == -INFINITY) return;
+    for (int32_t j = 0; j < n; ++j) {
+        double p = exp(s[j] - *m);
+        for (int32_t k = 0; k < dv; ++k) acc[k] += p * v[(int64_t)j * dv + k];
+    }
+}
+
+/* Merge rule m = max(m_a, m_b), d = d_a e^(m_a - m) + d_b e^(m_b - m)
+ * [TV3 "causalMask and online softmax"], applied to every partial; the
+ * accumulated outputs are rescaled the same way [FA2 worked example, block 2:
+ * O~ = 0.368 * 23.68 + 30].  L = m + ln l [FA2 "단계별 설명"]. */
+void orc_merge(int32_t nparts, const double* m, const double* l, const double* acc,
+               int32_t dv, double* m_out, double* l_out, double* acc_out, double* o,
+               double* lse) {
+    double ms = -INFINITY;
+    for (int32_t i = 0; i < nparts; ++i)
+        if (m[i] > ms) ms = m[i];
+    double ls = 0.0;
+    for (int32_t k = 0; k < dv; ++k) acc_out[k] = 0.0;
+    if (ms != -INFINITY) {
+        for (int32_t i = 0; i < nparts; ++i) {
+            if (m[i] == -INFINITY) continue; /* an empty part contributes nothing */
+            double c = exp(m[i] - ms);
+            ls += l[i] * c;
+            for (int32_t k = 0; k < dv; ++k) acc_out[k] += acc[(int64_t)i * dv + k] * c;
+        }
+    }
+    *m_out = ms;
+    *l_out = ls;
+    if (ls > 0.0) {
+        for (int32_t k = 0; k < dv; ++k) o[k] = acc_out[k] / ls;
+        *lse = ms + log(ls);
+    } else {
+        for (int32_t k = 0; k < dv; ++k) o[k] = 0.0;
+        *lse = -INFINITY;
+    }
+}
+
+/* ----------------------------------------------------------- attention */
+
+/* One output row: query qv[d] against keys 0..nkeys-1 of kv head hk, with
+ * keys j > last_key masked (causal).  s_buf has room for nkeys scores.
+ * Q head h reads kv head h / (Hq/Hkv) [TV3 "Per-head attention scores and
+ * GQA"; FA2 "4. MQA · GQA 지원"]. */
+static void attend_row(const orc_geom* g, const double* qv, const double* K, const double* V,
+                       int32_t hk, int32_t nkeys, int32_t last_key, double scale,
+                       double* s_buf, double* o, double* lse) {
+    const int32_t hkv = g->num_kv_heads, d = g->head_dim;
+    for (int32_t j = 0; j < nkeys; ++j) {
+        if (j > last_key) {
+            s_buf[j] = -INFINITY; /* causal mask: column after the row */
+            continue;
+        }
+        const double* kj = K + ((int64_t)j * hkv + hk) * d;
+        double dot = 0.0;
+        for (int32_t k = 0; k < d; ++k) dot += qv[k] * kj[k];
+        s_buf[j] = scale * dot;
+    }
+    double m, l;
+    orc_softmax_row(s_buf, nkeys, NULL, &m, &l);
+    if (l == 0.0) {
+        for (int32_t k = 0; k < d; ++k) o[k] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    for (int32_t k = 0; k < d; ++k) {
+        double acc = 0.0;
+        for (int32_t j = 0; j < nkeys; ++j) {
+            if (s_buf[j] == -INFINITY) continue;
+            acc += exp(s_buf[j] - m) * V[((int64_t)j * hkv + hk) * d + k];
+        }
+        o[k] = acc / l;
+    }
+    *lse = m + log(l);
+}
+
+/* ------------------------------------------------------ thread helpers */
+
+int32_t orc_default_threads(void) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int32_t)n : 1;
+}
+
+typedef struct {
+    void (*fn)(void* ctx, int64_t item, double* scratch);
+    void* ctx;
+    int64_t n_items;
+    int64_t next; /* shared work counter */
+    int64_t scratch_len;
+} pool_job;
+
+static void* pool_worker(void* arg) {
+    pool_job* job = (pool_job*)arg;
+    double* scratch = (double*)malloc(sizeof(double) * (size_t)(job->scratch_len + 1));
+    if (!scratch) return NULL;
+    for (;;) {
+        int64_t item = __atomic_fetch_add(&job->next, 1, __ATOMIC_RELAXED);
+        if (item >= job->n_items) break;
+        job->fn(job->ctx, item, scratch);
+    }
+    free(scratch);
+    return NULL;
+}
+
+/* Runs fn(ctx, item, scratch) for every item on nthreads threads. */
+static void run_items(void (*fn)(void*, int64_t, double*), void* ctx, int64_t n_items,
+                      int64_t scratch_len, int32_t nthreads) {
+    if (nthreads <= 0) nthreads = orc_default_threads();
+    if (nthreads > n_items) nthreads = (int32_t)(n_items > 0 ? n_items : 1);
+    pool_job job = {fn, ctx, n_items, 0, scratch_len};
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    int32_t started = 0;
+    for (int32_t i = 1; i < nthreads && th; ++i)
+        if (pthread_create(&th[started], NULL, pool_worker, &job) == 0) ++started;
+    pool_worker(&job);
+    for (int32_t i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+}
+
+/* ------------------------------------------------------------- prefill */
+
+typedef struct {
+    const orc_geom* g;
+    const uint16_t* q;
+    const int32_t* cu;
+    double scale;
+    double** K; /* per sequence gathered keys (NULL when not needed) */
+    double** V;
+    int32_t batch;
+    /* full prefill */
+    double* o;
+    double* lse;
+    /* sampled rows */
+    const int64_t* rows;
+    const int32_t* heads;
+} prefill_ctx;
+
+static int32_t seq_of_row(const int32_t* cu, int32_t batch, int64_t row) {
+    for (int32_t b = 0; b < batch; ++b)
+        if (row >= cu[b] && row < cu[b + 1]) return b;
+    return -1;
+}
+
+/* One (packed row, q head) output. */
+static void prefill_one(const prefill_ctx* c, int64_t row, int32_t hq, double* scratch,
+                        double* o, double* lse) {
+    const orc_geom* g = c->g;
+    const int32_t d = g->head_dim, hq_n = g->num_q_heads;
+    const int32_t group = g->num_q_heads / g->num_kv_heads;
+    int32_t b = seq_of_row(c->cu, c->batch, row);
+    int32_t n = c->cu[b + 1] - c->cu[b];
+    int32_t i = (int32_t)(row - c->cu[b]); /* position of this query in its sequence */
+    double* qv = scratch;                  /* d doubles, then n scores */
+    for (int32_t k = 0; k < d; ++k) qv[k] = bf16_to_double(c->q[(row * hq_n + hq) * d + k]);
+    attend_row(g, qv, c->K[b], c->V[b], hq / group, n, i, c->scale, scratch + d, o, lse);
+}
+
+static void prefill_item(void* ctx, int64_t item, double* scratch) {
+    const prefill_ctx* c = (const prefill_ctx*)ctx;
+    const int32_t hq_n = c->g->num_q_heads, d = c->g->head_dim;
+    int64_t row = item / hq_n;
+    int32_t hq = (int32_t)(item % hq_n);
+    prefill_one(c, row, hq, scratch, c->o + (row * hq_n + hq) * d, c->lse + row * hq_n + hq);
+}
+
+static void prefill_rows_item(void* ctx, int64_t item, double* scratch) {
+    const prefill_ctx* c = (const prefill_ctx*)ctx;
+    const int32_t d = c->g->head_dim;
+    prefill_one(c, c->rows[item], c->heads[item], scratch, c->o + item * d, c->lse + item);
+}
+
+static int check_batch(const orc_geom* g, int32_t batch, const int32_t* cu, const int32_t* slots,
+                       int32_t layer) {
+    if (!geom_ok(g) || batch < 0 || !cu || !slots) return 0;
+    if (layer < 0 || layer >= g->n_layers) return 0;
+    if (cu[0] != 0) return 0;
+    for (int32_t b = 0; b < batch; ++b)
+        if (cu[b + 1] < cu[b]) return 0;
+    return 1;
+}
+
+/* Gathers the sequences flagged in `need` (all when need == NULL). */
+static int gather_all(const orc_geom* g, const uint8_t* pool, const int32_t* bt, int32_t layer,
+                      int32_t batch, const int32_t* lens, const int32_t* slots,
+                      const char* need, double** K, double** V) {
+    const int64_t row = kv_dim(g);
+    for (int32_t b = 0; b < batch; ++b) {
+        K[b] = V[b] = NULL;
+        if (need && !need[b]) continue;
+        int64_t n = lens[b];
+        K[b] = (double*)malloc(sizeof(double) * (size_t)(n * row + 1));
+        V[b] = (double*)malloc(sizeof(double) * (size_t)(n * row + 1));
+        if (!K[b] || !V[b]) return ORC_BAD_ARG;
+        int st = orc_gather_kv(g, pool, bt, layer, slots[b], (int32_t)n, K[b], V[b]);
+        if (st != ORC_OK) return st;
+    }
+    return ORC_OK;
+}
+
+static void free_all(int32_t batch, double** K, double** V) {
+    for (int32_t b = 0; b < batch; ++b) {
+        free(K[b]);
+        free(V[b]);
+    }
+    free(K);
+    free(V);
+}
+
+static int prefill_common(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                          const int32_t* bt, int32_t layer, int32_t batch, const int32_t* cu,
+                          const int32_t* slots, float scale, int64_t nsamp,
+                          const int64_t* rows, const int32_t* heads, double* o, double* lse,
+                          int32_t nthreads) {
+    if (!check_batch(g, batch, cu, slots, layer) || !pool || !bt || !o || !lse) return ORC_BAD_ARG;
+    const int64_t T = cu[batch];
+    if (T > 0 && !q) return ORC_BAD_ARG;
+    int32_t* lens = (int32_t*)malloc(sizeof(int32_t) * (size_t)(batch + 1));
+    char* need = (char*)calloc((size_t)batch + 1, 1);
+    double** K = (double**)calloc((size_t)batch + 1, sizeof(double*));
+    double** V = (double**)calloc((size_t)batch + 1, sizeof(double*));
+    if (!lens || !need || !K || !V) {
+        free(lens); free(need); free(K); free(V);
+        return ORC_BAD_ARG;
+    }
+    int32_t nmax = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        lens[b] = cu[b + 1] - cu[b];
+        if (lens[b] > nmax) nmax = lens[b];
+    }
+    int st = ORC_OK;
+    if (rows) {
+        for (int64_t s = 0; s < nsamp; ++s) {
+            int32_t b = (rows[s] >= 0 && rows[s] < T) ? seq_of_row(cu, batch, rows[s]) : -1;
+            if (b < 0 || heads[s] < 0 || heads[s] >= g->num_q_heads) st = ORC_BAD_ARG;
+            else need[b] = 1;
+        }
+    }
+    if (st == ORC_OK) st = gather_all(g, pool, bt, layer, batch, lens, slots, rows ? need : NULL, K, V);
+    if (st == ORC_OK) {
+        prefill_ctx c = {g, q, cu, (double)scale, K, V, batch, o, lse, rows, heads};
+        if (rows)
+            run_items(prefill_rows_item, &c, nsamp, (int64_t)g->head_dim + nmax, nthreads);
+        else
+            run_items(prefill_item, &c, T * g->num_q_heads, (int64_t)g->head_dim + nmax, nthreads);
+    }
+    free_all(batch, K, V);
+    free(lens);
+    free(need);
+    return st;
+}
+
+int orc_prefill(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                const int32_t* block_table, int32_t layer, int32_t batch,
+                const int32_t* cu_seqlens, const int32_t* slots, float scale, double* o,
+                double* lse, int32_t nthreads) {
+    return prefill_common(g, q, pool, block_table, layer, batch, cu_seqlens, slots, scale, 0,
+                          NULL, NULL, o, lse, nthreads);
+}
+
+int orc_prefill_rows(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                     const int32_t* block_table, int32_t layer, int32_t batch,
+                     const int32_t* cu_seqlens, const int32_t* slots, float scale,
+                     int64_t nsamp, const int64_t* rows, const int32_t* heads, double* o,
+                     double* lse, int32_t nthreads) {
+    if (nsamp < 0 || (nsamp > 0 && (!rows || !heads))) return ORC_BAD_ARG;
+    static const int64_t no_rows = 0;
+    return prefill_common(g, q, pool, block_table, layer, batch, cu_seqlens, slots, scale,
+                          nsamp, rows ? rows : &no_rows, heads, o, lse, nthreads);
+}
+
+/* -------------------------------------------------------------- decode */
+
+typedef struct {
+    const orc_geom* g;
+    const uint16_t* q;
+    const uint8_t* pool;
+    const int32_t* bt;
+    int32_t layer;
+    const int32_t* lens;
+    const int32_t* slots;
+    double scale;
+    double* o;
+    double* lse;
+    int status; /* first error seen (written under the atomic below) */
+} decode_ctx;
+
+/* Query b sits at position seq_len - 1 and sees keys 0..seq_len-1: the length
+ * already counts the token just written, so nothing in the future is read
+ * [TV6 "논리 블록 → 물리 블록 → 바이트 주소"]. */
+static void decode_item(void* ctx, int64_t b, double* scratch) {
+    decode_ctx* c = (decode_ctx*)ctx;
+    const orc_geom* g = c->g;
+    const int32_t d = g->head_dim, hq_n = g->num_q_heads, hkv = g->num_kv_heads;
+    const int32_t group = hq_n / hkv;
+    const int32_t n = c->lens[b];
+    double* out = c->o + b * hq_n * d;
+    double* lse = c->lse + b * hq_n;
+    if (n <= 0) {
+        for (int32_t k = 0; k < hq_n * d; ++k) out[k] = 0.0;
+        for (int32_t h = 0; h < hq_n; ++h) lse[h] = -INFINITY;
+        return;
+    }
+    double* K = (double*)malloc(sizeof(double) * (size_t)n * (size_t)kv_dim(g));
+    double* V = (double*)malloc(sizeof(double) * (size_t)n * (size_t)kv_dim(g));
+    int st = (K && V) ? orc_gather_kv(g, c->pool, c->bt, c->layer, c->slots[b], n, K, V)
+                      : ORC_BAD_ARG;
+    if (st != ORC_OK) {
+        int expected = ORC_OK;
+        __atomic_compare_exchange_n(&c->status, &expected, st, 0, __ATOMIC_RELAXED,
+                                    __ATOMIC_RELAXED);
+    } else {
+        double* qv = scratch;
+        for (int32_t h = 0; h < hq_n; ++h) {
+            for (int32_t k = 0; k < d; ++k)
+                qv[k] = bf16_to_double(c->q[((int64_t)b * hq_n + h) * d + k]);
+            attend_row(g, qv, K, V, h / group, n, n - 1, c->scale, scratch + d, out + h * d,
+                       lse + h);
+        }
+    }
+    free(K);
+    free(V);
+}
+
+int orc_decode(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+               const int32_t* block_table, int32_t layer, int32_t batch,
+               const int32_t* seq_lens, const int32_t* slots, float scale, double* o,
+               double* lse, int32_t nthreads) {
+    if (!geom_ok(g) || batch < 0 || layer < 0 || layer >= g->n_layers) return ORC_BAD_ARG;
+    if (batch == 0) return ORC_OK;
+    if (!q || !pool || !block_table || !seq_lens || !slots || !o || !lse) return ORC_BAD_ARG;
+    int32_t nmax = 0;
+    for (int32_t b = 0; b < batch; ++b)
+        if (seq_lens[b] > nmax) nmax = seq_lens[b];
+    decode_ctx c = {g, q, pool, block_table, layer, seq_lens, slots, (double)scale, o, lse, ORC_OK};
+    run_items(decode_item, &c, batch, (int64_t)g->head_dim + nmax, nthreads);
+    return c.status;
+}

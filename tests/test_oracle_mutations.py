@@ -1,0 +1,68 @@
+"""Planted mistakes: each mutant of oracle.c must fail at least one pin.
+
+The mutants are built from a copy of the oracle source on the CPU; the real
+oracle is never changed.  This shows the pins would catch a dropped term, a
+wrong sign or index, or a transposed operand anywhere in the oracle.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "oracle.c")
+
+MUTANTS = {
+    "gqa_map_modulo": ("hq / group, n, i", "hq % g->num_kv_heads, n, i"),
+    "causal_off_by_one": ("if (j > last_key) {", "if (j >= last_key && j > 0) {"),
+    "log2_lse": ("*lse = m + log(l);", "*lse = m + log2(l);"),
+    "token_stride_head_dim": ("token_in_block * kv_dim(g) * 2 +\n", "token_in_block * g->head_dim * 2 +\n"),
+    "v_offset_wrong": ("memcpy(&vb, pool + addr + v_offset(g), 2);", "memcpy(&vb, pool + addr + v_offset(g) / 2, 2);"),
+    "scale_dropped": ("s_buf[j] = scale * dot;", "s_buf[j] = dot;"),
+    "table_index_transposed": ("(int64_t)slot * g->n_layers * g->max_blocks_per_seq +\n                  (int64_t)layer * g->max_blocks_per_seq",
+                               "(int64_t)layer * g->num_slots * g->max_blocks_per_seq +\n                  (int64_t)slot * g->max_blocks_per_seq"),
+    "merge_without_rescale": ("ls += l[i] * c;", "ls += l[i];"),
+    "normaliser_off": ("o[k] = acc / l;", "o[k] = acc / (l + 1e-3);"),
+    "write_v_at_k": ("uint8_t* v_dst = k_dst + v_offset(g);", "uint8_t* v_dst = k_dst + v_offset(g) + 2;"),
+    "max_not_subtracted": ("for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m);",
+                           "for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m) * (1 + 1e-9 * m);"),
+}
+
+PIN_TESTS = [
+    lambda gd: pins.test_worked_example_decode(gd),
+    lambda gd: pins.test_worked_example_prefill_rows(gd),
+    lambda gd: pins.test_worked_example_blocks_and_merge(gd),
+    lambda gd: pins.test_softmax_stress_rows(gd),
+    lambda gd: pins.test_layout_constants_and_offsets(gd),
+    lambda gd: pins.test_layout_as_array_shape(),
+    lambda gd: pins.test_zero_query_gives_running_mean(),
+    lambda gd: pins.test_causal_row0_is_first_value(),
+    lambda gd: pins.test_lse_split_merge_identity(),
+    lambda gd: pins.test_prefill_matches_library_sdpa(8, 2, 64, [40]),
+    lambda gd: pins.test_decode_matches_library_sdpa(),
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path, golden_dir):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor missing: " + name
+    mutated = src.replace(old, new)
+    c_path = tmp_path / "oracle.c"
+    c_path.write_text(mutated)
+    hdr = os.path.join(os.path.dirname(SRC), "oracle.h")
+    (tmp_path / "oracle.h").write_text(open(hdr).read())
+    so = tmp_path / "liboracle_mutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", str(so),
+                    str(c_path), "-lm"], check=True)
+    caught = []
+    with oracle.use_library(str(so)):
+        for i, t in enumerate(PIN_TESTS):
+            try:
+                t(golden_dir)
+            except AssertionError:
+                caught.append(i)
+    assert caught, "no pin caught mutant " + name
