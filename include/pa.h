@@ -1,0 +1,179 @@
+/*
+ * pa.h -- C ABI of the paged-attention library (libpa.so) for GB300 (sm_103a).
+ *
+ * Exact causal grouped-query attention over a paged KV cache, in three calls:
+ *   pa_write_kv  scatter new K/V rows into their pages,
+ *   pa_prefill   causal prefill of a packed batch of prompts (tcgen05 / TMEM),
+ *   pa_decode    one query per sequence over its whole cache (split-KV + LSE merge).
+ *
+ * The problem statement follows these web pages (cited by title and section):
+ *  - jaehun.me, "6. KV cache 를 16토큰 블록으로 쪼개기 -- block table 로 비연속 블록을
+ *    읽는 법" (tiny-vllm part 6): page layout ("블록 하나가 담는 것: K 는 앞, V 는
+ *    V_OFFSET 뒤"), block table ("block table: slot·레이어·논리 블록 세 항목의 배열"),
+ *    address and length rule ("논리 블록 → 물리 블록 → 바이트 주소"), in-place output
+ *    ("출력은 입력 자리에: in-place").
+ *  - jaehun.me, "3. The prefill path: flowing the entire prompt at once"
+ *    (tiny-vllm part 3): K/V scatter ("Distributing K/V into paged blocks"), GQA
+ *    ("Per-head attention scores and GQA"), causal mask and merge rule
+ *    ("causalMask and online softmax").
+ *  - base.kaita.kr, "플래시어텐션-2: 더 나은 병렬화" (FlashAttention-2 explainer):
+ *    deferred normalisation and L = m + log l ("단계별 설명 (순전파의 두 가지 손질)"),
+ *    causal tile skipping ("인과 마스크 처리"), GQA by index ("4. MQA · GQA 지원").
+ *
+ * Memory layout (all bf16 = IEEE binary32 upper half, little-endian):
+ *   page (block) of 16 tokens: K[16][KV_DIM] then V[16][KV_DIM], KV_DIM = Hkv * d;
+ *     page bytes = 64 * KV_DIM (32768 for 8 x 64); V starts 32 * KV_DIM bytes in.
+ *     Token t of page p, kv head h, dim k: K at p*page_bytes + t*KV_DIM*2 + h*d*2 + k*2.
+ *   pool: num_blocks pages, contiguous.
+ *   block_table: int32 [num_slots][n_layers][max_blocks_per_seq], -1 = unassigned;
+ *     token pos of (slot, layer) lives in page block_table[slot][layer][pos / 16].
+ *   q, o (prefill): [total_tokens][Hq][d] bf16, sequence b owns rows
+ *     cu_seqlens[b] .. cu_seqlens[b+1]-1; q, o (decode): [batch][Hq][d] bf16.
+ *   lse: fp32, prefill [total_tokens][Hq], decode [batch][Hq]; natural-log
+ *     log-sum-exp of the scaled scores, L = m + ln l.
+ *   GQA: q head h reads kv head h / (Hq / Hkv).
+ *
+ * Ownership: the caller allocates and owns every buffer (device memory unless
+ * stated).  The library allocates no memory and keeps no state between calls.
+ * All calls are asynchronous on `stream`; they return after validating the
+ * arguments and enqueueing the kernels.
+ *
+ * Errors:
+ *   synchronous   -- the return value (PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED,
+ *                    PA_ERR_CUDA); nothing is enqueued when it is not PA_OK.
+ *   asynchronous  -- kernels report data errors through *err_flag (device int32):
+ *                    PA_ERR_BAD_BLOCK for a table entry that is -1 or >= num_blocks
+ *                    where a page is needed, a slot outside [0, num_slots), a
+ *                    position beyond 16 * max_blocks_per_seq, or lengths that do
+ *                    not fit the call; PA_ERR_TIMEOUT if a bounded wait inside a
+ *                    kernel ran out.  The offending page or row is skipped (its
+ *                    output is unspecified) and the kernel never traps.  The caller
+ *                    zeroes *err_flag before the call and reads it after
+ *                    synchronising; the first error code written is kept.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned or aliased buffer */
+    PA_ERR_UNSUPPORTED = 2,  /* valid request outside what the kernels implement */
+    PA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    PA_ERR_BAD_BLOCK = 4,    /* device-reported through err_flag (see above) */
+    PA_ERR_TIMEOUT = 5       /* device-reported through err_flag (see above) */
+} pa_status;
+
+/* Tokens per page; fixed ("BLOCK_SIZE = 16", tiny-vllm part 6, page layout). */
+#define PA_BLOCK_TOKENS 16
+
+/* Cache geometry, validated on every call. */
+typedef struct pa_geom {
+    int32_t num_q_heads;        /* Hq > 0, a multiple of Hkv */
+    int32_t num_kv_heads;       /* Hkv > 0 */
+    int32_t head_dim;           /* d: 64 or 128 for attention; any multiple of 8 for write */
+    int32_t n_layers;           /* table dimension 1 */
+    int32_t num_slots;          /* table dimension 0 */
+    int32_t max_blocks_per_seq; /* table dimension 2 */
+    int64_t num_blocks;         /* pages in the pool */
+} pa_geom;
+
+/* Bytes of one page: 2 (K, V) * 16 tokens * Hkv * d * 2 bytes.  0 for a NULL
+ * or invalid geometry. */
+size_t pa_page_bytes(const pa_geom* geom);
+
+/*
+ * pa_write_kv -- scatter n_tokens new K/V rows into their pages.
+ * Definition: row i of k_new / v_new (each [n_tokens][KV_DIM] bf16, row-major)
+ * is copied to the K / V row of token tok_pos[i] of (tok_slot[i], layer):
+ *   pool + blk * page_bytes + (pos % 16) * KV_DIM * 2      (K)
+ *   ... + 32 * KV_DIM                                      (V)
+ * with blk = block_table[slot][layer][pos / 16] (tiny-vllm part 6, page
+ * layout; part 3, "Distributing K/V into paged blocks").  Bytes of the pool
+ * not named by a valid row are left untouched; the copy is bit-exact.
+ * Arguments: tok_slot, tok_pos: device int32 [n_tokens]; pool, k_new, v_new:
+ * device, 16-byte aligned; k_new / v_new must not overlap the pool.  Pages
+ * are not allocated here: the caller fills block_table first.  Two rows with
+ * the same (slot, layer, pos) in one call leave either row's bytes.
+ * Rows with an invalid slot, position or table entry are skipped and set
+ * *err_flag = PA_ERR_BAD_BLOCK.  n_tokens == 0 is a no-op.
+ */
+pa_status pa_write_kv(const pa_geom* geom, void* pool, const int32_t* block_table,
+                      int32_t layer, int32_t n_tokens, const int32_t* tok_slot,
+                      const int32_t* tok_pos, const void* k_new, const void* v_new,
+                      int32_t* err_flag, pa_stream_t stream);
+
+/*
+ * pa_prefill -- causal prefill of a packed batch of fresh prompts.
+ * Definition: for sequence b of length n_b = cu_seqlens[b+1] - cu_seqlens[b]
+ * (slot slots[b]), query row i (0 <= i < n_b) of q head h attends keys 0..i of
+ * (slots[b], layer), kv head h / (Hq/Hkv):
+ *   s_j = scale * <q_i, k_j>,  m = max_j s_j,  l = sum_j e^(s_j - m),
+ *   o_i = sum_j e^(s_j - m) v_j / l,   lse_i = m + ln l.
+ * (FlashAttention-2 explainer, "단계별 설명"; tiny-vllm part 3, "Per-head
+ * attention scores and GQA" and "causalMask and online softmax".)
+ * Arguments: q, o: device bf16 [total_tokens][Hq][d], 16-byte aligned; o may
+ * alias q (each output row is written only after every read of its query
+ * row).  lse: device fp32 [total_tokens][Hq] or NULL.  cu_seqlens: device int32
+ * [batch+1], cu_seqlens[0] = 0, non-decreasing, cu_seqlens[batch] <=
+ * total_tokens.  slots: device int32 [batch].  max_seqlen: host upper bound on
+ * every n_b (sizes the grid; longer sequences set PA_ERR_BAD_BLOCK).
+ * total_tokens: host row count of q / o.  Requires d in {64, 128}.  Rows of q
+ * not covered by cu_seqlens are neither read for output nor written.
+ */
+pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool,
+                     const int32_t* block_table, int32_t layer, int32_t batch,
+                     const int32_t* cu_seqlens, const int32_t* slots, int32_t max_seqlen,
+                     int32_t total_tokens, float scale, void* o, float* lse,
+                     int32_t* err_flag, pa_stream_t stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
+ * up to `batch` sequences of up to `max_seq_len` tokens.  Depends only on the
+ * geometry and these two numbers (not on the device).  0 for invalid input.
+ */
+size_t pa_decode_workspace_size(const pa_geom* geom, int32_t batch, int32_t max_seq_len);
+
+/*
+ * pa_decode -- one query per sequence over its whole cache.
+ * Definition: query b (q[b], slot slots[b]) sits at position seq_lens[b]-1 and
+ * attends keys 0..seq_lens[b]-1; the length includes the token just written
+ * (tiny-vllm part 6, "논리 블록 → 물리 블록 → 바이트 주소").  Same scores,
+ * softmax, o and lse as pa_prefill; seq_lens[b] == 0 gives o = 0, lse = -inf.
+ * The keys of long sequences are split across CTAs; partial results are
+ * merged by the rule m = max(m_a, m_b), l = l_a e^(m_a - m) + l_b e^(m_b - m)
+ * (tiny-vllm part 3, "causalMask and online softmax"), applied to the
+ * accumulated outputs as well.  The split depends only on the lengths and the
+ * launch shape, never on physical page ids, so results are bit-identical
+ * under any page permutation and from run to run.
+ * Arguments: q, o: device bf16 [batch][Hq][d], 16-byte aligned; o may alias q.
+ * lse: device fp32 [batch][Hq] or NULL.  seq_lens, slots: device int32
+ * [batch].  max_seq_len: host upper bound on every seq_len (sizes the grid
+ * and the workspace; lengths beyond 16 * max_blocks_per_seq set
+ * PA_ERR_BAD_BLOCK).  workspace: device, 16-byte aligned, at least
+ * pa_decode_workspace_size(geom, batch, max_seq_len) bytes, contents need not
+ * be initialised, not shared with a concurrent call.  Requires d in {64, 128},
+ * Hq/Hkv in {1, 2, 4, 8}, Hkv * ceil(Hq/Hkv/4) <= 16 and a page of at most 64 KiB.
+ */
+pa_status pa_decode(const pa_geom* geom, const void* q, const void* pool,
+                    const int32_t* block_table, int32_t layer, int32_t batch,
+                    const int32_t* seq_lens, const int32_t* slots, int32_t max_seq_len,
+                    float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                    int32_t* err_flag, pa_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

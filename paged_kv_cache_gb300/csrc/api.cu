@@ -1,0 +1,137 @@
+// api.cu -- the C ABI of libpa.so (declared in include/pa.h): argument
+// validation, then one asynchronous launch sequence per call.  No memory is
+// allocated and no state is kept between calls.
+#include <cmath>
+#include <cstdint>
+
+#include "pa_internal.cuh"
+
+#define PA_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Geometry fields that every call needs.
+bool geom_valid(const pa_geom* g) {
+    if (!g) return false;
+    if (g->num_q_heads <= 0 || g->num_kv_heads <= 0 || g->head_dim <= 0) return false;
+    if (g->num_q_heads % g->num_kv_heads != 0) return false;
+    if (g->head_dim % 8 != 0) return false;  // rows move in 16-byte chunks
+    if (g->n_layers <= 0 || g->num_slots <= 0 || g->max_blocks_per_seq <= 0) return false;
+    if (g->num_blocks <= 0) return false;
+    const long long kv_dim = static_cast<long long>(g->num_kv_heads) * g->head_dim;
+    if (kv_dim > (1 << 20)) return false;
+    return true;
+}
+
+pa::KGeom kgeom(const pa_geom* g) {
+    pa::KGeom k;
+    k.hq = g->num_q_heads;
+    k.hkv = g->num_kv_heads;
+    k.d = g->head_dim;
+    k.group = g->num_q_heads / g->num_kv_heads;
+    k.n_layers = g->n_layers;
+    k.num_slots = g->num_slots;
+    k.maxb = g->max_blocks_per_seq;
+    k.kv_dim = g->num_kv_heads * g->head_dim;
+    k.nblocks = g->num_blocks;
+    k.page_bytes = 64ll * k.kv_dim;
+    return k;
+}
+
+bool ranges_overlap(const void* a, size_t a_len, const void* b, size_t b_len) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + b_len && b0 < a0 + a_len;
+}
+
+pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+}  // namespace
+
+PA_API size_t pa_page_bytes(const pa_geom* geom) {
+    if (!geom_valid(geom)) return 0;
+    return static_cast<size_t>(kgeom(geom).page_bytes);
+}
+
+PA_API pa_status pa_write_kv(const pa_geom* geom, void* pool, const int32_t* block_table,
+                             int32_t layer, int32_t n_tokens, const int32_t* tok_slot,
+                             const int32_t* tok_pos, const void* k_new, const void* v_new,
+                             int32_t* err_flag, pa_stream_t stream) {
+    if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= geom->n_layers || n_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (n_tokens == 0) return PA_OK;
+    if (!pool || !block_table || !tok_slot || !tok_pos || !k_new || !v_new || !err_flag)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(pool) || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_INVALID_ARG;
+    const pa::KGeom g = kgeom(geom);
+    const size_t pool_len = static_cast<size_t>(g.nblocks) * static_cast<size_t>(g.page_bytes);
+    const size_t rows_len = static_cast<size_t>(n_tokens) * g.kv_dim * 2;
+    if (ranges_overlap(k_new, rows_len, pool, pool_len) ||
+        ranges_overlap(v_new, rows_len, pool, pool_len))
+        return PA_ERR_INVALID_ARG;
+    return cuda_status(pa::launch_write_kv(g, pool, block_table, layer, n_tokens, tok_slot,
+                                           tok_pos, k_new, v_new, err_flag,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+PA_API pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool,
+                            const int32_t* block_table, int32_t layer, int32_t batch,
+                            const int32_t* cu_seqlens, const int32_t* slots, int32_t max_seqlen,
+                            int32_t total_tokens, float scale, void* o, float* lse,
+                            int32_t* err_flag, pa_stream_t stream) {
+    if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= geom->n_layers) return PA_ERR_INVALID_ARG;
+    if (batch < 0 || max_seqlen < 0 || total_tokens < 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (geom->head_dim != 64 && geom->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (batch == 0 || total_tokens == 0 || max_seqlen == 0) return PA_OK;
+    if (!q || !pool || !block_table || !cu_seqlens || !slots || !o || !err_flag)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o) || !aligned16(pool)) return PA_ERR_INVALID_ARG;
+    const pa::KGeom g = kgeom(geom);
+    // TMA coordinates are int32: pool rows (32 per page) and q rows must fit.
+    if (g.nblocks * 32 >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    return cuda_status(pa::launch_prefill(g, q, pool, block_table, layer, batch, cu_seqlens,
+                                          slots, max_seqlen, total_tokens, scale, o, lse,
+                                          err_flag, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+PA_API size_t pa_decode_workspace_size(const pa_geom* geom, int32_t batch, int32_t max_seq_len) {
+    if (!geom_valid(geom) || batch < 0 || max_seq_len < 0) return 0;
+    return pa::decode_workspace_bytes(kgeom(geom), batch, max_seq_len);
+}
+
+PA_API pa_status pa_decode(const pa_geom* geom, const void* q, const void* pool,
+                           const int32_t* block_table, int32_t layer, int32_t batch,
+                           const int32_t* seq_lens, const int32_t* slots, int32_t max_seq_len,
+                           float scale, void* o, float* lse, void* workspace,
+                           size_t workspace_bytes, int32_t* err_flag, pa_stream_t stream) {
+    if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= geom->n_layers) return PA_ERR_INVALID_ARG;
+    if (batch < 0 || max_seq_len < 0 || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    const pa::KGeom g = kgeom(geom);
+    if (!pa::decode_supported(g)) return PA_ERR_UNSUPPORTED;
+    if (batch == 0) return PA_OK;
+    if (!q || !pool || !block_table || !seq_lens || !slots || !o || !workspace || !err_flag)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o) || !aligned16(pool) || !aligned16(workspace))
+        return PA_ERR_INVALID_ARG;
+    if (workspace_bytes < pa::decode_workspace_bytes(g, batch, max_seq_len))
+        return PA_ERR_INVALID_ARG;
+    return cuda_status(pa::launch_decode(g, q, pool, block_table, layer, batch, seq_lens, slots,
+                                         max_seq_len, scale, o, lse, workspace, err_flag,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+PA_API const char* pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "PA_OK: success";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG: invalid argument";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: configuration not supported";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime or launch error";
+        case PA_ERR_BAD_BLOCK: return "PA_ERR_BAD_BLOCK: invalid page, slot, position or length";
+        case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+    }
+    return "unknown pa_status";
+}

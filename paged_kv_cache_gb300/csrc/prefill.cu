@@ -1,0 +1,439 @@
+// prefill.cu -- causal prefill over a paged KV cache on the sm_103a tensor
+// cores (tcgen05.mma, accumulators in tensor memory, operands staged by TMA).
+//
+// What is computed: query row i of a sequence attends keys 0..i; scores
+// s = scale q.k (jaehun.me tiny-vllm part 3, "Per-head attention scores and
+// GQA"), masked above the diagonal ("causalMask and online softmax"), softmax
+// with the FlashAttention-2 deferred normalisation: keep the unnormalised
+// output and l, divide once at the end, store L = m + ln l (base.kaita.kr,
+// "플래시어텐션-2: 더 나은 병렬화", "단계별 설명 (순전파의 두 가지 손질)").
+// Tiles whose keys all lie after their rows are skipped and only the diagonal
+// tile is masked ("인과 마스크 처리").  Q head h reads kv head h / (Hq / Hkv)
+// without copying K/V ("4. MQA · GQA 지원").
+//
+// GB300 mapping (prior art on the pages: cuBLAS per head + separate mask and
+// softmax kernels; FA2's warp split on A100):
+//  * One CTA per (128-row query tile, sequence, q head); tiles are launched
+//    heaviest first (last row tiles own the most key tiles), heads of one GQA
+//    group next to each other so their K/V tiles are shared through L2.
+//  * Warp 0 (TMA producer): the Q tile with one 2D tensor copy per 64-dim
+//    chunk; each 128-key K/V tile as 8 pages, each page one {64 x 16} box per
+//    chunk for K and one for V, rows addressed through the block table -- the
+//    pool is one 2D tensor [pages * 32 rows][KV_DIM], page p's K rows at 32p,
+//    V rows at 32p + 16.  128-byte swizzled boxes stack into the canonical
+//    K-major (Q, K) / MN-major (V) operand layouts of the tensor core.  Pages
+//    past the sequence end are read at an out-of-range row, which the copy
+//    engine fills with zeros.  Two K/V stages.
+//  * Warp 1 (single-thread MMA issuer): S = Q K^T (M 128, N 128, K 16 steps)
+//    into 128 TMEM columns, commit; after the softmax hands back P, O += P V
+//    with P read straight from TMEM (M 128, N 64 per 64-dim chunk, K 16).
+//  * Warps 2-5 (softmax): thread r owns query row r, i.e. TMEM lane r: it
+//    loads its 128 scores, takes the row max, forms P = 2^(s*scale*log2e - m)
+//    in fp32, packs it to bf16 over the first 64 columns of S, and keeps l in
+//    a register.  The reference max only moves when a row max exceeds it by
+//    more than 2^8; then the thread rescales its O row in TMEM (exact, since
+//    the final division uses the same m).  The epilogue divides by l, writes
+//    o (bf16) and L = ln2 (m + log2 l).
+//  * A partial last page has its V rows past the sequence end zeroed in shared
+//    memory before the PV product (masked P is exactly 0, but 0 x NaN is not).
+#include <math_constants.h>
+
+#include <cstdio>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int BM = 128;               // query rows per CTA (TMEM lanes)
+constexpr int BN = 128;               // keys per K/V tile
+constexpr int kPagesPerTile = BN / kBlockTokens;
+constexpr int kThreads = 192;         // producer, MMA, 4 softmax warps
+constexpr int kTmemCols = 256;
+constexpr int kSCol = 0;              // S (fp32, 128 columns); P (bf16x2) over its first 64
+constexpr int kOCol = 128;            // O (fp32, d columns)
+constexpr int kChunkBytes = 128 * 128;  // 128 rows x 128 bytes: one 64-dim chunk of a tile
+
+template <int D>
+struct Cfg {
+    static constexpr int KCH = D / 64;
+    static constexpr int Q_BYTES = KCH * kChunkBytes;
+    static constexpr int K_BYTES = KCH * kChunkBytes;
+    static constexpr int STAGE_BYTES = 2 * K_BYTES;
+    static constexpr int NST = 2;
+    static constexpr int CTL_BYTES = 1024;
+    static constexpr int SMEM = 1024 + Q_BYTES + NST * STAGE_BYTES + CTL_BYTES;
+    static constexpr int MIN_BLOCKS = D == 64 ? 2 : 1;
+};
+
+struct PrefillParams {
+    KGeom g;
+    const int32_t* bt;
+    int layer;
+    int batch;
+    const int32_t* cu;
+    const int32_t* slots;
+    int max_seqlen;
+    int total_tokens;
+    int n_row_tiles;
+    float scale_log2;
+    __nv_bfloat16* o;
+    float* lse;
+    int32_t* err;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, Cfg<D>::MIN_BLOCKS)
+prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
+               const PrefillParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned operand tiles
+    uint8_t* sQ = smem;
+    uint8_t* sKV = smem + C::Q_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + C::NST * C::STAGE_BYTES);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = bars + 1 + C::NST;
+    uint64_t* s_full = bars + 1 + 2 * C::NST;
+    uint64_t* p_full = s_full + 1;
+    uint64_t* o_done = s_full + 2;
+    uint64_t* mma_done = s_full + 3;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const KGeom& g = p.g;
+
+    // ---- work item: row tile (heaviest first), sequence, q head
+    const int per_tile = p.batch * g.hq;
+    const int item = blockIdx.x;
+    const int i = p.n_row_tiles - 1 - item / per_tile;
+    const int rem = item % per_tile;
+    const int b = rem / g.hq;
+    const int hq = rem % g.hq;
+    const int hk = hq / g.group;
+    const int cu0 = p.cu[b], cu1 = p.cu[b + 1];
+    const int n = cu1 - cu0;
+    const bool bad_len = cu0 < 0 || n < 0 || cu1 > p.total_tokens || n > p.max_seqlen;
+    if (i == 0 && hq == 0 && tid == 0 && bad_len) set_error(p.err, PA_ERR_BAD_BLOCK);
+    if (cu0 < 0 || n <= 0 || cu1 > p.total_tokens) return;
+    if (i * BM >= n) return;
+    const int slot = p.slots[b];
+    const bool slot_ok = slot >= 0 && slot < g.num_slots;
+    if (!slot_ok && tid == 0) set_error(p.err, PA_ERR_BAD_BLOCK);
+    const int nkv = i + 1;  // causal: key tiles 0..i
+    const int pages_b = (n + kBlockTokens - 1) / kBlockTokens;
+    const long long tbase = (static_cast<long long>(slot_ok ? slot : 0) * g.n_layers + p.layer) * g.maxb;
+
+    if (tid == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < C::NST; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(o_done, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tensor_map(&qmap);
+            prefetch_tensor_map(&kvmap);
+            mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+                tma_load_2d(sQ + c * kChunkBytes, &qmap, hq * D + 64 * c, cu0 + i * BM, q_full);
+        }
+        const int oob_row = static_cast<int>(g.nblocks * 32);  // first row past the pool: zero fill
+        int issued = 0;
+        bool stop = false;
+        for (int j = 0; j < nkv; ++j) {
+            const int st = j % C::NST;
+            if (j >= C::NST &&
+                !__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((j / C::NST) - 1) & 1, abort_flag, p.err))) {
+                stop = true;
+                break;
+            }
+            // lanes 0..7 fetch the tile's page ids
+            const int lp = j * kPagesPerTile + lane;
+            int row = -1;
+            if (lane < kPagesPerTile && lp < pages_b) {
+                if (slot_ok && lp < g.maxb) {
+                    const int e = __ldg(p.bt + tbase + lp);
+                    if (e >= 0 && e < g.nblocks) row = e * 32;
+                }
+                if (row < 0) set_error(p.err, PA_ERR_BAD_BLOCK);
+            }
+            uint8_t* sK = sKV + st * C::STAGE_BYTES;
+            uint8_t* sV = sK + C::K_BYTES;
+            if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], C::STAGE_BYTES);
+#pragma unroll
+            for (int k = 0; k < kPagesPerTile; ++k) {
+                const int r = __shfl_sync(0xffffffffu, row, k);
+                if (lane == 0) {
+                    const int y = r < 0 ? oob_row : r;
+#pragma unroll
+                    for (int c = 0; c < C::KCH; ++c) {
+                        tma_load_2d(sK + c * kChunkBytes + k * 2048, &kvmap, hk * D + 64 * c, y, &kv_full[st]);
+                        tma_load_2d(sV + c * kChunkBytes + k * 2048, &kvmap, hk * D + 64 * c, y + 16, &kv_full[st]);
+                    }
+                }
+            }
+            ++issued;
+        }
+        if (stop && lane == 0) {  // let every copy in flight land before leaving
+            mbar_drain(q_full, 0);
+            for (int jj = issued > C::NST ? issued - C::NST : 0; jj < issued; ++jj)
+                mbar_drain(&kv_full[jj % C::NST], (jj / C::NST) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
+            constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
+            const uint32_t tS = tmem + kSCol, tO = tmem + kOCol;
+            const uint32_t sq = smem_u32(sQ);
+            bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int st = j % C::NST;
+                if (!mbar_wait(&kv_full[st], (j / C::NST) & 1, abort_flag, p.err)) break;
+                tc_fence_after_sync();
+                const uint32_t sK = smem_u32(sKV + st * C::STAGE_BYTES);
+                const uint32_t sV = sK + C::K_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * kChunkBytes + (ks % 4) * 32;
+                    umma_ss(tS, umma_sdesc_sw128(sq + off, 16, 1024), umma_sdesc_sw128(sK + off, 16, 1024),
+                            idesc_qk, ks > 0 ? 1u : 0u);
+                }
+                umma_commit(s_full);
+                if (!mbar_wait(p_full, j & 1, abort_flag, p.err)) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks) {
+#pragma unroll
+                    for (int c = 0; c < C::KCH; ++c)
+                        umma_ts(tO + 64 * c, tS + ks * 8,
+                                umma_sdesc_sw128(sV + c * kChunkBytes + ks * 2048, 1024, 1024), idesc_pv,
+                                (j > 0 || ks > 0) ? 1u : 0u);
+                }
+                umma_commit(o_done);
+                umma_commit(&kv_empty[st]);
+            }
+            umma_commit(mma_done);  // every MMA of this CTA done before TMEM is freed
+            mbar_drain(mma_done, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int r = (warp & 3) * 32 + lane;  // query row in the tile == TMEM lane
+        const uint32_t lane_base = tmem_lane_base(warp);
+        const uint32_t tS = tmem + lane_base + kSCol;
+        const uint32_t tO = tmem + lane_base + kOCol;
+        const int row_in_seq = i * BM + r;
+        float m_run = -CUDART_INF_F, l_run = 0.f;
+        bool ok = true;
+        // partial last page: its V rows past the end are zeroed before the PV product
+        const int last_lp = pages_b - 1;
+        const int tail_valid = n - last_lp * kBlockTokens;
+        const bool zero_tail = (i == (n - 1) / BM) && tail_valid < kBlockTokens;
+        for (int j = 0; j < nkv; ++j) {
+            if (!__all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            uint32_t sr[128];
+            tmem_ld_x128(tS, sr);
+            const bool diag = (j == i);
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                float x = __uint_as_float(sr[c]) * p.scale_log2;
+                if (diag && c > r) x = -CUDART_INF_F;
+                sr[c] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
+            }
+            const float m_new = fmaxf(m_run, mx);
+            const bool need = m_new > m_run + 8.f;
+            const float m_use = need ? m_new : m_run;
+            const float corr = need ? ex2_approx(m_run - m_new) : 1.f;
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // move O to the new reference max once the previous PV product is done
+                if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c) {
+                    uint32_t ov[64];
+                    tmem_ld_x64(tO + 64 * c, ov);
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
+                    tmem_st_x64(tO + 64 * c, ov);
+                }
+            }
+            m_run = m_use;
+            float lsum = 0.f;
+            // P over the first 64 columns of S, 16 columns (32 keys) at a time: every
+            // score is already in registers, so the overwritten columns are free
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ex2_approx(__uint_as_float(sr[32 * q4 + 2 * e]) - m_use);
+                    const float p1 = ex2_approx(__uint_as_float(sr[32 * q4 + 2 * e + 1]) - m_use);
+                    lsum += p0 + p1;
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                tmem_st_x16_nowait(tS + 16 * q4, pk);
+            }
+            tmem_wait_st();
+            l_run = l_run * corr + lsum;
+            if (diag && zero_tail) {
+                const int st = j % C::NST;
+                if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[st], (j / C::NST) & 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sV = sKV + st * C::STAGE_BYTES + C::K_BYTES;
+                const int kk = last_lp - j * kPagesPerTile;  // page of the tile
+                const int nz = (kBlockTokens - tail_valid) * 8 * C::KCH;  // 16-byte pieces
+                for (int t = r; t < nz; t += 128) {
+                    const int piece = t & 7;
+                    const int c = (t >> 3) % C::KCH;
+                    const int row = tail_valid + (t >> 3) / C::KCH;
+                    *reinterpret_cast<uint4*>(sV + c * kChunkBytes + (kk * kBlockTokens + row) * 128 + piece * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before_sync();
+            mbar_arrive(p_full);
+        }
+        if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, (nkv - 1) & 1, abort_flag, p.err))) {
+            tc_fence_after_sync();
+            const bool store = row_in_seq < n;
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const long long orow = static_cast<long long>(cu0 + row_in_seq) * g.hq + hq;
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c) {
+                uint32_t ov[64];
+                tmem_ld_x64(tO + 64 * c, ov);
+                if (store) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + 64 * c);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv);
+                        v.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv);
+                        v.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv);
+                        v.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv);
+                        dst[e] = v;
+                    }
+                }
+            }
+            if (store && p.lse)
+                p.lse[orow] = l_run > 0.f ? (m_run + lg2_approx(l_run)) * kLn2 : -CUDART_INF_F;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2D bf16 tensor [rows][cols] with row pitch `pitch_bytes`, box {64, box_rows},
+// 128-byte swizzle, zero fill out of range.
+bool encode_2d(CUtensorMap* map, const void* base, unsigned long long cols, unsigned long long rows,
+               unsigned long long pitch_bytes, unsigned box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, const PrefillParams& p, cudaStream_t stream) {
+    auto kern = prefill_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    const long long grid = static_cast<long long>(p.n_row_tiles) * p.batch * p.g.hq;
+    if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    kern<<<static_cast<unsigned>(grid), kThreads, Cfg<D>::SMEM, stream>>>(qmap, kvmap, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, const int32_t* block_table, int layer,
+                           int batch, const int32_t* cu_seqlens, const int32_t* slots, int max_seqlen,
+                           int total_tokens, float scale, void* o, float* lse, int32_t* err, cudaStream_t stream) {
+    CUtensorMap qmap, kvmap;
+    if (!encode_2d(&qmap, q, static_cast<unsigned long long>(g.hq) * g.d, static_cast<unsigned long long>(total_tokens),
+                   static_cast<unsigned long long>(g.hq) * g.d * 2, BM))
+        return cudaErrorInvalidValue;
+    if (!encode_2d(&kvmap, pool, static_cast<unsigned long long>(g.kv_dim),
+                   static_cast<unsigned long long>(g.nblocks) * 32, static_cast<unsigned long long>(g.kv_dim) * 2,
+                   kBlockTokens))
+        return cudaErrorInvalidValue;
+    PrefillParams p;
+    p.g = g;
+    p.bt = block_table;
+    p.layer = layer;
+    p.batch = batch;
+    p.cu = cu_seqlens;
+    p.slots = slots;
+    p.max_seqlen = max_seqlen;
+    p.total_tokens = total_tokens;
+    p.n_row_tiles = (max_seqlen + BM - 1) / BM;
+    p.scale_log2 = scale * kLog2e;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.err = err;
+    return g.d == 64 ? launch<64>(qmap, kvmap, p, stream) : launch<128>(qmap, kvmap, p, stream);
+}
+
+}  // namespace pa
