@@ -1,0 +1,528 @@
+"""Benchmark of the paged-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch, inputs resident in HBM:
+  pa_write_kv  (the batch's prompt K/V, 4 x 8192 rows, into shuffled pages)
+  pa_prefill   (causal, 4 x 8192 tokens, 32 q / 8 kv heads, d 64)
+  pa_write_kv  (one new token per sequence at position 8192)
+  pa_decode    (4 sequences of 8193 tokens)
+The headline value is the step's algorithmic causal-attention FLOPs per
+second (TFLOP/s; exact causal count 4 d Hq sum_b n_b (n_b + 1) / 2 plus the
+decode's 4 d Hq n).  The line also carries:
+  roofline     -- the prefill kernel (the dominant launch) against the measured
+                  dense bf16 peak;
+  decode       -- decode KV-read GB/s on the large mixed-length batch (256
+                  sequences, log-normal lengths, new-token write + decode per
+                  step) against the measured HBM copy bandwidth;
+  e2e          -- the same metric through the C ABI with host buffers: pinned
+                  H2D of the step's inputs and D2H of its outputs inside the
+                  timed region;
+  cpu_baseline -- the fp64 CPU oracle timed on a bounded sample of the same
+                  workload on this host's cores.
+N > 1 (torchrun): independent replicas, one per GPU, no collective on the
+data path ("weak" scaling); timing is the max over ranks.
+``--impl reference`` times the CPU oracle itself as the reference arm.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20  # > the 129 MB L2
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--variant", choices=["d64", "d128"], default="d64")
+    ap.add_argument("--decode-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample time")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("prefill.cu", "decode.cu", "write_kv.cu", "pa_internal.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        m = re.match(r"\|\s*%s\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9.eE+]+)\s*\|" % re.escape(kernel_tag), line)
+        if m and m.group(1) == want:
+            return float(m.group(2))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "pa_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- workloads
+
+def causal_flops(d, hq, lens):
+    return float(sum(4.0 * d * hq * n * (n + 1) / 2.0 for n in lens))
+
+
+class PrefillStep:
+    """Device-resident inputs of the main step (write + prefill + write + decode)."""
+
+    def __init__(self, torch, pa, W, variant, seed=1003):
+        self.torch, self.pa = torch, pa
+        self.case = W.c4_long(variant, seed=seed)
+        c = self.case
+        geom = c.geom
+        # one more page per sequence for the decoded token (position 8192)
+        self.geom = W.Geometry(geom.num_q_heads, geom.num_kv_heads, geom.head_dim, 1, c.batch,
+                               geom.max_blocks_per_seq + 1, geom.num_blocks)
+        table = np.full((c.batch, 1, self.geom.max_blocks_per_seq), -1, np.int32)
+        table[:, :, :geom.max_blocks_per_seq] = c.block_table
+        used = set(c.block_table[c.block_table >= 0].tolist())
+        spare = [p for p in range(geom.num_blocks - 1, -1, -1) if p not in used][:c.batch]
+        table[np.arange(c.batch), 0, geom.max_blocks_per_seq] = spare
+        self.table_np = table
+        self.g = pa.geom(*self.geom.as_tuple())
+        rng = np.random.default_rng(seed + 50)
+        n = int(c.lens[0])
+        self.new_slot = np.arange(c.batch, dtype=np.int32)
+        self.new_pos = np.full(c.batch, n, np.int32)
+        self.new_k = W.normal_bf16(rng, (c.batch, geom.kv_dim))
+        self.new_v = W.normal_bf16(rng, (c.batch, geom.kv_dim))
+        self.dec_q = W.normal_bf16(rng, (c.batch, geom.num_q_heads, geom.head_dim))
+        self.dec_lens = np.full(c.batch, n + 1, np.int32)
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        w = c.writes[0]
+        self.h = {"q": c.q, "k": w.k, "v": w.v, "tok_slot": w.tok_slot, "tok_pos": w.tok_pos,
+                  "cu": c.cu_seqlens, "slots": c.slots, "bt": table, "new_slot": self.new_slot,
+                  "new_pos": self.new_pos, "new_k": self.new_k, "new_v": self.new_v, "dec_q": self.dec_q,
+                  "dec_lens": self.dec_lens}
+        self.d = {k: dev(v) for k, v in self.h.items()}
+        self.pool = torch.empty(self.geom.pool_bytes, dtype=torch.uint8, device="cuda")
+        T, Hq, D = c.total_tokens, geom.num_q_heads, geom.head_dim
+        self.o = torch.empty((T, Hq, D), dtype=torch.int16, device="cuda")
+        self.lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+        self.dec_o = torch.empty((c.batch, Hq, D), dtype=torch.int16, device="cuda")
+        self.dec_lse = torch.empty((c.batch, Hq), dtype=torch.float32, device="cuda")
+        self.ws = torch.empty(pa.pa_decode_workspace_size(self.g, c.batch, n + 1), dtype=torch.uint8,
+                              device="cuda")
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.n = n
+        self.flops_prefill = causal_flops(geom.head_dim, Hq, c.lens)
+        self.flops_decode = float(4.0 * geom.head_dim * Hq * np.sum(self.dec_lens))
+        self.flops = self.flops_prefill + self.flops_decode
+        self.launches = 5  # write, prefill, write, attend, merge
+
+    def run(self, d=None, ev=None):
+        pa, c = self.pa, self.case
+        d = self.d if d is None else d
+        pa.pa_write_kv(self.g, self.pool, d["bt"], 0, d["tok_slot"], d["tok_pos"], d["k"], d["v"], self.err)
+        if ev is not None:
+            ev[0].record()
+        pa.pa_prefill(self.g, d["q"], self.pool, d["bt"], 0, d["cu"], d["slots"], self.n, c.scale, self.o,
+                      self.lse, self.err)
+        if ev is not None:
+            ev[1].record()
+        pa.pa_write_kv(self.g, self.pool, d["bt"], 0, d["new_slot"], d["new_pos"], d["new_k"], d["new_v"],
+                       self.err)
+        pa.pa_decode(self.g, d["dec_q"], self.pool, d["bt"], 0, d["dec_lens"], d["slots"], self.n + 1,
+                     c.scale, self.dec_o, self.dec_lse, self.ws, self.err)
+
+
+class DecodeStep:
+    """The large mixed decode batch: 256 sequences, log-normal lengths, 4 GiB
+    pool; c-1 tokens preloaded, each step writes the token at c-1 and decodes c."""
+
+    def __init__(self, torch, pa, W, seed=1004):
+        self.torch, self.pa = torch, pa
+        lens = W.c5_lens(seed)
+        self.lens_np = lens
+        B = lens.shape[0]
+        self.geom = W.Geometry(32, 8, 64, 1, B, 1024, 131072)
+        rng = np.random.default_rng(seed + 1)
+        table = W.empty_table(self.geom)
+        free = W.FreeList(self.geom.num_blocks, rng)
+        for b in range(B):
+            W.assign_pages(table, free, b, 0, int(lens[b]))
+        self.g = pa.geom(*self.geom.as_tuple())
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed)
+        kv_dim = self.geom.kv_dim
+        pre = np.maximum(lens - 1, 0)
+        tok_slot = np.repeat(np.arange(B, dtype=np.int32), pre)
+        tok_pos = np.concatenate([np.arange(n, dtype=np.int32) for n in pre])
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        self.bt = dev(table)
+        self.pool = torch.empty(self.geom.pool_bytes, dtype=torch.uint8, device="cuda")
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        k = torch.randn((int(pre.sum()), kv_dim), generator=gen, device="cuda").to(torch.bfloat16)
+        v = torch.randn((int(pre.sum()), kv_dim), generator=gen, device="cuda").to(torch.bfloat16)
+        pa.pa_write_kv(self.g, self.pool, self.bt, 0, dev(tok_slot), dev(tok_pos), k, v, self.err)
+        del k, v
+        self.new_slot = dev(np.arange(B, dtype=np.int32))
+        self.new_pos = dev((lens - 1).astype(np.int32))
+        self.new_k = torch.randn((B, kv_dim), generator=gen, device="cuda").to(torch.bfloat16)
+        self.new_v = torch.randn((B, kv_dim), generator=gen, device="cuda").to(torch.bfloat16)
+        self.q = torch.randn((B, 32, 64), generator=gen, device="cuda").to(torch.bfloat16)
+        self.lens = dev(lens)
+        self.slots = dev(np.arange(B, dtype=np.int32))
+        self.o = torch.empty((B, 32, 64), dtype=torch.bfloat16, device="cuda")
+        self.lse = torch.empty((B, 32), dtype=torch.float32, device="cuda")
+        self.max_len = int(lens.max())
+        self.ws = torch.empty(pa.pa_decode_workspace_size(self.g, B, self.max_len), dtype=torch.uint8,
+                              device="cuda")
+        self.kv_bytes = float(np.sum(lens)) * 2 * kv_dim * 2  # K and V rows read
+        torch.cuda.synchronize()
+        assert int(self.err.item()) == 0
+
+    def run(self, ev=None):
+        pa = self.pa
+        pa.pa_write_kv(self.g, self.pool, self.bt, 0, self.new_slot, self.new_pos, self.new_k, self.new_v,
+                       self.err)
+        if ev is not None:
+            ev[0].record()
+        pa.pa_decode(self.g, self.q, self.pool, self.bt, 0, self.lens, self.slots, self.max_len, 0.125,
+                     self.o, self.lse, self.ws, self.err)
+        if ev is not None:
+            ev[1].record()
+
+
+# ----------------------------------------------------------------- timing
+
+def timed(torch, fn, steps, warmup, flush, dist=None, kernel_events=True):
+    """Runs fn(ev) warmup + steps times; L2 flushed before every step outside
+    the timed events.  Returns (step seconds list, kernel seconds list)."""
+    for _ in range(warmup):
+        flush.zero_()
+        fn(None)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    E = torch.cuda.Event
+    marks = [(E(enable_timing=True), E(enable_timing=True), E(enable_timing=True), E(enable_timing=True))
+             for _ in range(steps)]
+    for m in marks:
+        flush.zero_()
+        m[0].record()
+        fn((m[2], m[3]) if kernel_events else None)
+        m[1].record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_s = [m[0].elapsed_time(m[1]) * 1e-3 for m in marks]
+    kern_s = [m[2].elapsed_time(m[3]) * 1e-3 for m in marks] if kernel_events else []
+    return step_s, kern_s
+
+
+def max_over_ranks(torch, dist, x):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(torch, dist, x):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(case, seconds, rng_seed=5):
+    """Times the oracle on sampled (row, head) outputs of a prefill case,
+    growing the sample until it takes about `seconds`.  Returns
+    (flops, wall seconds, threads, description)."""
+    import oracle
+    from paged_kv_cache_gb300 import workloads as W
+    g = oracle.geom(*case.geom.as_tuple())
+    pool = W.initial_pool(case.geom, "zero", 0)
+    for w in case.writes:
+        oracle.write_kv(g, pool, case.block_table, w.layer, w.tok_slot, w.tok_pos, w.k, w.v)
+    rng = np.random.default_rng(rng_seed)
+    cu = case.cu_seqlens
+    n_pairs, flops, wall = 16, 0.0, 0.0
+    threads = oracle.default_threads()
+    while True:
+        rows = rng.integers(0, case.total_tokens, n_pairs)
+        heads = rng.integers(0, case.geom.num_q_heads, n_pairs).astype(np.int32)
+        b = np.searchsorted(cu, rows, side="right") - 1
+        pos = rows - cu[b]
+        f = float(np.sum(4.0 * case.geom.head_dim * (pos + 1)))
+        t0 = time.perf_counter()
+        st, _, _ = oracle.prefill_rows(g, case.q, pool, case.block_table, case.layer, cu, case.slots,
+                                       case.scale, rows, heads)
+        dt = time.perf_counter() - t0
+        assert st == 0
+        flops, wall = f, dt
+        if dt >= seconds * 0.5 or n_pairs >= 1 << 20:
+            break
+        n_pairs = int(n_pairs * min(64.0, max(2.0, seconds / max(dt, 1e-3))))
+    desc = ("%d random (row, q head) outputs of the 4 x 8192 causal prefill (%.3g GFLOP exact-causal), "
+            "K/V gathered through the block table, fp64, %d threads" % (n_pairs, flops / 1e9, threads))
+    return flops, wall, threads, desc
+
+
+# ------------------------------------------------------------------- arms
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from paged_kv_cache_gb300 import workloads as W
+    case = W.c4_long(args.variant)
+    per_step = min(5.0, max(0.5, 150.0 / max(1, args.steps + args.warmup)))
+    import oracle
+    g = oracle.geom(*case.geom.as_tuple())
+    pool = W.initial_pool(case.geom, "zero", 0)
+    for w in case.writes:
+        oracle.write_kv(g, pool, case.block_table, w.layer, w.tok_slot, w.tok_pos, w.k, w.v)
+    # calibrate a sample size for ~per_step seconds
+    flops1, wall1, threads, _ = oracle_sample(case, per_step)
+    rate = flops1 / wall1
+    rng = np.random.default_rng(11)
+    cu = case.cu_seqlens
+    avg_flops_per_pair = 4.0 * case.geom.head_dim * (case.lens.mean() + 1) / 2
+    pairs = max(8, int(rate * per_step / avg_flops_per_pair))
+    tot_f, tot_t = 0.0, 0.0
+    for s in range(args.warmup + args.steps):
+        rows = rng.integers(0, case.total_tokens, pairs)
+        heads = rng.integers(0, case.geom.num_q_heads, pairs).astype(np.int32)
+        b = np.searchsorted(cu, rows, side="right") - 1
+        f = float(np.sum(4.0 * case.geom.head_dim * (rows - cu[b] + 1)))
+        t0 = time.perf_counter()
+        st, _, _ = oracle.prefill_rows(g, case.q, pool, case.block_table, 0, cu, case.slots, case.scale,
+                                       rows, heads)
+        dt = time.perf_counter() - t0
+        assert st == 0
+        if s >= args.warmup:
+            tot_f += f
+            tot_t += dt
+    value = tot_f / tot_t / 1e12
+    sample = ("per step: %d random (row, q head) outputs of the 4 x 8192 causal prefill, fp64 oracle, "
+              "K/V gathered through the block table" % pairs)
+    line = {
+        "impl": "reference", "metric": "causal prefill TFLOP/s (exact causal count, step incl. KV write + decode)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "long-context causal prefill 4 x 8192, 32 q / 8 kv heads, d 64"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        dist = dist_mod
+    import paged_kv_cache_gb300 as pa
+    from paged_kv_cache_gb300 import workloads as W
+    pa.load_library()
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    # ---------------------------------------------------------- main step
+    step = PrefillStep(torch, pa, W, args.variant)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    step_s, pre_s = timed(torch, lambda ev: step.run(ev=ev), args.steps, args.warmup, flush, dist)
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    err = int(step.err.item())
+    if err != 0:
+        raise SystemExit("device error during the timed steps: %s" % pa.pa_status_string(err))
+    total_s = max_over_ranks(torch, dist, float(np.sum(step_s)))
+    all_flops = sum_over_ranks(torch, dist, step.flops * args.steps)
+    value = all_flops / total_s / 1e12
+    prefill_avg = float(np.mean(pre_s))
+    achieved = step.flops_prefill / prefill_avg / 1e12
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": achieved / bf16_peak, "traffic": profiled_traffic("prefill_" + args.variant),
+                "kernel": "prefill_kernel<%d>" % step.geom.head_dim,
+                "peak_source": "%s bf16_tflops (burst)" % peak_src,
+                "algorithmic_flops_per_launch": step.flops_prefill}
+
+    # ------------------------------------------------------ decode (C5)
+    dstep = DecodeStep(torch, pa, W)
+    dsteps = args.decode_steps or max(20, args.steps)
+    dstep_s, dk_s = timed(torch, lambda ev: dstep.run(ev=ev), dsteps, args.warmup, flush, dist)
+    torch.cuda.synchronize()
+    if int(dstep.err.item()) != 0:
+        raise SystemExit("device error in decode steps: %s" % pa.pa_status_string(int(dstep.err.item())))
+    dec_avg = float(np.mean(dk_s))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    dec_gbs = dstep.kv_bytes / dec_avg / 1e9
+    d_total = max_over_ranks(torch, dist, float(np.sum(dstep_s)))
+    d_all = sum_over_ranks(torch, dist, dstep.kv_bytes * dsteps)
+    decode = {"metric": "decode KV-read GB/s (256 seqs, log-normal lengths, write + decode per step)",
+              "value": d_all / d_total / 1e9, "unit": "GB/s", "ms_per_step": d_total / dsteps * 1e3,
+              "kv_bytes_per_step": dstep.kv_bytes,
+              "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
+                           "frac": dec_gbs / hbm_peak, "traffic": profiled_traffic("decode_c5"),
+                           "kernel": "decode_attend_kernel<64,4> + decode_merge_kernel<64>",
+                           "peak_source": "%s hbm_gbs" % peak_src,
+                           "algorithmic_bytes_per_launch": dstep.kv_bytes}}
+    del dstep
+
+    # ------------------------------------------------------------ e2e
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in step.h.items()}
+        o_host = torch.empty(step.o.shape, dtype=torch.int16).pin_memory()
+        lse_host = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
+        do_host = torch.empty(step.dec_o.shape, dtype=torch.int16).pin_memory()
+        dl_host = torch.empty(step.dec_lse.shape, dtype=torch.float32).pin_memory()
+        d_in = {k: torch.empty_like(v, device="cuda") for k, v in pin.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in (o_host, lse_host, do_host, dl_host))
+
+        def e2e_step(ev):
+            for k, v in pin.items():
+                d_in[k].copy_(v, non_blocking=True)
+            step.run(d=d_in)
+            o_host.copy_(step.o, non_blocking=True)
+            lse_host.copy_(step.lse, non_blocking=True)
+            do_host.copy_(step.dec_o, non_blocking=True)
+            dl_host.copy_(step.dec_lse, non_blocking=True)
+
+        e_steps = max(10, args.steps // 4)
+        es, _ = timed(torch, e2e_step, e_steps, args.warmup, flush, dist, kernel_events=False)
+        e_total = max_over_ranks(torch, dist, float(np.sum(es)))
+        e_flops = sum_over_ranks(torch, dist, step.flops * e_steps)
+        e2e = {"value": e_flops / e_total / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": e_steps}
+
+    # ------------------------------------------------------- CPU oracle
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        flops, wall, threads, desc = oracle_sample(step.case, args.cpu_seconds)
+        cpu = {"value": flops / wall / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": desc, "seconds": wall}
+
+    if rank == 0:
+        line = {
+            "metric": "causal prefill TFLOP/s (exact causal count, step incl. KV write + decode)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "long-context causal prefill 4 x 8192, %d q / %d kv heads, d %d, "
+                                   "paged through shuffled 16-token pages; step = write_kv + prefill + "
+                                   "write_kv(new token) + decode(8193)" % (
+                                       step.geom.num_q_heads, step.geom.num_kv_heads, step.geom.head_dim),
+                       "global_batch": step.case.batch * world, "seq_len": step.n,
+                       "parallelism": "replicas x%d" % world,
+                       "l2": "flushed (256 MiB write) before every timed step, outside the events"},
+            "gpu_launches": step.launches * args.steps,
+            "roofline": roofline,
+            "decode": decode,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+            "kernel_source": kernel_source_hash(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

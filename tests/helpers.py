@@ -144,7 +144,8 @@ def assert_close(o_gpu, l_gpu, o_ref, l_ref, vmax, what=""):
     assert err_o <= tol_o, "%s: max |dO| %.3g > %.3g" % (what, err_o, tol_o)
     if l_gpu is not None:
         same_inf = np.isinf(l_ref) & (l_gpu == l_ref)
-        d = np.where(same_inf, 0.0, np.abs(l_gpu - l_ref))
+        with np.errstate(invalid="ignore"):
+            d = np.where(same_inf, 0.0, np.abs(l_gpu - l_ref))
         err_l = float(np.max(d)) if d.size else 0.0
         assert err_l <= 1e-3, "%s: max |dL| %.3g > 1e-3" % (what, err_l)
     return err_o
