@@ -52,6 +52,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample time")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="profiling aid: run only the main (prefill) step or only the decode step")
+    ap.add_argument("--batch", type=int, default=4, help="prefill sequences (profiling aid)")
+    ap.add_argument("--seqlen", type=int, default=8192, help="prefill length (profiling aid)")
     return ap.parse_args()
 
 
@@ -144,9 +148,9 @@ def causal_flops(d, hq, lens):
 class PrefillStep:
     """Device-resident inputs of the main step (write + prefill + write + decode)."""
 
-    def __init__(self, torch, pa, W, variant, seed=1003):
+    def __init__(self, torch, pa, W, variant, seed=1003, batch=4, seqlen=8192):
         self.torch, self.pa = torch, pa
-        self.case = W.c4_long(variant, seed=seed)
+        self.case = W.c4_long(variant, seed=seed, batch=batch, seqlen=seqlen)
         c = self.case
         geom = c.geom
         # one more page per sequence for the decoded token (position 8192)
@@ -156,7 +160,10 @@ class PrefillStep:
         table[:, :, :geom.max_blocks_per_seq] = c.block_table
         used = set(c.block_table[c.block_table >= 0].tolist())
         spare = [p for p in range(geom.num_blocks - 1, -1, -1) if p not in used][:c.batch]
-        table[np.arange(c.batch), 0, geom.max_blocks_per_seq] = spare
+        n_prompt = int(c.lens[0])
+        for b in range(c.batch):  # page of the decoded token, if the prompt left none
+            if table[b, 0, n_prompt // 16] < 0:
+                table[b, 0, n_prompt // 16] = spare[b]
         self.table_np = table
         self.g = pa.geom(*self.geom.as_tuple())
         rng = np.random.default_rng(seed + 50)
@@ -418,53 +425,60 @@ def main():
     peaks, peak_src = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
-    # ---------------------------------------------------------- main step
-    step = PrefillStep(torch, pa, W, args.variant)
+    roofline = decode = e2e = None
+    value = total_s = None
+    step = None
+    clk = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
     clocks = ClockSampler(local_rank)
     clocks.start()
-    step_s, pre_s = timed(torch, lambda ev: step.run(ev=ev), args.steps, args.warmup, flush, dist)
+    if args.only in ("all", "prefill"):
+        # ------------------------------------------------------ main step
+        step = PrefillStep(torch, pa, W, args.variant, batch=args.batch, seqlen=args.seqlen)
+        step_s, pre_s = timed(torch, lambda ev: step.run(ev=ev), args.steps, args.warmup, flush, dist)
+        torch.cuda.synchronize()
+        err = int(step.err.item())
+        if err != 0:
+            raise SystemExit("device error during the timed steps: %s" % pa.pa_status_string(err))
+        total_s = max_over_ranks(torch, dist, float(np.sum(step_s)))
+        all_flops = sum_over_ranks(torch, dist, step.flops * args.steps)
+        value = all_flops / total_s / 1e12
+        prefill_avg = float(np.mean(pre_s))
+        achieved = step.flops_prefill / prefill_avg / 1e12
+        bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                    "frac": achieved / bf16_peak, "traffic": profiled_traffic("prefill_" + args.variant),
+                    "kernel": "prefill_kernel<%d>" % step.geom.head_dim,
+                    "peak_source": "%s bf16_tflops (burst)" % peak_src,
+                    "algorithmic_flops_per_launch": step.flops_prefill,
+                    "avg_launch_ms": prefill_avg * 1e3}
+
+    if args.only in ("all", "decode"):
+        # -------------------------------------------------- decode (C5)
+        dstep = DecodeStep(torch, pa, W)
+        dsteps = args.decode_steps or max(20, args.steps)
+        dstep_s, dk_s = timed(torch, lambda ev: dstep.run(ev=ev), dsteps, args.warmup, flush, dist)
+        torch.cuda.synchronize()
+        if int(dstep.err.item()) != 0:
+            raise SystemExit("device error in decode steps: %s" % pa.pa_status_string(int(dstep.err.item())))
+        dec_avg = float(np.mean(dk_s))
+        hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        dec_gbs = dstep.kv_bytes / dec_avg / 1e9
+        d_total = max_over_ranks(torch, dist, float(np.sum(dstep_s)))
+        d_all = sum_over_ranks(torch, dist, dstep.kv_bytes * dsteps)
+        decode = {"metric": "decode KV-read GB/s (256 seqs, log-normal lengths, write + decode per step)",
+                  "value": d_all / d_total / 1e9, "unit": "GB/s", "ms_per_step": d_total / dsteps * 1e3,
+                  "kv_bytes_per_step": dstep.kv_bytes, "steps": dsteps,
+                  "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
+                               "frac": dec_gbs / hbm_peak, "traffic": profiled_traffic("decode_c5"),
+                               "kernel": "decode_attend_kernel<64,4> + decode_merge_kernel<64>",
+                               "peak_source": "%s hbm_gbs" % peak_src,
+                               "algorithmic_bytes_per_launch": dstep.kv_bytes,
+                               "avg_launch_ms": dec_avg * 1e3}}
+        del dstep
     clk = clocks.stop()
-    torch.cuda.synchronize()
-    err = int(step.err.item())
-    if err != 0:
-        raise SystemExit("device error during the timed steps: %s" % pa.pa_status_string(err))
-    total_s = max_over_ranks(torch, dist, float(np.sum(step_s)))
-    all_flops = sum_over_ranks(torch, dist, step.flops * args.steps)
-    value = all_flops / total_s / 1e12
-    prefill_avg = float(np.mean(pre_s))
-    achieved = step.flops_prefill / prefill_avg / 1e12
-    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
-                "frac": achieved / bf16_peak, "traffic": profiled_traffic("prefill_" + args.variant),
-                "kernel": "prefill_kernel<%d>" % step.geom.head_dim,
-                "peak_source": "%s bf16_tflops (burst)" % peak_src,
-                "algorithmic_flops_per_launch": step.flops_prefill}
 
-    # ------------------------------------------------------ decode (C5)
-    dstep = DecodeStep(torch, pa, W)
-    dsteps = args.decode_steps or max(20, args.steps)
-    dstep_s, dk_s = timed(torch, lambda ev: dstep.run(ev=ev), dsteps, args.warmup, flush, dist)
-    torch.cuda.synchronize()
-    if int(dstep.err.item()) != 0:
-        raise SystemExit("device error in decode steps: %s" % pa.pa_status_string(int(dstep.err.item())))
-    dec_avg = float(np.mean(dk_s))
-    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    dec_gbs = dstep.kv_bytes / dec_avg / 1e9
-    d_total = max_over_ranks(torch, dist, float(np.sum(dstep_s)))
-    d_all = sum_over_ranks(torch, dist, dstep.kv_bytes * dsteps)
-    decode = {"metric": "decode KV-read GB/s (256 seqs, log-normal lengths, write + decode per step)",
-              "value": d_all / d_total / 1e9, "unit": "GB/s", "ms_per_step": d_total / dsteps * 1e3,
-              "kv_bytes_per_step": dstep.kv_bytes,
-              "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
-                           "frac": dec_gbs / hbm_peak, "traffic": profiled_traffic("decode_c5"),
-                           "kernel": "decode_attend_kernel<64,4> + decode_merge_kernel<64>",
-                           "peak_source": "%s hbm_gbs" % peak_src,
-                           "algorithmic_bytes_per_launch": dstep.kv_bytes}}
-    del dstep
-
-    # ------------------------------------------------------------ e2e
-    e2e = None
-    if not args.no_e2e:
+    if step is not None and not args.no_e2e:
+        # ------------------------------------------------------------ e2e
         pin = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in step.h.items()}
         o_host = torch.empty(step.o.shape, dtype=torch.int16).pin_memory()
         lse_host = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
@@ -492,17 +506,19 @@ def main():
 
     # ------------------------------------------------------- CPU oracle
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and step is not None and not args.no_cpu_baseline:
         flops, wall, threads, desc = oracle_sample(step.case, args.cpu_seconds)
         cpu = {"value": flops / wall / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": desc, "seconds": wall}
 
-    if rank == 0:
+    if rank == 0 and step is None:
+        print(json.dumps({"metric": "decode only (profiling aid)", "decode": decode, "clocks": clk}), flush=True)
+    elif rank == 0:
         line = {
             "metric": "causal prefill TFLOP/s (exact causal count, step incl. KV write + decode)",
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, shuffled pages)",
             "config": {"workload": "long-context causal prefill 4 x 8192, %d q / %d kv heads, d %d, "
                                    "paged through shuffled 16-token pages; step = write_kv + prefill + "
                                    "write_kv(new token) + decode(8193)" % (
