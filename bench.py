@@ -154,9 +154,9 @@ class PrefillStep:
         c = self.case
         geom = c.geom
         # one more page per sequence for the decoded token (position 8192)
-        self.geom = W.Geometry(geom.num_q_heads, geom.num_kv_heads, geom.head_dim, 1, c.batch,
+        self.geom = W.Geometry(geom.num_q_heads, geom.num_kv_heads, geom.head_dim, 1, geom.num_slots,
                                geom.max_blocks_per_seq + 1, geom.num_blocks)
-        table = np.full((c.batch, 1, self.geom.max_blocks_per_seq), -1, np.int32)
+        table = np.full((geom.num_slots, 1, self.geom.max_blocks_per_seq), -1, np.int32)
         table[:, :, :geom.max_blocks_per_seq] = c.block_table
         used = set(c.block_table[c.block_table >= 0].tolist())
         spare = [p for p in range(geom.num_blocks - 1, -1, -1) if p not in used][:c.batch]
