@@ -34,7 +34,9 @@
  *   GQA: q head h reads kv head h / (Hq / Hkv).
  *
  * Ownership: the caller allocates and owns every buffer (device memory unless
- * stated).  The library allocates no memory and keeps no state between calls.
+ * stated).  The library allocates no memory and keeps no state between calls
+ * (pa_decode_noalloc's fixed scratch, described at that call, is the one
+ * exception to the second point).
  * All calls are asynchronous on `stream`; they return after validating the
  * arguments and enqueueing the kernels.
  *
@@ -169,6 +171,38 @@ pa_status pa_decode(const pa_geom* geom, const void* q, const void* pool,
                     const int32_t* seq_lens, const int32_t* slots, int32_t max_seq_len,
                     float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
                     int32_t* err_flag, pa_stream_t stream);
+
+/*
+ * PA_DECODE_STATIC_SCRATCH_BYTES / pa_decode_noalloc -- decode without a
+ * caller-provided workspace.  The paper has no counterpart to this call; it
+ * exists for callers that cannot allocate device memory at the point where
+ * they decode: for example a plugin inside a host application that reserves
+ * all device memory up front for its own allocator, or a serving loop that
+ * must not call cudaMalloc (which can synchronise the device) between steps.
+ *
+ * Same arguments, definition and results as pa_decode, minus the workspace.
+ * The split partials go to a fixed scratch array of
+ * PA_DECODE_STATIC_SCRATCH_BYTES that lives inside libpa.so's device code:
+ * every GPU on which the library's kernels are loaded holds these bytes until
+ * the process exits.  The call allocates nothing.
+ *   - Size limit: a request whose pa_decode_workspace_size(geom, batch,
+ *     max_seq_len) exceeds PA_DECODE_STATIC_SCRATCH_BYTES is rejected with
+ *     PA_ERR_UNSUPPORTED before anything is enqueued (use pa_decode then).
+ *   - Set-up: the first call on each device (with that device current) looks
+ *     up the scratch array's device address; make that first call before any
+ *     stream capture.
+ *   - Sharing: every call on a device uses the same scratch, which keeps the
+ *     previous call's contents (nothing in it needs to start at zero).  Calls
+ *     that can overlap on the GPU -- on different streams without ordering,
+ *     or from different host threads -- race on it; serialise them.
+ */
+#define PA_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+
+pa_status pa_decode_noalloc(const pa_geom* geom, const void* q, const void* pool,
+                            const int32_t* block_table, int32_t layer, int32_t batch,
+                            const int32_t* seq_lens, const int32_t* slots, int32_t max_seq_len,
+                            float scale, void* o, float* lse, int32_t* err_flag,
+                            pa_stream_t stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* pa_status_string(pa_status status);

@@ -11,6 +11,7 @@ Calls (same names as the C ABI):
 * ``pa_write_kv(geom, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new, err_flag)``
 * ``pa_prefill(geom, q, pool, block_table, layer, cu_seqlens, slots, max_seqlen, scale, o, lse, err_flag)``
 * ``pa_decode(geom, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse, workspace, err_flag)``
+* ``pa_decode_noalloc(geom, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse, err_flag)``
 * ``pa_decode_workspace_size(geom, batch, max_seq_len)``, ``pa_page_bytes(geom)``, ``pa_status_string(code)``
 
 Tensors are torch CUDA tensors (bf16 data may be given as bfloat16 or int16
@@ -30,7 +31,8 @@ PA_BLOCK_TOKENS = 16
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libpa.so")
 EXPORTED = ("pa_page_bytes", "pa_write_kv", "pa_prefill", "pa_decode_workspace_size", "pa_decode",
-            "pa_status_string")
+            "pa_decode_noalloc", "pa_status_string")
+PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class PaGeom(C.Structure):
@@ -78,6 +80,9 @@ def load_library(path: str = None):
     L.pa_decode.restype = C.c_int
     L.pa_decode.argtypes = [C.POINTER(PaGeom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, C.c_int32,
                             C.c_float, _P, _P, _P, C.c_size_t, _P, _P]
+    L.pa_decode_noalloc.restype = C.c_int
+    L.pa_decode_noalloc.argtypes = [C.POINTER(PaGeom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P,
+                                    C.c_int32, C.c_float, _P, _P, _P, _P]
     L.pa_status_string.restype = C.c_char_p
     L.pa_status_string.argtypes = [C.c_int]
     if path == LIB_PATH:
@@ -155,3 +160,15 @@ def pa_decode(g, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scal
         C.byref(g), _ptr(q), _ptr(pool), _ptr(block_table), layer, batch, _ptr(seq_lens),
         _ptr(slots), int(max_seq_len), float(scale), _ptr(o), _ptr(lse), _ptr(workspace),
         int(workspace_bytes), _ptr(err_flag), _stream(stream)))
+
+
+def pa_decode_noalloc(g, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse,
+                      err_flag, stream=None, batch=None):
+    """pa_decode without a workspace argument, for callers that cannot
+    allocate device memory where they decode (see include/pa.h): the split
+    partials use a fixed scratch array inside the library's device code."""
+    batch = int(seq_lens.shape[0]) if batch is None else int(batch)
+    _check("pa_decode_noalloc", lib().pa_decode_noalloc(
+        C.byref(g), _ptr(q), _ptr(pool), _ptr(block_table), layer, batch, _ptr(seq_lens),
+        _ptr(slots), int(max_seq_len), float(scale), _ptr(o), _ptr(lse), _ptr(err_flag),
+        _stream(stream)))

@@ -35,6 +35,8 @@
 //    more than 2^8 (exact: o and l share the same reference m).
 #include <math_constants.h>
 
+#include <mutex>
+
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -613,3 +615,58 @@ cudaError_t launch_decode(const KGeom& g, const void* q, const void* pool, const
 }
 
 }  // namespace pa
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode (pa_decode_noalloc, declared in pa.h).
+//
+// For callers that cannot allocate device memory where they decode -- a
+// plugin whose host application has already reserved the device memory for
+// its own allocator, or a serving loop that must not call cudaMalloc between
+// steps -- the split partials go to this fixed array instead of a caller
+// workspace.  It is part of the library's device code, so every GPU that
+// loads these kernels holds it until the process exits.  Nothing in it has to
+// start at zero: every byte the merge kernel reads is written earlier in the
+// same call.  Calls that overlap on the GPU share it and race.
+namespace pa {
+namespace {
+
+constexpr size_t kStaticScratchBytes = PA_DECODE_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_decode_scratch on the current device, looked up once
+// per device (in host code the array's name is only a host-side stand-in).
+cudaError_t static_scratch(void** out) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" __attribute__((visibility("default"))) pa_status pa_decode_noalloc(
+    const pa_geom* geom, const void* q, const void* pool, const int32_t* block_table, int32_t layer,
+    int32_t batch, const int32_t* seq_lens, const int32_t* slots, int32_t max_seq_len, float scale,
+    void* o, float* lse, int32_t* err_flag, pa_stream_t stream) {
+    if (pa_decode_workspace_size(geom, batch, max_seq_len) > pa::kStaticScratchBytes)
+        return PA_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if (pa::static_scratch(&scratch) != cudaSuccess) return PA_ERR_CUDA;
+    return pa_decode(geom, q, pool, block_table, layer, batch, seq_lens, slots, max_seq_len, scale, o,
+                     lse, scratch, pa::kStaticScratchBytes, err_flag, stream);
+}
+
