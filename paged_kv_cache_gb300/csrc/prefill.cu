@@ -49,9 +49,8 @@ constexpr int BM = 128;               // query rows per CTA (TMEM lanes)
 constexpr int BN = 128;               // keys per K/V tile
 constexpr int kPagesPerTile = BN / kBlockTokens;
 constexpr int kThreads = 192;         // producer, MMA, 4 softmax warps
-constexpr int kTmemCols = 256;
-constexpr int kSCol = 0;              // S (fp32, 128 columns); P (bf16x2) over its first 64
-constexpr int kOCol = 128;            // O (fp32, d columns)
+constexpr int kSCol = 0;              // S (fp32, 128 columns)
+constexpr int kOCol = 128;            // O (fp32, d columns); P (bf16 pairs, 64 columns) after it
 constexpr int kChunkBytes = 128 * 128;  // 128 rows x 128 bytes: one 64-dim chunk of a tile
 
 template <int D>
@@ -64,6 +63,8 @@ struct Cfg {
     static constexpr int CTL_BYTES = 1024;
     static constexpr int SMEM = 1024 + Q_BYTES + NST * STAGE_BYTES + CTL_BYTES;
     static constexpr int MIN_BLOCKS = D == 64 ? 2 : 1;
+    static constexpr int P_COL = kOCol + D;            // 192 or 256
+    static constexpr int TMEM_COLS = D == 64 ? 256 : 512;  // power of two >= P_COL + 64
 };
 
 struct PrefillParams {
@@ -81,6 +82,77 @@ struct PrefillParams {
     float* lse;
     int32_t* err;
 };
+
+// Softmax of one tile for the calling thread's query row r (= its TMEM lane).
+// The 128 scores are streamed from TMEM 32 columns at a time, the next chunk's
+// load in flight while the current one is processed.  On the diagonal tile the
+// keys after the row are masked to -inf.
+
+// Row max of the raw scores.
+template <bool DIAG>
+__device__ __forceinline__ float tile_row_max(uint32_t tS, int r) {
+    uint32_t b0[32], b1[32];
+    float mx = -CUDART_INF_F;
+    tmem_ld_x32_nowait(tS, b0);
+    tmem_wait_ld_dep(b0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t(&cur)[32] = (q & 1) ? b1 : b0;
+        uint32_t(&nxt)[32] = (q & 1) ? b0 : b1;
+        if (q < 3) tmem_ld_x32_nowait(tS + 32 * (q + 1), nxt);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            float s0 = __uint_as_float(cur[e]), s1 = __uint_as_float(cur[e + 1]);
+            if (DIAG) {
+                if (32 * q + e > r) s0 = -CUDART_INF_F;
+                if (32 * q + e + 1 > r) s1 = -CUDART_INF_F;
+            }
+            mx = fmax3(mx, s0, s1);
+        }
+        if (q < 3) tmem_wait_ld_dep(nxt);
+    }
+    return mx;
+}
+
+// P = 2^(s * sc - m_ref) as bf16 pairs into the 64 TMEM columns at tP (one
+// packed FMA per two scores, one ex2 each); returns the sum of the fp32 P and,
+// through mx, the raw row max of the tile (tracked in the same pass).
+template <bool DIAG>
+__device__ __forceinline__ float tile_row_p(uint32_t tS, uint32_t tP, int r, float sc, float m_ref, float& mx) {
+    const float nm = -m_ref;
+    float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 4 independent pair sums
+    float m = -CUDART_INF_F;
+    uint32_t b0[32], b1[32];
+    tmem_ld_x32_nowait(tS, b0);
+    tmem_wait_ld_dep(b0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t(&cur)[32] = (q & 1) ? b1 : b0;
+        uint32_t(&nxt)[32] = (q & 1) ? b0 : b1;
+        if (q < 3) tmem_ld_x32_nowait(tS + 32 * (q + 1), nxt);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
+            if (DIAG) {
+                if (32 * q + 2 * e > r) s0 = -CUDART_INF_F;
+                if (32 * q + 2 * e + 1 > r) s1 = -CUDART_INF_F;
+            }
+            m = fmax3(m, s0, s1);
+            float x0, x1;
+            ffma2(x0, x1, s0, s1, sc, sc, nm, nm);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const int a = 2 * (e & 3);
+            fadd2(ls[a], ls[a + 1], ls[a], ls[a + 1], p0, p1);
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_x16_nowait(tP + 16 * q, pk);
+        if (q < 3) tmem_wait_ld_dep(nxt);
+    }
+    tmem_wait_st();
+    mx = m;
+    return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, Cfg<D>::MIN_BLOCKS)
@@ -141,7 +213,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         mbar_init_fence();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -206,7 +278,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (lane == 0) {
             constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
             constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
-            const uint32_t tS = tmem + kSCol, tO = tmem + kOCol;
+            const uint32_t tS = tmem + kSCol, tO = tmem + kOCol, tP = tmem + C::P_COL;
             const uint32_t sq = smem_u32(sQ);
             bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
             for (int j = 0; ok && j < nkv; ++j) {
@@ -228,7 +300,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 for (int ks = 0; ks < BN / 16; ++ks) {
 #pragma unroll
                     for (int c = 0; c < C::KCH; ++c)
-                        umma_ts(tO + 64 * c, tS + ks * 8,
+                        umma_ts(tO + 64 * c, tP + ks * 8,
                                 umma_sdesc_sw128(sV + c * kChunkBytes + ks * 2048, 1024, 1024), idesc_pv,
                                 (j > 0 || ks > 0) ? 1u : 0u);
                 }
@@ -241,12 +313,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
+        // Thread r owns query row r.  O in TMEM holds sum_t P_t V_t with every P_t
+        // relative to one reference m_o (log2 units of the scaled score); l_run is
+        // relative to the same m_o.  P_j is formed against the current m_o in one
+        // pass that also finds the tile max; only the first tile (no reference yet)
+        // or a jump of more than 2^64 takes a separate max pass.  When a tile max
+        // exceeds m_o by more than 2^8 the reference moves up: l_run now, the O row
+        // (after the PV product that used the old reference) before the next
+        // product or at the epilogue.  Exact: o = O / l uses one reference.
         const int r = (warp & 3) * 32 + lane;  // query row in the tile == TMEM lane
         const uint32_t lane_base = tmem_lane_base(warp);
         const uint32_t tS = tmem + lane_base + kSCol;
         const uint32_t tO = tmem + lane_base + kOCol;
+        const uint32_t tP = tmem + lane_base + C::P_COL;
         const int row_in_seq = i * BM + r;
-        float m_run = -CUDART_INF_F, l_run = 0.f;
+        const float sc = p.scale_log2;
+        float m_o = -CUDART_INF_F, l_run = 0.f;
+        float o_pending = 1.f;  // factor O still owes for the move of m_o
         bool ok = true;
         // partial last page: its V rows past the end are zeroed before the PV product
         const int last_lp = pages_b - 1;
@@ -258,55 +341,48 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 break;
             }
             tc_fence_after_sync();
-            uint32_t sr[128];
-            tmem_ld_x128(tS, sr);
             const bool diag = (j == i);
-            float mx = -CUDART_INF_F;
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                float x = __uint_as_float(sr[c]) * p.scale_log2;
-                if (diag && c > r) x = -CUDART_INF_F;
-                sr[c] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
-            }
-            const float m_new = fmaxf(m_run, mx);
-            const bool need = m_new > m_run + 8.f;
-            const float m_use = need ? m_new : m_run;
-            const float corr = need ? ex2_approx(m_run - m_new) : 1.f;
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
-                // move O to the new reference max once the previous PV product is done
-                if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err))) {
-                    ok = false;
-                    break;
+            float mx, lsum;
+            if (j == 0) {
+                m_o = sc * (diag ? tile_row_max<true>(tS, r) : tile_row_max<false>(tS, r));
+                lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
+            } else {
+                lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
+                const float m_tile = mx * sc;
+                if (__any_sync(0xffffffffu, m_tile > m_o + 64.f)) {  // rare: redo against the new max
+                    const float m_new = fmaxf(m_o, m_tile);
+                    const float f = ex2_approx(m_o - m_new);
+                    l_run *= f;
+                    o_pending *= f;
+                    m_o = m_new;
+                    lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
                 }
-                tc_fence_after_sync();
+                if (__any_sync(0xffffffffu, o_pending != 1.f)) {
+                    // O must follow the reference before this tile's PV product
+                    if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
 #pragma unroll
-                for (int c = 0; c < C::KCH; ++c) {
-                    uint32_t ov[64];
-                    tmem_ld_x64(tO + 64 * c, ov);
+                    for (int c = 0; c < C::KCH; ++c) {
+                        uint32_t ov[64];
+                        tmem_ld_x64(tO + 64 * c, ov);
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
-                    tmem_st_x64(tO + 64 * c, ov);
+                        for (int e = 0; e < 64; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * o_pending);
+                        tmem_st_x64(tO + 64 * c, ov);
+                    }
+                    o_pending = 1.f;
                 }
             }
-            m_run = m_use;
-            float lsum = 0.f;
-            // P over the first 64 columns of S, 16 columns (32 keys) at a time: every
-            // score is already in registers, so the overwritten columns are free
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2_approx(__uint_as_float(sr[32 * q4 + 2 * e]) - m_use);
-                    const float p1 = ex2_approx(__uint_as_float(sr[32 * q4 + 2 * e + 1]) - m_use);
-                    lsum += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
-                }
-                tmem_st_x16_nowait(tS + 16 * q4, pk);
+            l_run += lsum;
+            const float m_tile = mx * sc;
+            if (m_tile > m_o + 8.f) {  // move the reference up; O follows after this PV
+                const float f = ex2_approx(m_o - m_tile);
+                l_run *= f;
+                o_pending = f;
+                m_o = m_tile;
             }
-            tmem_wait_st();
-            l_run = l_run * corr + lsum;
             if (diag && zero_tail) {
                 const int st = j % C::NST;
                 if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[st], (j / C::NST) & 1, abort_flag, p.err))) {
@@ -331,7 +407,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, (nkv - 1) & 1, abort_flag, p.err))) {
             tc_fence_after_sync();
             const bool store = row_in_seq < n;
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float inv = l_run > 0.f ? o_pending / l_run : 0.f;
             const long long orow = static_cast<long long>(cu0 + row_in_seq) * g.hq + hq;
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c) {
@@ -351,7 +427,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
             }
             if (store && p.lse)
-                p.lse[orow] = l_run > 0.f ? (m_run + lg2_approx(l_run)) * kLn2 : -CUDART_INF_F;
+                p.lse[orow] = l_run > 0.f ? (m_o + lg2_approx(l_run)) * kLn2 : -CUDART_INF_F;
         }
     }
 
@@ -359,7 +435,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 

@@ -307,3 +307,54 @@ def test_host_validation_errors():
         pa.pa_decode(g, qd, pool, bt, 0, ks, ks, 64, 0.1, qd, None, ws, err)  # workspace too small
     assert e.value.code == pa.PA_ERR_INVALID_ARG
     assert int(err.item()) == 0
+
+
+# -------------------------------------------- running-max paths of the softmax
+
+def _scale_keys(case, factor_of_pos):
+    """Multiplies each token's K row by factor_of_pos(pos) (then rounds to bf16)."""
+    out = []
+    for w in case.writes:
+        f = factor_of_pos(w.tok_pos.astype(np.float32))[:, None]
+        k = W.bf16_bits(W.bf16_to_f32(w.k) * f)
+        out.append(W.KVWrite(w.layer, w.tok_slot, w.tok_pos, k, w.v))
+    case.writes = out
+    return case
+
+
+@pytest.mark.parametrize("kind", ["prefill", "decode"])
+def test_growing_scores_move_the_reference_max(kind):
+    """Keys whose magnitude grows with position: the running max keeps rising,
+    so the reference max moves (and O is rescaled) many times per row."""
+    geom = W.Geometry(8, 2, 64, 1, 3, 64, 120)
+    lens = [700, 300, 129]
+    mk = W.make_prefill_case if kind == "prefill" else W.make_decode_case
+    case = mk("ramp", geom, lens, seed=91, pool_fill="nan")
+    _scale_keys(case, lambda pos: 0.25 + pos / 60.0)
+    pool, bt, werr = H.gpu_setup(case)
+    assert werr == 0
+    run = H.gpu_prefill if kind == "prefill" else H.gpu_decode
+    o, l, err = run(case, pool, bt)
+    assert err == 0
+    ref = H.oracle_prefill if kind == "prefill" else H.oracle_decode
+    ro, rl = ref(case, H.oracle_pool(case))
+    H.assert_close(o, l, ro, rl, H.max_abs_v(case), "ramp " + kind)
+
+
+@pytest.mark.parametrize("kind", ["prefill", "decode"])
+def test_large_score_jump(kind):
+    """Keys from position 300 on are 40x larger: the tile max jumps by far more
+    than 2^64 over the running max (the redo path of the prefill softmax)."""
+    geom = W.Geometry(8, 2, 64, 1, 2, 64, 80)
+    lens = [520, 310]
+    mk = W.make_prefill_case if kind == "prefill" else W.make_decode_case
+    case = mk("jump", geom, lens, seed=92, pool_fill="nan")
+    _scale_keys(case, lambda pos: np.where(pos >= 300, 40.0, 0.05).astype(np.float32))
+    pool, bt, werr = H.gpu_setup(case)
+    assert werr == 0
+    run = H.gpu_prefill if kind == "prefill" else H.gpu_decode
+    o, l, err = run(case, pool, bt)
+    assert err == 0
+    ref = H.oracle_prefill if kind == "prefill" else H.oracle_decode
+    ro, rl = ref(case, H.oracle_pool(case))
+    H.assert_close(o, l, ro, rl, H.max_abs_v(case), "jump " + kind)
