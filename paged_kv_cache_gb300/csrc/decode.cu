@@ -20,19 +20,23 @@
 //    form a monotone staircase in (b, c)), and a second kernel merges them.
 //    The split depends only on the lengths and G, never on page ids.
 //  * Memory pipeline.  Warp 0 is the producer: it walks the CTA's pages,
-//    prefetches 32 block-table entries per warp load, and streams each whole
-//    page (K half and V half, contiguous: 32 KiB for 8 x 64) into a shared-
-//    memory stage with one cp.async.bulk (two for a partial last page, which
-//    copies only its valid rows), plus the sequence's query row at the start
-//    of a unit.  Several stages stay in flight per SM, so HBM sees long
-//    sequential reads with enough bytes outstanding to cover its latency.
-//  * Compute.  One consumer warp per KV head (two when the GQA group is 8)
-//    packs the group's query heads: each lane owns 16 dims of one token row,
-//    so a warp covers 8 (d 64) or 4 (d 128) tokens per pass; dot products
-//    reduce over 4 or 8 lanes with xor-shuffles; each token subgroup keeps its
-//    own online-softmax state (m, l, acc) in registers and the subgroups merge
-//    once per unit.  The running max is only moved when a score exceeds it by
-//    more than 2^8 (exact: o and l share the same reference m).
+//    prefetches 32 block-table entries per warp load, and streams each page
+//    (32 KiB for 8 x 64, read front to back) into a shared-memory stage with
+//    one cp.async.bulk per K or V row, issued by the warp's 32 lanes at once
+//    (a partial last page copies only its valid rows), plus the sequence's
+//    query row at the start of a unit.  Several stages stay in flight per SM,
+//    so HBM sees long sequential reads with enough bytes outstanding.
+//  * Compute.  One consumer warp per KV head; the GQA group's query heads are
+//    the rows of a 16-row warp-level MMA (mma.sync m16n8k16, bf16 in, fp32
+//    accumulate; rows past the group are zero): per page S = Q K^T is 8 MMAs
+//    (d 64) with K fragments from ldmatrix, the online softmax runs on the
+//    accumulator fragments (one row per lane quad, a 2-step xor-shuffle max),
+//    and P goes straight from those fragments into the A operand of O += P V
+//    (V fragments from ldmatrix.trans).  Each K/V row sits at a pitch of
+//    2*KV_DIM + 16 bytes in shared memory (the producer lays every row down
+//    with its own bulk copy) so the 8 rows an ldmatrix touches hit 8 distinct
+//    bank groups.  The running max is only moved when a page's max exceeds it
+//    by more than 2^8 (exact: o and l share the same reference m).
 #include <math_constants.h>
 
 #include <mutex>
@@ -44,7 +48,8 @@ namespace {
 
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kMaxGrid = 1024;
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 112 * 1024;  // per CTA: two CTAs share an SM
+constexpr int kCtasPerSm = 2;
 constexpr int kMaxStages = 8;
 constexpr int kCtlBytes = 1024;  // barriers + control words before the stages
 
@@ -76,9 +81,9 @@ struct DecodeParams {
     int32_t* err;
     int attend_grid;      // CTAs of the attend kernel (G)
     int nst;              // pipeline stages
-    int stage_bytes;      // page + q row + header, 128-byte multiple
+    int stage_bytes;      // 32 padded rows + q row + header, 128-byte multiple
     int q_bytes;          // hq * d * 2
-    int wph;              // consumer warps per kv head
+    int row_pitch;        // 2 * kv_dim + 16: shared-memory pitch of a K or V row
 };
 
 __host__ __device__ inline long long align_up(long long x, long long a) { return (x + a - 1) / a * a; }
@@ -146,12 +151,9 @@ __device__ long long block_scan(long long v, long long* red, long long* total) {
     return v + before;
 }
 
-template <int D, int GW>
-__global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
+template <int D>
+__global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), D == 64 ? kCtasPerSm : 1)
 decode_attend_kernel(const DecodeParams p) {
-    constexpr int LPT = D / 16;        // lanes per token row (16 dims each)
-    constexpr int TPP = 32 / LPT;      // tokens per warp pass
-    constexpr int PASSES = kBlockTokens / TPP;
 
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -263,7 +265,7 @@ decode_attend_kernel(const DecodeParams p) {
             }
             if (lane == 0) {
                 uint8_t* stage = stages + static_cast<long long>(st) * p.stage_bytes;
-                StageHeader* hdr = reinterpret_cast<StageHeader*>(stage + g.page_bytes + p.q_bytes);
+                StageHeader* hdr = reinterpret_cast<StageHeader*>(stage + 32 * p.row_pitch + p.q_bytes);
                 if (lp == 0) {  // this CTA holds the sequence's first page: record its CTA span
                     int2 meta;
                     meta.x = static_cast<int>(c);
@@ -277,21 +279,18 @@ decode_attend_kernel(const DecodeParams p) {
                 hdr->slot_idx = static_cast<int>(b + c);
                 const uint32_t kv_bytes = bad ? 0u : static_cast<uint32_t>(2ll * ntok * row_bytes);
                 mbar_arrive_expect_tx(&full[st], kv_bytes + (first ? static_cast<uint32_t>(p.q_bytes) : 0u));
-                if (!bad) {
-                    const uint8_t* src = p.pool + static_cast<long long>(entry) * g.page_bytes;
-                    if (ntok == kBlockTokens) {
-                        bulk_g2s(stage, src, static_cast<uint32_t>(g.page_bytes), &full[st]);
-                    } else {
-                        const uint32_t part = static_cast<uint32_t>(ntok * row_bytes);
-                        bulk_g2s(stage, src, part, &full[st]);
-                        bulk_g2s(stage + half_page, src + half_page, part, &full[st]);
-                    }
-                }
                 if (first)
-                    bulk_g2s(stage + g.page_bytes, p.q + static_cast<long long>(b) * p.q_bytes,
+                    bulk_g2s(stage + 32 * p.row_pitch, p.q + static_cast<long long>(b) * p.q_bytes,
                              static_cast<uint32_t>(p.q_bytes), &full[st]);
             }
             __syncwarp();
+            // lanes 0-15 copy K rows, lanes 16-31 V rows, each to its padded slot
+            if (!bad && (lane & 15) < ntok) {
+                uint8_t* stage = stages + static_cast<long long>(st) * p.stage_bytes;
+                const uint8_t* src = p.pool + static_cast<long long>(entry) * g.page_bytes +
+                                     (lane >= 16 ? half_page : 0) + (lane & 15) * row_bytes;
+                bulk_g2s(stage + lane * p.row_pitch, src, static_cast<uint32_t>(row_bytes), &full[st]);
+            }
         }
         // Drain: the copies of the last stages must land before the CTA exits.
         if (stop && lane == 0) {
@@ -303,149 +302,126 @@ decode_attend_kernel(const DecodeParams p) {
     }
 
     // ---------------------------------------------------------- consumers
-    const int cw = warp - 1;
-    const int h = cw / p.wph;                 // kv head
-    const int slice = cw % p.wph;             // which GW query heads of the group
-    const int hq0 = h * g.group + slice * GW; // first query head of this warp
-    const int sub = lane / LPT;               // token subgroup
-    const int part = lane % LPT;              // 16-dim slice of the row
+    const int h = warp - 1;                   // kv head of this warp
+    const int gid = lane >> 2, tq = lane & 3; // MMA fragment row group / column pair
+    const bool row_real = gid < g.group;      // fragment row gid is a real query head
+    const int hq_row = h * g.group + gid;
+    const int rp = p.row_pitch;
+    const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix and row this lane addresses
+    // K: matrices (tokens 0-7 | 8-15) x (dims 0-7 | 8-15) of a 16-dim step
+    const uint32_t k_off = ((mi >> 1) * 8 + rr) * rp + (h * D + (mi & 1) * 8) * 2;
+    // V (transposed load): matrices (tokens 0-7 | 8-15) x (dims 0-7 | 8-15) of 16 dims
+    const uint32_t v_off = (16 + (mi & 1) * 8 + rr) * rp + (h * D + (mi >> 1) * 8) * 2;
+    const float sl2 = p.scale_log2;
 
-    float q[GW][16], acc[GW][16], m[GW], l[GW];
+    uint32_t qa[D / 16][2];  // A fragments of Q (rows gid; the rows gid+8 are zero)
+    float oacc[D / 8][4];    // O accumulator fragments, 8 dims per tile
+    float m_ref = -CUDART_INF_F, l_part = 0.f;
 #pragma unroll
-    for (int j = 0; j < GW; ++j) {
-        m[j] = -CUDART_INF_F;
-        l[j] = 0.f;
+    for (int ks = 0; ks < D / 16; ++ks) qa[ks][0] = qa[ks][1] = 0u;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc[j][e] = 0.f, q[j][e] = 0.f;
-    }
+    for (int nt = 0; nt < D / 8; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.f;
 
     for (long long k = 0; k < n_pages; ++k) {
         const int st = static_cast<int>(k % p.nst);
         if (!mbar_wait(&full[st], static_cast<uint32_t>((k / p.nst) & 1), abort_flag, p.err)) break;
-        const uint8_t* stage = stages + static_cast<long long>(st) * p.stage_bytes;
-        const StageHeader hdr = *reinterpret_cast<const StageHeader*>(stage + g.page_bytes + p.q_bytes);
+        uint8_t* stage = stages + static_cast<long long>(st) * p.stage_bytes;
+        const StageHeader hdr = *reinterpret_cast<const StageHeader*>(stage + 32 * rp + p.q_bytes);
+        const uint32_t sbase = smem_u32(stage);
 
         if (hdr.flags & kFirst) {
-            const uint8_t* qs = stage + g.page_bytes;
+            const uint8_t* qrow = stage + 32 * rp + hq_row * D * 2;
 #pragma unroll
-            for (int j = 0; j < GW; ++j) {
-                const uint4* src = reinterpret_cast<const uint4*>(qs + ((hq0 + j) * D + part * 16) * 2);
-                const uint4 a = src[0], bq = src[1];
-                const uint32_t w[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    q[j][2 * e] = bf16lo(w[e]);
-                    q[j][2 * e + 1] = bf16hi(w[e]);
-                }
-                m[j] = -CUDART_INF_F;
-                l[j] = 0.f;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) acc[j][e] = 0.f;
+            for (int ks = 0; ks < D / 16; ++ks) {
+                qa[ks][0] = row_real ? *reinterpret_cast<const uint32_t*>(qrow + (16 * ks + 2 * tq) * 2) : 0u;
+                qa[ks][1] = row_real ? *reinterpret_cast<const uint32_t*>(qrow + (16 * ks + 8 + 2 * tq) * 2) : 0u;
             }
+            m_ref = -CUDART_INF_F;
+            l_part = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.f;
         }
 
-        const uint8_t* kbase = stage + (h * D + part * 16) * 2;
-#pragma unroll
-        for (int pass = 0; pass < PASSES; ++pass) {
-            const int t = pass * TPP + sub;
-            const bool valid = t < hdr.ntok;
-            float dot[GW];
-            uint32_t vw[8];
-#pragma unroll
-            for (int j = 0; j < GW; ++j) dot[j] = 0.f;
-            if (valid) {
-                const uint4* kp = reinterpret_cast<const uint4*>(kbase + t * row_bytes);
-                const uint4* vp = reinterpret_cast<const uint4*>(kbase + half_page + t * row_bytes);
-                // neighbouring token rows sit 2*KV_DIM bytes apart (same banks): odd
-                // subgroups read their second 16-byte chunk first so a quarter-warp
-                // touches every bank once
-                const int f = sub & 1;
-                const uint4 ka = kp[f], kb = kp[f ^ 1], va = vp[f], vb = vp[f ^ 1];
-                const uint4 k0 = f ? kb : ka, k1 = f ? ka : kb, v0 = f ? vb : va, v1 = f ? va : vb;
-                const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-                vw[0] = v0.x; vw[1] = v0.y; vw[2] = v0.z; vw[3] = v0.w;
-                vw[4] = v1.x; vw[5] = v1.y; vw[6] = v1.z; vw[7] = v1.w;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x0 = bf16lo(kw[e]), x1 = bf16hi(kw[e]);
-#pragma unroll
-                    for (int j = 0; j < GW; ++j) dot[j] = fmaf(q[j][2 * e + 1], x1, fmaf(q[j][2 * e], x0, dot[j]));
+        if (!(hdr.flags & kSkip)) {
+            const int ntok = hdr.ntok;
+            if (ntok < kBlockTokens) {  // rows past the end: zero this head's V slice (0 x NaN guard)
+                for (int idx = lane; idx < (kBlockTokens - ntok) * (D / 8); idx += 32) {
+                    const int row = ntok + idx / (D / 8);
+                    *reinterpret_cast<uint4*>(stage + (16 + row) * rp + h * D * 2 + (idx % (D / 8)) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) vw[e] = 0u;
+                __syncwarp();
             }
+            // S = Q K^T: two 8-token tiles
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int off = 1; off < LPT; off <<= 1)
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t kb[4];
+                ldmatrix_x4(kb, sbase + k_off + ks * 32);
+                const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+                mma_bf16_16816(s0, a, kb[0], kb[1]);
+                mma_bf16_16816(s1, a, kb[2], kb[3]);
+            }
+            // this lane's scores: row gid, tokens 2tq, 2tq+1, 8+2tq, 9+2tq
+            float x0 = s0[0], x1 = s0[1], x2 = s1[0], x3 = s1[1];
+            if (ntok < kBlockTokens) {
+                if (2 * tq >= ntok) x0 = -CUDART_INF_F;
+                if (2 * tq + 1 >= ntok) x1 = -CUDART_INF_F;
+                if (8 + 2 * tq >= ntok) x2 = -CUDART_INF_F;
+                if (9 + 2 * tq >= ntok) x3 = -CUDART_INF_F;
+            }
+            float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_tile = mx * sl2;
+            if (m_tile > m_ref + 8.f) {  // move the reference max (same decision across the quad)
+                const float corr = ex2_approx(m_ref - m_tile);
+                l_part *= corr;
 #pragma unroll
-                for (int j = 0; j < GW; ++j) dot[j] += __shfl_xor_sync(0xffffffffu, dot[j], off);
-            if (valid) {
-#pragma unroll
-                for (int j = 0; j < GW; ++j) {
-                    const float s = dot[j] * p.scale_log2;
-                    if (s > m[j] + 8.f) {  // move the reference max (rare after the first token)
-                        const float corr = ex2_approx(m[j] - s);
-                        l[j] *= corr;
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) acc[j][e] *= corr;
-                        m[j] = s;
-                    }
-                    const float pw = ex2_approx(s - m[j]);
-                    l[j] += pw;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        acc[j][2 * e] = fmaf(pw, bf16lo(vw[e]), acc[j][2 * e]);
-                        acc[j][2 * e + 1] = fmaf(pw, bf16hi(vw[e]), acc[j][2 * e + 1]);
-                    }
+                for (int nt = 0; nt < D / 8; ++nt) {
+                    oacc[nt][0] *= corr;
+                    oacc[nt][1] *= corr;
                 }
+                m_ref = m_tile;
             }
+            float e0, e1, e2, e3;
+            ffma2(e0, e1, x0, x1, sl2, sl2, -m_ref, -m_ref);
+            ffma2(e2, e3, x2, x3, sl2, sl2, -m_ref, -m_ref);
+            const float p0 = ex2_approx(e0), p1 = ex2_approx(e1), p2 = ex2_approx(e2), p3 = ex2_approx(e3);
+            l_part += (p0 + p1) + (p2 + p3);
+            const uint32_t pa[4] = {pack_bf16x2(p0, p1), 0u, pack_bf16x2(p2, p3), 0u};
+            // O += P V
+#pragma unroll
+            for (int np = 0; np < D / 16; ++np) {
+                uint32_t vb[4];
+                ldmatrix_x4_trans(vb, sbase + v_off + np * 32);
+                mma_bf16_16816(oacc[2 * np], pa, vb[0], vb[1]);
+                mma_bf16_16816(oacc[2 * np + 1], pa, vb[2], vb[3]);
+            }
+            if (ntok < kBlockTokens) fence_proxy_async_smem();  // our zeros before the next bulk copy
         }
 
         if (hdr.flags & kLast) {
-            // merge the token subgroups (lanes LPT, 2 LPT, ... apart)
+            float l = l_part + __shfl_xor_sync(0xffffffffu, l_part, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            if (row_real) {
+                const bool any = l > 0.f;
+                const float inv = any ? 1.f / l : 0.f;
+                const float L = any ? (m_ref + lg2_approx(l)) * kLn2 : -CUDART_INF_F;
+                if (hdr.flags & kWhole) {
+                    __nv_bfloat16* dst = p.o + (static_cast<long long>(hdr.b) * g.hq + hq_row) * D + 2 * tq;
 #pragma unroll
-            for (int off = LPT; off < 32; off <<= 1) {
+                    for (int nt = 0; nt < D / 8; ++nt)
+                        *reinterpret_cast<uint32_t*>(dst + 8 * nt) = pack_bf16x2(oacc[nt][0] * inv, oacc[nt][1] * inv);
+                    if (tq == 0 && p.lse) p.lse[static_cast<long long>(hdr.b) * g.hq + hq_row] = L;
+                } else {
+                    float* dst = reinterpret_cast<float*>(p.ws + p.ws_o) +
+                                 (static_cast<long long>(hdr.slot_idx) * g.hq + hq_row) * D + 2 * tq;
 #pragma unroll
-                for (int j = 0; j < GW; ++j) {
-                    const float mo = __shfl_xor_sync(0xffffffffu, m[j], off);
-                    const float lo = __shfl_xor_sync(0xffffffffu, l[j], off);
-                    const float mn = fmaxf(m[j], mo);
-                    const float a = (m[j] == -CUDART_INF_F) ? 0.f : ex2_approx(m[j] - mn);
-                    const float bw = (mo == -CUDART_INF_F) ? 0.f : ex2_approx(mo - mn);
-                    l[j] = l[j] * a + lo * bw;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float ao = __shfl_xor_sync(0xffffffffu, acc[j][e], off);
-                        acc[j][e] = acc[j][e] * a + ao * bw;
-                    }
-                    m[j] = mn;
-                }
-            }
-            if (sub == 0) {
-#pragma unroll
-                for (int j = 0; j < GW; ++j) {
-                    const int hq = hq0 + j;
-                    const bool any = l[j] > 0.f;
-                    const float inv = any ? 1.f / l[j] : 0.f;
-                    const float L = any ? (m[j] + lg2_approx(l[j])) * kLn2 : -CUDART_INF_F;
-                    if (hdr.flags & kWhole) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(acc[j][2 * e] * inv, acc[j][2 * e + 1] * inv);
-                        uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<long long>(hdr.b) * g.hq + hq) * D + part * 16);
-                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                        if (part == 0 && p.lse) p.lse[static_cast<long long>(hdr.b) * g.hq + hq] = L;
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(
-                            p.ws + p.ws_o + ((static_cast<long long>(hdr.slot_idx) * g.hq + hq) * D + part * 16) * 4);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            dst[e] = make_float4(acc[j][4 * e] * inv, acc[j][4 * e + 1] * inv,
-                                                 acc[j][4 * e + 2] * inv, acc[j][4 * e + 3] * inv);
-                        if (part == 0)
-                            reinterpret_cast<float*>(p.ws + p.ws_lse)[static_cast<long long>(hdr.slot_idx) * g.hq + hq] = L;
-                    }
+                    for (int nt = 0; nt < D / 8; ++nt)
+                        *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(oacc[nt][0] * inv, oacc[nt][1] * inv);
+                    if (tq == 0)
+                        reinterpret_cast<float*>(p.ws + p.ws_lse)[static_cast<long long>(hdr.slot_idx) * g.hq + hq_row] = L;
                 }
             }
         }
@@ -515,19 +491,19 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
 }
 
 struct LaunchShape {
-    int gw, wph, nw, nst, stage_bytes, q_bytes, smem;
+    int nw, nst, stage_bytes, q_bytes, row_pitch, smem;
 };
 
 bool decode_shape(const KGeom& g, LaunchShape* s) {
     if (g.d != 64 && g.d != 128) return false;
     if (g.group != 1 && g.group != 2 && g.group != 4 && g.group != 8) return false;
-    s->gw = g.group < 4 ? g.group : 4;
-    s->wph = g.group / s->gw;
-    s->nw = g.hkv * s->wph;
+    s->nw = g.hkv;  // one consumer warp per kv head
     if (s->nw > kMaxConsumerWarps) return false;
     s->q_bytes = g.hq * g.d * 2;
-    const long long stage = align_up(g.page_bytes + s->q_bytes + static_cast<long long>(sizeof(StageHeader)), 128);
-    if (stage > 64 * 1024 + 16 * 1024) return false;
+    s->row_pitch = g.kv_dim * 2 + 16;
+    const long long stage =
+        align_up(32ll * s->row_pitch + s->q_bytes + static_cast<long long>(sizeof(StageHeader)), 128);
+    if (stage > 80 * 1024) return false;
     s->stage_bytes = static_cast<int>(stage);
     int nst = static_cast<int>((kSmemBudget - kCtlBytes) / stage);
     if (nst > kMaxStages) nst = kMaxStages;
@@ -537,9 +513,9 @@ bool decode_shape(const KGeom& g, LaunchShape* s) {
     return true;
 }
 
-template <int D, int GW>
+template <int D>
 cudaError_t launch_attend(const DecodeParams& p, const LaunchShape& s, int grid, cudaStream_t stream) {
-    auto kern = decode_attend_kernel<D, GW>;
+    auto kern = decode_attend_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, 32 * (1 + s.nw), s.smem, stream>>>(p);
@@ -570,7 +546,7 @@ cudaError_t launch_decode(const KGeom& g, const void* q, const void* pool, const
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     long long grid = grid_cap(batch, max_seq_len);
-    if (grid > sms) grid = sms;
+    if (grid > static_cast<long long>(kCtasPerSm) * sms) grid = static_cast<long long>(kCtasPerSm) * sms;
     const long long nslots = batch + grid_cap(batch, max_seq_len) - 1;
     const WsLayout w = ws_layout(batch, nslots, g.hq, g.d);
 
@@ -594,20 +570,16 @@ cudaError_t launch_decode(const KGeom& g, const void* q, const void* pool, const
     p.nst = s.nst;
     p.stage_bytes = s.stage_bytes;
     p.q_bytes = s.q_bytes;
-    p.wph = s.wph;
+    p.row_pitch = s.row_pitch;
 
     const int gi = static_cast<int>(grid);
     p.attend_grid = gi;
     if (g.d == 64) {
-        e = s.gw == 1 ? launch_attend<64, 1>(p, s, gi, stream)
-          : s.gw == 2 ? launch_attend<64, 2>(p, s, gi, stream)
-                      : launch_attend<64, 4>(p, s, gi, stream);
+        e = launch_attend<64>(p, s, gi, stream);
         if (e != cudaSuccess) return e;
         decode_merge_kernel<64><<<batch, 256, 0, stream>>>(p);
     } else {
-        e = s.gw == 1 ? launch_attend<128, 1>(p, s, gi, stream)
-          : s.gw == 2 ? launch_attend<128, 2>(p, s, gi, stream)
-                      : launch_attend<128, 4>(p, s, gi, stream);
+        e = launch_attend<128>(p, s, gi, stream);
         if (e != cudaSuccess) return e;
         decode_merge_kernel<128><<<batch, 256, 0, stream>>>(p);
     }
