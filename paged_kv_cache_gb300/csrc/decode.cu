@@ -20,23 +20,25 @@
 //    form a monotone staircase in (b, c)), and a second kernel merges them.
 //    The split depends only on the lengths and G, never on page ids.
 //  * Memory pipeline.  Warp 0 is the producer: it walks the CTA's pages,
-//    prefetches 32 block-table entries per warp load, and streams each page
-//    (32 KiB for 8 x 64, read front to back) into a shared-memory stage with
-//    one cp.async.bulk per K or V row, issued by the warp's 32 lanes at once
-//    (a partial last page copies only its valid rows), plus the sequence's
-//    query row at the start of a unit.  Several stages stay in flight per SM,
-//    so HBM sees long sequential reads with enough bytes outstanding.
+//    prefetches 32 block-table entries per warp load, and moves each page
+//    (32 KiB for 8 x 64) into a shared-memory stage with two TMA tensor copies,
+//    one for the K half and one for the V half.  The tensor map views the
+//    pool as [64 dims][rows of 2*KV_DIM bytes][KV_DIM/64 column blocks of 128
+//    bytes]: one {64, 16, KV_DIM/64} box is a whole half page, laid down as
+//    128-byte lines (column block major, token minor) with the 128-byte
+//    swizzle, so the 16-byte pieces of 8 consecutive token rows sit in 8
+//    different bank groups.  The sequence's query row rides along at the start
+//    of a unit.  Two CTAs per SM, three stages each, keep enough bytes in
+//    flight for HBM; the page is read front to back in two large requests.
 //  * Compute.  One consumer warp per KV head; the GQA group's query heads are
 //    the rows of a 16-row warp-level MMA (mma.sync m16n8k16, bf16 in, fp32
 //    accumulate; rows past the group are zero): per page S = Q K^T is 8 MMAs
 //    (d 64) with K fragments from ldmatrix, the online softmax runs on the
 //    accumulator fragments (one row per lane quad, a 2-step xor-shuffle max),
 //    and P goes straight from those fragments into the A operand of O += P V
-//    (V fragments from ldmatrix.trans).  Each K/V row sits at a pitch of
-//    2*KV_DIM + 16 bytes in shared memory (the producer lays every row down
-//    with its own bulk copy) so the 8 rows an ldmatrix touches hit 8 distinct
-//    bank groups.  The running max is only moved when a page's max exceeds it
-//    by more than 2^8 (exact: o and l share the same reference m).
+//    (V fragments from ldmatrix.trans, addresses following the swizzle).  The
+//    running max is only moved when a page's max exceeds it by more than 2^8
+//    (exact: o and l share the same reference m).
 #include <math_constants.h>
 
 #include <mutex>
@@ -51,7 +53,7 @@ constexpr int kMaxGrid = 1024;
 constexpr int kSmemBudget = 112 * 1024;  // per CTA: two CTAs share an SM
 constexpr int kCtasPerSm = 2;
 constexpr int kMaxStages = 8;
-constexpr int kCtlBytes = 1024;  // barriers + control words before the stages
+constexpr int kCtlBytes = 1024;  // barriers + control words, then the q slots, then the stages
 
 enum : int { kFirst = 1, kLast = 2, kWhole = 4, kSkip = 8 };
 
@@ -81,9 +83,10 @@ struct DecodeParams {
     int32_t* err;
     int attend_grid;      // CTAs of the attend kernel (G)
     int nst;              // pipeline stages
-    int stage_bytes;      // 32 padded rows + q row + header, 128-byte multiple
+    int kv_stage_bytes;   // 64 * kv_dim: a whole page, K half then V half
     int q_bytes;          // hq * d * 2
-    int row_pitch;        // 2 * kv_dim + 16: shared-memory pitch of a K or V row
+    int qslot_bytes;      // q row + stage header, 64-byte multiple
+    int stages_off;       // offset of the (1024-aligned) page stages in shared memory
 };
 
 __host__ __device__ inline long long align_up(long long x, long long a) { return (x + a - 1) / a * a; }
@@ -153,15 +156,17 @@ __device__ long long block_scan(long long v, long long* red, long long* total) {
 
 template <int D>
 __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), D == 64 ? kCtasPerSm : 1)
-decode_attend_kernel(const DecodeParams p) {
-
-    extern __shared__ __align__(1024) uint8_t smem[];
+decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // swizzled stages want 1024 B
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kMaxStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 256);
     long long* ctl = reinterpret_cast<long long*>(smem + 512);  // scan scratch and results
     long long* red = ctl + 8;                                   // per-warp partials
-    uint8_t* stages = smem + kCtlBytes;
+    uint8_t* qslots = smem + kCtlBytes;                         // per stage: q row, header
+    uint8_t* stages = smem + p.stages_off;
 
     const KGeom& g = p.g;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -264,8 +269,9 @@ decode_attend_kernel(const DecodeParams p) {
                 break;
             }
             if (lane == 0) {
-                uint8_t* stage = stages + static_cast<long long>(st) * p.stage_bytes;
-                StageHeader* hdr = reinterpret_cast<StageHeader*>(stage + 32 * p.row_pitch + p.q_bytes);
+                uint8_t* stage = stages + static_cast<long long>(st) * p.kv_stage_bytes;
+                uint8_t* qslot = qslots + st * p.qslot_bytes;
+                StageHeader* hdr = reinterpret_cast<StageHeader*>(qslot + p.q_bytes);
                 if (lp == 0) {  // this CTA holds the sequence's first page: record its CTA span
                     int2 meta;
                     meta.x = static_cast<int>(c);
@@ -277,20 +283,17 @@ decode_attend_kernel(const DecodeParams p) {
                 hdr->ntok = bad ? 0 : ntok;
                 hdr->flags = (first ? kFirst : 0) | (last ? kLast : 0) | (whole ? kWhole : 0) | (bad ? kSkip : 0);
                 hdr->slot_idx = static_cast<int>(b + c);
-                const uint32_t kv_bytes = bad ? 0u : static_cast<uint32_t>(2ll * ntok * row_bytes);
+                const uint32_t kv_bytes = bad ? 0u : static_cast<uint32_t>(p.kv_stage_bytes);
                 mbar_arrive_expect_tx(&full[st], kv_bytes + (first ? static_cast<uint32_t>(p.q_bytes) : 0u));
+                if (!bad) {  // whole K half and whole V half (a partial page's tail is not used)
+                    tma_load_3d(stage, &kvmap, 0, entry * 32, 0, &full[st]);
+                    tma_load_3d(stage + p.kv_stage_bytes / 2, &kvmap, 0, entry * 32 + 16, 0, &full[st]);
+                }
                 if (first)
-                    bulk_g2s(stage + 32 * p.row_pitch, p.q + static_cast<long long>(b) * p.q_bytes,
-                             static_cast<uint32_t>(p.q_bytes), &full[st]);
+                    bulk_g2s(qslot, p.q + static_cast<long long>(b) * p.q_bytes, static_cast<uint32_t>(p.q_bytes),
+                             &full[st]);
             }
             __syncwarp();
-            // lanes 0-15 copy K rows, lanes 16-31 V rows, each to its padded slot
-            if (!bad && (lane & 15) < ntok) {
-                uint8_t* stage = stages + static_cast<long long>(st) * p.stage_bytes;
-                const uint8_t* src = p.pool + static_cast<long long>(entry) * g.page_bytes +
-                                     (lane >= 16 ? half_page : 0) + (lane & 15) * row_bytes;
-                bulk_g2s(stage + lane * p.row_pitch, src, static_cast<uint32_t>(row_bytes), &full[st]);
-            }
         }
         // Drain: the copies of the last stages must land before the CTA exits.
         if (stop && lane == 0) {
@@ -306,12 +309,14 @@ decode_attend_kernel(const DecodeParams p) {
     const int gid = lane >> 2, tq = lane & 3; // MMA fragment row group / column pair
     const bool row_real = gid < g.group;      // fragment row gid is a real query head
     const int hq_row = h * g.group + gid;
-    const int rp = p.row_pitch;
     const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix and row this lane addresses
-    // K: matrices (tokens 0-7 | 8-15) x (dims 0-7 | 8-15) of a 16-dim step
-    const uint32_t k_off = ((mi >> 1) * 8 + rr) * rp + (h * D + (mi & 1) * 8) * 2;
-    // V (transposed load): matrices (tokens 0-7 | 8-15) x (dims 0-7 | 8-15) of 16 dims
-    const uint32_t v_off = (16 + (mi & 1) * 8 + rr) * rp + (h * D + (mi >> 1) * 8) * 2;
+    // Address of 16-byte piece (token t, dims d0..d0+7 of this warp's head) in a
+    // half page: line = 16 * (column block) + t, piece swizzled by t % 8.
+    auto piece = [&](int t, int d0) -> uint32_t {
+        const int col = h * D + d0;
+        return static_cast<uint32_t>((((col >> 6) * 16 + t) << 7) + ((((col & 63) >> 3) ^ (t & 7)) << 4));
+    };
+    const int half = p.kv_stage_bytes / 2;
     const float sl2 = p.scale_log2;
 
     uint32_t qa[D / 16][2];  // A fragments of Q (rows gid; the rows gid+8 are zero)
@@ -325,12 +330,13 @@ decode_attend_kernel(const DecodeParams p) {
     for (long long k = 0; k < n_pages; ++k) {
         const int st = static_cast<int>(k % p.nst);
         if (!mbar_wait(&full[st], static_cast<uint32_t>((k / p.nst) & 1), abort_flag, p.err)) break;
-        uint8_t* stage = stages + static_cast<long long>(st) * p.stage_bytes;
-        const StageHeader hdr = *reinterpret_cast<const StageHeader*>(stage + 32 * rp + p.q_bytes);
-        const uint32_t sbase = smem_u32(stage);
+        uint8_t* stage = stages + static_cast<long long>(st) * p.kv_stage_bytes;
+        const uint8_t* qslot = qslots + st * p.qslot_bytes;
+        const StageHeader hdr = *reinterpret_cast<const StageHeader*>(qslot + p.q_bytes);
+        const uint32_t kbase = smem_u32(stage), vbase = kbase + half;
 
         if (hdr.flags & kFirst) {
-            const uint8_t* qrow = stage + 32 * rp + hq_row * D * 2;
+            const uint8_t* qrow = qslot + hq_row * D * 2;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 qa[ks][0] = row_real ? *reinterpret_cast<const uint32_t*>(qrow + (16 * ks + 2 * tq) * 2) : 0u;
@@ -344,20 +350,22 @@ decode_attend_kernel(const DecodeParams p) {
 
         if (!(hdr.flags & kSkip)) {
             const int ntok = hdr.ntok;
-            if (ntok < kBlockTokens) {  // rows past the end: zero this head's V slice (0 x NaN guard)
-                for (int idx = lane; idx < (kBlockTokens - ntok) * (D / 8); idx += 32) {
-                    const int row = ntok + idx / (D / 8);
-                    *reinterpret_cast<uint4*>(stage + (16 + row) * rp + h * D * 2 + (idx % (D / 8)) * 16) =
+            if (ntok < kBlockTokens) {  // rows past the end: zero this head's V lines (0 x NaN guard)
+                constexpr int LINES = D / 64;  // 128-byte lines per token row of one head
+                for (int idx = lane; idx < (kBlockTokens - ntok) * LINES * 8; idx += 32) {
+                    const int t = ntok + idx / (LINES * 8);
+                    const int blk = (idx / 8) % LINES;
+                    *reinterpret_cast<uint4*>(stage + half + (((h * LINES + blk) * 16 + t) << 7) + ((idx & 7) << 4)) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 __syncwarp();
             }
-            // S = Q K^T: two 8-token tiles
+            // S = Q K^T: two 8-token tiles; matrices (tokens 0-7 | 8-15) x (dims +0 | +8)
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 uint32_t kb[4];
-                ldmatrix_x4(kb, sbase + k_off + ks * 32);
+                ldmatrix_x4(kb, kbase + piece((mi >> 1) * 8 + rr, 16 * ks + (mi & 1) * 8));
                 const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
                 mma_bf16_16816(s0, a, kb[0], kb[1]);
                 mma_bf16_16816(s1, a, kb[2], kb[3]);
@@ -392,13 +400,13 @@ decode_attend_kernel(const DecodeParams p) {
             const uint32_t pa[4] = {pack_bf16x2(p0, p1), 0u, pack_bf16x2(p2, p3), 0u};
             // O += P V
 #pragma unroll
-            for (int np = 0; np < D / 16; ++np) {
+            for (int np = 0; np < D / 16; ++np) {  // matrices (tokens 0-7 | 8-15) x (dims +0 | +8)
                 uint32_t vb[4];
-                ldmatrix_x4_trans(vb, sbase + v_off + np * 32);
+                ldmatrix_x4_trans(vb, vbase + piece((mi & 1) * 8 + rr, 16 * np + (mi >> 1) * 8));
                 mma_bf16_16816(oacc[2 * np], pa, vb[0], vb[1]);
                 mma_bf16_16816(oacc[2 * np + 1], pa, vb[2], vb[3]);
             }
-            if (ntok < kBlockTokens) fence_proxy_async_smem();  // our zeros before the next bulk copy
+            if (ntok < kBlockTokens) fence_proxy_async_smem();  // our zeros before the next TMA copy
         }
 
         if (hdr.flags & kLast) {
@@ -491,7 +499,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
 }
 
 struct LaunchShape {
-    int nw, nst, stage_bytes, q_bytes, row_pitch, smem;
+    int nw, nst, kv_stage_bytes, q_bytes, qslot_bytes, stages_off, smem;
 };
 
 bool decode_shape(const KGeom& g, LaunchShape* s) {
@@ -499,26 +507,63 @@ bool decode_shape(const KGeom& g, LaunchShape* s) {
     if (g.group != 1 && g.group != 2 && g.group != 4 && g.group != 8) return false;
     s->nw = g.hkv;  // one consumer warp per kv head
     if (s->nw > kMaxConsumerWarps) return false;
+    if (g.kv_dim / 64 > 256) return false;  // TMA box dimension
     s->q_bytes = g.hq * g.d * 2;
-    s->row_pitch = g.kv_dim * 2 + 16;
-    const long long stage =
-        align_up(32ll * s->row_pitch + s->q_bytes + static_cast<long long>(sizeof(StageHeader)), 128);
-    if (stage > 80 * 1024) return false;
-    s->stage_bytes = static_cast<int>(stage);
-    int nst = static_cast<int>((kSmemBudget - kCtlBytes) / stage);
-    if (nst > kMaxStages) nst = kMaxStages;
+    s->qslot_bytes = static_cast<int>(align_up(s->q_bytes + static_cast<long long>(sizeof(StageHeader)), 64));
+    s->kv_stage_bytes = static_cast<int>(g.page_bytes);
+    if (s->kv_stage_bytes > 64 * 1024) return false;
+    // 1024 B of slack to align the dynamic base, control words, q slots, stages
+    int nst = kMaxStages;
+    for (; nst >= 2; --nst) {
+        const long long off = align_up(kCtlBytes + static_cast<long long>(nst) * s->qslot_bytes, 1024);
+        if (1024 + off + static_cast<long long>(nst) * s->kv_stage_bytes <= kSmemBudget) break;
+    }
     if (nst < 2) return false;
     s->nst = nst;
-    s->smem = kCtlBytes + nst * s->stage_bytes;
+    s->stages_off = static_cast<int>(align_up(kCtlBytes + static_cast<long long>(nst) * s->qslot_bytes, 1024));
+    s->smem = 1024 + s->stages_off + nst * s->kv_stage_bytes;
     return true;
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// The pool as a 3D tensor {64 dims, pages*32 rows of 2*KV_DIM bytes,
+// KV_DIM/64 column blocks of 128 bytes}; one box {64, 16, KV_DIM/64} is a
+// half page (16 token rows, all heads).
+bool encode_pool_map(CUtensorMap* map, const KGeom& g, const void* pool) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(g.nblocks) * 32, static_cast<cuuint64_t>(g.kv_dim / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.kv_dim) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockTokens), static_cast<cuuint32_t>(g.kv_dim / 64)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
-cudaError_t launch_attend(const DecodeParams& p, const LaunchShape& s, int grid, cudaStream_t stream) {
+cudaError_t launch_attend(const CUtensorMap& map, const DecodeParams& p, const LaunchShape& s, int grid,
+                          cudaStream_t stream) {
     auto kern = decode_attend_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 32 * (1 + s.nw), s.smem, stream>>>(p);
+    kern<<<grid, 32 * (1 + s.nw), s.smem, stream>>>(map, p);
     return cudaGetLastError();
 }
 
@@ -568,18 +613,21 @@ cudaError_t launch_decode(const KGeom& g, const void* q, const void* pool, const
     p.ws_o = w.o;
     p.err = err;
     p.nst = s.nst;
-    p.stage_bytes = s.stage_bytes;
+    p.kv_stage_bytes = s.kv_stage_bytes;
     p.q_bytes = s.q_bytes;
-    p.row_pitch = s.row_pitch;
+    p.qslot_bytes = s.qslot_bytes;
+    p.stages_off = s.stages_off;
+    CUtensorMap map;
+    if (!encode_pool_map(&map, g, pool)) return cudaErrorInvalidValue;
 
     const int gi = static_cast<int>(grid);
     p.attend_grid = gi;
     if (g.d == 64) {
-        e = launch_attend<64>(p, s, gi, stream);
+        e = launch_attend<64>(map, p, s, gi, stream);
         if (e != cudaSuccess) return e;
         decode_merge_kernel<64><<<batch, 256, 0, stream>>>(p);
     } else {
-        e = launch_attend<128>(p, s, gi, stream);
+        e = launch_attend<128>(map, p, s, gi, stream);
         if (e != cudaSuccess) return e;
         decode_merge_kernel<128><<<batch, 256, 0, stream>>>(p);
     }
