@@ -439,63 +439,115 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
 }
 
 // Merges the partial units of every split sequence; writes o = 0, lse = -inf
-// for empty sequences.  One CTA per sequence, one thread per (head, 8 dims).
+// for empty sequences.  One CTA per (sequence, q head), 4 warps: the partials
+// of a sequence are spread over the warps (lanes over dims, loads of several
+// partials in flight), then the warps combine through shared memory.
+// Launched as a programmatic dependent of the attend kernel: everything the
+// attend kernel writes is read only after griddepcontrol.wait.
+constexpr int kMergeThreads = 128;
+
 template <int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
+    constexpr int PER = D / 32;  // dims per lane
+    __shared__ float red_m[kMergeThreads / 32];
+    __shared__ float red_s[kMergeThreads / 32];
+    __shared__ float red_o[kMergeThreads / 32][D];
     const KGeom& g = p.g;
-    const int b = blockIdx.x;
+    const int b = blockIdx.x, hq = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int len = p.seq_lens[b];
-    const int chunks = g.hq * (D / 8);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (len <= 0) {
-        for (int w = threadIdx.x; w < chunks; w += blockDim.x) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + static_cast<long long>(b) * g.hq * D) + w;
-            *dst = make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (p.lse)
-            for (int h = threadIdx.x; h < g.hq; h += blockDim.x) p.lse[static_cast<long long>(b) * g.hq + h] = -CUDART_INF_F;
+        if (tid < D) p.o[(static_cast<long long>(b) * g.hq + hq) * D + tid] = __float2bfloat16_rn(0.f);
+        if (tid == 0 && p.lse) p.lse[static_cast<long long>(b) * g.hq + hq] = -CUDART_INF_F;
         return;
     }
     const int2 meta = *reinterpret_cast<const int2*>(p.ws + p.ws_meta + 8ll * b);
     const long long G = p.attend_grid;
     if (meta.x < 0 || meta.y >= G || meta.x > meta.y) {  // attend kernel gave up early
-        if (threadIdx.x == 0) set_error(p.err, PA_ERR_TIMEOUT);
+        if (tid == 0) set_error(p.err, PA_ERR_TIMEOUT);
         return;
     }
     if (meta.x == meta.y) return;  // one unit: the attend kernel wrote the result
     const long long T = *reinterpret_cast<const long long*>(p.ws);
     const float* lse_part = reinterpret_cast<const float*>(p.ws + p.ws_lse);
     const float* o_part = reinterpret_cast<const float*>(p.ws + p.ws_o);
-    for (int w = threadIdx.x; w < chunks; w += blockDim.x) {
-        const int hq = w / (D / 8);
-        const int e0 = (w % (D / 8)) * 8;
-        float M = -CUDART_INF_F, S = 0.f, acc[8];
+    // CTAs of the attend grid whose page range is empty wrote nothing
+    auto has_pages = [&](long long cc) { return range_start(cc, T, G) != range_start(cc + 1, T, G); };
+
+    // 1. max of the partial L
+    float M = -CUDART_INF_F;
+    for (long long cc = meta.x + tid; cc <= meta.y; cc += kMergeThreads)
+        if (has_pages(cc)) M = fmaxf(M, lse_part[(b + cc) * g.hq + hq]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (long long cc = meta.x; cc <= meta.y; ++cc) {
-            if (range_start(cc, T, G) == range_start(cc + 1, T, G)) continue;  // CTA without pages
-            const long long slot = b + cc;
-            const float Lc = lse_part[slot * g.hq + hq];
-            if (Lc == -CUDART_INF_F) continue;
-            const float4* src = reinterpret_cast<const float4*>(o_part + (slot * g.hq + hq) * D + e0);
-            const float4 x0 = src[0], x1 = src[1];
-            const float Mn = fmaxf(M, Lc);
-            const float a = (M == -CUDART_INF_F) ? 0.f : ex2_approx((M - Mn) * kLog2e);
-            const float wgt = ex2_approx((Lc - Mn) * kLog2e);
-            S = S * a + wgt;
-            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0) red_m[warp] = M;
+    __syncthreads();
+    M = red_m[0];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = acc[e] * a + xv[e] * wgt;
-            M = Mn;
+    for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red_m[w]);
+
+    // 2. weighted sums, partials spread over the warps
+    float acc[PER], S = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    if (M != -CUDART_INF_F) {
+#pragma unroll 4
+        for (long long cc = meta.x + warp; cc <= meta.y; cc += kMergeThreads / 32) {
+            if (!has_pages(cc)) continue;
+            const long long slot = (b + cc) * g.hq + hq;
+            const float Lc = lse_part[slot];
+            float x[PER];
+            if (PER == 2) {
+                const float2 v = *reinterpret_cast<const float2*>(o_part + slot * D + lane * PER);
+                x[0] = v.x;
+                x[PER - 1] = v.y;
+            } else {
+                const float4 v = *reinterpret_cast<const float4*>(o_part + slot * D + lane * PER);
+                x[0] = v.x;
+                x[1 % PER] = v.y;
+                x[2 % PER] = v.z;
+                x[3 % PER] = v.w;
+            }
+            const float w = (Lc == -CUDART_INF_F) ? 0.f : ex2_approx((Lc - M) * kLog2e);
+            S += w;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, x[e], acc[e]);
         }
-        const float inv = S > 0.f ? 1.f / S : 0.f;
-        uint32_t packed[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) packed[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-        *reinterpret_cast<uint4*>(p.o + (static_cast<long long>(b) * g.hq + hq) * D + e0) =
-            make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        if (e0 == 0 && p.lse)
-            p.lse[static_cast<long long>(b) * g.hq + hq] = S > 0.f ? M + lg2_approx(S) * kLn2 : -CUDART_INF_F;
     }
+    if (lane == 0) red_s[warp] = S;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) red_o[warp][lane * PER + e] = acc[e];
+    __syncthreads();
+
+    // 3. combine the warps and write the row
+    float St = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) St += red_s[w];
+    const float inv = St > 0.f ? 1.f / St : 0.f;
+    if (tid < D) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeThreads / 32; ++w) v += red_o[w][tid];
+        p.o[(static_cast<long long>(b) * g.hq + hq) * D + tid] = __float2bfloat16_rn(v * inv);
+    }
+    if (tid == 0 && p.lse)
+        p.lse[static_cast<long long>(b) * g.hq + hq] = St > 0.f ? M + lg2_approx(St) * kLn2 : -CUDART_INF_F;
+}
+
+template <int D>
+cudaError_t launch_merge(const DecodeParams& p, int batch, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(batch), static_cast<unsigned>(p.g.hq), 1);
+    cfg.blockDim = dim3(kMergeThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
 }
 
 struct LaunchShape {
@@ -625,11 +677,13 @@ cudaError_t launch_decode(const KGeom& g, const void* q, const void* pool, const
     if (g.d == 64) {
         e = launch_attend<64>(map, p, s, gi, stream);
         if (e != cudaSuccess) return e;
-        decode_merge_kernel<64><<<batch, 256, 0, stream>>>(p);
+        e = launch_merge<64>(p, batch, stream);
+        if (e != cudaSuccess) return e;
     } else {
         e = launch_attend<128>(map, p, s, gi, stream);
         if (e != cudaSuccess) return e;
-        decode_merge_kernel<128><<<batch, 256, 0, stream>>>(p);
+        e = launch_merge<128>(p, batch, stream);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

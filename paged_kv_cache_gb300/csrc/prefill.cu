@@ -13,58 +13,62 @@
 //
 // GB300 mapping (prior art on the pages: cuBLAS per head + separate mask and
 // softmax kernels; FA2's warp split on A100):
-//  * One CTA per (128-row query tile, sequence, q head); tiles are launched
-//    heaviest first (last row tiles own the most key tiles), heads of one GQA
-//    group next to each other so their K/V tiles are shared through L2.
-//  * Warp 0 (TMA producer): the Q tile with one 2D tensor copy per 64-dim
+//  * One CTA per SM-sized work item: a 128-row query tile of a sequence for two
+//    q heads of the same GQA group (tiles A and B; one head when the group size
+//    is odd).  Both tiles read the same K/V tiles, staged once.  Items are
+//    launched heaviest first (the last row tiles own the most key tiles).
+//  * Warp 0 (TMA producer): the two Q tiles with one 2D tensor copy per 64-dim
 //    chunk; each 128-key K/V tile as 8 pages, each page one {64 x 16} box per
 //    chunk for K and one for V, rows addressed through the block table -- the
 //    pool is one 2D tensor [pages * 32 rows][KV_DIM], page p's K rows at 32p,
 //    V rows at 32p + 16.  128-byte swizzled boxes stack into the canonical
 //    K-major (Q, K) / MN-major (V) operand layouts of the tensor core.  Pages
 //    past the sequence end are read at an out-of-range row, which the copy
-//    engine fills with zeros.  Two K/V stages.
+//    engine fills with zeros.  Three K/V stages at d 64, two at d 128.
 //  * Warp 1 (single-thread MMA issuer): S = Q K^T (M 128, N 128, K 16 steps)
-//    into 128 TMEM columns, commit; after the softmax hands back P, O += P V
-//    with P read straight from TMEM (M 128, N 64 per 64-dim chunk, K 16).
-//  * Warps 2-5 (softmax): thread r owns query row r, i.e. TMEM lane r: it
-//    loads its 128 scores, takes the row max, forms P = 2^(s*scale*log2e - m)
-//    in fp32, packs it to bf16 over the first 64 columns of S, and keeps l in
-//    a register.  The reference max only moves when a row max exceeds it by
-//    more than 2^8; then the thread rescales its O row in TMEM (exact, since
-//    the final division uses the same m).  The epilogue divides by l, writes
-//    o (bf16) and L = ln2 (m + log2 l).
+//    into TMEM; after a softmax warpgroup hands back P, O += P V with P read
+//    straight from TMEM (M 128, N 64 per 64-dim chunk, K 16).  Issue order
+//    PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1): while one tile's softmax runs, the
+//    tensor core works on the other tile.
+//  * Warps 4-7 and 8-11 (softmax, one warpgroup per tile): thread r owns query
+//    row r, i.e. TMEM lane r; scores stream out of TMEM 32 columns at a time;
+//    P = 2^(s*scale*log2e - m) is formed with packed fp32 FMAs and the SFU
+//    exp2, packed to bf16 into TMEM; l stays in a register.  The reference max
+//    only moves when a row max exceeds it by more than 2^8; then the thread
+//    rescales its O row in TMEM (exact, since the final division uses the same
+//    m).  The epilogue divides by l, writes o (bf16) and L = ln2 (m + log2 l).
+//  * TMEM (512 columns): S_A, S_B, O_A, O_B, and P_A, P_B in their own columns
+//    at d 64; at d 128 P overwrites the S it came from.
 //  * A partial last page has its V rows past the sequence end zeroed in shared
 //    memory before the PV product (masked P is exactly 0, but 0 x NaN is not).
 #include <math_constants.h>
-
-#include <cstdio>
 
 #include "pa_internal.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int BM = 128;               // query rows per CTA (TMEM lanes)
+constexpr int BM = 128;               // query rows per tile (TMEM lanes)
 constexpr int BN = 128;               // keys per K/V tile
 constexpr int kPagesPerTile = BN / kBlockTokens;
-constexpr int kThreads = 192;         // producer, MMA, 4 softmax warps
-constexpr int kSCol = 0;              // S (fp32, 128 columns)
-constexpr int kOCol = 128;            // O (fp32, d columns); P (bf16 pairs, 64 columns) after it
+constexpr int kThreads = 384;         // TMA warp, MMA warp, 2 idle, 2 softmax warpgroups
 constexpr int kChunkBytes = 128 * 128;  // 128 rows x 128 bytes: one 64-dim chunk of a tile
+constexpr int kTmemCols = 512;
 
 template <int D>
 struct Cfg {
     static constexpr int KCH = D / 64;
-    static constexpr int Q_BYTES = KCH * kChunkBytes;
+    static constexpr int Q_BYTES = KCH * kChunkBytes;  // one query tile
     static constexpr int K_BYTES = KCH * kChunkBytes;
     static constexpr int STAGE_BYTES = 2 * K_BYTES;
-    static constexpr int NST = 2;
-    static constexpr int CTL_BYTES = 1024;
-    static constexpr int SMEM = 1024 + Q_BYTES + NST * STAGE_BYTES + CTL_BYTES;
-    static constexpr int MIN_BLOCKS = D == 64 ? 2 : 1;
-    static constexpr int P_COL = kOCol + D;            // 192 or 256
-    static constexpr int TMEM_COLS = D == 64 ? 256 : 512;  // power of two >= P_COL + 64
+    static constexpr int NST = D == 64 ? 3 : 2;
+    static constexpr int SMEM = 1024 + 2 * Q_BYTES + NST * STAGE_BYTES + 1024;
+    // tensor memory: S_A S_B (128 columns each), O_A O_B (d each), P_A P_B (64
+    // each) -- at d 128 there is no room left, so P overwrites the S it came from
+    static constexpr bool P_ALIAS = D == 128;
+    static __device__ __forceinline__ uint32_t s_col(int t) { return 128u * t; }
+    static __device__ __forceinline__ uint32_t o_col(int t) { return 256u + D * t; }
+    static __device__ __forceinline__ uint32_t p_col(int t) { return P_ALIAS ? 128u * t : 384u + 64u * t; }
 };
 
 struct PrefillParams {
@@ -77,6 +81,7 @@ struct PrefillParams {
     int max_seqlen;
     int total_tokens;
     int n_row_tiles;
+    int pair;             // 1: a CTA takes two q heads of one GQA group
     float scale_log2;
     __nv_bfloat16* o;
     float* lse;
@@ -154,42 +159,175 @@ __device__ __forceinline__ float tile_row_p(uint32_t tS, uint32_t tP, int r, flo
     return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
 }
 
+// Softmax role of one query tile: the warpgroup's thread r owns query row r
+// (TMEM lane r).  O in TMEM holds sum_t P_t V_t with every P_t relative to one
+// reference m_o (log2 units of the scaled score); l_run is relative to the same
+// m_o.  With a separate P region (d 64) P_j is formed against the current m_o in
+// one pass that also finds the tile max; only the first tile or a jump of more
+// than 2^64 takes a separate max pass.  With P over S (d 128) the max pass
+// always comes first.  When a tile max exceeds m_o by more than 2^8 the
+// reference moves up: l_run at once, the O row before the next PV product
+// (or in the epilogue).  Exact: o = O / l uses a single reference.
 template <int D>
-__global__ void __launch_bounds__(kThreads, Cfg<D>::MIN_BLOCKS)
+__device__ __forceinline__ void softmax_role(uint32_t tS, uint32_t tO, uint32_t tP, int r, int i, int nkv, int n,
+                                             int cu0, int hq, bool zero_tail_owner, uint8_t* sKV, uint64_t* s_full,
+                                             uint64_t* p_full, uint64_t* o_done, uint64_t* kv_full,
+                                             volatile int* abort_flag, const PrefillParams& p) {
+    using C = Cfg<D>;
+    const KGeom& g = p.g;
+    const float sc = p.scale_log2;
+    const int row_in_seq = i * BM + r;
+    float m_o = -CUDART_INF_F, l_run = 0.f;
+    float o_pending = 1.f;  // factor O still owes for a move of m_o
+    bool ok = true;
+    const int last_lp = (n + kBlockTokens - 1) / kBlockTokens - 1;
+    const int tail_valid = n - last_lp * kBlockTokens;
+    const bool zero_tail = zero_tail_owner && (i == (n - 1) / BM) && tail_valid < kBlockTokens;
+    for (int j = 0; j < nkv; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, p.err))) {
+            ok = false;
+            break;
+        }
+        tc_fence_after_sync();
+        const bool diag = (j == i);
+        float mx, lsum;
+        if (C::P_ALIAS || j == 0) {
+            const float m_tile = sc * (diag ? tile_row_max<true>(tS, r) : tile_row_max<false>(tS, r));
+            if (j == 0) {
+                m_o = m_tile;
+            } else if (m_tile > m_o + 8.f) {  // move the reference before this product
+                const float f = ex2_approx(m_o - m_tile);
+                l_run *= f;
+                o_pending *= f;
+                m_o = m_tile;
+            }
+            lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
+        } else {
+            lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
+            const float m_tile = mx * sc;
+            if (__any_sync(0xffffffffu, m_tile > m_o + 64.f)) {  // rare: redo against the new max
+                const float m_new = fmaxf(m_o, m_tile);
+                const float f = ex2_approx(m_o - m_new);
+                l_run *= f;
+                o_pending *= f;
+                m_o = m_new;
+                lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
+            }
+        }
+        if (j > 0 && __any_sync(0xffffffffu, o_pending != 1.f)) {
+            // O must follow the reference before this tile's PV product
+            if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c) {
+                uint32_t ov[64];
+                tmem_ld_x64(tO + 64 * c, ov);
+#pragma unroll
+                for (int e = 0; e < 64; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * o_pending);
+                tmem_st_x64(tO + 64 * c, ov);
+            }
+            o_pending = 1.f;
+        }
+        l_run += lsum;
+        if (!C::P_ALIAS) {
+            const float m_tile = mx * sc;
+            if (m_tile > m_o + 8.f) {  // move the reference up; O follows after this product
+                const float f = ex2_approx(m_o - m_tile);
+                l_run *= f;
+                o_pending = f;
+                m_o = m_tile;
+            }
+        }
+        if (diag && zero_tail) {
+            const int st = j % C::NST;
+            if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[st], (j / C::NST) & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            uint8_t* sV = sKV + st * C::STAGE_BYTES + C::K_BYTES;
+            const int kk = last_lp - j * kPagesPerTile;  // page of the tile
+            const int nz = (kBlockTokens - tail_valid) * 8 * C::KCH;  // 16-byte pieces
+            for (int t = r; t < nz; t += 128) {
+                const int piece = t & 7;
+                const int c = (t >> 3) % C::KCH;
+                const int row = tail_valid + (t >> 3) / C::KCH;
+                *reinterpret_cast<uint4*>(sV + c * kChunkBytes + (kk * kBlockTokens + row) * 128 + piece * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+        }
+        tc_fence_before_sync();
+        mbar_arrive(p_full);
+    }
+    if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, (nkv - 1) & 1, abort_flag, p.err))) {
+        tc_fence_after_sync();
+        const bool store = row_in_seq < n;
+        const float inv = l_run > 0.f ? o_pending / l_run : 0.f;
+        const long long orow = static_cast<long long>(cu0 + row_in_seq) * g.hq + hq;
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c) {
+            uint32_t ov[64];
+            tmem_ld_x64(tO + 64 * c, ov);
+            if (store) {
+                uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + 64 * c);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv);
+                    v.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv);
+                    v.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv);
+                    v.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv);
+                    dst[e] = v;
+                }
+            }
+        }
+        if (store && p.lse) p.lse[orow] = l_run > 0.f ? (m_o + lg2_approx(l_run)) * kLn2 : -CUDART_INF_F;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
                const PrefillParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned operand tiles
-    uint8_t* sQ = smem;
-    uint8_t* sKV = smem + C::Q_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + C::NST * C::STAGE_BYTES);
+    uint8_t* sQ = smem;                                            // tile A, then tile B
+    uint8_t* sKV = smem + 2 * C::Q_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::NST * C::STAGE_BYTES);
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;
     uint64_t* kv_empty = bars + 1 + C::NST;
-    uint64_t* s_full = bars + 1 + 2 * C::NST;
-    uint64_t* p_full = s_full + 1;
-    uint64_t* o_done = s_full + 2;
-    uint64_t* mma_done = s_full + 3;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+    uint64_t* s_full = bars + 1 + 2 * C::NST;  // [2]
+    uint64_t* p_full = s_full + 2;             // [2]
+    uint64_t* o_done = s_full + 4;             // [2]
+    uint64_t* mma_done = s_full + 6;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 25);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const KGeom& g = p.g;
 
-    // ---- work item: row tile (heaviest first), sequence, q head
-    const int per_tile = p.batch * g.hq;
+    // ---- work item: row tile (heaviest first), sequence, q head (pair)
+    const int units = p.pair ? g.hq / 2 : g.hq;
+    const int per_tile = p.batch * units;
     const int item = blockIdx.x;
     const int i = p.n_row_tiles - 1 - item / per_tile;
     const int rem = item % per_tile;
-    const int b = rem / g.hq;
-    const int hq = rem % g.hq;
-    const int hk = hq / g.group;
+    const int b = rem / units;
+    const int u = rem % units;
+    const int hq_a = p.pair ? 2 * u : u;
+    const bool has_b = p.pair != 0;
+    const int hq_b = hq_a + 1;
+    const int hk = hq_a / g.group;
     const int cu0 = p.cu[b], cu1 = p.cu[b + 1];
     const int n = cu1 - cu0;
     const bool bad_len = cu0 < 0 || n < 0 || cu1 > p.total_tokens || n > p.max_seqlen;
-    if (i == 0 && hq == 0 && tid == 0 && bad_len) set_error(p.err, PA_ERR_BAD_BLOCK);
+    if (i == 0 && u == 0 && tid == 0 && bad_len) set_error(p.err, PA_ERR_BAD_BLOCK);
     if (cu0 < 0 || n <= 0 || cu1 > p.total_tokens) return;
     if (i * BM >= n) return;
     const int slot = p.slots[b];
@@ -205,15 +343,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
-        mbar_init(o_done, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&o_done[t], 1);
+        }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -226,10 +366,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (lane == 0) {
             prefetch_tensor_map(&qmap);
             prefetch_tensor_map(&kvmap);
-            mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+            mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_BYTES);
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-                tma_load_2d(sQ + c * kChunkBytes, &qmap, hq * D + 64 * c, cu0 + i * BM, q_full);
+            for (int c = 0; c < C::KCH; ++c) {
+                tma_load_2d(sQ + c * kChunkBytes, &qmap, hq_a * D + 64 * c, cu0 + i * BM, q_full);
+                if (has_b)
+                    tma_load_2d(sQ + C::Q_BYTES + c * kChunkBytes, &qmap, hq_b * D + 64 * c, cu0 + i * BM, q_full);
+            }
         }
         const int oob_row = static_cast<int>(g.nblocks * 32);  // first row past the pool: zero fill
         int issued = 0;
@@ -256,9 +399,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], C::STAGE_BYTES);
 #pragma unroll
             for (int k = 0; k < kPagesPerTile; ++k) {
-                const int r = __shfl_sync(0xffffffffu, row, k);
+                const int rr = __shfl_sync(0xffffffffu, row, k);
                 if (lane == 0) {
-                    const int y = r < 0 ? oob_row : r;
+                    const int y = rr < 0 ? oob_row : rr;
 #pragma unroll
                     for (int c = 0; c < C::KCH; ++c) {
                         tma_load_2d(sK + c * kChunkBytes + k * 2048, &kvmap, hk * D + 64 * c, y, &kv_full[st]);
@@ -275,159 +418,74 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Tile A's softmax runs while the tensor core works on tile B and the
+        // reverse: PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1), ...
         if (lane == 0) {
             constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
             constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
-            const uint32_t tS = tmem + kSCol, tO = tmem + kOCol, tP = tmem + C::P_COL;
             const uint32_t sq = smem_u32(sQ);
-            bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int st = j % C::NST;
-                if (!mbar_wait(&kv_full[st], (j / C::NST) & 1, abort_flag, p.err)) break;
-                tc_fence_after_sync();
+            auto qk = [&](int t, int st) {
                 const uint32_t sK = smem_u32(sKV + st * C::STAGE_BYTES);
-                const uint32_t sV = sK + C::K_BYTES;
+                const uint32_t sqt = sq + t * C::Q_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks / 4) * kChunkBytes + (ks % 4) * 32;
-                    umma_ss(tS, umma_sdesc_sw128(sq + off, 16, 1024), umma_sdesc_sw128(sK + off, 16, 1024),
-                            idesc_qk, ks > 0 ? 1u : 0u);
+                    umma_ss(tmem + C::s_col(t), umma_sdesc_sw128(sqt + off, 16, 1024),
+                            umma_sdesc_sw128(sK + off, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
                 }
-                umma_commit(s_full);
-                if (!mbar_wait(p_full, j & 1, abort_flag, p.err)) break;
-                tc_fence_after_sync();
+                umma_commit(&s_full[t]);
+            };
+            auto pv = [&](int t, int st, bool acc) {
+                const uint32_t sV = smem_u32(sKV + st * C::STAGE_BYTES) + C::K_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks) {
 #pragma unroll
                     for (int c = 0; c < C::KCH; ++c)
-                        umma_ts(tO + 64 * c, tP + ks * 8,
+                        umma_ts(tmem + C::o_col(t) + 64 * c, tmem + C::p_col(t) + ks * 8,
                                 umma_sdesc_sw128(sV + c * kChunkBytes + ks * 2048, 1024, 1024), idesc_pv,
-                                (j > 0 || ks > 0) ? 1u : 0u);
+                                (acc || ks > 0) ? 1u : 0u);
                 }
-                umma_commit(o_done);
+                umma_commit(&o_done[t]);
+            };
+            bool ok = mbar_wait(q_full, 0, abort_flag, p.err) && mbar_wait(&kv_full[0], 0, abort_flag, p.err);
+            if (ok) {
+                tc_fence_after_sync();
+                qk(0, 0);
+                if (has_b) qk(1, 0);
+            }
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int st = j % C::NST;
+                const int st1 = (j + 1) % C::NST;
+                const bool more = j + 1 < nkv;
+                if (!mbar_wait(&p_full[0], j & 1, abort_flag, p.err)) break;
+                tc_fence_after_sync();
+                pv(0, st, j > 0);
+                if (more) {
+                    if (!mbar_wait(&kv_full[st1], ((j + 1) / C::NST) & 1, abort_flag, p.err)) break;
+                    tc_fence_after_sync();
+                    qk(0, st1);
+                }
+                if (has_b) {
+                    if (!mbar_wait(&p_full[1], j & 1, abort_flag, p.err)) break;
+                    tc_fence_after_sync();
+                    pv(1, st, j > 0);
+                }
                 umma_commit(&kv_empty[st]);
+                if (has_b && more) qk(1, st1);
             }
             umma_commit(mma_done);  // every MMA of this CTA done before TMEM is freed
             mbar_drain(mma_done, 0);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax
-        // Thread r owns query row r.  O in TMEM holds sum_t P_t V_t with every P_t
-        // relative to one reference m_o (log2 units of the scaled score); l_run is
-        // relative to the same m_o.  P_j is formed against the current m_o in one
-        // pass that also finds the tile max; only the first tile (no reference yet)
-        // or a jump of more than 2^64 takes a separate max pass.  When a tile max
-        // exceeds m_o by more than 2^8 the reference moves up: l_run now, the O row
-        // (after the PV product that used the old reference) before the next
-        // product or at the epilogue.  Exact: o = O / l uses one reference.
-        const int r = (warp & 3) * 32 + lane;  // query row in the tile == TMEM lane
-        const uint32_t lane_base = tmem_lane_base(warp);
-        const uint32_t tS = tmem + lane_base + kSCol;
-        const uint32_t tO = tmem + lane_base + kOCol;
-        const uint32_t tP = tmem + lane_base + C::P_COL;
-        const int row_in_seq = i * BM + r;
-        const float sc = p.scale_log2;
-        float m_o = -CUDART_INF_F, l_run = 0.f;
-        float o_pending = 1.f;  // factor O still owes for the move of m_o
-        bool ok = true;
-        // partial last page: its V rows past the end are zeroed before the PV product
-        const int last_lp = pages_b - 1;
-        const int tail_valid = n - last_lp * kBlockTokens;
-        const bool zero_tail = (i == (n - 1) / BM) && tail_valid < kBlockTokens;
-        for (int j = 0; j < nkv; ++j) {
-            if (!__all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, p.err))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            const bool diag = (j == i);
-            float mx, lsum;
-            if (j == 0) {
-                m_o = sc * (diag ? tile_row_max<true>(tS, r) : tile_row_max<false>(tS, r));
-                lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
-            } else {
-                lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
-                const float m_tile = mx * sc;
-                if (__any_sync(0xffffffffu, m_tile > m_o + 64.f)) {  // rare: redo against the new max
-                    const float m_new = fmaxf(m_o, m_tile);
-                    const float f = ex2_approx(m_o - m_new);
-                    l_run *= f;
-                    o_pending *= f;
-                    m_o = m_new;
-                    lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
-                }
-                if (__any_sync(0xffffffffu, o_pending != 1.f)) {
-                    // O must follow the reference before this tile's PV product
-                    if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-#pragma unroll
-                    for (int c = 0; c < C::KCH; ++c) {
-                        uint32_t ov[64];
-                        tmem_ld_x64(tO + 64 * c, ov);
-#pragma unroll
-                        for (int e = 0; e < 64; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * o_pending);
-                        tmem_st_x64(tO + 64 * c, ov);
-                    }
-                    o_pending = 1.f;
-                }
-            }
-            l_run += lsum;
-            const float m_tile = mx * sc;
-            if (m_tile > m_o + 8.f) {  // move the reference up; O follows after this PV
-                const float f = ex2_approx(m_o - m_tile);
-                l_run *= f;
-                o_pending = f;
-                m_o = m_tile;
-            }
-            if (diag && zero_tail) {
-                const int st = j % C::NST;
-                if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[st], (j / C::NST) & 1, abort_flag, p.err))) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* sV = sKV + st * C::STAGE_BYTES + C::K_BYTES;
-                const int kk = last_lp - j * kPagesPerTile;  // page of the tile
-                const int nz = (kBlockTokens - tail_valid) * 8 * C::KCH;  // 16-byte pieces
-                for (int t = r; t < nz; t += 128) {
-                    const int piece = t & 7;
-                    const int c = (t >> 3) % C::KCH;
-                    const int row = tail_valid + (t >> 3) / C::KCH;
-                    *reinterpret_cast<uint4*>(sV + c * kChunkBytes + (kk * kBlockTokens + row) * 128 + piece * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
-            }
-            tc_fence_before_sync();
-            mbar_arrive(p_full);
-        }
-        if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, (nkv - 1) & 1, abort_flag, p.err))) {
-            tc_fence_after_sync();
-            const bool store = row_in_seq < n;
-            const float inv = l_run > 0.f ? o_pending / l_run : 0.f;
-            const long long orow = static_cast<long long>(cu0 + row_in_seq) * g.hq + hq;
-#pragma unroll
-            for (int c = 0; c < C::KCH; ++c) {
-                uint32_t ov[64];
-                tmem_ld_x64(tO + 64 * c, ov);
-                if (store) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + 64 * c);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv);
-                        dst[e] = v;
-                    }
-                }
-            }
-            if (store && p.lse)
-                p.lse[orow] = l_run > 0.f ? (m_o + lg2_approx(l_run)) * kLn2 : -CUDART_INF_F;
+        const int t = (warp - 4) >> 2;  // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
+        if (t == 0 || has_b) {
+            const int r = (warp & 3) * 32 + lane;
+            const uint32_t lane_base = tmem_lane_base(warp);
+            softmax_role<D>(tmem + lane_base + C::s_col(t), tmem + lane_base + C::o_col(t),
+                            tmem + lane_base + C::p_col(t), r, i, nkv, n, cu0, t ? hq_b : hq_a, t == 0, sKV,
+                            &s_full[t], &p_full[t], &o_done[t], kv_full, abort_flag, p);
         }
     }
 
@@ -435,7 +493,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -476,7 +534,7 @@ cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, const Pref
     auto kern = prefill_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
     if (e != cudaSuccess) return e;
-    const long long grid = static_cast<long long>(p.n_row_tiles) * p.batch * p.g.hq;
+    const long long grid = static_cast<long long>(p.n_row_tiles) * p.batch * (p.pair ? p.g.hq / 2 : p.g.hq);
     if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     kern<<<static_cast<unsigned>(grid), kThreads, Cfg<D>::SMEM, stream>>>(qmap, kvmap, p);
     return cudaGetLastError();
@@ -505,6 +563,7 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, cons
     p.max_seqlen = max_seqlen;
     p.total_tokens = total_tokens;
     p.n_row_tiles = (max_seqlen + BM - 1) / BM;
+    p.pair = (g.group % 2 == 0) ? 1 : 0;
     p.scale_log2 = scale * kLog2e;
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
