@@ -129,8 +129,9 @@ pa_status pa_write_kv(const pa_geom* geom, void* pool, const int32_t* block_tabl
  * [batch+1], cu_seqlens[0] = 0, non-decreasing, cu_seqlens[batch] <=
  * total_tokens.  slots: device int32 [batch].  max_seqlen: host upper bound on
  * every n_b (sizes the grid; longer sequences set PA_ERR_BAD_BLOCK).
- * total_tokens: host row count of q / o.  Requires d in {64, 128}.  Rows of q
- * not covered by cu_seqlens are neither read for output nor written.
+ * total_tokens: host row count of q / o.  scale: finite and > 0 (else
+ * PA_ERR_INVALID_ARG).  Requires d in {64, 128}.  Rows of q not covered by
+ * cu_seqlens are neither read for output nor written.
  */
 pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool,
                      const int32_t* block_table, int32_t layer, int32_t batch,
@@ -163,8 +164,9 @@ size_t pa_decode_workspace_size(const pa_geom* geom, int32_t batch, int32_t max_
  * and the workspace; lengths beyond 16 * max_blocks_per_seq set
  * PA_ERR_BAD_BLOCK).  workspace: device, 16-byte aligned, at least
  * pa_decode_workspace_size(geom, batch, max_seq_len) bytes, contents need not
- * be initialised, not shared with a concurrent call.  Requires d in {64, 128},
- * Hq/Hkv in {1, 2, 4, 8}, Hkv * ceil(Hq/Hkv/4) <= 16 and a page of at most 64 KiB.
+ * be initialised, not shared with a concurrent call.  scale: finite and > 0
+ * (else PA_ERR_INVALID_ARG).  Requires d in {64, 128}, Hq/Hkv in {1, 2, 4, 8},
+ * Hkv <= 8 and a page of at most 64 KiB (else PA_ERR_UNSUPPORTED).
  */
 pa_status pa_decode(const pa_geom* geom, const void* q, const void* pool,
                     const int32_t* block_table, int32_t layer, int32_t batch,

@@ -82,7 +82,7 @@ PA_API pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool
                             int32_t* err_flag, pa_stream_t stream) {
     if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
     if (layer < 0 || layer >= geom->n_layers) return PA_ERR_INVALID_ARG;
-    if (batch < 0 || max_seqlen < 0 || total_tokens < 0 || !std::isfinite(scale))
+    if (batch < 0 || max_seqlen < 0 || total_tokens < 0 || !std::isfinite(scale) || !(scale > 0.f))
         return PA_ERR_INVALID_ARG;
     if (geom->head_dim != 64 && geom->head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (batch == 0 || total_tokens == 0 || max_seqlen == 0) return PA_OK;
@@ -109,7 +109,7 @@ PA_API pa_status pa_decode(const pa_geom* geom, const void* q, const void* pool,
                            size_t workspace_bytes, int32_t* err_flag, pa_stream_t stream) {
     if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
     if (layer < 0 || layer >= geom->n_layers) return PA_ERR_INVALID_ARG;
-    if (batch < 0 || max_seq_len < 0 || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (batch < 0 || max_seq_len < 0 || !std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
     const pa::KGeom g = kgeom(geom);
     if (!pa::decode_supported(g)) return PA_ERR_UNSUPPORTED;
     if (batch == 0) return PA_OK;

@@ -7,40 +7,41 @@
 // with the FlashAttention-2 deferred normalisation: keep the unnormalised
 // output and l, divide once at the end, store L = m + ln l (base.kaita.kr,
 // "플래시어텐션-2: 더 나은 병렬화", "단계별 설명 (순전파의 두 가지 손질)").
-// Tiles whose keys all lie after their rows are skipped and only the diagonal
-// tile is masked ("인과 마스크 처리").  Q head h reads kv head h / (Hq / Hkv)
-// without copying K/V ("4. MQA · GQA 지원").
+// Key tiles that lie wholly after a row tile are skipped and only the tiles
+// that cross the diagonal are masked ("인과 마스크 처리").  Q head h reads kv
+// head h / (Hq / Hkv) without copying K/V ("4. MQA · GQA 지원").
 //
 // GB300 mapping (prior art on the pages: cuBLAS per head + separate mask and
 // softmax kernels; FA2's warp split on A100):
-//  * One CTA per SM-sized work item: a 128-row query tile of a sequence for two
-//    q heads of the same GQA group (tiles A and B; one head when the group size
-//    is odd).  Both tiles read the same K/V tiles, staged once.  Items are
+//  * One CTA per work item: a 128-row query tile of a sequence for T q heads of
+//    one GQA group (T = 4 at d 64, 2 at d 128 when the group size allows; 1
+//    otherwise).  The T tiles read the same K/V, staged once.  Items are
 //    launched heaviest first (the last row tiles own the most key tiles).
-//  * Warp 0 (TMA producer): the two Q tiles with one 2D tensor copy per 64-dim
-//    chunk; each 128-key K/V tile as 8 pages, each page one {64 x 16} box per
-//    chunk for K and one for V, rows addressed through the block table -- the
-//    pool is one 2D tensor [pages * 32 rows][KV_DIM], page p's K rows at 32p,
-//    V rows at 32p + 16.  128-byte swizzled boxes stack into the canonical
+//  * Warp 4T (TMA producer): the T query tiles with one 2D tensor copy per
+//    64-dim chunk; each 64-key K/V tile as 4 pages, each page one {64 x 16} box
+//    per chunk for K and one for V, rows addressed through the block table --
+//    the pool is one 2D tensor [pages * 32 rows][KV_DIM], page p's K rows at
+//    32p, V rows at 32p + 16.  128-byte swizzled boxes stack into the canonical
 //    K-major (Q, K) / MN-major (V) operand layouts of the tensor core.  Pages
 //    past the sequence end are read at an out-of-range row, which the copy
-//    engine fills with zeros.  Three K/V stages at d 64, two at d 128.
-//  * Warp 1 (single-thread MMA issuer): S = Q K^T (M 128, N 128, K 16 steps)
-//    into TMEM; after a softmax warpgroup hands back P, O += P V with P read
-//    straight from TMEM (M 128, N 64 per 64-dim chunk, K 16).  Issue order
-//    PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1): while one tile's softmax runs, the
-//    tensor core works on the other tile.
-//  * Warps 4-7 and 8-11 (softmax, one warpgroup per tile): thread r owns query
-//    row r, i.e. TMEM lane r; scores stream out of TMEM 32 columns at a time;
-//    P = 2^(s*scale*log2e - m) is formed with packed fp32 FMAs and the SFU
-//    exp2, packed to bf16 into TMEM; l stays in a register.  The reference max
-//    only moves when a row max exceeds it by more than 2^8; then the thread
-//    rescales its O row in TMEM (exact, since the final division uses the same
-//    m).  The epilogue divides by l, writes o (bf16) and L = ln2 (m + log2 l).
-//  * TMEM (512 columns): S_A, S_B, O_A, O_B, and P_A, P_B in their own columns
-//    at d 64; at d 128 P overwrites the S it came from.
+//    engine fills with zeros.
+//  * Warp 4T+1 (MMA issuer, the whole warp runs the loop and one elected lane
+//    issues): S_t = Q_t K^T (M 128, N 64, K 16 steps) into TMEM; after tile t's
+//    softmax hands back P_t, O_t += P_t V (M 128, N 64 per 64-dim chunk, K 16
+//    with P read from TMEM), then the next S_t.  The tiles take turns, so the
+//    tensor core works on the others while one tile's softmax runs.
+//  * Warps 4t..4t+3 (softmax of tile t): thread r owns query row r, i.e. TMEM
+//    lane r, and all 64 scores of the key tile: it loads them into registers,
+//    takes the row max first, moves the reference max if the tile max exceeds
+//    it by more than 2^8 (l at once, its O row in TMEM in place -- no PV
+//    product is in flight then), and forms P = 2^(s*scale*log2e - m) with
+//    packed fp32 FMAs and the SFU exp2, packed to bf16 over the first half of
+//    the scores' own TMEM columns.  The epilogue divides by l, writes o (bf16)
+//    and L = ln2 (m + log2 l).  Exact: o = O / l uses the one reference.
+//  * TMEM: tile t owns 64 + d columns from t (64 + d): S (P over its first
+//    half), then O.
 //  * A partial last page has its V rows past the sequence end zeroed in shared
-//    memory before the PV product (masked P is exactly 0, but 0 x NaN is not).
+//    memory before the PV products (masked P is exactly 0, but 0 x NaN is not).
 #include <math_constants.h>
 
 #include "pa_internal.cuh"
@@ -48,27 +49,34 @@
 namespace pa {
 namespace {
 
-constexpr int BM = 128;               // query rows per tile (TMEM lanes)
-constexpr int BN = 128;               // keys per K/V tile
+constexpr int BM = 128;                 // query rows per tile (TMEM lanes)
+constexpr int BN = 64;                  // keys per K/V tile
 constexpr int kPagesPerTile = BN / kBlockTokens;
-constexpr int kThreads = 384;         // TMA warp, MMA warp, 2 idle, 2 softmax warpgroups
-constexpr int kChunkBytes = 128 * 128;  // 128 rows x 128 bytes: one 64-dim chunk of a tile
-constexpr int kTmemCols = 512;
+constexpr int kQChunkBytes = BM * 128;  // 128 rows x 128 bytes: one 64-dim chunk of a query tile
+constexpr int kKChunkBytes = BN * 128;  // 64 keys x 128 bytes: one 64-dim chunk of a K or V tile
+constexpr float kMoveAbove = 8.f;       // the reference max moves when a tile max exceeds it by 2^8
 
-template <int D>
+template <int D, int T>
 struct Cfg {
     static constexpr int KCH = D / 64;
-    static constexpr int Q_BYTES = KCH * kChunkBytes;  // one query tile
-    static constexpr int K_BYTES = KCH * kChunkBytes;
+    static constexpr int PRODUCER_WARP = 4 * T;
+    static constexpr int MMA_WARP = 4 * T + 1;
+    static constexpr int THREADS = 32 * (4 * T + 2);
+    static constexpr int Q_BYTES = KCH * kQChunkBytes;  // one query tile
+    static constexpr int K_BYTES = KCH * kKChunkBytes;
     static constexpr int STAGE_BYTES = 2 * K_BYTES;
-    static constexpr int NST = D == 64 ? 3 : 2;
-    static constexpr int SMEM = 1024 + 2 * Q_BYTES + NST * STAGE_BYTES + 1024;
-    // tensor memory: S_A S_B (128 columns each), O_A O_B (d each), P_A P_B (64
-    // each) -- at d 128 there is no room left, so P overwrites the S it came from
-    static constexpr bool P_ALIAS = D == 128;
-    static __device__ __forceinline__ uint32_t s_col(int t) { return 128u * t; }
-    static __device__ __forceinline__ uint32_t o_col(int t) { return 256u + D * t; }
-    static __device__ __forceinline__ uint32_t p_col(int t) { return P_ALIAS ? 128u * t : 384u + 64u * t; }
+    static constexpr int CTL_BYTES = 1024;
+    static constexpr int NST_FIT = (220 * 1024 - T * Q_BYTES - CTL_BYTES - 1024) / STAGE_BYTES;
+    static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
+    static constexpr int SMEM = 1024 + T * Q_BYTES + NST * STAGE_BYTES + CTL_BYTES;
+    static constexpr int TILE_COLS = BN + D;
+    static constexpr uint32_t TMEM_COLS = T * TILE_COLS <= 128 ? 128u : T * TILE_COLS <= 256 ? 256u : 512u;
+    static_assert(T * TILE_COLS <= 512, "tensor memory holds S and O of every tile");
+    static_assert(NST >= 2, "two K/V stages at least");
+    static __device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(TILE_COLS * t); }
+    static __device__ __forceinline__ uint32_t o_col(int t) { return static_cast<uint32_t>(TILE_COLS * t + BN); }
+    // P columns of key step ks (16 keys) of tile t: over the first half of S
+    static __device__ __forceinline__ uint32_t p_col(int t, int ks) { return s_col(t) + 8u * ks; }
 };
 
 struct PrefillParams {
@@ -81,249 +89,192 @@ struct PrefillParams {
     int max_seqlen;
     int total_tokens;
     int n_row_tiles;
-    int pair;             // 1: a CTA takes two q heads of one GQA group
+    int heads_per_cta;    // T
     float scale_log2;
     __nv_bfloat16* o;
     float* lse;
     int32_t* err;
 };
 
-// Softmax of one tile for the calling thread's query row r (= its TMEM lane).
-// The 128 scores are streamed from TMEM 32 columns at a time, the next chunk's
-// load in flight while the current one is processed.  On the diagonal tile the
-// keys after the row are masked to -inf.
-
-// Row max of the raw scores.
-template <bool DIAG>
-__device__ __forceinline__ float tile_row_max(uint32_t tS, int r) {
-    uint32_t b0[32], b1[32];
-    float mx = -CUDART_INF_F;
-    tmem_ld_x32_nowait(tS, b0);
-    tmem_wait_ld_dep(b0);
+// P = 2^(s * sc + nm) of 32 scores, packed to bf16 pairs; adds the fp32 P to ls.
+__device__ __forceinline__ void p_chunk(const uint32_t (&v)[32], float sc, float nm, float (&ls)[8],
+                                        uint32_t (&pk)[16]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t(&cur)[32] = (q & 1) ? b1 : b0;
-        uint32_t(&nxt)[32] = (q & 1) ? b0 : b1;
-        if (q < 3) tmem_ld_x32_nowait(tS + 32 * (q + 1), nxt);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-            float s0 = __uint_as_float(cur[e]), s1 = __uint_as_float(cur[e + 1]);
-            if (DIAG) {
-                if (32 * q + e > r) s0 = -CUDART_INF_F;
-                if (32 * q + e + 1 > r) s1 = -CUDART_INF_F;
-            }
-            mx = fmax3(mx, s0, s1);
-        }
-        if (q < 3) tmem_wait_ld_dep(nxt);
+    for (int e = 0; e < 16; ++e) {
+        float x0, x1;
+        ffma2(x0, x1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), sc, sc, nm, nm);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        const int a = 2 * (e & 3);
+        fadd2(ls[a], ls[a + 1], ls[a], ls[a + 1], p0, p1);
+        pk[e] = pack_bf16x2(p0, p1);
     }
-    return mx;
 }
 
-// P = 2^(s * sc - m_ref) as bf16 pairs into the 64 TMEM columns at tP (one
-// packed FMA per two scores, one ex2 each); returns the sum of the fp32 P and,
-// through mx, the raw row max of the tile (tracked in the same pass).
-template <bool DIAG>
-__device__ __forceinline__ float tile_row_p(uint32_t tS, uint32_t tP, int r, float sc, float m_ref, float& mx) {
-    const float nm = -m_ref;
-    float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 4 independent pair sums
-    float m = -CUDART_INF_F;
-    uint32_t b0[32], b1[32];
-    tmem_ld_x32_nowait(tS, b0);
-    tmem_wait_ld_dep(b0);
+// Scores of keys after the row become -inf: element e sits at key c0 + e
+// relative to the first row of the tile.
+__device__ __forceinline__ void mask_chunk(uint32_t (&v)[32], int c0, int r) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t(&cur)[32] = (q & 1) ? b1 : b0;
-        uint32_t(&nxt)[32] = (q & 1) ? b0 : b1;
-        if (q < 3) tmem_ld_x32_nowait(tS + 32 * (q + 1), nxt);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
-            if (DIAG) {
-                if (32 * q + 2 * e > r) s0 = -CUDART_INF_F;
-                if (32 * q + 2 * e + 1 > r) s1 = -CUDART_INF_F;
-            }
-            m = fmax3(m, s0, s1);
-            float x0, x1;
-            ffma2(x0, x1, s0, s1, sc, sc, nm, nm);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            const int a = 2 * (e & 3);
-            fadd2(ls[a], ls[a + 1], ls[a], ls[a + 1], p0, p1);
-            pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st_x16_nowait(tP + 16 * q, pk);
-        if (q < 3) tmem_wait_ld_dep(nxt);
-    }
-    tmem_wait_st();
-    mx = m;
-    return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+    for (int e = 0; e < 32; ++e)
+        if (c0 + e > r) v[e] = __float_as_uint(-CUDART_INF_F);
 }
 
-// Softmax role of one query tile: the warpgroup's thread r owns query row r
-// (TMEM lane r).  O in TMEM holds sum_t P_t V_t with every P_t relative to one
-// reference m_o (log2 units of the scaled score); l_run is relative to the same
-// m_o.  With a separate P region (d 64) P_j is formed against the current m_o in
-// one pass that also finds the tile max; only the first tile or a jump of more
-// than 2^64 takes a separate max pass.  With P over S (d 128) the max pass
-// always comes first.  When a tile max exceeds m_o by more than 2^8 the
-// reference moves up: l_run at once, the O row before the next PV product
-// (or in the epilogue).  Exact: o = O / l uses a single reference.
-template <int D>
-__device__ __forceinline__ void softmax_role(uint32_t tS, uint32_t tO, uint32_t tP, int r, int i, int nkv, int n,
-                                             int cu0, int hq, bool zero_tail_owner, uint8_t* sKV, uint64_t* s_full,
-                                             uint64_t* p_full, uint64_t* o_done, uint64_t* kv_full,
-                                             volatile int* abort_flag, const PrefillParams& p) {
-    using C = Cfg<D>;
+__device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], float m) {
+    float mx[4] = {m, m, m, m};
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// Softmax of query tile t: the warp's thread owns row r (TMEM lane r).
+template <int D, int T>
+__device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, int i, int nkv, int n, int cu0, int hq,
+                                             uint8_t* sKV, uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
+                                             uint64_t* kv_full, volatile int* abort_flag, const PrefillParams& p) {
+    using C = Cfg<D, T>;
     const KGeom& g = p.g;
     const float sc = p.scale_log2;
-    const int row_in_seq = i * BM + r;
-    float m_o = -CUDART_INF_F, l_run = 0.f;
-    float o_pending = 1.f;  // factor O still owes for a move of m_o
-    bool ok = true;
+    const uint32_t tS = tmem_lane + C::s_col(t);
+    const uint32_t tO = tmem_lane + C::o_col(t);
+    const int row = i * BM + r;  // query row within the sequence
     const int last_lp = (n + kBlockTokens - 1) / kBlockTokens - 1;
     const int tail_valid = n - last_lp * kBlockTokens;
-    const bool zero_tail = zero_tail_owner && (i == (n - 1) / BM) && tail_valid < kBlockTokens;
+    const int j_tail = (t == 0 && tail_valid < kBlockTokens) ? last_lp / kPagesPerTile : -1;
+    float m_o = -CUDART_INF_F, l = 0.f;
+    bool ok = true;
     for (int j = 0; j < nkv; ++j) {
         if (!__all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, p.err))) {
             ok = false;
             break;
         }
         tc_fence_after_sync();
-        const bool diag = (j == i);
-        float mx, lsum;
-        if (C::P_ALIAS || j == 0) {
-            const float m_tile = sc * (diag ? tile_row_max<true>(tS, r) : tile_row_max<false>(tS, r));
-            if (j == 0) {
-                m_o = m_tile;
-            } else if (m_tile > m_o + 8.f) {  // move the reference before this product
-                const float f = ex2_approx(m_o - m_tile);
-                l_run *= f;
-                o_pending *= f;
-                m_o = m_tile;
-            }
-            lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
-        } else {
-            lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
-            const float m_tile = mx * sc;
-            if (__any_sync(0xffffffffu, m_tile > m_o + 64.f)) {  // rare: redo against the new max
-                const float m_new = fmaxf(m_o, m_tile);
-                const float f = ex2_approx(m_o - m_new);
-                l_run *= f;
-                o_pending *= f;
-                m_o = m_new;
-                lsum = diag ? tile_row_p<true>(tS, tP, r, sc, m_o, mx) : tile_row_p<false>(tS, tP, r, sc, m_o, mx);
-            }
+        // pass 1: the row max of the 64 scores, 32 at a time
+        const int rel = BN * j - BM * i;  // first key of the tile relative to the first row of the tile
+        const bool diag = rel > -BN;      // the tile crosses the diagonal
+        float m_tile;
+        {
+            uint32_t v[32];
+            tmem_ld_x32(tS, v);
+            if (diag) mask_chunk(v, rel, r);
+            m_tile = chunk_max(v, -CUDART_INF_F);
+            tmem_ld_x32(tS + 32, v);
+            if (diag) mask_chunk(v, rel + 32, r);
+            m_tile = sc * chunk_max(v, m_tile);
         }
-        if (j > 0 && __any_sync(0xffffffffu, o_pending != 1.f)) {
-            // O must follow the reference before this tile's PV product
-            if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err))) {
-                ok = false;
-                break;
+        if (__any_sync(0xffffffffu, m_tile > m_o + kMoveAbove)) {
+            float f = 1.f;
+            if (m_tile > m_o + kMoveAbove) {
+                f = ex2_approx(m_o - m_tile);  // 0 from -inf
+                l *= f;
+                m_o = m_tile;
             }
-            tc_fence_after_sync();
+            if (j > 0) {  // this row of O follows the reference (no PV product is in flight)
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c) {
-                uint32_t ov[64];
-                tmem_ld_x64(tO + 64 * c, ov);
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld_x32(tO + 32 * c, ov);
 #pragma unroll
-                for (int e = 0; e < 64; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * o_pending);
-                tmem_st_x64(tO + 64 * c, ov);
-            }
-            o_pending = 1.f;
-        }
-        l_run += lsum;
-        if (!C::P_ALIAS) {
-            const float m_tile = mx * sc;
-            if (m_tile > m_o + 8.f) {  // move the reference up; O follows after this product
-                const float f = ex2_approx(m_o - m_tile);
-                l_run *= f;
-                o_pending = f;
-                m_o = m_tile;
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+                    tmem_st_x32(tO + 32 * c, ov);
+                }
             }
         }
-        if (diag && zero_tail) {
+        const float nm = m_o == -CUDART_INF_F ? 0.f : -m_o;
+        // pass 2: P, 32 scores at a time, over the scores already read
+        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t v[32], pk[16];
+            tmem_ld_x32(tS + 32 * h, v);
+            if (diag) mask_chunk(v, rel + 32 * h, r);
+            p_chunk(v, sc, nm, ls, pk);
+            tmem_st_x16_nowait(tS + 16 * h, pk);  // keys 32h..32h+31 over the scores of keys 16h..16h+15
+        }
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        if (j == j_tail) {
+            // V rows past the sequence end in the last page: zero (0 x NaN is NaN)
             const int st = j % C::NST;
             if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[st], (j / C::NST) & 1, abort_flag, p.err))) {
                 ok = false;
                 break;
             }
             uint8_t* sV = sKV + st * C::STAGE_BYTES + C::K_BYTES;
-            const int kk = last_lp - j * kPagesPerTile;  // page of the tile
+            const int kk = last_lp % kPagesPerTile;  // page within the tile
             const int nz = (kBlockTokens - tail_valid) * 8 * C::KCH;  // 16-byte pieces
-            for (int t = r; t < nz; t += 128) {
-                const int piece = t & 7;
-                const int c = (t >> 3) % C::KCH;
-                const int row = tail_valid + (t >> 3) / C::KCH;
-                *reinterpret_cast<uint4*>(sV + c * kChunkBytes + (kk * kBlockTokens + row) * 128 + piece * 16) =
+            for (int x = r; x < nz; x += BM) {
+                const int piece = x & 7;
+                const int c = (x >> 3) % C::KCH;
+                const int rr = tail_valid + (x >> 3) / C::KCH;
+                *reinterpret_cast<uint4*>(sV + c * kKChunkBytes + (kk * kBlockTokens + rr) * 128 + piece * 16) =
                     make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
         }
+        tmem_wait_st();
         tc_fence_before_sync();
         mbar_arrive(p_full);
     }
-    if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, (nkv - 1) & 1, abort_flag, p.err))) {
+    if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, 0, abort_flag, p.err))) {
         tc_fence_after_sync();
-        const bool store = row_in_seq < n;
-        const float inv = l_run > 0.f ? o_pending / l_run : 0.f;
-        const long long orow = static_cast<long long>(cu0 + row_in_seq) * g.hq + hq;
+        const bool store = row < n;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const long long orow = static_cast<long long>(cu0 + row) * g.hq + hq;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c) {
-            uint32_t ov[64];
-            tmem_ld_x64(tO + 64 * c, ov);
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld_x32(tO + 32 * c, ov);
             if (store) {
-                uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + 64 * c);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < 4; ++e) {
                     uint4 v;
                     v.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv);
                     v.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv);
                     v.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv);
                     v.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv);
-                    dst[e] = v;
+                    dst[4 * c + e] = v;
                 }
             }
         }
-        if (store && p.lse) p.lse[orow] = l_run > 0.f ? (m_o + lg2_approx(l_run)) * kLn2 : -CUDART_INF_F;
+        if (store && p.lse) p.lse[orow] = l > 0.f ? (m_o + lg2_approx(l)) * kLn2 : -CUDART_INF_F;
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int T>
+__global__ void __launch_bounds__(Cfg<D, T>::THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
                const PrefillParams p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, T>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned operand tiles
-    uint8_t* sQ = smem;                                            // tile A, then tile B
-    uint8_t* sKV = smem + 2 * C::Q_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::NST * C::STAGE_BYTES);
+    uint8_t* sQ = smem;                                            // T query tiles
+    uint8_t* sKV = smem + T * C::Q_BYTES;
+    uint8_t* ctl = sKV + C::NST * C::STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ctl);
     uint64_t* q_full = bars;
-    uint64_t* kv_full = bars + 1;
-    uint64_t* kv_empty = bars + 1 + C::NST;
-    uint64_t* s_full = bars + 1 + 2 * C::NST;  // [2]
-    uint64_t* p_full = s_full + 2;             // [2]
-    uint64_t* o_done = s_full + 4;             // [2]
-    uint64_t* mma_done = s_full + 6;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 25);
+    uint64_t* kv_full = bars + 1;                 // [NST]
+    uint64_t* kv_empty = bars + 1 + C::NST;       // [NST]
+    uint64_t* s_full = bars + 1 + 2 * C::NST;     // [T] scores of a tile in TMEM
+    uint64_t* p_full = s_full + T;                // [T] P of a tile in TMEM
+    uint64_t* o_done = s_full + 2 * T;            // [T] the last PV product of a tile done
+    uint64_t* mma_done = s_full + 3 * T;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 64);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 65);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const KGeom& g = p.g;
 
-    // ---- work item: row tile (heaviest first), sequence, q head (pair)
-    const int units = p.pair ? g.hq / 2 : g.hq;
+    // ---- work item: row tile (heaviest first), sequence, kv head, group of T q heads
+    const int qgroups = g.group / T;
+    const int units = g.hkv * qgroups;
     const int per_tile = p.batch * units;
     const int item = blockIdx.x;
     const int i = p.n_row_tiles - 1 - item / per_tile;
     const int rem = item % per_tile;
     const int b = rem / units;
     const int u = rem % units;
-    const int hq_a = p.pair ? 2 * u : u;
-    const bool has_b = p.pair != 0;
-    const int hq_b = hq_a + 1;
-    const int hk = hq_a / g.group;
+    const int hk = u / qgroups;
+    const int hq0 = hk * g.group + (u % qgroups) * T;
     const int cu0 = p.cu[b], cu1 = p.cu[b + 1];
     const int n = cu1 - cu0;
     const bool bad_len = cu0 < 0 || n < 0 || cu1 > p.total_tokens || n > p.max_seqlen;
@@ -333,7 +284,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int slot = p.slots[b];
     const bool slot_ok = slot >= 0 && slot < g.num_slots;
     if (!slot_ok && tid == 0) set_error(p.err, PA_ERR_BAD_BLOCK);
-    const int nkv = i + 1;  // causal: key tiles 0..i
+    // causal: key tiles up to the one holding key BM (i + 1) - 1, and none past the sequence
+    const int nkv = min(2 * i + 2, (n + BN - 1) / BN);
     const int pages_b = (n + kBlockTokens - 1) / kBlockTokens;
     const long long tbase = (static_cast<long long>(slot_ok ? slot : 0) * g.n_layers + p.layer) * g.maxb;
 
@@ -343,17 +295,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < T; ++t) {
             mbar_init(&s_full[t], 1);
-            mbar_init(&p_full[t], 128);
+            mbar_init(&p_full[t], BM);
             mbar_init(&o_done[t], 1);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == C::MMA_WARP) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -361,18 +313,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
+    if (warp == C::PRODUCER_WARP) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tensor_map(&qmap);
             prefetch_tensor_map(&kvmap);
-            mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_BYTES);
+            mbar_arrive_expect_tx(q_full, T * C::Q_BYTES);
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c) {
-                tma_load_2d(sQ + c * kChunkBytes, &qmap, hq_a * D + 64 * c, cu0 + i * BM, q_full);
-                if (has_b)
-                    tma_load_2d(sQ + C::Q_BYTES + c * kChunkBytes, &qmap, hq_b * D + 64 * c, cu0 + i * BM, q_full);
-            }
+            for (int t = 0; t < T; ++t)
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_2d(sQ + t * C::Q_BYTES + c * kQChunkBytes, &qmap, (hq0 + t) * D + 64 * c, cu0 + i * BM,
+                                q_full);
         }
         const int oob_row = static_cast<int>(g.nblocks * 32);  // first row past the pool: zero fill
         int issued = 0;
@@ -384,7 +336,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 stop = true;
                 break;
             }
-            // lanes 0..7 fetch the tile's page ids
+            // lanes 0..3 fetch the tile's page ids
             const int lp = j * kPagesPerTile + lane;
             int row = -1;
             if (lane < kPagesPerTile && lp < pages_b) {
@@ -404,8 +356,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     const int y = rr < 0 ? oob_row : rr;
 #pragma unroll
                     for (int c = 0; c < C::KCH; ++c) {
-                        tma_load_2d(sK + c * kChunkBytes + k * 2048, &kvmap, hk * D + 64 * c, y, &kv_full[st]);
-                        tma_load_2d(sV + c * kChunkBytes + k * 2048, &kvmap, hk * D + 64 * c, y + 16, &kv_full[st]);
+                        tma_load_2d(sK + c * kKChunkBytes + k * 2048, &kvmap, hk * D + 64 * c, y, &kv_full[st]);
+                        tma_load_2d(sV + c * kKChunkBytes + k * 2048, &kvmap, hk * D + 64 * c, y + 16, &kv_full[st]);
                     }
                 }
             }
@@ -416,84 +368,89 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             for (int jj = issued > C::NST ? issued - C::NST : 0; jj < issued; ++jj)
                 mbar_drain(&kv_full[jj % C::NST], (jj / C::NST) & 1);
         }
-    } else if (warp == 1) {
+    } else if (warp == C::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
-        // Tile A's softmax runs while the tensor core works on tile B and the
-        // reverse: PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1), ...
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
-            constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
-            const uint32_t sq = smem_u32(sQ);
-            auto qk = [&](int t, int st) {
-                const uint32_t sK = smem_u32(sKV + st * C::STAGE_BYTES);
-                const uint32_t sqt = sq + t * C::Q_BYTES;
+        // Per key tile j, for each query tile in turn: once its P is in TMEM,
+        // O_t += P_t V_j, then S_t = Q_t K_{j+1}^T over the same columns (the
+        // tensor core runs the two in order, so PV has read P before QK
+        // overwrites it).  While tile t waits for its softmax, the products
+        // of the other tiles keep the tensor core busy.
+        constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
+        constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
+        const uint32_t sq = smem_u32(sQ);
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err));
+        };
+        auto qk = [&](int t, int st) {
+            const uint32_t sK = smem_u32(sKV + st * C::STAGE_BYTES);
+            const uint32_t sqt = sq + t * C::Q_BYTES;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * kChunkBytes + (ks % 4) * 32;
-                    umma_ss(tmem + C::s_col(t), umma_sdesc_sw128(sqt + off, 16, 1024),
-                            umma_sdesc_sw128(sK + off, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks)
+                umma_ss_elect(tmem + C::s_col(t),
+                              umma_sdesc_sw128(sqt + (ks / 4) * kQChunkBytes + (ks % 4) * 32, 16, 1024),
+                              umma_sdesc_sw128(sK + (ks / 4) * kKChunkBytes + (ks % 4) * 32, 16, 1024), idesc_qk,
+                              ks > 0 ? 1u : 0u);
+            umma_commit_elect(&s_full[t]);
+        };
+        auto pv = [&](int t, int st, bool acc) {
+            const uint32_t sV = smem_u32(sKV + st * C::STAGE_BYTES) + C::K_BYTES;
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks)
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c)
+                    umma_ts_elect(tmem + C::o_col(t) + 64 * c, tmem + C::p_col(t, ks),
+                                  umma_sdesc_sw128(sV + c * kKChunkBytes + ks * 2048, 1024, 1024), idesc_pv,
+                                  (acc || ks > 0) ? 1u : 0u);
+        };
+        bool ok = wait_all(q_full, 0) && wait_all(&kv_full[0], 0);
+        if (ok) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int t = 0; t < T; ++t) qk(t, 0);
+        }
+        for (int j = 0; ok && j < nkv; ++j) {
+            const int st = j % C::NST;
+            const int st1 = (j + 1) % C::NST;
+            const bool more = j + 1 < nkv;
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                if (!wait_all(&p_full[t], j & 1)) {
+                    ok = false;
+                    break;
                 }
-                umma_commit(&s_full[t]);
-            };
-            auto pv = [&](int t, int st, bool acc) {
-                const uint32_t sV = smem_u32(sKV + st * C::STAGE_BYTES) + C::K_BYTES;
-#pragma unroll
-                for (int ks = 0; ks < BN / 16; ++ks) {
-#pragma unroll
-                    for (int c = 0; c < C::KCH; ++c)
-                        umma_ts(tmem + C::o_col(t) + 64 * c, tmem + C::p_col(t) + ks * 8,
-                                umma_sdesc_sw128(sV + c * kChunkBytes + ks * 2048, 1024, 1024), idesc_pv,
-                                (acc || ks > 0) ? 1u : 0u);
-                }
-                umma_commit(&o_done[t]);
-            };
-            bool ok = mbar_wait(q_full, 0, abort_flag, p.err) && mbar_wait(&kv_full[0], 0, abort_flag, p.err);
-            if (ok) {
                 tc_fence_after_sync();
-                qk(0, 0);
-                if (has_b) qk(1, 0);
-            }
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int st = j % C::NST;
-                const int st1 = (j + 1) % C::NST;
-                const bool more = j + 1 < nkv;
-                if (!mbar_wait(&p_full[0], j & 1, abort_flag, p.err)) break;
-                tc_fence_after_sync();
-                pv(0, st, j > 0);
+                pv(t, st, j > 0);
+                if (t == T - 1) umma_commit_elect(&kv_empty[st]);
                 if (more) {
-                    if (!mbar_wait(&kv_full[st1], ((j + 1) / C::NST) & 1, abort_flag, p.err)) break;
-                    tc_fence_after_sync();
-                    qk(0, st1);
+                    if (t == 0) {
+                        if (!wait_all(&kv_full[st1], ((j + 1) / C::NST) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                    }
+                    qk(t, st1);
+                } else {
+                    umma_commit_elect(&o_done[t]);
                 }
-                if (has_b) {
-                    if (!mbar_wait(&p_full[1], j & 1, abort_flag, p.err)) break;
-                    tc_fence_after_sync();
-                    pv(1, st, j > 0);
-                }
-                umma_commit(&kv_empty[st]);
-                if (has_b && more) qk(1, st1);
             }
-            umma_commit(mma_done);  // every MMA of this CTA done before TMEM is freed
-            mbar_drain(mma_done, 0);
         }
+        umma_commit_elect(mma_done);  // every MMA of this CTA done before TMEM is freed
+        mbar_drain(mma_done, 0);
         __syncwarp();
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------------------ softmax
-        const int t = (warp - 4) >> 2;  // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
-        if (t == 0 || has_b) {
-            const int r = (warp & 3) * 32 + lane;
-            const uint32_t lane_base = tmem_lane_base(warp);
-            softmax_role<D>(tmem + lane_base + C::s_col(t), tmem + lane_base + C::o_col(t),
-                            tmem + lane_base + C::p_col(t), r, i, nkv, n, cu0, t ? hq_b : hq_a, t == 0, sKV,
-                            &s_full[t], &p_full[t], &o_done[t], kv_full, abort_flag, p);
-        }
+        const int t = warp >> 2;
+        const int r = (warp & 3) * 32 + lane;  // query row = TMEM lane
+        softmax_role<D, T>(t, r, tmem + tmem_lane_base(warp), i, nkv, n, cu0, hq0 + t, sKV, &s_full[t], &p_full[t],
+                           &o_done[t], kv_full, abort_flag, p);
     }
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == C::MMA_WARP) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
@@ -529,14 +486,15 @@ bool encode_2d(CUtensorMap* map, const void* base, unsigned long long cols, unsi
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int T>
 cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, const PrefillParams& p, cudaStream_t stream) {
-    auto kern = prefill_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+    using C = Cfg<D, T>;
+    auto kern = prefill_kernel<D, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    const long long grid = static_cast<long long>(p.n_row_tiles) * p.batch * (p.pair ? p.g.hq / 2 : p.g.hq);
+    const long long grid = static_cast<long long>(p.n_row_tiles) * p.batch * (p.g.hq / T);
     if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
-    kern<<<static_cast<unsigned>(grid), kThreads, Cfg<D>::SMEM, stream>>>(qmap, kvmap, p);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(qmap, kvmap, p);
     return cudaGetLastError();
 }
 
@@ -563,12 +521,21 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, cons
     p.max_seqlen = max_seqlen;
     p.total_tokens = total_tokens;
     p.n_row_tiles = (max_seqlen + BM - 1) / BM;
-    p.pair = (g.group % 2 == 0) ? 1 : 0;
+    // q heads per CTA: as many of one GQA group as tensor memory holds (S and O
+    // of every tile: 4 at d 64, 2 at d 128)
+    const int tmax = g.d == 64 ? 4 : 2;
+    p.heads_per_cta = (g.group % 4 == 0 && tmax >= 4) ? 4 : (g.group % 2 == 0) ? 2 : 1;
     p.scale_log2 = scale * kLog2e;
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
     p.err = err;
-    return g.d == 64 ? launch<64>(qmap, kvmap, p, stream) : launch<128>(qmap, kvmap, p, stream);
+    if (g.d == 64) {
+        if (p.heads_per_cta == 4) return launch<64, 4>(qmap, kvmap, p, stream);
+        if (p.heads_per_cta == 2) return launch<64, 2>(qmap, kvmap, p, stream);
+        return launch<64, 1>(qmap, kvmap, p, stream);
+    }
+    if (p.heads_per_cta == 2) return launch<128, 2>(qmap, kvmap, p, stream);
+    return launch<128, 1>(qmap, kvmap, p, stream);
 }
 
 }  // namespace pa

@@ -82,6 +82,12 @@ def test_validation_without_gpu(lib):
                           NULL, NULL, NULL, NULL) == pa.PA_OK  # empty batch
     assert lib.pa_prefill(C.byref(g), NULL, NULL, NULL, 0, 1, NULL, NULL, 4, 4, C.c_float(float("nan")),
                           NULL, NULL, NULL, NULL) == pa.PA_ERR_INVALID_ARG
+    # the softmax scale must be positive (the row max is taken on unscaled scores)
+    for bad in (0.0, -0.125):
+        assert lib.pa_prefill(C.byref(g), NULL, NULL, NULL, 0, 1, NULL, NULL, 4, 4, C.c_float(bad),
+                              NULL, NULL, NULL, NULL) == pa.PA_ERR_INVALID_ARG
+        assert lib.pa_decode(C.byref(g), NULL, NULL, NULL, 0, 1, NULL, NULL, 4, C.c_float(bad), NULL, NULL,
+                             NULL, 0, NULL, NULL) == pa.PA_ERR_INVALID_ARG
     # decode: unsupported group size 3, too-small workspace
     g3 = pa.geom(6, 2, 64, 1, 1, 4, 8)
     assert lib.pa_decode(C.byref(g3), NULL, NULL, NULL, 0, 1, NULL, NULL, 4, C.c_float(0.1), NULL, NULL,
