@@ -25,21 +25,21 @@
 //    K-major (Q, K) / MN-major (V) operand layouts of the tensor core.  Pages
 //    past the sequence end are read at an out-of-range row, which the copy
 //    engine fills with zeros.
-//  * Warp 4T+1 (MMA issuer, the whole warp runs the loop and one elected lane
-//    issues): S_t = Q_t K^T (M 128, N 64, K 16 steps) into TMEM; after tile t's
-//    softmax hands back P_t, O_t += P_t V (M 128, N 64 per 64-dim chunk, K 16
-//    with P read from TMEM), then the next S_t.  The tiles take turns, so the
-//    tensor core works on the others while one tile's softmax runs.
+//  * Warps 4T+1 (and 4T+2 when T = 4) issue the MMAs; the whole warp runs the
+//    loop and one elected lane issues.  S_t = Q_t K^T (M 128, N 64, K 16
+//    steps) into TMEM; after tile t's softmax hands back P_t, O_t += P_t V (M
+//    128, N 64 per 64-dim chunk, K 16, P read from TMEM), then the next S_t.
+//    The tiles take turns, so the tensor core works on the others while one
+//    tile's softmax runs; with two issuing warps, tile t belongs to warp t % 2.
 //  * Warps 4t..4t+3 (softmax of tile t): thread r owns query row r, i.e. TMEM
-//    lane r, and all 64 scores of the key tile: it loads them into registers,
-//    takes the row max first, moves the reference max if the tile max exceeds
-//    it by more than 2^8 (l at once, its O row in TMEM in place -- no PV
-//    product is in flight then), and forms P = 2^(s*scale*log2e - m) with
-//    packed fp32 FMAs and the SFU exp2, packed to bf16 over the first half of
-//    the scores' own TMEM columns.  The epilogue divides by l, writes o (bf16)
-//    and L = ln2 (m + log2 l).  Exact: o = O / l uses the one reference.
-//  * TMEM: tile t owns 64 + d columns from t (64 + d): S (P over its first
-//    half), then O.
+//    lane r, and all 64 scores of the key tile.  It takes the row max first,
+//    moves the reference max if the tile max exceeds it by more than 2^8 (l at
+//    once, its O row in TMEM in place -- no PV product is in flight then), and
+//    forms P = 2^(s*scale*log2e - m) with packed fp32 FMAs and the SFU exp2,
+//    packed to bf16.  The epilogue divides by l, writes o (bf16) and
+//    L = ln2 (m + log2 l).  Exact: o = O / l uses the one reference.
+//  * TMEM: tile t owns 64 + d columns from t (64 + d): S (each 32-key half
+//    holds its P in its first 16 columns), then O.
 //  * A partial last page has its V rows past the sequence end zeroed in shared
 //    memory before the PV products (masked P is exactly 0, but 0 x NaN is not).
 #include <math_constants.h>
@@ -60,8 +60,9 @@ template <int D, int T>
 struct Cfg {
     static constexpr int KCH = D / 64;
     static constexpr int PRODUCER_WARP = 4 * T;
-    static constexpr int MMA_WARP = 4 * T + 1;
-    static constexpr int THREADS = 32 * (4 * T + 2);
+    static constexpr int MMA_WARPS = T >= 4 ? 2 : 1;  // tile t is issued by MMA warp t % MMA_WARPS
+    static constexpr int MMA_WARP = 4 * T + 1;        // the first one; it also owns the TMEM allocation
+    static constexpr int THREADS = 32 * (4 * T + 1 + MMA_WARPS);
     static constexpr int Q_BYTES = KCH * kQChunkBytes;  // one query tile
     static constexpr int K_BYTES = KCH * kKChunkBytes;
     static constexpr int STAGE_BYTES = 2 * K_BYTES;
@@ -75,8 +76,11 @@ struct Cfg {
     static_assert(NST >= 2, "two K/V stages at least");
     static __device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(TILE_COLS * t); }
     static __device__ __forceinline__ uint32_t o_col(int t) { return static_cast<uint32_t>(TILE_COLS * t + BN); }
-    // P columns of key step ks (16 keys) of tile t: over the first half of S
-    static __device__ __forceinline__ uint32_t p_col(int t, int ks) { return s_col(t) + 8u * ks; }
+    // P columns of key step ks (16 keys) of tile t: the 32 keys of each half of
+    // the tile put their P over the first 16 of their own score columns
+    static __device__ __forceinline__ uint32_t p_col(int t, int ks) {
+        return s_col(t) + 32u * (ks >> 1) + 8u * (ks & 1);
+    }
 };
 
 struct PrefillParams {
@@ -138,7 +142,9 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
     const int row = i * BM + r;  // query row within the sequence
     const int last_lp = (n + kBlockTokens - 1) / kBlockTokens - 1;
     const int tail_valid = n - last_lp * kBlockTokens;
-    const int j_tail = (t == 0 && tail_valid < kBlockTokens) ? last_lp / kPagesPerTile : -1;
+    // every tile zeroes the V tail itself before its P is handed over: the
+    // tiles' PV products are issued by different warps in no fixed order
+    const int j_tail = tail_valid < kBlockTokens ? last_lp / kPagesPerTile : -1;
     float m_o = -CUDART_INF_F, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
@@ -147,47 +153,52 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
             break;
         }
         tc_fence_after_sync();
-        // pass 1: the row max of the 64 scores, 32 at a time
+        // the row max of the 64 scores; the second half stays in registers
         const int rel = BN * j - BM * i;  // first key of the tile relative to the first row of the tile
         const bool diag = rel > -BN;      // the tile crosses the diagonal
+        uint32_t vb[32];
         float m_tile;
         {
-            uint32_t v[32];
-            tmem_ld_x32(tS, v);
-            if (diag) mask_chunk(v, rel, r);
-            m_tile = chunk_max(v, -CUDART_INF_F);
-            tmem_ld_x32(tS + 32, v);
-            if (diag) mask_chunk(v, rel + 32, r);
-            m_tile = sc * chunk_max(v, m_tile);
+            uint32_t va[32];
+            tmem_ld_x32(tS, va);
+            if (diag) mask_chunk(va, rel, r);
+            m_tile = chunk_max(va, -CUDART_INF_F);
         }
-        if (__any_sync(0xffffffffu, m_tile > m_o + kMoveAbove)) {
-            float f = 1.f;
-            if (m_tile > m_o + kMoveAbove) {
-                f = ex2_approx(m_o - m_tile);  // 0 from -inf
-                l *= f;
-                m_o = m_tile;
-            }
-            if (j > 0) {  // this row of O follows the reference (no PV product is in flight)
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld_x32(tO + 32 * c, ov);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-                    tmem_st_x32(tO + 32 * c, ov);
-                }
-            }
+        tmem_ld_x32(tS + 32, vb);
+        if (diag) mask_chunk(vb, rel + 32, r);
+        m_tile = sc * chunk_max(vb, m_tile);
+        float f = 1.f;  // factor for l and this row of O when the reference moves
+        if (m_tile > m_o + kMoveAbove) {
+            f = ex2_approx(m_o - m_tile);  // 0 from -inf
+            l *= f;
+            m_o = m_tile;
         }
         const float nm = m_o == -CUDART_INF_F ? 0.f : -m_o;
-        // pass 2: P, 32 scores at a time, over the scores already read
+        // P of the second half from registers, over its own first 16 columns;
+        // then the first half read again
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        {
+            uint32_t pk[16];
+            p_chunk(vb, sc, nm, ls, pk);
+            tmem_st_x16_nowait(tS + 32, pk);
+        }
+        if (j > 0 && __any_sync(0xffffffffu, f != 1.f)) {
+            // this row of O follows the reference (no PV product is in flight)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t v[32], pk[16];
-            tmem_ld_x32(tS + 32 * h, v);
-            if (diag) mask_chunk(v, rel + 32 * h, r);
-            p_chunk(v, sc, nm, ls, pk);
-            tmem_st_x16_nowait(tS + 16 * h, pk);  // keys 32h..32h+31 over the scores of keys 16h..16h+15
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld_x32(tO + 32 * c, ov);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+                tmem_st_x32(tO + 32 * c, ov);
+            }
+        }
+        {
+            uint32_t va[32], pk[16];
+            tmem_ld_x32(tS, va);
+            if (diag) mask_chunk(va, rel, r);
+            p_chunk(va, sc, nm, ls, pk);
+            tmem_st_x16_nowait(tS, pk);
         }
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         if (j == j_tail) {
@@ -257,7 +268,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint64_t* s_full = bars + 1 + 2 * C::NST;     // [T] scores of a tile in TMEM
     uint64_t* p_full = s_full + T;                // [T] P of a tile in TMEM
     uint64_t* o_done = s_full + 2 * T;            // [T] the last PV product of a tile done
-    uint64_t* mma_done = s_full + 3 * T;
+    uint64_t* mma_done = s_full + 3 * T;          // [MMA_WARPS]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 65);
 
@@ -293,14 +304,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         mbar_init(q_full, 1);
         for (int s = 0; s < C::NST; ++s) {
             mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&kv_empty[s], C::MMA_WARPS);
         }
         for (int t = 0; t < T; ++t) {
             mbar_init(&s_full[t], 1);
             mbar_init(&p_full[t], BM);
             mbar_init(&o_done[t], 1);
         }
-        mbar_init(mma_done, 1);
+        for (int m = 0; m < C::MMA_WARPS; ++m) mbar_init(&mma_done[m], 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -368,13 +379,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             for (int jj = issued > C::NST ? issued - C::NST : 0; jj < issued; ++jj)
                 mbar_drain(&kv_full[jj % C::NST], (jj / C::NST) & 1);
         }
-    } else if (warp == C::MMA_WARP) {
-        // ------------------------------------------------------------ MMA issuer
-        // Per key tile j, for each query tile in turn: once its P is in TMEM,
-        // O_t += P_t V_j, then S_t = Q_t K_{j+1}^T over the same columns (the
-        // tensor core runs the two in order, so PV has read P before QK
-        // overwrites it).  While tile t waits for its softmax, the products
-        // of the other tiles keep the tensor core busy.
+    } else if (warp >= C::MMA_WARP) {
+        // ------------------------------------------------------------ MMA issuers
+        // Per key tile j, for each of this warp's query tiles in turn: once its
+        // P is in TMEM, O_t += P_t V_j, then S_t = Q_t K_{j+1}^T over the same
+        // columns (the tensor core runs one thread's products in order, so PV
+        // has read P before QK overwrites it).  While tile t waits for its
+        // softmax, the products of the other tiles keep the tensor core busy.
+        // Two warps share the tiles so that the issue of one warp's products
+        // overlaps the other warp's waits; a K/V stage is released once both
+        // have committed their last product on it.
+        const int mw = warp - C::MMA_WARP;
         constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
         constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
         const uint32_t sq = smem_u32(sQ);
@@ -406,7 +421,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (ok) {
             tc_fence_after_sync();
 #pragma unroll
-            for (int t = 0; t < T; ++t) qk(t, 0);
+            for (int t = 0; t < T; ++t)
+                if (t % C::MMA_WARPS == mw) qk(t, 0);
         }
         for (int j = 0; ok && j < nkv; ++j) {
             const int st = j % C::NST;
@@ -414,15 +430,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const bool more = j + 1 < nkv;
 #pragma unroll
             for (int t = 0; t < T; ++t) {
+                if (t % C::MMA_WARPS != mw) continue;
                 if (!wait_all(&p_full[t], j & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 pv(t, st, j > 0);
-                if (t == T - 1) umma_commit_elect(&kv_empty[st]);
+                if (t + C::MMA_WARPS >= T) umma_commit_elect(&kv_empty[st]);  // this warp's last tile
                 if (more) {
-                    if (t == 0) {
+                    if (t < C::MMA_WARPS) {  // this warp's first tile
                         if (!wait_all(&kv_full[st1], ((j + 1) / C::NST) & 1)) {
                             ok = false;
                             break;
@@ -435,8 +452,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
             }
         }
-        umma_commit_elect(mma_done);  // every MMA of this CTA done before TMEM is freed
-        mbar_drain(mma_done, 0);
+        umma_commit_elect(&mma_done[mw]);  // every MMA of this warp done before TMEM is freed
+        mbar_drain(&mma_done[mw], 0);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
