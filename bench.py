@@ -79,6 +79,15 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def prefill_heads_per_cta(geom):
+    """q heads of one GQA group that one prefill CTA takes (the library's rule:
+    as many as tensor memory holds, 4 at d 64 and 2 at d 128)."""
+    group = geom.num_q_heads // geom.num_kv_heads
+    if geom.head_dim == 64 and group % 4 == 0:
+        return 4
+    return 2 if group % 2 == 0 else 1
+
+
 def profiled_traffic(kernel_tag):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources (else None)."""
@@ -447,7 +456,7 @@ def main():
         bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
                     "frac": achieved / bf16_peak, "traffic": profiled_traffic("prefill_" + args.variant),
-                    "kernel": "prefill_kernel<%d>" % step.geom.head_dim,
+                    "kernel": "prefill_kernel<%d, %d>" % (step.geom.head_dim, prefill_heads_per_cta(step.geom)),
                     "peak_source": "%s bf16_tflops (burst)" % peak_src,
                     "algorithmic_flops_per_launch": step.flops_prefill,
                     "avg_launch_ms": prefill_avg * 1e3}
