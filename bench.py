@@ -491,7 +491,7 @@ def main():
                   "kv_bytes_per_step": dstep.kv_bytes, "steps": dsteps,
                   "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
                                "frac": dec_gbs / hbm_peak, "traffic": profiled_traffic("decode_c5"),
-                               "kernel": "decode_attend_kernel<64,4> + decode_merge_kernel<64>",
+                               "kernel": "decode_attend_kernel<64> + decode_merge_kernel<64>",
                                "peak_source": "%s hbm_gbs" % peak_src,
                                "algorithmic_bytes_per_launch": dstep.kv_bytes,
                                "avg_launch_ms": dec_avg * 1e3}}

@@ -439,33 +439,35 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
 }
 
 // Merges the partial units of every split sequence; writes o = 0, lse = -inf
-// for empty sequences.  One CTA per (sequence, q head), 4 warps: the partials
-// of a sequence are spread over the warps (lanes over dims, loads of several
-// partials in flight), then the warps combine through shared memory.
+// for empty sequences.  One CTA per (sequence, 8 q heads), one warp per head:
+// the lanes first take one partial each for the max and the weights of the
+// LSE rule, then run over the dims while the partial rows stream in.
 // Launched as a programmatic dependent of the attend kernel: everything the
 // attend kernel writes is read only after griddepcontrol.wait.
-constexpr int kMergeThreads = 128;
+constexpr int kMergeHeadsPerCta = 8;
+constexpr int kMergeThreads = 32 * kMergeHeadsPerCta;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
     constexpr int PER = D / 32;  // dims per lane
-    __shared__ float red_m[kMergeThreads / 32];
-    __shared__ float red_s[kMergeThreads / 32];
-    __shared__ float red_o[kMergeThreads / 32][D];
     const KGeom& g = p.g;
-    const int b = blockIdx.x, hq = blockIdx.y;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hq = blockIdx.y * kMergeHeadsPerCta + warp;
     const int len = p.seq_lens[b];
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (hq >= g.hq) return;
+    const long long row = static_cast<long long>(b) * g.hq + hq;
     if (len <= 0) {
-        if (tid < D) p.o[(static_cast<long long>(b) * g.hq + hq) * D + tid] = __float2bfloat16_rn(0.f);
-        if (tid == 0 && p.lse) p.lse[static_cast<long long>(b) * g.hq + hq] = -CUDART_INF_F;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) p.o[row * D + lane * PER + e] = __float2bfloat16_rn(0.f);
+        if (lane == 0 && p.lse) p.lse[row] = -CUDART_INF_F;
         return;
     }
     const int2 meta = *reinterpret_cast<const int2*>(p.ws + p.ws_meta + 8ll * b);
     const long long G = p.attend_grid;
     if (meta.x < 0 || meta.y >= G || meta.x > meta.y) {  // attend kernel gave up early
-        if (tid == 0) set_error(p.err, PA_ERR_TIMEOUT);
+        if (lane == 0) set_error(p.err, PA_ERR_TIMEOUT);
         return;
     }
     if (meta.x == meta.y) return;  // one unit: the attend kernel wrote the result
@@ -475,70 +477,61 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     // CTAs of the attend grid whose page range is empty wrote nothing
     auto has_pages = [&](long long cc) { return range_start(cc, T, G) != range_start(cc + 1, T, G); };
 
-    // 1. max of the partial L
+    // 1. max of the partial L (lanes over partials)
     float M = -CUDART_INF_F;
-    for (long long cc = meta.x + tid; cc <= meta.y; cc += kMergeThreads)
+    for (long long cc = meta.x + lane; cc <= meta.y; cc += 32)
         if (has_pages(cc)) M = fmaxf(M, lse_part[(b + cc) * g.hq + hq]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (lane == 0) red_m[warp] = M;
-    __syncthreads();
-    M = red_m[0];
-#pragma unroll
-    for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red_m[w]);
 
-    // 2. weighted sums, partials spread over the warps
+    // 2. weighted sum (lanes over dims), 32 partials' weights at a time
     float acc[PER], S = 0.f;
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
     if (M != -CUDART_INF_F) {
-#pragma unroll 4
-        for (long long cc = meta.x + warp; cc <= meta.y; cc += kMergeThreads / 32) {
-            if (!has_pages(cc)) continue;
-            const long long slot = (b + cc) * g.hq + hq;
-            const float Lc = lse_part[slot];
-            float x[PER];
-            if (PER == 2) {
-                const float2 v = *reinterpret_cast<const float2*>(o_part + slot * D + lane * PER);
-                x[0] = v.x;
-                x[PER - 1] = v.y;
-            } else {
-                const float4 v = *reinterpret_cast<const float4*>(o_part + slot * D + lane * PER);
-                x[0] = v.x;
-                x[1 % PER] = v.y;
-                x[2 % PER] = v.z;
-                x[3 % PER] = v.w;
+        for (long long c0 = meta.x; c0 <= meta.y; c0 += 32) {
+            const long long mine = c0 + lane;
+            float w = 0.f;
+            if (mine <= meta.y && has_pages(mine)) {
+                const float Lc = lse_part[(b + mine) * g.hq + hq];
+                w = (Lc == -CUDART_INF_F) ? 0.f : ex2_approx((Lc - M) * kLog2e);
             }
-            const float w = (Lc == -CUDART_INF_F) ? 0.f : ex2_approx((Lc - M) * kLog2e);
             S += w;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+            const int n = static_cast<int>(min(32ll, meta.y - c0 + 1));
+#pragma unroll 4
+            for (int k = 0; k < n; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, w, k);
+                if (wk == 0.f) continue;
+                const float* src = o_part + ((b + c0 + k) * g.hq + hq) * D + lane * PER;
+                if (PER == 2) {
+                    const float2 v = *reinterpret_cast<const float2*>(src);
+                    acc[0] = fmaf(wk, v.x, acc[0]);
+                    acc[PER - 1] = fmaf(wk, v.y, acc[PER - 1]);
+                } else {
+                    const float4 v = *reinterpret_cast<const float4*>(src);
+                    acc[0] = fmaf(wk, v.x, acc[0]);
+                    acc[1 % PER] = fmaf(wk, v.y, acc[1 % PER]);
+                    acc[2 % PER] = fmaf(wk, v.z, acc[2 % PER]);
+                    acc[3 % PER] = fmaf(wk, v.w, acc[3 % PER]);
+                }
+            }
         }
     }
-    if (lane == 0) red_s[warp] = S;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) red_o[warp][lane * PER + e] = acc[e];
-    __syncthreads();
+    for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
 
-    // 3. combine the warps and write the row
-    float St = 0.f;
+    // 3. the row
+    const float inv = S > 0.f ? 1.f / S : 0.f;
 #pragma unroll
-    for (int w = 0; w < kMergeThreads / 32; ++w) St += red_s[w];
-    const float inv = St > 0.f ? 1.f / St : 0.f;
-    if (tid < D) {
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kMergeThreads / 32; ++w) v += red_o[w][tid];
-        p.o[(static_cast<long long>(b) * g.hq + hq) * D + tid] = __float2bfloat16_rn(v * inv);
-    }
-    if (tid == 0 && p.lse)
-        p.lse[static_cast<long long>(b) * g.hq + hq] = St > 0.f ? M + lg2_approx(St) * kLn2 : -CUDART_INF_F;
+    for (int e = 0; e < PER; ++e) p.o[row * D + lane * PER + e] = __float2bfloat16_rn(acc[e] * inv);
+    if (lane == 0 && p.lse) p.lse[row] = S > 0.f ? M + lg2_approx(S) * kLn2 : -CUDART_INF_F;
 }
 
 template <int D>
 cudaError_t launch_merge(const DecodeParams& p, int batch, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(batch), static_cast<unsigned>(p.g.hq), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(batch),
+                       static_cast<unsigned>((p.g.hq + kMergeHeadsPerCta - 1) / kMergeHeadsPerCta), 1);
     cfg.blockDim = dim3(kMergeThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
