@@ -57,6 +57,12 @@ def lib():
         L.orc_prefill_rows.restype = C.c_int
         L.orc_prefill_rows.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P,
                                        C.c_float, C.c_int64, _P, _P, _P, _P, C.c_int32]
+        L.orc_prefill_cached.restype = C.c_int
+        L.orc_prefill_cached.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, _P,
+                                         C.c_float, _P, _P, C.c_int32]
+        L.orc_prefill_cached_rows.restype = C.c_int
+        L.orc_prefill_cached_rows.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, _P,
+                                              C.c_float, C.c_int64, _P, _P, _P, _P, C.c_int32]
         L.orc_decode.restype = C.c_int
         L.orc_decode.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P,
                                  C.c_float, _P, _P, C.c_int32]
@@ -178,6 +184,39 @@ def prefill_rows(g, q, pool, block_table, layer, cu_seqlens, slots, scale, rows,
     st = lib().orc_prefill_rows(C.byref(g), _ptr(q), _ptr(pool), _ptr(_c(block_table, np.int32)),
                                 layer, cu.shape[0] - 1, _ptr(cu), _ptr(sl), C.c_float(scale), n,
                                 _ptr(rows), _ptr(heads), _ptr(o), _ptr(lse), nthreads)
+    return int(st), o, lse
+
+
+def prefill_cached(g, q, pool, block_table, layer, cu_seqlens, prefix_lens, slots, scale, nthreads=0):
+    """Chunked prefill over a cached prefix: (status, O[T][Hq][d], L[T][Hq])."""
+    cu = _c(cu_seqlens, np.int32)
+    pre = _c(prefix_lens, np.int32)
+    sl = _c(slots, np.int32)
+    T = int(cu[-1])
+    q = _c(q, np.uint16)
+    o = np.zeros((T, g.num_q_heads, g.head_dim), np.float64)
+    lse = np.zeros((T, g.num_q_heads), np.float64)
+    st = lib().orc_prefill_cached(C.byref(g), _ptr(q), _ptr(pool), _ptr(_c(block_table, np.int32)), layer,
+                                  cu.shape[0] - 1, _ptr(cu), _ptr(pre), _ptr(sl), C.c_float(scale), _ptr(o),
+                                  _ptr(lse), nthreads)
+    return int(st), o, lse
+
+
+def prefill_cached_rows(g, q, pool, block_table, layer, cu_seqlens, prefix_lens, slots, scale, rows, heads,
+                        nthreads=0):
+    """prefill_cached at sampled (packed row, q head) pairs: (status, O[n][d], L[n])."""
+    cu = _c(cu_seqlens, np.int32)
+    pre = _c(prefix_lens, np.int32)
+    sl = _c(slots, np.int32)
+    rows = _c(rows, np.int64)
+    heads = _c(heads, np.int32)
+    q = _c(q, np.uint16)
+    n = rows.shape[0]
+    o = np.zeros((n, g.head_dim), np.float64)
+    lse = np.zeros(n, np.float64)
+    st = lib().orc_prefill_cached_rows(C.byref(g), _ptr(q), _ptr(pool), _ptr(_c(block_table, np.int32)),
+                                       layer, cu.shape[0] - 1, _ptr(cu), _ptr(pre), _ptr(sl), C.c_float(scale),
+                                       n, _ptr(rows), _ptr(heads), _ptr(o), _ptr(lse), nthreads)
     return int(st), o, lse
 
 

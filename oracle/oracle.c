@@ -290,6 +290,7 @@ typedef struct {
     const orc_geom* g;
     const uint16_t* q;
     const int32_t* cu;
+    const int32_t* prefix; /* cached tokens before each sequence's queries (NULL: none) */
     double scale;
     double** K; /* per sequence gathered keys (NULL when not needed) */
     double** V;
@@ -308,18 +309,24 @@ static int32_t seq_of_row(const int32_t* cu, int32_t batch, int64_t row) {
     return -1;
 }
 
-/* One (packed row, q head) output. */
+/* One (packed row, q head) output.  The i-th query of sequence b sits at
+ * position prefix[b] + i of its sequence, after the prefix[b] cached tokens,
+ * and attends keys 0..prefix[b] + i: the causal rule of a fresh prompt, with
+ * the cache read up to and including the query's own token, whose K/V were
+ * written first [TV6 "논리 블록 → 물리 블록 → 바이트 주소"; TV3 "causalMask
+ * and online softmax"].  Without a prefix this is the fresh-prompt prefill. */
 static void prefill_one(const prefill_ctx* c, int64_t row, int32_t hq, double* scratch,
                         double* o, double* lse) {
     const orc_geom* g = c->g;
     const int32_t d = g->head_dim, hq_n = g->num_q_heads;
     const int32_t group = g->num_q_heads / g->num_kv_heads;
     int32_t b = seq_of_row(c->cu, c->batch, row);
+    int32_t pre = c->prefix ? c->prefix[b] : 0;
     int32_t n = c->cu[b + 1] - c->cu[b];
-    int32_t i = (int32_t)(row - c->cu[b]); /* position of this query in its sequence */
-    double* qv = scratch;                  /* d doubles, then n scores */
+    int32_t i = (int32_t)(row - c->cu[b]); /* index of this query among its sequence's queries */
+    double* qv = scratch;                  /* d doubles, then pre + n scores */
     for (int32_t k = 0; k < d; ++k) qv[k] = bf16_to_double(c->q[(row * hq_n + hq) * d + k]);
-    attend_row(g, qv, c->K[b], c->V[b], hq / group, n, i, c->scale, scratch + d, o, lse);
+    attend_row(g, qv, c->K[b], c->V[b], hq / group, pre + n, pre + i, c->scale, scratch + d, o, lse);
 }
 
 static void prefill_item(void* ctx, int64_t item, double* scratch) {
@@ -375,7 +382,7 @@ static void free_all(int32_t batch, double** K, double** V) {
 
 static int prefill_common(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
                           const int32_t* bt, int32_t layer, int32_t batch, const int32_t* cu,
-                          const int32_t* slots, float scale, int64_t nsamp,
+                          const int32_t* prefix, const int32_t* slots, float scale, int64_t nsamp,
                           const int64_t* rows, const int32_t* heads, double* o, double* lse,
                           int32_t nthreads) {
     if (!check_batch(g, batch, cu, slots, layer) || !pool || !bt || !o || !lse) return ORC_BAD_ARG;
@@ -390,11 +397,14 @@ static int prefill_common(const orc_geom* g, const uint16_t* q, const uint8_t* p
         return ORC_BAD_ARG;
     }
     int32_t nmax = 0;
+    int st = ORC_OK;
     for (int32_t b = 0; b < batch; ++b) {
-        lens[b] = cu[b + 1] - cu[b];
+        /* keys of sequence b: its cached prefix, then its queries' own tokens */
+        const int64_t nk = (int64_t)(prefix ? prefix[b] : 0) + (cu[b + 1] - cu[b]);
+        if ((prefix && prefix[b] < 0) || nk > 0x7FFFFFFF) st = ORC_BAD_ARG;
+        lens[b] = (int32_t)(nk > 0x7FFFFFFF ? 0 : nk);
         if (lens[b] > nmax) nmax = lens[b];
     }
-    int st = ORC_OK;
     if (rows) {
         for (int64_t s = 0; s < nsamp; ++s) {
             int32_t b = (rows[s] >= 0 && rows[s] < T) ? seq_of_row(cu, batch, rows[s]) : -1;
@@ -404,7 +414,7 @@ static int prefill_common(const orc_geom* g, const uint16_t* q, const uint8_t* p
     }
     if (st == ORC_OK) st = gather_all(g, pool, bt, layer, batch, lens, slots, rows ? need : NULL, K, V);
     if (st == ORC_OK) {
-        prefill_ctx c = {g, q, cu, (double)scale, K, V, batch, o, lse, rows, heads};
+        prefill_ctx c = {g, q, cu, prefix, (double)scale, K, V, batch, o, lse, rows, heads};
         if (rows)
             run_items(prefill_rows_item, &c, nsamp, (int64_t)g->head_dim + nmax, nthreads);
         else
@@ -420,8 +430,16 @@ int orc_prefill(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
                 const int32_t* block_table, int32_t layer, int32_t batch,
                 const int32_t* cu_seqlens, const int32_t* slots, float scale, double* o,
                 double* lse, int32_t nthreads) {
-    return prefill_common(g, q, pool, block_table, layer, batch, cu_seqlens, slots, scale, 0,
+    return prefill_common(g, q, pool, block_table, layer, batch, cu_seqlens, NULL, slots, scale, 0,
                           NULL, NULL, o, lse, nthreads);
+}
+
+int orc_prefill_cached(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                       const int32_t* block_table, int32_t layer, int32_t batch,
+                       const int32_t* cu_seqlens, const int32_t* prefix_lens, const int32_t* slots,
+                       float scale, double* o, double* lse, int32_t nthreads) {
+    return prefill_common(g, q, pool, block_table, layer, batch, cu_seqlens, prefix_lens, slots, scale,
+                          0, NULL, NULL, o, lse, nthreads);
 }
 
 int orc_prefill_rows(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
@@ -431,7 +449,18 @@ int orc_prefill_rows(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
                      double* lse, int32_t nthreads) {
     if (nsamp < 0 || (nsamp > 0 && (!rows || !heads))) return ORC_BAD_ARG;
     static const int64_t no_rows = 0;
-    return prefill_common(g, q, pool, block_table, layer, batch, cu_seqlens, slots, scale,
+    return prefill_common(g, q, pool, block_table, layer, batch, cu_seqlens, NULL, slots, scale,
+                          nsamp, rows ? rows : &no_rows, heads, o, lse, nthreads);
+}
+
+int orc_prefill_cached_rows(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                            const int32_t* block_table, int32_t layer, int32_t batch,
+                            const int32_t* cu_seqlens, const int32_t* prefix_lens,
+                            const int32_t* slots, float scale, int64_t nsamp, const int64_t* rows,
+                            const int32_t* heads, double* o, double* lse, int32_t nthreads) {
+    if (nsamp < 0 || (nsamp > 0 && (!rows || !heads))) return ORC_BAD_ARG;
+    static const int64_t no_rows = 0;
+    return prefill_common(g, q, pool, block_table, layer, batch, cu_seqlens, prefix_lens, slots, scale,
                           nsamp, rows ? rows : &no_rows, heads, o, lse, nthreads);
 }
 

@@ -103,6 +103,27 @@ int orc_prefill_rows(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
                      int64_t nsamp, const int64_t* rows, const int32_t* heads,
                      double* o, double* lse, int32_t nthreads);
 
+/* Causal prefill of query chunks over a cached prefix.  The cache of slots[b]
+ * already holds prefix_lens[b] tokens followed by the K/V of sequence b's
+ * queries (rows cu_seqlens[b] .. cu_seqlens[b+1]-1); the i-th of them sits at
+ * position prefix_lens[b] + i and attends keys 0..prefix_lens[b] + i (the
+ * decode's "length includes the token just written" rule applied to every
+ * query of the chunk [TV6 "논리 블록 → 물리 블록 → 바이트 주소"], with the
+ * prompt's causal mask inside the chunk [TV3 "causalMask and online
+ * softmax"]).  prefix_lens == NULL or all zero is orc_prefill; a chunk of one
+ * query at prefix seq_len - 1 is orc_decode.  Outputs as orc_prefill. */
+int orc_prefill_cached(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                       const int32_t* block_table, int32_t layer, int32_t batch,
+                       const int32_t* cu_seqlens, const int32_t* prefix_lens, const int32_t* slots,
+                       float scale, double* o, double* lse, int32_t nthreads);
+
+/* orc_prefill_cached at nsamp (row, q head) pairs, as orc_prefill_rows. */
+int orc_prefill_cached_rows(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                            const int32_t* block_table, int32_t layer, int32_t batch,
+                            const int32_t* cu_seqlens, const int32_t* prefix_lens,
+                            const int32_t* slots, float scale, int64_t nsamp, const int64_t* rows,
+                            const int32_t* heads, double* o, double* lse, int32_t nthreads);
+
 /* Single-query decode [TV6 "논리 블록 → 물리 블록 → 바이트 주소"]: query b
  * (q[B][Hq][d]) attends keys 0..seq_lens[b]-1 of slots[b]; the length
  * includes the token just written.  seq_len 0 gives O = 0, L = -inf.

@@ -222,6 +222,35 @@ def make_prefill_case(name, geom: Geometry, lens, seed: int, scale=None, layers=
                 pool_fill, seed)
 
 
+def make_chunked_case(name, geom: Geometry, prefix_lens, chunk_lens, seed: int, scale=None, layer=0,
+                      pool_fill="random", slots=None, shuffle_pages=True) -> Case:
+    """Prefill of query chunks over a cached prefix: sequence b already holds
+    prefix_lens[b] tokens (one write, as an earlier step left them) and then
+    scatters its chunk of chunk_lens[b] new tokens (a second write) before the
+    attention call; q holds the chunks' rows only.  extra["prefix"] = prefix_lens."""
+    rng = np.random.default_rng(seed)
+    pre = np.asarray(prefix_lens, np.int32)
+    lens = np.asarray(chunk_lens, np.int32)
+    B = lens.shape[0]
+    slots = np.arange(B, dtype=np.int32) if slots is None else np.asarray(slots, np.int32)
+    table = empty_table(geom)
+    free = FreeList(geom.num_blocks, rng, shuffle=shuffle_pages)
+    for b in range(B):
+        assign_pages(table, free, int(slots[b]), layer, int(pre[b] + lens[b]))
+    writes = []
+    for first, count in ((np.zeros(B, np.int32), pre), (pre, lens)):
+        T = int(np.sum(count))
+        tok_slot = np.repeat(slots, count).astype(np.int32)
+        tok_pos = (np.concatenate([np.arange(f, f + c, dtype=np.int32) for f, c in zip(first, count)])
+                   if T else np.zeros(0, np.int32))
+        writes.append(KVWrite(layer, tok_slot, tok_pos, normal_bf16(rng, (T, geom.kv_dim)),
+                              normal_bf16(rng, (T, geom.kv_dim))))
+    q = normal_bf16(rng, (int(lens.sum()), geom.num_q_heads, geom.head_dim))
+    scale = 1.0 / np.sqrt(geom.head_dim) if scale is None else scale
+    return Case(name, geom, float(scale), layer, slots, lens, table, writes, q, "chunked", pool_fill, seed,
+                extra={"prefix": pre})
+
+
 def make_decode_case(name, geom: Geometry, lens, seed: int, scale=None, layer=0,
                      pool_fill="random", slots=None, shuffle_pages=True,
                      split_last_write=True) -> Case:

@@ -10,12 +10,13 @@ import subprocess
 import pytest
 
 import oracle
+from tests import test_oracle_chunked_pins as cpins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "oracle.c")
 
 MUTANTS = {
-    "gqa_map_modulo": ("hq / group, n, i", "hq % g->num_kv_heads, n, i"),
+    "gqa_map_modulo": ("hq / group, pre + n, pre + i", "hq % g->num_kv_heads, pre + n, pre + i"),
     "causal_off_by_one": ("if (j > last_key) {", "if (j >= last_key && j > 0) {"),
     "log2_lse": ("*lse = m + log(l);", "*lse = m + log2(l);"),
     "token_stride_head_dim": ("token_in_block * kv_dim(g) * 2 +\n", "token_in_block * g->head_dim * 2 +\n"),
@@ -26,6 +27,9 @@ MUTANTS = {
     "merge_without_rescale": ("ls += l[i] * c;", "ls += l[i];"),
     "normaliser_off": ("o[k] = acc / l;", "o[k] = acc / (l + 1e-3);"),
     "write_v_at_k": ("uint8_t* v_dst = k_dst + v_offset(g);", "uint8_t* v_dst = k_dst + v_offset(g) + 2;"),
+    "prefix_ignored": ("int32_t pre = c->prefix ? c->prefix[b] : 0;", "int32_t pre = 0;"),
+    "prefix_last_key_off_by_one": ("pre + n, pre + i, c->scale", "pre + n, pre + i - 1, c->scale"),
+    "prefix_not_in_position": ("pre + n, pre + i, c->scale", "pre + n, i, c->scale"),
     "max_not_subtracted": ("for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m);",
                            "for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m) * (1 + 1e-9 * m);"),
 }
@@ -42,6 +46,8 @@ PIN_TESTS = [
     lambda gd: pins.test_lse_split_merge_identity(),
     lambda gd: pins.test_prefill_matches_library_sdpa(8, 2, 64, [40]),
     lambda gd: pins.test_decode_matches_library_sdpa(),
+    lambda gd: cpins.test_chunked_matches_library_sdpa(8, 2, 64, [0, 16, 23], [40, 17, 1]),
+    lambda gd: cpins.test_chunk_of_one_is_decode(),
 ]
 
 
