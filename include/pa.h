@@ -140,6 +140,32 @@ pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool,
                      int32_t* err_flag, pa_stream_t stream);
 
 /*
+ * pa_prefill_cached -- causal prefill of query chunks over a cached prefix
+ * (chunked prefill).
+ * Definition: the cache of (slots[b], layer) already holds prefix_lens[b]
+ * tokens followed by the K/V of sequence b's n_b = cu_seqlens[b+1] -
+ * cu_seqlens[b] new tokens (written with pa_write_kv before this call); the
+ * i-th query row of sequence b sits at position prefix_lens[b] + i and
+ * attends keys 0..prefix_lens[b] + i, with the scores, softmax, o and lse of
+ * pa_prefill.  This is the decode's rule that a query reads the cache up to
+ * and including its own token (tiny-vllm part 6, "논리 블록 → 물리 블록 →
+ * 바이트 주소") applied to every query of the chunk, with the prompt's causal
+ * mask inside the chunk (part 3, "causalMask and online softmax").
+ * prefix_lens == NULL means all zero (pa_prefill); a chunk of one query at
+ * prefix seq_len - 1 is pa_decode's result for that sequence.
+ * Arguments: as pa_prefill, plus prefix_lens: device int32 [batch] or NULL,
+ * each >= 0 with prefix_lens[b] + n_b <= 16 * max_blocks_per_seq (larger or
+ * negative values set PA_ERR_BAD_BLOCK and leave that sequence's output
+ * unspecified).  max_seqlen bounds the chunk lengths n_b only.
+ */
+pa_status pa_prefill_cached(const pa_geom* geom, const void* q, const void* pool,
+                            const int32_t* block_table, int32_t layer, int32_t batch,
+                            const int32_t* cu_seqlens, const int32_t* prefix_lens,
+                            const int32_t* slots, int32_t max_seqlen, int32_t total_tokens,
+                            float scale, void* o, float* lse, int32_t* err_flag,
+                            pa_stream_t stream);
+
+/*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
  * up to `batch` sequences of up to `max_seq_len` tokens.  Depends only on the
  * geometry and these two numbers (not on the device).  0 for invalid input.

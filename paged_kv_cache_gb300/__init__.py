@@ -10,6 +10,7 @@ Calls (same names as the C ABI):
 
 * ``pa_write_kv(geom, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new, err_flag)``
 * ``pa_prefill(geom, q, pool, block_table, layer, cu_seqlens, slots, max_seqlen, scale, o, lse, err_flag)``
+* ``pa_prefill_cached(geom, q, pool, block_table, layer, cu_seqlens, prefix_lens, slots, max_seqlen, scale, o, lse, err_flag)``
 * ``pa_decode(geom, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse, workspace, err_flag)``
 * ``pa_decode_noalloc(geom, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse, err_flag)``
 * ``pa_decode_workspace_size(geom, batch, max_seq_len)``, ``pa_page_bytes(geom)``, ``pa_status_string(code)``
@@ -30,7 +31,7 @@ PA_BLOCK_TOKENS = 16
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libpa.so")
-EXPORTED = ("pa_page_bytes", "pa_write_kv", "pa_prefill", "pa_decode_workspace_size", "pa_decode",
+EXPORTED = ("pa_page_bytes", "pa_write_kv", "pa_prefill", "pa_prefill_cached", "pa_decode_workspace_size", "pa_decode",
             "pa_decode_noalloc", "pa_status_string")
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -75,6 +76,9 @@ def load_library(path: str = None):
     L.pa_prefill.restype = C.c_int
     L.pa_prefill.argtypes = [C.POINTER(PaGeom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, C.c_int32,
                              C.c_int32, C.c_float, _P, _P, _P, _P]
+    L.pa_prefill_cached.restype = C.c_int
+    L.pa_prefill_cached.argtypes = [C.POINTER(PaGeom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, _P, C.c_int32,
+                                    C.c_int32, C.c_float, _P, _P, _P, _P]
     L.pa_decode_workspace_size.restype = C.c_size_t
     L.pa_decode_workspace_size.argtypes = [C.POINTER(PaGeom), C.c_int32, C.c_int32]
     L.pa_decode.restype = C.c_int
@@ -149,6 +153,17 @@ def pa_prefill(g, q, pool, block_table, layer, cu_seqlens, slots, max_seqlen, sc
         C.byref(g), _ptr(q), _ptr(pool), _ptr(block_table), layer, batch, _ptr(cu_seqlens),
         _ptr(slots), int(max_seqlen), total, float(scale), _ptr(o), _ptr(lse), _ptr(err_flag),
         _stream(stream)))
+
+
+def pa_prefill_cached(g, q, pool, block_table, layer, cu_seqlens, prefix_lens, slots, max_seqlen, scale, o, lse,
+                      err_flag, stream=None, batch=None, total_tokens=None):
+    """Prefill of query chunks after prefix_lens[b] cached tokens (None: no prefix)."""
+    batch = int(cu_seqlens.shape[0]) - 1 if batch is None else int(batch)
+    total = int(q.shape[0]) if total_tokens is None else int(total_tokens)
+    _check("pa_prefill_cached", lib().pa_prefill_cached(
+        C.byref(g), _ptr(q), _ptr(pool), _ptr(block_table), layer, batch, _ptr(cu_seqlens),
+        _ptr(prefix_lens), _ptr(slots), int(max_seqlen), total, float(scale), _ptr(o), _ptr(lse),
+        _ptr(err_flag), _stream(stream)))
 
 
 def pa_decode(g, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse,

@@ -75,11 +75,12 @@ PA_API pa_status pa_write_kv(const pa_geom* geom, void* pool, const int32_t* blo
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
-PA_API pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool,
-                            const int32_t* block_table, int32_t layer, int32_t batch,
-                            const int32_t* cu_seqlens, const int32_t* slots, int32_t max_seqlen,
-                            int32_t total_tokens, float scale, void* o, float* lse,
-                            int32_t* err_flag, pa_stream_t stream) {
+PA_API pa_status pa_prefill_cached(const pa_geom* geom, const void* q, const void* pool,
+                                   const int32_t* block_table, int32_t layer, int32_t batch,
+                                   const int32_t* cu_seqlens, const int32_t* prefix_lens,
+                                   const int32_t* slots, int32_t max_seqlen, int32_t total_tokens,
+                                   float scale, void* o, float* lse, int32_t* err_flag,
+                                   pa_stream_t stream) {
     if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
     if (layer < 0 || layer >= geom->n_layers) return PA_ERR_INVALID_ARG;
     if (batch < 0 || max_seqlen < 0 || total_tokens < 0 || !std::isfinite(scale) || !(scale > 0.f))
@@ -93,8 +94,17 @@ PA_API pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool
     // TMA coordinates are int32: pool rows (32 per page) and q rows must fit.
     if (g.nblocks * 32 >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     return cuda_status(pa::launch_prefill(g, q, pool, block_table, layer, batch, cu_seqlens,
-                                          slots, max_seqlen, total_tokens, scale, o, lse,
-                                          err_flag, reinterpret_cast<cudaStream_t>(stream)));
+                                          prefix_lens, slots, max_seqlen, total_tokens, scale, o,
+                                          lse, err_flag, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+PA_API pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool,
+                            const int32_t* block_table, int32_t layer, int32_t batch,
+                            const int32_t* cu_seqlens, const int32_t* slots, int32_t max_seqlen,
+                            int32_t total_tokens, float scale, void* o, float* lse,
+                            int32_t* err_flag, pa_stream_t stream) {
+    return pa_prefill_cached(geom, q, pool, block_table, layer, batch, cu_seqlens, nullptr, slots,
+                             max_seqlen, total_tokens, scale, o, lse, err_flag, stream);
 }
 
 PA_API size_t pa_decode_workspace_size(const pa_geom* geom, int32_t batch, int32_t max_seq_len) {

@@ -518,9 +518,9 @@ cudaError_t launch_write_kv(const KGeom& g, void* pool, const int32_t* block_tab
 
 cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool,
                            const int32_t* block_table, int layer, int batch,
-                           const int32_t* cu_seqlens, const int32_t* slots, int max_seqlen,
-                           int total_tokens, float scale, void* o, float* lse, int32_t* err,
-                           cudaStream_t stream);
+                           const int32_t* cu_seqlens, const int32_t* prefix_lens,
+                           const int32_t* slots, int max_seqlen, int total_tokens, float scale,
+                           void* o, float* lse, int32_t* err, cudaStream_t stream);
 
 size_t decode_workspace_bytes(const KGeom& g, int batch, int max_seq_len);
 bool decode_supported(const KGeom& g);

@@ -89,6 +89,7 @@ struct PrefillParams {
     int layer;
     int batch;
     const int32_t* cu;
+    const int32_t* prefix;  // cached tokens before each sequence's queries, or null
     const int32_t* slots;
     int max_seqlen;
     int total_tokens;
@@ -131,7 +132,8 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], float m) {
 
 // Softmax of query tile t: the warp's thread owns row r (TMEM lane r).
 template <int D, int T>
-__device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, int i, int nkv, int n, int cu0, int hq,
+__device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, int i, int nkv, int n, int pos0,
+                                             int kv_len, int cu0, int hq,
                                              uint8_t* sKV, uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
                                              uint64_t* kv_full, volatile int* abort_flag, const PrefillParams& p) {
     using C = Cfg<D, T>;
@@ -139,9 +141,9 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
     const float sc = p.scale_log2;
     const uint32_t tS = tmem_lane + C::s_col(t);
     const uint32_t tO = tmem_lane + C::o_col(t);
-    const int row = i * BM + r;  // query row within the sequence
-    const int last_lp = (n + kBlockTokens - 1) / kBlockTokens - 1;
-    const int tail_valid = n - last_lp * kBlockTokens;
+    const int row = i * BM + r;  // query row within the chunk; its position is pos0 + r
+    const int last_lp = (kv_len + kBlockTokens - 1) / kBlockTokens - 1;
+    const int tail_valid = kv_len - last_lp * kBlockTokens;
     // every tile zeroes the V tail itself before its P is handed over: the
     // tiles' PV products are issued by different warps in no fixed order
     const int j_tail = tail_valid < kBlockTokens ? last_lp / kPagesPerTile : -1;
@@ -154,7 +156,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
         }
         tc_fence_after_sync();
         // the row max of the 64 scores; the second half stays in registers
-        const int rel = BN * j - BM * i;  // first key of the tile relative to the first row of the tile
+        const int rel = BN * j - pos0;  // first key of the tile relative to the first row's position
         const bool diag = rel > -BN;      // the tile crosses the diagonal
         uint32_t vb[32];
         float m_tile;
@@ -288,16 +290,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int hq0 = hk * g.group + (u % qgroups) * T;
     const int cu0 = p.cu[b], cu1 = p.cu[b + 1];
     const int n = cu1 - cu0;
-    const bool bad_len = cu0 < 0 || n < 0 || cu1 > p.total_tokens || n > p.max_seqlen;
+    const int pre = p.prefix ? p.prefix[b] : 0;
+    const bool bad_len = cu0 < 0 || n < 0 || cu1 > p.total_tokens || n > p.max_seqlen || pre < 0 ||
+                         static_cast<long long>(pre) + n > static_cast<long long>(g.maxb) * kBlockTokens;
     if (i == 0 && u == 0 && tid == 0 && bad_len) set_error(p.err, PA_ERR_BAD_BLOCK);
-    if (cu0 < 0 || n <= 0 || cu1 > p.total_tokens) return;
+    if (bad_len || n <= 0) return;
     if (i * BM >= n) return;
     const int slot = p.slots[b];
     const bool slot_ok = slot >= 0 && slot < g.num_slots;
     if (!slot_ok && tid == 0) set_error(p.err, PA_ERR_BAD_BLOCK);
-    // causal: key tiles up to the one holding key BM (i + 1) - 1, and none past the sequence
-    const int nkv = min(2 * i + 2, (n + BN - 1) / BN);
-    const int pages_b = (n + kBlockTokens - 1) / kBlockTokens;
+    // causal: key tiles up to the one holding the last row's key pre + BM (i + 1) - 1,
+    // and none past the cached sequence
+    const int kv_len = pre + n;
+    const int nkv = min((pre + BM * (i + 1) + BN - 1) / BN, (kv_len + BN - 1) / BN);
+    const int pages_b = (kv_len + kBlockTokens - 1) / kBlockTokens;
     const long long tbase = (static_cast<long long>(slot_ok ? slot : 0) * g.n_layers + p.layer) * g.maxb;
 
     if (tid == 0) {
@@ -459,7 +465,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // ------------------------------------------------------------ softmax
         const int t = warp >> 2;
         const int r = (warp & 3) * 32 + lane;  // query row = TMEM lane
-        softmax_role<D, T>(t, r, tmem + tmem_lane_base(warp), i, nkv, n, cu0, hq0 + t, sKV, &s_full[t], &p_full[t],
+        softmax_role<D, T>(t, r, tmem + tmem_lane_base(warp), i, nkv, n, pre + BM * i, kv_len, cu0, hq0 + t, sKV,
+                           &s_full[t], &p_full[t],
                            &o_done[t], kv_full, abort_flag, p);
     }
 
@@ -518,8 +525,9 @@ cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, const Pref
 }  // namespace
 
 cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, const int32_t* block_table, int layer,
-                           int batch, const int32_t* cu_seqlens, const int32_t* slots, int max_seqlen,
-                           int total_tokens, float scale, void* o, float* lse, int32_t* err, cudaStream_t stream) {
+                           int batch, const int32_t* cu_seqlens, const int32_t* prefix_lens, const int32_t* slots,
+                           int max_seqlen, int total_tokens, float scale, void* o, float* lse, int32_t* err,
+                           cudaStream_t stream) {
     CUtensorMap qmap, kvmap;
     if (!encode_2d(&qmap, q, static_cast<unsigned long long>(g.hq) * g.d, static_cast<unsigned long long>(total_tokens),
                    static_cast<unsigned long long>(g.hq) * g.d * 2, BM))
@@ -534,6 +542,7 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, cons
     p.layer = layer;
     p.batch = batch;
     p.cu = cu_seqlens;
+    p.prefix = prefix_lens;
     p.slots = slots;
     p.max_seqlen = max_seqlen;
     p.total_tokens = total_tokens;

@@ -33,6 +33,18 @@ def oracle_prefill(case, pool):
     return o, lse
 
 
+def oracle_prefill_cached(case, pool, rows=None, heads=None):
+    g = oracle_geom(case)
+    if rows is None:
+        st, o, lse = oracle.prefill_cached(g, case.q, pool, case.block_table, case.layer, case.cu_seqlens,
+                                           case.extra["prefix"], case.slots, case.scale)
+    else:
+        st, o, lse = oracle.prefill_cached_rows(g, case.q, pool, case.block_table, case.layer, case.cu_seqlens,
+                                                case.extra["prefix"], case.slots, case.scale, rows, heads)
+    assert st == 0
+    return o, lse
+
+
 def oracle_decode(case, pool):
     st, o, lse = oracle.decode(oracle_geom(case), case.q, pool, case.block_table, case.layer,
                                case.lens, case.slots, case.scale)
@@ -107,6 +119,26 @@ def gpu_prefill(case, pool, bt, q=None, o=None, with_lse=True):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pa.pa_prefill(g, q, pool, bt, case.layer, to_dev(case.cu_seqlens), to_dev(case.slots),
                   case.max_len, case.scale, o, lse, err)
+    torch.cuda.synchronize()
+    o_np = f32(o.cpu().numpy().view(np.uint16))
+    l_np = lse.cpu().numpy().astype(np.float64) if with_lse else None
+    return o_np, l_np, int(err.item())
+
+
+def gpu_prefill_cached(case, pool, bt, prefix=None, with_lse=True):
+    """pa_prefill_cached of a chunked case; prefix=None passes the case's
+    prefix lengths, prefix="null" passes a null pointer."""
+    torch = torch_mod()
+    g = pa_geom(case)
+    q = to_dev(case.q)
+    T = case.total_tokens
+    o = torch.empty((T, case.geom.num_q_heads, case.geom.head_dim), dtype=torch.int16, device="cuda")
+    lse = torch.empty((T, case.geom.num_q_heads), dtype=torch.float32, device="cuda") if with_lse else None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pre = None if (isinstance(prefix, str) and prefix == "null") else to_dev(
+        case.extra["prefix"] if prefix is None else np.asarray(prefix, np.int32))
+    pa.pa_prefill_cached(g, q, pool, bt, case.layer, to_dev(case.cu_seqlens), pre, to_dev(case.slots),
+                         case.max_len, case.scale, o, lse, err)
     torch.cuda.synchronize()
     o_np = f32(o.cpu().numpy().view(np.uint16))
     l_np = lse.cpu().numpy().astype(np.float64) if with_lse else None
