@@ -13,6 +13,8 @@ decode's 4 d Hq n).  The line also carries:
   decode       -- decode KV-read GB/s on the large mixed-length batch (256
                   sequences, log-normal lengths, new-token write + decode per
                   step) against the measured HBM copy bandwidth;
+  chunked      -- pa_prefill_cached: 4 x 2048-query chunks after 6144 cached
+                  tokens, exact-causal TFLOP/s against the same bf16 peak;
   e2e          -- the same metric through the C ABI with host buffers: pinned
                   H2D of the step's inputs and D2H of its outputs inside the
                   timed region;
@@ -52,7 +54,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time (10-30 s)")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "chunked"], default="all",
                     help="profiling aid: run only the main (prefill) step or only the decode step")
     ap.add_argument("--batch", type=int, default=4, help="prefill sequences (profiling aid)")
     ap.add_argument("--seqlen", type=int, default=8192, help="prefill length (profiling aid)")
@@ -219,6 +221,46 @@ class PrefillStep:
                        self.err)
         pa.pa_decode(self.g, d["dec_q"], self.pool, d["bt"], 0, d["dec_lens"], d["slots"], self.n + 1,
                      c.scale, self.dec_o, self.dec_lse, self.ws, self.err)
+
+
+class ChunkedStep:
+    """Prefill of query chunks over a cached prefix: 4 sequences, each a
+    2048-query chunk after 6144 cached tokens (the last quarter of the long
+    prompt of the main step), 32 q / 8 kv heads, d 64.  A step = scatter of
+    the chunks' K/V + pa_prefill_cached; the prefix is written once."""
+
+    def __init__(self, torch, pa, W, seed=1006, batch=4, prefix=6144, chunk=2048):
+        self.torch, self.pa = torch, pa
+        pages = (prefix + chunk) // 16
+        geom = W.Geometry(32, 8, 64, 1, batch, pages, batch * pages + 64)
+        self.case = W.make_chunked_case("chunk", geom, [prefix] * batch, [chunk] * batch, seed)
+        c = self.case
+        self.geom, self.g = geom, pa.geom(*geom.as_tuple())
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        w_pre, w_chunk = c.writes
+        self.d = {"q": dev(c.q), "bt": dev(c.block_table), "cu": dev(c.cu_seqlens), "pre": dev(c.extra["prefix"]),
+                  "slots": dev(c.slots), "tok_slot": dev(w_chunk.tok_slot), "tok_pos": dev(w_chunk.tok_pos),
+                  "k": dev(w_chunk.k), "v": dev(w_chunk.v)}
+        self.pool = torch.empty(geom.pool_bytes, dtype=torch.uint8, device="cuda")
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pa.pa_write_kv(self.g, self.pool, self.d["bt"], 0, dev(w_pre.tok_slot), dev(w_pre.tok_pos), dev(w_pre.k),
+                       dev(w_pre.v), self.err)
+        T, Hq, D = c.total_tokens, geom.num_q_heads, geom.head_dim
+        self.o = torch.empty((T, Hq, D), dtype=torch.int16, device="cuda")
+        self.lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+        self.chunk = chunk
+        # exact causal count: query i of a chunk sees prefix + i + 1 keys
+        self.flops = float(batch * 4.0 * D * Hq * (chunk * prefix + chunk * (chunk + 1) / 2))
+
+    def run(self, ev=None):
+        pa, c, d = self.pa, self.case, self.d
+        pa.pa_write_kv(self.g, self.pool, d["bt"], 0, d["tok_slot"], d["tok_pos"], d["k"], d["v"], self.err)
+        if ev is not None:
+            ev[0].record()
+        pa.pa_prefill_cached(self.g, d["q"], self.pool, d["bt"], 0, d["cu"], d["pre"], d["slots"], self.chunk,
+                             c.scale, self.o, self.lse, self.err)
+        if ev is not None:
+            ev[1].record()
 
 
 class DecodeStep:
@@ -496,6 +538,30 @@ def main():
                                "algorithmic_bytes_per_launch": dstep.kv_bytes,
                                "avg_launch_ms": dec_avg * 1e3}}
         del dstep
+
+    chunked = None
+    if args.only in ("all", "chunked"):
+        # ------------------------------- prefill of chunks over a cached prefix
+        cstep = ChunkedStep(torch, pa, W)
+        csteps = max(20, args.steps // 2)
+        cstep_s, ck_s = timed(torch, lambda ev: cstep.run(ev=ev), csteps, args.warmup, flush, dist)
+        torch.cuda.synchronize()
+        if int(cstep.err.item()) != 0:
+            raise SystemExit("device error in chunked steps: %s" % pa.pa_status_string(int(cstep.err.item())))
+        c_avg = float(np.mean(ck_s))
+        c_rate, c_total, _ = job_rate(torch, dist, cstep.flops * csteps, float(np.sum(cstep_s)))
+        bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        c_ach = cstep.flops / c_avg / 1e12
+        chunked = {"metric": "chunked prefill TFLOP/s (4 x 2048-query chunks after 6144 cached tokens, "
+                             "exact causal count, step incl. the chunks' KV write)",
+                   "value": c_rate / 1e12, "unit": "TFLOP/s", "ms_per_step": c_total / csteps * 1e3,
+                   "steps": csteps,
+                   "roofline": {"bound": "tensor", "achieved": c_ach, "peak": bf16_peak, "unit": "TFLOP/s",
+                                "frac": c_ach / bf16_peak, "traffic": profiled_traffic("chunked_d64"),
+                                "kernel": "prefill_kernel<64, 4> (prefix)",
+                                "peak_source": "%s bf16_tflops (burst)" % peak_src,
+                                "algorithmic_flops_per_launch": cstep.flops, "avg_launch_ms": c_avg * 1e3}}
+        del cstep
     clk = clocks.stop()
 
     if step is not None and not args.no_e2e:
@@ -532,7 +598,8 @@ def main():
                "sample": desc, "seconds": wall}
 
     if rank == 0 and step is None:
-        print(json.dumps({"metric": "decode only (profiling aid)", "decode": decode, "clocks": clk}), flush=True)
+        print(json.dumps({"metric": "%s only (profiling aid)" % args.only, "decode": decode, "chunked": chunked,
+                          "clocks": clk}), flush=True)
     elif rank == 0:
         line = {
             "metric": "causal prefill TFLOP/s (exact causal count, step incl. KV write + decode)",
@@ -549,6 +616,7 @@ def main():
             "gpu_launches": step.launches * args.steps,
             "roofline": roofline,
             "decode": decode,
+            "chunked": chunked,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,
