@@ -43,6 +43,9 @@ def lib():
         L = C.CDLL(path)
         L.orc_write_kv.restype = C.c_int64
         L.orc_write_kv.argtypes = [C.POINTER(Geom), _P, _P, C.c_int32, C.c_int64, _P, _P, _P, _P]
+        L.orc_write_kv_rope.restype = C.c_int64
+        L.orc_write_kv_rope.argtypes = [C.POINTER(Geom), _P, _P, C.c_int32, C.c_int64, _P, _P, _P, _P, _P, _P,
+                                        C.c_int32]
         L.orc_gather_kv.restype = C.c_int
         L.orc_gather_kv.argtypes = [C.POINTER(Geom), _P, _P, C.c_int32, C.c_int32, C.c_int32, _P, _P]
         L.orc_softmax_row.restype = None
@@ -116,6 +119,19 @@ def write_kv(g, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new):
     n = ts.shape[0]
     r = lib().orc_write_kv(C.byref(g), _ptr(pool), _ptr(bt), layer, n, _ptr(ts), _ptr(tp),
                            _ptr(k), _ptr(v))
+    return int(r)
+
+
+def write_kv_rope(g, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new, cos_tab, sin_tab):
+    """Scatter with K rotated by RoPE (tables [max_pos][d/2] fp32); returns skipped-row count."""
+    assert pool.dtype == np.uint8 and pool.flags.c_contiguous
+    bt = _c(block_table, np.int32)
+    ts, tp = _c(tok_slot, np.int32), _c(tok_pos, np.int32)
+    k, v = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    ct, st = _c(cos_tab, np.float32), _c(sin_tab, np.float32)
+    n = ts.shape[0]
+    r = lib().orc_write_kv_rope(C.byref(g), _ptr(pool), _ptr(bt), layer, n, _ptr(ts), _ptr(tp),
+                                _ptr(k), _ptr(v), _ptr(ct), _ptr(st), int(ct.shape[0]))
     return int(r)
 
 

@@ -25,7 +25,7 @@ def build(force: bool = False) -> str:
     if force or needs_build():
         os.makedirs(OUT_DIR, exist_ok=True)
         tmp = LIB + ".tmp%d" % os.getpid()
-        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
                "-Wall", "-Wextra", "-o", tmp, SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, LIB)

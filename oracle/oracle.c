@@ -106,6 +106,79 @@ int64_t orc_write_kv(const orc_geom* g, uint8_t* pool, const int32_t* block_tabl
     return skipped;
 }
 
+/* bf16 bits of a float, round to nearest even (NaN stays a quiet NaN). */
+static uint16_t float_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x0040u);
+    const uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+static float bf16_to_float(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* RoPE of one K row [TV3 "RoPE: a rotation that references a table"]: in each
+ * kv head, element i and element i + d/2 form a pair rotated by the angle of
+ * the token's position, read from caller tables cos/sin[pos][d/2]:
+ *   x1' = x1 c - x2 s,   x2' = x1 s + x2 c,
+ * in fp32 with every product and sum rounded on its own (this file is built
+ * as ISO C, so nothing is contracted into an FMA), then rounded to bf16. */
+static void rope_row(const orc_geom* g, const uint16_t* k, const float* cos_row, const float* sin_row,
+                     uint16_t* out) {
+    const int32_t d = g->head_dim, half = d / 2;
+    for (int32_t h = 0; h < g->num_kv_heads; ++h) {
+        const uint16_t* x = k + (int64_t)h * d;
+        uint16_t* y = out + (int64_t)h * d;
+        for (int32_t i = 0; i < half; ++i) {
+            const float x1 = bf16_to_float(x[i]), x2 = bf16_to_float(x[i + half]);
+            const float c = cos_row[i], s = sin_row[i];
+            const float a = x1 * c, b = x2 * s, e = x1 * s, f = x2 * c;
+            const float y1 = a - b, y2 = e + f;
+            y[i] = float_to_bf16(y1);
+            y[i + half] = float_to_bf16(y2);
+        }
+    }
+}
+
+/* orc_write_kv with K rotated by RoPE at each row's position; V is copied.
+ * Rows with a position >= max_pos are skipped like invalid table entries. */
+int64_t orc_write_kv_rope(const orc_geom* g, uint8_t* pool, const int32_t* block_table,
+                          int32_t layer, int64_t n_tokens, const int32_t* tok_slot,
+                          const int32_t* tok_pos, const uint16_t* k_new, const uint16_t* v_new,
+                          const float* cos_tab, const float* sin_tab, int32_t max_pos) {
+    if (!geom_ok(g) || n_tokens < 0 || max_pos < 0 || (g->head_dim & 1)) return ORC_BAD_ARG;
+    if (n_tokens == 0) return 0;
+    if (!pool || !block_table || !tok_slot || !tok_pos || !k_new || !v_new || !cos_tab || !sin_tab)
+        return ORC_BAD_ARG;
+    const int64_t row_bytes = kv_dim(g) * 2;
+    const int32_t half = g->head_dim / 2;
+    uint16_t* rot = (uint16_t*)malloc((size_t)row_bytes);
+    if (!rot) return ORC_BAD_ARG;
+    int64_t skipped = 0;
+    for (int64_t t = 0; t < n_tokens; ++t) {
+        int64_t blk = block_of(g, block_table, tok_slot[t], layer, tok_pos[t]);
+        if (blk < 0 || tok_pos[t] >= max_pos) {
+            ++skipped;
+            continue;
+        }
+        rope_row(g, k_new + t * kv_dim(g), cos_tab + (int64_t)tok_pos[t] * half,
+                 sin_tab + (int64_t)tok_pos[t] * half, rot);
+        int64_t token_in_block = tok_pos[t] % TOKENS_PER_BLOCK;
+        uint8_t* k_dst = pool + blk * block_bytes(g) + token_in_block * row_bytes;
+        uint8_t* v_dst = k_dst + v_offset(g);
+        memcpy(k_dst, rot, (size_t)row_bytes);
+        memcpy(v_dst, (const uint8_t*)v_new + t * row_bytes, (size_t)row_bytes);
+    }
+    free(rot);
+    return skipped;
+}
+
 /* -------------------------------------------------------------- gather */
 
 /* Element (token, kv head, dim) of K lives at

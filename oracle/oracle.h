@@ -61,6 +61,19 @@ int64_t orc_write_kv(const orc_geom* g, uint8_t* pool, const int32_t* block_tabl
                      int32_t layer, int64_t n_tokens, const int32_t* tok_slot,
                      const int32_t* tok_pos, const uint16_t* k_new, const uint16_t* v_new);
 
+/* orc_write_kv with K rotated by RoPE at each row's position [TV3 "RoPE: a
+ * rotation that references a table"]: in every kv head, element i and
+ * element i + head_dim/2 are rotated as
+ *   x1' = x1 cos - x2 sin,   x2' = x1 sin + x2 cos
+ * with cos/sin read from caller tables [max_pos][head_dim/2] fp32 at the row's
+ * position, in fp32 with each product and sum rounded separately, then
+ * rounded to bf16 (nearest even).  V is copied unchanged.  Rows at a position
+ * >= max_pos count as skipped. */
+int64_t orc_write_kv_rope(const orc_geom* g, uint8_t* pool, const int32_t* block_table,
+                          int32_t layer, int64_t n_tokens, const int32_t* tok_slot,
+                          const int32_t* tok_pos, const uint16_t* k_new, const uint16_t* v_new,
+                          const float* cos_tab, const float* sin_tab, int32_t max_pos);
+
 /* Gather the first n tokens of (slot, layer) into K[n][Hkv][d], V[n][Hkv][d]
  * (fp64) through the block table [TV6 address rule].  Returns ORC_OK or
  * ORC_BAD_BLOCK / ORC_BAD_ARG. */

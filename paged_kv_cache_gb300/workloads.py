@@ -105,6 +105,19 @@ class Case:
         return int(self.lens.max()) if self.batch else 0
 
 
+# ------------------------------------------------------------- RoPE tables
+
+def rope_tables(max_pos: int, head_dim: int, base: float = 500000.0):
+    """cos / sin tables [max_pos][head_dim/2] fp32 of the usual RoPE angles
+    pos * base^(-2i/head_dim) (input data for the RoPE calls; the pages'
+    program fills such tables once at start-up and the kernel only reads
+    them).  base 500000 is the Llama-3 family's value."""
+    half = head_dim // 2
+    inv = base ** (-2.0 * np.arange(half, dtype=np.float64) / head_dim)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
 # ---------------------------------------------------------------- helpers
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:

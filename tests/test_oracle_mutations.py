@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_chunked_pins as cpins
+from tests import test_oracle_rope_pins as rpins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "oracle.c")
@@ -30,6 +31,12 @@ MUTANTS = {
     "prefix_ignored": ("int32_t pre = c->prefix ? c->prefix[b] : 0;", "int32_t pre = 0;"),
     "prefix_last_key_off_by_one": ("pre + n, pre + i, c->scale", "pre + n, pre + i - 1, c->scale"),
     "prefix_not_in_position": ("pre + n, pre + i, c->scale", "pre + n, i, c->scale"),
+    "rope_signs_swapped": ("const float y1 = a - b, y2 = e + f;", "const float y1 = a + b, y2 = e - f;"),
+    "rope_interleaved_pairs": ("const float x1 = bf16_to_float(x[i]), x2 = bf16_to_float(x[i + half]);",
+                               "const float x1 = bf16_to_float(x[2 * i]), x2 = bf16_to_float(x[2 * i + 1]);"),
+    "rope_next_table_row": ("rope_row(g, k_new + t * kv_dim(g), cos_tab + (int64_t)tok_pos[t] * half,",
+                            "rope_row(g, k_new + t * kv_dim(g), cos_tab + (int64_t)(tok_pos[t] + 1 < max_pos ? tok_pos[t] + 1 : tok_pos[t]) * half,"),
+    "rope_truncating_round": ("u += 0x7FFFu + lsb;", "u += 0u * lsb;"),
     "max_not_subtracted": ("for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m);",
                            "for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m) * (1 + 1e-9 * m);"),
 }
@@ -48,6 +55,9 @@ PIN_TESTS = [
     lambda gd: pins.test_decode_matches_library_sdpa(),
     lambda gd: cpins.test_chunked_matches_library_sdpa(8, 2, 64, [0, 16, 23], [40, 17, 1]),
     lambda gd: cpins.test_chunk_of_one_is_decode(),
+    lambda gd: rpins.test_worked_example_pairing(gd),
+    lambda gd: rpins.test_special_angles(),
+    lambda gd: rpins.test_matches_torch_fp32_ops_byte_for_byte(),
 ]
 
 
@@ -62,7 +72,7 @@ def test_mutant_is_caught(name, tmp_path, golden_dir):
     hdr = os.path.join(os.path.dirname(SRC), "oracle.h")
     (tmp_path / "oracle.h").write_text(open(hdr).read())
     so = tmp_path / "liboracle_mutant.so"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", str(so),
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread", "-o", str(so),
                     str(c_path), "-lm"], check=True)
     caught = []
     with oracle.use_library(str(so)):
