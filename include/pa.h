@@ -115,6 +115,27 @@ pa_status pa_write_kv(const pa_geom* geom, void* pool, const int32_t* block_tabl
                       int32_t* err_flag, pa_stream_t stream);
 
 /*
+ * pa_write_kv_rope -- pa_write_kv with RoPE applied to K on the way into the
+ * pages (jaehun.me tiny-vllm part 3, "RoPE: a rotation that references a
+ * table"): in every kv head, element i and element i + head_dim/2 of row t's
+ * K form a pair rotated by the angle of position tok_pos[t],
+ *   x1' = x1 c - x2 s,   x2' = x1 s + x2 c,
+ * with c = cos_table[tok_pos[t]][i], s = sin_table[tok_pos[t]][i], computed in
+ * fp32 with every product and sum rounded on its own, then rounded to bf16
+ * (nearest even).  V is stored unchanged, exactly as pa_write_kv.
+ * Arguments: as pa_write_kv, plus cos_table, sin_table: device fp32
+ * [max_pos][head_dim/2], 16-byte aligned, read only (the caller fills them,
+ * e.g. with cos/sin of pos * base^(-2i/head_dim) and any frequency scaling its
+ * model uses).  Rows with tok_pos >= max_pos are skipped and set
+ * PA_ERR_BAD_BLOCK like an invalid table entry.  Requires head_dim % 16 == 0.
+ */
+pa_status pa_write_kv_rope(const pa_geom* geom, void* pool, const int32_t* block_table,
+                           int32_t layer, int32_t n_tokens, const int32_t* tok_slot,
+                           const int32_t* tok_pos, const void* k_new, const void* v_new,
+                           const float* cos_table, const float* sin_table, int32_t max_pos,
+                           int32_t* err_flag, pa_stream_t stream);
+
+/*
  * pa_prefill -- causal prefill of a packed batch of fresh prompts.
  * Definition: for sequence b of length n_b = cu_seqlens[b+1] - cu_seqlens[b]
  * (slot slots[b]), query row i (0 <= i < n_b) of q head h attends keys 0..i of

@@ -9,6 +9,7 @@ raises, and every call that fails returns an error that is raised here.
 Calls (same names as the C ABI):
 
 * ``pa_write_kv(geom, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new, err_flag)``
+* ``pa_write_kv_rope(geom, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new, cos_table, sin_table, err_flag)``
 * ``pa_prefill(geom, q, pool, block_table, layer, cu_seqlens, slots, max_seqlen, scale, o, lse, err_flag)``
 * ``pa_prefill_cached(geom, q, pool, block_table, layer, cu_seqlens, prefix_lens, slots, max_seqlen, scale, o, lse, err_flag)``
 * ``pa_decode(geom, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse, workspace, err_flag)``
@@ -31,7 +32,7 @@ PA_BLOCK_TOKENS = 16
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libpa.so")
-EXPORTED = ("pa_page_bytes", "pa_write_kv", "pa_prefill", "pa_prefill_cached", "pa_decode_workspace_size", "pa_decode",
+EXPORTED = ("pa_page_bytes", "pa_write_kv", "pa_write_kv_rope", "pa_prefill", "pa_prefill_cached", "pa_decode_workspace_size", "pa_decode",
             "pa_decode_noalloc", "pa_status_string")
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -73,6 +74,9 @@ def load_library(path: str = None):
     L.pa_page_bytes.argtypes = [C.POINTER(PaGeom)]
     L.pa_write_kv.restype = C.c_int
     L.pa_write_kv.argtypes = [C.POINTER(PaGeom), _P, _P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P]
+    L.pa_write_kv_rope.restype = C.c_int
+    L.pa_write_kv_rope.argtypes = [C.POINTER(PaGeom), _P, _P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P,
+                                   C.c_int32, _P, _P]
     L.pa_prefill.restype = C.c_int
     L.pa_prefill.argtypes = [C.POINTER(PaGeom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, C.c_int32,
                              C.c_int32, C.c_float, _P, _P, _P, _P]
@@ -143,6 +147,16 @@ def pa_write_kv(g, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new, er
     _check("pa_write_kv", lib().pa_write_kv(
         C.byref(g), _ptr(pool), _ptr(block_table), layer, n, _ptr(tok_slot), _ptr(tok_pos),
         _ptr(k_new), _ptr(v_new), _ptr(err_flag), _stream(stream)))
+
+
+def pa_write_kv_rope(g, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new, cos_table, sin_table,
+                     err_flag, stream=None, n_tokens=None):
+    """pa_write_kv with RoPE on K; cos_table / sin_table: fp32 [max_pos][head_dim/2] CUDA tensors."""
+    n = int(tok_slot.shape[0]) if n_tokens is None else int(n_tokens)
+    _check("pa_write_kv_rope", lib().pa_write_kv_rope(
+        C.byref(g), _ptr(pool), _ptr(block_table), layer, n, _ptr(tok_slot), _ptr(tok_pos),
+        _ptr(k_new), _ptr(v_new), _ptr(cos_table), _ptr(sin_table), int(cos_table.shape[0]),
+        _ptr(err_flag), _stream(stream)))
 
 
 def pa_prefill(g, q, pool, block_table, layer, cu_seqlens, slots, max_seqlen, scale, o, lse,

@@ -75,6 +75,33 @@ PA_API pa_status pa_write_kv(const pa_geom* geom, void* pool, const int32_t* blo
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
+
+PA_API pa_status pa_write_kv_rope(const pa_geom* geom, void* pool, const int32_t* block_table,
+                                  int32_t layer, int32_t n_tokens, const int32_t* tok_slot,
+                                  const int32_t* tok_pos, const void* k_new, const void* v_new,
+                                  const float* cos_table, const float* sin_table, int32_t max_pos,
+                                  int32_t* err_flag, pa_stream_t stream) {
+    if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= geom->n_layers || n_tokens < 0 || max_pos < 0) return PA_ERR_INVALID_ARG;
+    if (geom->head_dim % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return PA_OK;
+    if (!pool || !block_table || !tok_slot || !tok_pos || !k_new || !v_new || !cos_table || !sin_table ||
+        !err_flag)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(pool) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cos_table) ||
+        !aligned16(sin_table))
+        return PA_ERR_INVALID_ARG;
+    const pa::KGeom g = kgeom(geom);
+    const size_t pool_len = static_cast<size_t>(g.nblocks) * static_cast<size_t>(g.page_bytes);
+    const size_t rows_len = static_cast<size_t>(n_tokens) * g.kv_dim * 2;
+    if (ranges_overlap(k_new, rows_len, pool, pool_len) ||
+        ranges_overlap(v_new, rows_len, pool, pool_len))
+        return PA_ERR_INVALID_ARG;
+    return cuda_status(pa::launch_write_kv_rope(g, pool, block_table, layer, n_tokens, tok_slot, tok_pos,
+                                                k_new, v_new, cos_table, sin_table, max_pos, err_flag,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
 PA_API pa_status pa_prefill_cached(const pa_geom* geom, const void* q, const void* pool,
                                    const int32_t* block_table, int32_t layer, int32_t batch,
                                    const int32_t* cu_seqlens, const int32_t* prefix_lens,

@@ -515,6 +515,10 @@ cudaError_t launch_write_kv(const KGeom& g, void* pool, const int32_t* block_tab
                             int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,
                             const void* k_new, const void* v_new, int32_t* err,
                             cudaStream_t stream);
+cudaError_t launch_write_kv_rope(const KGeom& g, void* pool, const int32_t* block_table, int layer,
+                                 int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,
+                                 const void* k_new, const void* v_new, const float* cos_tab,
+                                 const float* sin_tab, int max_pos, int32_t* err, cudaStream_t stream);
 
 cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool,
                            const int32_t* block_table, int layer, int batch,

@@ -57,7 +57,115 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
     }
 }
 
+// The same scatter with K rotated by RoPE on the way (jaehun.me tiny-vllm part
+// 3, "RoPE: a rotation that references a table"): in each kv head, element i
+// and element i + d/2 form a pair turned by the angle of the row's position,
+//   x1' = x1 c - x2 s,   x2' = x1 s + x2 c,
+// with c, s from caller tables [max_pos][d/2] fp32.  Each product and sum is
+// rounded on its own (no FMA contraction), then to bf16 nearest-even.  Per
+// row, the first kv_dim/16 threads each take 8 pairs of one head (16 bytes of
+// each half, read and written whole), the next kv_dim/8 threads copy V.
+__device__ __forceinline__ void rope8(uint4& lo, uint4& hi, const float4 c0, const float4 c1, const float4 s0,
+                                      const float4 s1) {
+    const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t ra = 0, rb = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int e = 2 * w + h;
+            const float x1 = __uint_as_float((a[w] >> (16 * h)) << 16);
+            const float x2 = __uint_as_float((b[w] >> (16 * h)) << 16);
+            const float y1 = __fsub_rn(__fmul_rn(x1, cs[e]), __fmul_rn(x2, sn[e]));
+            const float y2 = __fadd_rn(__fmul_rn(x1, sn[e]), __fmul_rn(x2, cs[e]));
+            ra |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(y1))) << (16 * h);
+            rb |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(y2))) << (16 * h);
+        }
+        a[w] = ra;
+        b[w] = rb;
+    }
+    lo = make_uint4(a[0], a[1], a[2], a[3]);
+    hi = make_uint4(b[0], b[1], b[2], b[3]);
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __restrict__ pool,
+                                                            const int32_t* __restrict__ block_table, int layer,
+                                                            int n_tokens, const int32_t* __restrict__ tok_slot,
+                                                            const int32_t* __restrict__ tok_pos,
+                                                            const uint4* __restrict__ k_new,
+                                                            const uint4* __restrict__ v_new,
+                                                            const float* __restrict__ cos_tab,
+                                                            const float* __restrict__ sin_tab, int max_pos,
+                                                            int32_t* err) {
+    const int kq = g.kv_dim / 16;  // K threads per row: 8 pairs each
+    const int vc = g.kv_dim / 8;   // V threads per row: one 16-byte chunk each
+    const int per_row = kq + vc;
+    const int hc = g.d / 16;       // pair chunks per head
+    const long long total = static_cast<long long>(n_tokens) * per_row;
+    const long long half_page = g.page_bytes / 2;  // V_OFFSET
+    const long long row_bytes = static_cast<long long>(g.kv_dim) * 2;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = idx / per_row;
+        const int rem = static_cast<int>(idx - row * per_row);
+        const int slot = __ldg(tok_slot + row);
+        const int pos = __ldg(tok_pos + row);
+        long long blk = -1;
+        if (slot >= 0 && slot < g.num_slots && pos >= 0 && pos < max_pos && pos / kBlockTokens < g.maxb) {
+            const long long tidx =
+                (static_cast<long long>(slot) * g.n_layers + layer) * g.maxb + pos / kBlockTokens;
+            const int e = __ldg(block_table + tidx);
+            if (e >= 0 && e < g.nblocks) blk = e;
+        }
+        if (blk < 0) {
+            if (rem == 0) set_error(err, PA_ERR_BAD_BLOCK);
+            continue;
+        }
+        uint8_t* dst_row = pool + blk * g.page_bytes + static_cast<long long>(pos % kBlockTokens) * row_bytes;
+        if (rem < kq) {
+            const int head = rem / hc, c = rem % hc;
+            const long long e_lo = static_cast<long long>(head) * g.d + 8 * c;  // element index in the row
+            const long long e_hi = e_lo + g.d / 2;
+            uint4 lo = ld_stream(k_new + (row * g.kv_dim + e_lo) / 8);
+            uint4 hi = ld_stream(k_new + (row * g.kv_dim + e_hi) / 8);
+            const float4* ct = reinterpret_cast<const float4*>(cos_tab + static_cast<long long>(pos) * (g.d / 2) + 8 * c);
+            const float4* st = reinterpret_cast<const float4*>(sin_tab + static_cast<long long>(pos) * (g.d / 2) + 8 * c);
+            rope8(lo, hi, __ldg(ct), __ldg(ct + 1), __ldg(st), __ldg(st + 1));
+            *reinterpret_cast<uint4*>(dst_row + e_lo * 2) = lo;
+            *reinterpret_cast<uint4*>(dst_row + e_hi * 2) = hi;
+        } else {
+            const int c = rem - kq;
+            *reinterpret_cast<uint4*>(dst_row + half_page + static_cast<long long>(c) * 16) =
+                ld_stream(v_new + row * vc + c);
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_write_kv_rope(const KGeom& g, void* pool, const int32_t* block_table, int layer,
+                                 int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,
+                                 const void* k_new, const void* v_new, const float* cos_tab,
+                                 const float* sin_tab, int max_pos, int32_t* err, cudaStream_t stream) {
+    const long long total = static_cast<long long>(n_tokens) * (g.kv_dim / 16 + g.kv_dim / 8);
+    const int threads = 256;
+    long long blocks = (total + threads - 1) / threads;
+    if (blocks > (1ll << 30)) blocks = 1ll << 30;  // grid-stride covers the rest
+    write_kv_rope_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), cos_tab, sin_tab, max_pos, err);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_write_kv(const KGeom& g, void* pool, const int32_t* block_table, int layer,
                             int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,

@@ -82,6 +82,15 @@ def test_validation_without_gpu(lib):
                           NULL, NULL, NULL, NULL) == pa.PA_OK  # empty batch
     assert lib.pa_prefill(C.byref(g), NULL, NULL, NULL, 0, 1, NULL, NULL, 4, 4, C.c_float(float("nan")),
                           NULL, NULL, NULL, NULL) == pa.PA_ERR_INVALID_ARG
+    # RoPE scatter: tables required and 16-byte aligned, max_pos >= 0
+    assert lib.pa_write_kv_rope(C.byref(g), 16, 16, 0, 3, 16, 16, 32, 48, NULL, NULL, 8, 16,
+                                NULL) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_write_kv_rope(C.byref(g), 16, 16, 0, 3, 16, 16, 32, 48, 64, 72, 8, 16,
+                                NULL) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_write_kv_rope(C.byref(g), NULL, NULL, 0, 3, NULL, NULL, NULL, NULL, NULL, NULL, -1, NULL,
+                                NULL) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_write_kv_rope(C.byref(g), NULL, NULL, 0, 0, NULL, NULL, NULL, NULL, NULL, NULL, 8, NULL,
+                                NULL) == pa.PA_OK  # no rows
     # the softmax scale must be positive (the row max is taken on unscaled scores)
     for bad in (0.0, -0.125):
         assert lib.pa_prefill(C.byref(g), NULL, NULL, NULL, 0, 1, NULL, NULL, 4, 4, C.c_float(bad),
