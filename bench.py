@@ -13,6 +13,8 @@ decode's 4 d Hq n).  The line also carries:
   decode       -- decode KV-read GB/s on the large mixed-length batch (256
                   sequences, log-normal lengths, new-token write + decode per
                   step) against the measured HBM copy bandwidth;
+  scatter      -- pa_write_kv and pa_write_kv_rope GB/s on the prompt rows
+                  against the measured HBM copy bandwidth;
   chunked      -- pa_prefill_cached: 4 x 2048-query chunks after 6144 cached
                   tokens, exact-causal TFLOP/s against the same bf16 peak;
   e2e          -- the same metric through the C ABI with host buffers: pinned
@@ -54,7 +56,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time (10-30 s)")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "chunked"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "chunked", "scatter"], default="all",
                     help="profiling aid: run only the main (prefill) step or only the decode step")
     ap.add_argument("--batch", type=int, default=4, help="prefill sequences (profiling aid)")
     ap.add_argument("--seqlen", type=int, default=8192, help="prefill length (profiling aid)")
@@ -221,6 +223,41 @@ class PrefillStep:
                        self.err)
         pa.pa_decode(self.g, d["dec_q"], self.pool, d["bt"], 0, d["dec_lens"], d["slots"], self.n + 1,
                      c.scale, self.dec_o, self.dec_lse, self.ws, self.err)
+
+
+class ScatterStep:
+    """The prompt K/V scatter of the main step (4 x 8192 rows of 2 x 512 bf16
+    into shuffled pages), plain and with RoPE on K.  Algorithmic bytes per
+    call: K and V rows read once and written once, plus (RoPE) one cos and one
+    sin table row of head_dim/2 fp32 per token."""
+
+    def __init__(self, torch, pa, W, seed=1003):
+        self.torch, self.pa = torch, pa
+        c = W.c4_long("d64", seed=seed)
+        self.case, self.geom = c, c.geom
+        self.g = pa.geom(*c.geom.as_tuple())
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        w = c.writes[0]
+        cos_t, sin_t = W.rope_tables(int(c.lens.max()), c.geom.head_dim)
+        self.d = {"bt": dev(c.block_table), "tok_slot": dev(w.tok_slot), "tok_pos": dev(w.tok_pos),
+                  "k": dev(w.k), "v": dev(w.v), "cos": dev(cos_t), "sin": dev(sin_t)}
+        self.pool = torch.empty(c.geom.pool_bytes, dtype=torch.uint8, device="cuda")
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        n = int(w.tok_slot.shape[0])
+        self.bytes_plain = float(n * c.geom.kv_dim * 2 * 2 * 2)
+        self.bytes_rope = self.bytes_plain + float(n * c.geom.head_dim // 2 * 4 * 2)
+
+    def run(self, rope, ev=None):
+        pa, d = self.pa, self.d
+        if ev is not None:
+            ev[0].record()
+        if rope:
+            pa.pa_write_kv_rope(self.g, self.pool, d["bt"], 0, d["tok_slot"], d["tok_pos"], d["k"], d["v"],
+                                d["cos"], d["sin"], self.err)
+        else:
+            pa.pa_write_kv(self.g, self.pool, d["bt"], 0, d["tok_slot"], d["tok_pos"], d["k"], d["v"], self.err)
+        if ev is not None:
+            ev[1].record()
 
 
 class ChunkedStep:
@@ -562,6 +599,29 @@ def main():
                                 "peak_source": "%s bf16_tflops (burst)" % peak_src,
                                 "algorithmic_flops_per_launch": cstep.flops, "avg_launch_ms": c_avg * 1e3}}
         del cstep
+
+    scatter = None
+    if args.only in ("all", "scatter"):
+        # ------------------------------------------------- K/V scatter (a1, f2)
+        sstep = ScatterStep(torch, pa, W)
+        hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        scatter = {"metric": "K/V scatter GB/s (4 x 8192 prompt rows of 2 x 512 bf16 into shuffled pages)"}
+        for name, rope, nbytes in (("write_kv", False, sstep.bytes_plain), ("write_kv_rope", True, sstep.bytes_rope)):
+            ssteps = max(20, args.steps // 2)
+            s_s, sk_s = timed(torch, lambda ev: sstep.run(rope, ev=ev), ssteps, args.warmup, flush, dist)
+            torch.cuda.synchronize()
+            if int(sstep.err.item()) != 0:
+                raise SystemExit("device error in scatter steps: %s" % pa.pa_status_string(int(sstep.err.item())))
+            s_avg = float(np.mean(sk_s))
+            s_rate, _, _ = job_rate(torch, dist, nbytes * ssteps, float(np.sum(sk_s)))
+            scatter[name] = {"value": s_rate / 1e9, "unit": "GB/s",
+                             "roofline": {"bound": "hbm", "achieved": nbytes / s_avg / 1e9, "peak": hbm_peak,
+                                          "unit": "GB/s", "frac": nbytes / s_avg / 1e9 / hbm_peak,
+                                          "traffic": None,
+                                          "kernel": "write_kv_rope_kernel" if rope else "write_kv_kernel",
+                                          "peak_source": "%s hbm_gbs" % peak_src,
+                                          "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": s_avg * 1e3}}
+        del sstep
     clk = clocks.stop()
 
     if step is not None and not args.no_e2e:
@@ -599,7 +659,7 @@ def main():
 
     if rank == 0 and step is None:
         print(json.dumps({"metric": "%s only (profiling aid)" % args.only, "decode": decode, "chunked": chunked,
-                          "clocks": clk}), flush=True)
+                          "scatter": scatter, "clocks": clk}), flush=True)
     elif rank == 0:
         line = {
             "metric": "causal prefill TFLOP/s (exact causal count, step incl. KV write + decode)",
@@ -617,6 +677,7 @@ def main():
             "roofline": roofline,
             "decode": decode,
             "chunked": chunked,
+            "scatter": scatter,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,
