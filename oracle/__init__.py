@@ -46,6 +46,10 @@ def lib():
         L.orc_write_kv_rope.restype = C.c_int64
         L.orc_write_kv_rope.argtypes = [C.POINTER(Geom), _P, _P, C.c_int32, C.c_int64, _P, _P, _P, _P, _P, _P,
                                         C.c_int32]
+        L.orc_alloc_pages.restype = C.c_int64
+        L.orc_alloc_pages.argtypes = [C.POINTER(Geom), _P, C.c_int32, _P, _P, _P, _P, _P]
+        L.orc_release_slots.restype = C.c_int64
+        L.orc_release_slots.argtypes = [C.POINTER(Geom), _P, C.c_int32, _P, _P, _P]
         L.orc_gather_kv.restype = C.c_int
         L.orc_gather_kv.argtypes = [C.POINTER(Geom), _P, _P, C.c_int32, C.c_int32, C.c_int32, _P, _P]
         L.orc_softmax_row.restype = None
@@ -133,6 +137,28 @@ def write_kv_rope(g, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new, 
     r = lib().orc_write_kv_rope(C.byref(g), _ptr(pool), _ptr(bt), layer, n, _ptr(ts), _ptr(tp),
                                 _ptr(k), _ptr(v), _ptr(ct), _ptr(st), int(ct.shape[0]))
     return int(r)
+
+
+def alloc_pages(g, block_table, slots, seq_lens, free_pages, free_count, old_lens=None):
+    """Pops pages for every -1 entry the lengths need (in place on the int32
+    arrays block_table, free_pages and the one-element free_count); returns
+    the number of pages taken or a negative status."""
+    for a in (block_table, free_pages, free_count):
+        assert a.dtype == np.int32 and a.flags.c_contiguous
+    sl, ln = _c(slots, np.int32), _c(seq_lens, np.int32)
+    old = None if old_lens is None else _c(old_lens, np.int32)
+    return int(lib().orc_alloc_pages(C.byref(g), _ptr(block_table), int(sl.shape[0]), _ptr(sl),
+                                     None if old is None else _ptr(old), _ptr(ln), _ptr(free_pages),
+                                     _ptr(free_count)))
+
+
+def release_slots(g, block_table, slots, free_pages, free_count):
+    """Pushes every page of the slots back (in place); returns the count or a negative status."""
+    for a in (block_table, free_pages, free_count):
+        assert a.dtype == np.int32 and a.flags.c_contiguous
+    sl = _c(slots, np.int32)
+    return int(lib().orc_release_slots(C.byref(g), _ptr(block_table), int(sl.shape[0]), _ptr(sl),
+                                       _ptr(free_pages), _ptr(free_count)))
 
 
 def gather_kv(g, pool, block_table, layer, slot, n):

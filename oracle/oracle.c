@@ -179,6 +179,77 @@ int64_t orc_write_kv_rope(const orc_geom* g, uint8_t* pool, const int32_t* block
     return skipped;
 }
 
+/* ------------------------------------------------------ page lifetime */
+
+/* Every logical block that positions 0..seq_lens[b]-1 of slots[b] need gets a
+ * physical page, in every layer: a table entry that is -1 takes the page on
+ * top of the free stack (pop_back), walking sequences in order, then layers,
+ * then logical blocks [TV6 "물리 블록의 수명: free_blocks 가 관리한다": prefill
+ * takes a page when its logical block is -1, decode when a new block starts].
+ * Entries below old_lens[b] / 16 (old_lens may be NULL) are not looked at.
+ * All or nothing: when the stack holds fewer pages than needed nothing
+ * changes and ORC_BAD_ARG is returned.  Returns the number of pages taken. */
+int64_t orc_alloc_pages(const orc_geom* g, int32_t* block_table, int32_t batch, const int32_t* slots,
+                        const int32_t* old_lens, const int32_t* seq_lens, int32_t* free_pages,
+                        int32_t* free_count) {
+    if (!geom_ok(g) || batch < 0 || !block_table || !free_pages || !free_count) return ORC_BAD_ARG;
+    if (batch > 0 && (!slots || !seq_lens)) return ORC_BAD_ARG;
+    const int32_t mb = g->max_blocks_per_seq;
+    int64_t need = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        int32_t top = *free_count;
+        for (int32_t b = 0; b < batch; ++b) {
+            const int32_t slot = slots[b], len = seq_lens[b];
+            if (slot < 0 || slot >= g->num_slots || len < 0 || len > mb * TOKENS_PER_BLOCK) return ORC_BAD_ARG;
+            const int32_t lo = old_lens ? old_lens[b] / TOKENS_PER_BLOCK : 0;
+            const int32_t hi = (len + TOKENS_PER_BLOCK - 1) / TOKENS_PER_BLOCK;
+            for (int32_t layer = 0; layer < g->n_layers; ++layer)
+                for (int32_t lb = lo < 0 ? 0 : lo; lb < hi; ++lb) {
+                    int32_t* e = block_table + ((int64_t)slot * g->n_layers + layer) * mb + lb;
+                    if (*e != -1) continue;
+                    if (pass == 0) {
+                        ++need;
+                    } else {
+                        *e = free_pages[--top]; /* pop_back */
+                    }
+                }
+        }
+        if (pass == 0 && need > *free_count) return ORC_BAD_ARG;
+        if (pass == 1) *free_count = top;
+    }
+    return need;
+}
+
+/* Every page held by slots[0..n-1], in every layer, goes back on the free
+ * stack (push_back), walking slots in order, then layers, then logical
+ * blocks, and its table entry becomes -1 [TV6 "물리 블록의 수명: free_blocks
+ * 가 관리한다": the loop that ends a slot].  Returns the pages returned, or
+ * ORC_BAD_ARG (nothing changes) when the stack would overflow num_blocks. */
+int64_t orc_release_slots(const orc_geom* g, int32_t* block_table, int32_t n, const int32_t* slots,
+                          int32_t* free_pages, int32_t* free_count) {
+    if (!geom_ok(g) || n < 0 || !block_table || !free_pages || !free_count) return ORC_BAD_ARG;
+    if (n > 0 && !slots) return ORC_BAD_ARG;
+    const int32_t mb = g->max_blocks_per_seq;
+    int64_t held = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        if (slots[i] < 0 || slots[i] >= g->num_slots) return ORC_BAD_ARG;
+        for (int64_t k = 0; k < (int64_t)g->n_layers * mb; ++k)
+            if (block_table[(int64_t)slots[i] * g->n_layers * mb + k] != -1) ++held;
+    }
+    if (*free_count + held > g->num_blocks) return ORC_BAD_ARG;
+    int32_t top = *free_count;
+    for (int32_t i = 0; i < n; ++i)
+        for (int32_t layer = 0; layer < g->n_layers; ++layer)
+            for (int32_t lb = 0; lb < mb; ++lb) {
+                int32_t* e = block_table + ((int64_t)slots[i] * g->n_layers + layer) * mb + lb;
+                if (*e == -1) continue;
+                free_pages[top++] = *e; /* push_back */
+                *e = -1;
+            }
+    *free_count = top;
+    return held;
+}
+
 /* -------------------------------------------------------------- gather */
 
 /* Element (token, kv head, dim) of K lives at

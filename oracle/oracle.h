@@ -61,6 +61,22 @@ int64_t orc_write_kv(const orc_geom* g, uint8_t* pool, const int32_t* block_tabl
                      int32_t layer, int64_t n_tokens, const int32_t* tok_slot,
                      const int32_t* tok_pos, const uint16_t* k_new, const uint16_t* v_new);
 
+/* Page lifetime on a free stack [TV6 "물리 블록의 수명: free_blocks 가
+ * 관리한다"].  free_pages[0..*free_count-1] is the stack, its top last.
+ * orc_alloc_pages: every logical block of positions 0..seq_lens[b]-1 of
+ * slots[b], in every layer, whose entry is -1 pops the top page, walking
+ * sequences, then layers, then logical blocks in order (entries below
+ * old_lens[b] / 16 are not looked at; old_lens may be NULL); all or nothing
+ * when the stack runs short.  orc_release_slots: every page held by the
+ * slots goes back (push) in the same walking order and its entry becomes -1.
+ * Both return the number of pages moved, or ORC_BAD_ARG with nothing
+ * changed. */
+int64_t orc_alloc_pages(const orc_geom* g, int32_t* block_table, int32_t batch, const int32_t* slots,
+                        const int32_t* old_lens, const int32_t* seq_lens, int32_t* free_pages,
+                        int32_t* free_count);
+int64_t orc_release_slots(const orc_geom* g, int32_t* block_table, int32_t n, const int32_t* slots,
+                          int32_t* free_pages, int32_t* free_count);
+
 /* orc_write_kv with K rotated by RoPE at each row's position [TV3 "RoPE: a
  * rotation that references a table"]: in every kv head, element i and
  * element i + head_dim/2 are rotated as

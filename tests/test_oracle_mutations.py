@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_chunked_pins as cpins
+from tests import test_oracle_pages_pins as ppins
 from tests import test_oracle_rope_pins as rpins
 from tests import test_oracle_pins as pins
 
@@ -37,6 +38,13 @@ MUTANTS = {
     "rope_next_table_row": ("rope_row(g, k_new + t * kv_dim(g), cos_tab + (int64_t)tok_pos[t] * half,",
                             "rope_row(g, k_new + t * kv_dim(g), cos_tab + (int64_t)(tok_pos[t] + 1 < max_pos ? tok_pos[t] + 1 : tok_pos[t]) * half,"),
     "rope_truncating_round": ("u += 0x7FFFu + lsb;", "u += 0u * lsb;"),
+    "alloc_pop_order": ("*e = free_pages[--top]; /* pop_back */", "*e = free_pages[(--top) ^ 1]; /* pop_back */"),
+    "alloc_last_block_missing": ("const int32_t hi = (len + TOKENS_PER_BLOCK - 1) / TOKENS_PER_BLOCK;",
+                                 "const int32_t hi = len / TOKENS_PER_BLOCK;"),
+    "alloc_sequences_reversed": ("        for (int32_t b = 0; b < batch; ++b) {\n            const int32_t slot = slots[b], len = seq_lens[b];",
+                          "        for (int32_t b = batch - 1; b >= 0; --b) {\n            const int32_t slot = slots[b], len = seq_lens[b];"),
+    "release_keeps_entry": ("                free_pages[top++] = *e; /* push_back */\n                *e = -1;",
+                            "                free_pages[top++] = *e; /* push_back */"),
     "max_not_subtracted": ("for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m);",
                            "for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m) * (1 + 1e-9 * m);"),
 }
@@ -58,6 +66,8 @@ PIN_TESTS = [
     lambda gd: rpins.test_worked_example_pairing(gd),
     lambda gd: rpins.test_special_angles(),
     lambda gd: rpins.test_matches_torch_fp32_ops_byte_for_byte(),
+    lambda gd: ppins.test_worked_example(gd),
+    lambda gd: ppins.test_decode_takes_a_page_only_at_a_new_block(),
 ]
 
 
