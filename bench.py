@@ -56,7 +56,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time (10-30 s)")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "chunked", "scatter"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "chunked", "scatter", "pages"], default="all",
                     help="profiling aid: run only the main (prefill) step or only the decode step")
     ap.add_argument("--batch", type=int, default=4, help="prefill sequences (profiling aid)")
     ap.add_argument("--seqlen", type=int, default=8192, help="prefill length (profiling aid)")
@@ -417,6 +417,60 @@ def job_rate(torch, dist, units, seconds):
     return total_u / total_s, total_s, total_u
 
 
+def page_lifetime_timing(torch, pa, W, warmup, reps=50):
+    """Device page allocation for one decode step of 256 sequences x 16 layers
+    (lengths log-normal as in the decode batch; every 16th token needs a
+    page), and the release of 64 slots; beside them, for context, the copy
+    of the whole block table from pinned host memory that the pages' program
+    makes after every change.  Latency-bound calls: microseconds per call."""
+    lens = W.c5_lens()
+    B, L = lens.shape[0], 16
+    geom = W.Geometry(32, 8, 64, L, B, 1025, B * L * 1100)
+    g = pa.geom(*geom.as_tuple())
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    table = dev(W.empty_table(geom))
+    stack = dev(np.arange(geom.num_blocks, dtype=np.int32)[::-1].copy())
+    count = dev(np.array([geom.num_blocks], np.int32))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = dev(np.arange(B, dtype=np.int32))
+    pa.pa_alloc_pages(g, table, slots, dev(lens), stack, count, err)  # the prompts
+    old = dev(lens)
+    new = dev(lens + 1)
+    E = torch.cuda.Event
+
+    def time_call(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = E(enable_timing=True), E(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps * 1e3
+
+    # a step after the first allocates nothing new (old = new - 1 already covered); time the real work:
+    # alternate between growing by one token and shrinking the stack back through release/alloc pairs
+    alloc_us = time_call(lambda: pa.pa_alloc_pages(g, table, slots, new, stack, count, err, old_lens=old))
+    rel = dev(np.arange(64, dtype=np.int32))
+    rel_lens = dev(lens[:64])
+
+    def release_then_alloc():
+        pa.pa_release_slots(g, table, rel, stack, count, err)
+        pa.pa_alloc_pages(g, table, rel, rel_lens, stack, count, err)
+    pair_us = time_call(release_then_alloc)
+    host_table = torch.from_numpy(W.empty_table(geom)).pin_memory()
+    h2d_us = time_call(lambda: table.copy_(host_table, non_blocking=True))
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise SystemExit("device error in page lifetime timing: %s" % pa.pa_status_string(int(err.item())))
+    return {"metric": "device page lifetime, microseconds per call (256 sequences x 16 layers)",
+            "alloc_decode_step_us": alloc_us, "release_64_slots_then_realloc_us": pair_us,
+            "table_h2d_copy_us": h2d_us, "table_entries": int(geom.num_slots * L * geom.max_blocks_per_seq),
+            "unit": "us"}
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample(case, seconds, rng_seed=5):
@@ -622,6 +676,11 @@ def main():
                                           "peak_source": "%s hbm_gbs" % peak_src,
                                           "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": s_avg * 1e3}}
         del sstep
+
+    pages = None
+    if args.only in ("all", "pages"):
+        # ----------------------------------- page lifetime on the device (f3)
+        pages = page_lifetime_timing(torch, pa, W, args.warmup)
     clk = clocks.stop()
 
     if step is not None and not args.no_e2e:
@@ -659,7 +718,7 @@ def main():
 
     if rank == 0 and step is None:
         print(json.dumps({"metric": "%s only (profiling aid)" % args.only, "decode": decode, "chunked": chunked,
-                          "scatter": scatter, "clocks": clk}), flush=True)
+                          "scatter": scatter, "pages": pages, "clocks": clk}), flush=True)
     elif rank == 0:
         line = {
             "metric": "causal prefill TFLOP/s (exact causal count, step incl. KV write + decode)",
@@ -678,6 +737,7 @@ def main():
             "decode": decode,
             "chunked": chunked,
             "scatter": scatter,
+            "pages": pages,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,

@@ -48,7 +48,8 @@
  *                    where a page is needed, a slot outside [0, num_slots), a
  *                    position beyond 16 * max_blocks_per_seq, or lengths that do
  *                    not fit the call; PA_ERR_TIMEOUT if a bounded wait inside a
- *                    kernel ran out.  The offending page or row is skipped (its
+ *                    kernel ran out; PA_ERR_OUT_OF_PAGES if a page allocation
+ *                    would take more pages than the free stack holds.  The offending page or row is skipped (its
  *                    output is unspecified) and the kernel never traps.  The caller
  *                    zeroes *err_flag before the call and reads it after
  *                    synchronising; the first error code written is kept.
@@ -72,7 +73,8 @@ typedef enum pa_status {
     PA_ERR_UNSUPPORTED = 2,  /* valid request outside what the kernels implement */
     PA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
     PA_ERR_BAD_BLOCK = 4,    /* device-reported through err_flag (see above) */
-    PA_ERR_TIMEOUT = 5       /* device-reported through err_flag (see above) */
+    PA_ERR_TIMEOUT = 5,      /* device-reported through err_flag (see above) */
+    PA_ERR_OUT_OF_PAGES = 6  /* device-reported: the free stack ran short (or would overflow) */
 } pa_status;
 
 /* Tokens per page; fixed ("BLOCK_SIZE = 16", tiny-vllm part 6, page layout). */
@@ -252,6 +254,40 @@ pa_status pa_decode_noalloc(const pa_geom* geom, const void* q, const void* pool
                             const int32_t* seq_lens, const int32_t* slots, int32_t max_seq_len,
                             float scale, void* o, float* lse, int32_t* err_flag,
                             pa_stream_t stream);
+
+/*
+ * Page lifetime on the device (NEXT to the hot path: keeps the block table
+ * resident instead of copying it from the host after every change).
+ * The free stack is free_pages[0 .. *free_count - 1] (device int32
+ * [num_blocks] and a device int32), its top last; the caller fills it once
+ * (e.g. with 0 .. num_blocks - 1) and owns both buffers.  Calls that touch the
+ * same stack or table must not overlap on the GPU (they race).
+ *
+ * pa_alloc_pages -- every logical block that positions 0 .. seq_lens[b] - 1 of
+ * slots[b] need, in every layer, whose table entry is -1 takes the page on top
+ * of the stack, walking sequences in order, then layers, then logical blocks
+ * (tiny-vllm part 6, "물리 블록의 수명: free_blocks 가 관리한다": a page is
+ * popped when a logical block's entry is -1, a prompt's blocks at prefill and a
+ * new block when a decode step's token starts one).  Entries below
+ * old_lens[b] / 16 are not looked at (old_lens: device int32 [batch] or NULL
+ * for 0).  All or nothing: if the stack holds fewer pages than needed, nothing
+ * changes and *err_flag gets PA_ERR_OUT_OF_PAGES; an invalid slot or length
+ * sets PA_ERR_BAD_BLOCK, also with nothing changed, as does a slot named
+ * twice in one call (checked for slots below 65536).  slots, seq_lens: device
+ * int32 [batch]; block_table: device, the layout of pa_write_kv.
+ *
+ * pa_release_slots -- every page held by slots[0 .. n-1], in every layer, goes
+ * back on the stack in the same walking order and its entry becomes -1 (the
+ * pages' slot-end loop).  Nothing changes (PA_ERR_OUT_OF_PAGES) if the stack
+ * would grow past num_blocks, which means a page was freed twice.
+ */
+pa_status pa_alloc_pages(const pa_geom* geom, int32_t* block_table, int32_t batch,
+                         const int32_t* slots, const int32_t* old_lens, const int32_t* seq_lens,
+                         int32_t* free_pages, int32_t* free_count, int32_t* err_flag,
+                         pa_stream_t stream);
+pa_status pa_release_slots(const pa_geom* geom, int32_t* block_table, int32_t n,
+                           const int32_t* slots, int32_t* free_pages, int32_t* free_count,
+                           int32_t* err_flag, pa_stream_t stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* pa_status_string(pa_status status);

@@ -194,6 +194,9 @@ int64_t orc_alloc_pages(const orc_geom* g, int32_t* block_table, int32_t batch, 
                         int32_t* free_count) {
     if (!geom_ok(g) || batch < 0 || !block_table || !free_pages || !free_count) return ORC_BAD_ARG;
     if (batch > 0 && (!slots || !seq_lens)) return ORC_BAD_ARG;
+    for (int32_t b = 0; b < batch; ++b) /* a slot named twice is refused */
+        for (int32_t c = 0; c < b; ++c)
+            if (slots[c] == slots[b]) return ORC_BAD_ARG;
     const int32_t mb = g->max_blocks_per_seq;
     int64_t need = 0;
     for (int pass = 0; pass < 2; ++pass) {
@@ -229,6 +232,9 @@ int64_t orc_release_slots(const orc_geom* g, int32_t* block_table, int32_t n, co
                           int32_t* free_pages, int32_t* free_count) {
     if (!geom_ok(g) || n < 0 || !block_table || !free_pages || !free_count) return ORC_BAD_ARG;
     if (n > 0 && !slots) return ORC_BAD_ARG;
+    for (int32_t i = 0; i < n; ++i) /* a slot named twice is refused */
+        for (int32_t c = 0; c < i; ++c)
+            if (slots[c] == slots[i]) return ORC_BAD_ARG;
     const int32_t mb = g->max_blocks_per_seq;
     int64_t held = 0;
     for (int32_t i = 0; i < n; ++i) {

@@ -70,7 +70,7 @@ int64_t orc_write_kv(const orc_geom* g, uint8_t* pool, const int32_t* block_tabl
  * when the stack runs short.  orc_release_slots: every page held by the
  * slots goes back (push) in the same walking order and its entry becomes -1.
  * Both return the number of pages moved, or ORC_BAD_ARG with nothing
- * changed. */
+ * changed (also when a slot is named twice in one call). */
 int64_t orc_alloc_pages(const orc_geom* g, int32_t* block_table, int32_t batch, const int32_t* slots,
                         const int32_t* old_lens, const int32_t* seq_lens, int32_t* free_pages,
                         int32_t* free_count);

@@ -14,6 +14,8 @@ Calls (same names as the C ABI):
 * ``pa_prefill_cached(geom, q, pool, block_table, layer, cu_seqlens, prefix_lens, slots, max_seqlen, scale, o, lse, err_flag)``
 * ``pa_decode(geom, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse, workspace, err_flag)``
 * ``pa_decode_noalloc(geom, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse, err_flag)``
+* ``pa_alloc_pages(geom, block_table, slots, seq_lens, free_pages, free_count, err_flag, old_lens=None)``
+* ``pa_release_slots(geom, block_table, slots, free_pages, free_count, err_flag)``
 * ``pa_decode_workspace_size(geom, batch, max_seq_len)``, ``pa_page_bytes(geom)``, ``pa_status_string(code)``
 
 Tensors are torch CUDA tensors (bf16 data may be given as bfloat16 or int16
@@ -28,12 +30,13 @@ PA_ERR_UNSUPPORTED = 2
 PA_ERR_CUDA = 3
 PA_ERR_BAD_BLOCK = 4
 PA_ERR_TIMEOUT = 5
+PA_ERR_OUT_OF_PAGES = 6
 PA_BLOCK_TOKENS = 16
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libpa.so")
 EXPORTED = ("pa_page_bytes", "pa_write_kv", "pa_write_kv_rope", "pa_prefill", "pa_prefill_cached", "pa_decode_workspace_size", "pa_decode",
-            "pa_decode_noalloc", "pa_status_string")
+            "pa_decode_noalloc", "pa_alloc_pages", "pa_release_slots", "pa_status_string")
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -91,6 +94,10 @@ def load_library(path: str = None):
     L.pa_decode_noalloc.restype = C.c_int
     L.pa_decode_noalloc.argtypes = [C.POINTER(PaGeom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P,
                                     C.c_int32, C.c_float, _P, _P, _P, _P]
+    L.pa_alloc_pages.restype = C.c_int
+    L.pa_alloc_pages.argtypes = [C.POINTER(PaGeom), _P, C.c_int32, _P, _P, _P, _P, _P, _P, _P]
+    L.pa_release_slots.restype = C.c_int
+    L.pa_release_slots.argtypes = [C.POINTER(PaGeom), _P, C.c_int32, _P, _P, _P, _P, _P]
     L.pa_status_string.restype = C.c_char_p
     L.pa_status_string.argtypes = [C.c_int]
     if path == LIB_PATH:
@@ -201,3 +208,17 @@ def pa_decode_noalloc(g, q, pool, block_table, layer, seq_lens, slots, max_seq_l
         C.byref(g), _ptr(q), _ptr(pool), _ptr(block_table), layer, batch, _ptr(seq_lens),
         _ptr(slots), int(max_seq_len), float(scale), _ptr(o), _ptr(lse), _ptr(err_flag),
         _stream(stream)))
+
+
+def pa_alloc_pages(g, block_table, slots, seq_lens, free_pages, free_count, err_flag, old_lens=None, stream=None):
+    """Pages for every -1 entry the new lengths need, popped from the device free stack."""
+    _check("pa_alloc_pages", lib().pa_alloc_pages(
+        C.byref(g), _ptr(block_table), int(slots.shape[0]), _ptr(slots), _ptr(old_lens), _ptr(seq_lens),
+        _ptr(free_pages), _ptr(free_count), _ptr(err_flag), _stream(stream)))
+
+
+def pa_release_slots(g, block_table, slots, free_pages, free_count, err_flag, stream=None):
+    """Every page of the slots back on the device free stack; their entries become -1."""
+    _check("pa_release_slots", lib().pa_release_slots(
+        C.byref(g), _ptr(block_table), int(slots.shape[0]), _ptr(slots), _ptr(free_pages), _ptr(free_count),
+        _ptr(err_flag), _stream(stream)))

@@ -161,6 +161,30 @@ PA_API pa_status pa_decode(const pa_geom* geom, const void* q, const void* pool,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+PA_API pa_status pa_alloc_pages(const pa_geom* geom, int32_t* block_table, int32_t batch,
+                                const int32_t* slots, const int32_t* old_lens, const int32_t* seq_lens,
+                                int32_t* free_pages, int32_t* free_count, int32_t* err_flag,
+                                pa_stream_t stream) {
+    if (!geom_valid(geom) || batch < 0) return PA_ERR_INVALID_ARG;
+    if (!block_table || !free_pages || !free_count || !err_flag) return PA_ERR_INVALID_ARG;
+    if (batch > 0 && (!slots || !seq_lens)) return PA_ERR_INVALID_ARG;
+    if (batch == 0) return PA_OK;
+    return cuda_status(pa::launch_alloc_pages(kgeom(geom), block_table, batch, slots, old_lens, seq_lens,
+                                              free_pages, free_count, err_flag,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+PA_API pa_status pa_release_slots(const pa_geom* geom, int32_t* block_table, int32_t n,
+                                  const int32_t* slots, int32_t* free_pages, int32_t* free_count,
+                                  int32_t* err_flag, pa_stream_t stream) {
+    if (!geom_valid(geom) || n < 0) return PA_ERR_INVALID_ARG;
+    if (!block_table || !free_pages || !free_count || !err_flag) return PA_ERR_INVALID_ARG;
+    if (n > 0 && !slots) return PA_ERR_INVALID_ARG;
+    if (n == 0) return PA_OK;
+    return cuda_status(pa::launch_release_slots(kgeom(geom), block_table, n, slots, free_pages, free_count,
+                                                err_flag, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 PA_API const char* pa_status_string(pa_status status) {
     switch (status) {
         case PA_OK: return "PA_OK: success";
@@ -169,6 +193,7 @@ PA_API const char* pa_status_string(pa_status status) {
         case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime or launch error";
         case PA_ERR_BAD_BLOCK: return "PA_ERR_BAD_BLOCK: invalid page, slot, position or length";
         case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+        case PA_ERR_OUT_OF_PAGES: return "PA_ERR_OUT_OF_PAGES: the free page stack ran short (or would overflow)";
     }
     return "unknown pa_status";
 }

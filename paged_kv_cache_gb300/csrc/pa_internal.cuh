@@ -515,6 +515,11 @@ cudaError_t launch_write_kv(const KGeom& g, void* pool, const int32_t* block_tab
                             int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,
                             const void* k_new, const void* v_new, int32_t* err,
                             cudaStream_t stream);
+cudaError_t launch_alloc_pages(const KGeom& g, int32_t* table, int batch, const int32_t* slots,
+                               const int32_t* old_lens, const int32_t* seq_lens, int32_t* free_pages,
+                               int32_t* free_count, int32_t* err, cudaStream_t stream);
+cudaError_t launch_release_slots(const KGeom& g, int32_t* table, int n, const int32_t* slots, int32_t* free_pages,
+                                 int32_t* free_count, int32_t* err, cudaStream_t stream);
 cudaError_t launch_write_kv_rope(const KGeom& g, void* pool, const int32_t* block_table, int layer,
                                  int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,
                                  const void* k_new, const void* v_new, const float* cos_tab,
