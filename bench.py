@@ -509,6 +509,18 @@ def oracle_sample(case, seconds, rng_seed=5):
 
 # ------------------------------------------------------------------- arms
 
+METRIC = "causal prefill TFLOP/s (exact causal count, step incl. KV write + decode)"
+
+
+def step_config(geom, batch, seqlen, world):
+    """The workload both arms report: the main step's shape."""
+    return {"workload": "long-context causal prefill %d x %d, %d q / %d kv heads, d %d, paged through shuffled "
+                        "16-token pages; step = write_kv + prefill + write_kv(new token) + decode(%d)" % (
+                            batch, seqlen, geom.num_q_heads, geom.num_kv_heads, geom.head_dim, seqlen + 1),
+            "global_batch": batch * world, "seq_len": seqlen, "parallelism": "replicas x%d" % world,
+            "l2": "flushed (256 MiB write) before every timed step, outside the events"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -545,11 +557,11 @@ def run_reference(args, rank, world):
     sample = ("per step: %d random (row, q head) outputs of the 4 x 8192 causal prefill, fp64 oracle, "
               "K/V gathered through the block table" % pairs)
     line = {
-        "impl": "reference", "metric": "causal prefill TFLOP/s (exact causal count, step incl. KV write + decode)",
+        "impl": "reference", "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "long-context causal prefill 4 x 8192, 32 q / 8 kv heads, d 64"},
+        "config": step_config(case.geom, case.batch, int(case.lens[0]), world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -721,17 +733,11 @@ def main():
                           "scatter": scatter, "pages": pages, "clocks": clk}), flush=True)
     elif rank == 0:
         line = {
-            "metric": "causal prefill TFLOP/s (exact causal count, step incl. KV write + decode)",
+            "metric": METRIC,
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, shuffled pages)",
-            "config": {"workload": "long-context causal prefill 4 x 8192, %d q / %d kv heads, d %d, "
-                                   "paged through shuffled 16-token pages; step = write_kv + prefill + "
-                                   "write_kv(new token) + decode(8193)" % (
-                                       step.geom.num_q_heads, step.geom.num_kv_heads, step.geom.head_dim),
-                       "global_batch": step.case.batch * world, "seq_len": step.n,
-                       "parallelism": "replicas x%d" % world,
-                       "l2": "flushed (256 MiB write) before every timed step, outside the events"},
+            "config": step_config(step.geom, step.case.batch, step.n, world),
             "gpu_launches": step.launches * args.steps,
             "roofline": roofline,
             "decode": decode,
