@@ -172,6 +172,9 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_consumers = (blockDim.x >> 5) - 1;
     const long long G = gridDim.x, c = blockIdx.x;
+    // The merge grid may be scheduled now: its CTAs wait (griddepcontrol.wait)
+    // until this grid has finished and its writes are visible.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
         for (int s = 0; s < p.nst; ++s) {
@@ -221,8 +224,6 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
     const long long sp_first = ctl[1];
     if (n_pages <= 0 || b_first < 0) return;
 
-    const long long row_bytes = static_cast<long long>(g.kv_dim) * 2;
-    const long long half_page = g.page_bytes / 2;
 
     if (warp == 0) {
         // ------------------------------------------------------ producer
