@@ -70,6 +70,9 @@ def lib():
         L.orc_prefill_cached_rows.restype = C.c_int
         L.orc_prefill_cached_rows.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, _P,
                                               C.c_float, C.c_int64, _P, _P, _P, _P, C.c_int32]
+        L.orc_prefill_backward.restype = C.c_int
+        L.orc_prefill_backward.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, C.c_float, _P,
+                                           _P, _P, _P, C.c_int32]
         L.orc_decode.restype = C.c_int
         L.orc_decode.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P,
                                  C.c_float, _P, _P, C.c_int32]
@@ -260,6 +263,22 @@ def prefill_cached_rows(g, q, pool, block_table, layer, cu_seqlens, prefix_lens,
                                        layer, cu.shape[0] - 1, _ptr(cu), _ptr(pre), _ptr(sl), C.c_float(scale),
                                        n, _ptr(rows), _ptr(heads), _ptr(o), _ptr(lse), nthreads)
     return int(st), o, lse
+
+
+def prefill_backward(g, q, pool, block_table, layer, cu_seqlens, slots, scale, dout, nthreads=0):
+    """Gradients of the causal prefill: (status, dQ[T][Hq][d], dK[T][Hkv][d], dV[T][Hkv][d]) float64."""
+    cu = _c(cu_seqlens, np.int32)
+    sl = _c(slots, np.int32)
+    T = int(cu[-1])
+    q = _c(q, np.uint16)
+    do = _c(dout, np.uint16)
+    dq = np.zeros((T, g.num_q_heads, g.head_dim), np.float64)
+    dk = np.zeros((T, g.num_kv_heads, g.head_dim), np.float64)
+    dv = np.zeros_like(dk)
+    st = lib().orc_prefill_backward(C.byref(g), _ptr(q), _ptr(pool), _ptr(_c(block_table, np.int32)), layer,
+                                    cu.shape[0] - 1, _ptr(cu), _ptr(sl), C.c_float(scale), _ptr(do), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), nthreads)
+    return int(st), dq, dk, dv
 
 
 def decode(g, q, pool, block_table, layer, seq_lens, slots, scale, nthreads=0):

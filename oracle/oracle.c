@@ -614,6 +614,125 @@ int orc_prefill_cached_rows(const orc_geom* g, const uint16_t* q, const uint8_t*
                           nsamp, rows ? rows : &no_rows, heads, o, lse, nthreads);
 }
 
+/* ------------------------------------------------------------ backward */
+
+typedef struct {
+    const orc_geom* g;
+    const uint16_t* q;
+    const uint16_t* dout;
+    const int32_t* cu;
+    double scale;
+    double** K;
+    double** V;
+    double* dq;
+    double* dk;
+    double* dv;
+    int32_t batch;
+} backward_ctx;
+
+/* Gradients of the causal prefill of sequence b for the q heads of kv head hk
+ * (one work item: it alone writes these dQ rows and these dK / dV rows).  The
+ * definition, by the chain rule through o_i = sum_j p_ij v_j and the softmax
+ * p_ij = e^(s_ij) / sum_k e^(s_ik), s_ij = scale q_i . k_j, j <= i:
+ *   dv_j += sum_i p_ij do_i          dp_ij = do_i . v_j
+ *   D_i   = sum_j p_ij dp_ij         ds_ij = p_ij (dp_ij - D_i)
+ *   dq_i  = scale sum_j ds_ij k_j    dk_j += scale sum_i ds_ij q_i
+ * with dk, dv summed over the q heads that read kv head hk [FA2 "4. MQA · GQA
+ * 지원": the gradients of the implicitly repeated heads are added]; p is
+ * recomputed here from the scores, as the FA2 backward recomputes it from the
+ * stored L [FA2, 전체 흐름: "L로 P 재계산"]. */
+static void backward_item(void* ctx, int64_t item, double* scratch) {
+    const backward_ctx* c = (const backward_ctx*)ctx;
+    const orc_geom* g = c->g;
+    const int32_t hq_n = g->num_q_heads, hkv = g->num_kv_heads, d = g->head_dim;
+    const int32_t group = hq_n / hkv;
+    const int32_t b = (int32_t)(item / hkv), hk = (int32_t)(item % hkv);
+    const int64_t r0 = c->cu[b];
+    const int32_t n = c->cu[b + 1] - c->cu[b];
+    const double* K = c->K[b];
+    const double* V = c->V[b];
+    double* qv = scratch;        /* d */
+    double* dov = qv + d;        /* d */
+    double* p = dov + d;         /* n */
+    double* ds = p + n;          /* n */
+    for (int32_t r = 0; r < group; ++r) {
+        const int32_t h = hk * group + r;
+        for (int32_t i = 0; i < n; ++i) {
+            const int64_t row = r0 + i;
+            for (int32_t k = 0; k < d; ++k) {
+                qv[k] = bf16_to_double(c->q[(row * hq_n + h) * d + k]);
+                dov[k] = bf16_to_double(c->dout[(row * hq_n + h) * d + k]);
+            }
+            double m = -INFINITY;
+            for (int32_t j = 0; j <= i; ++j) {
+                const double* kj = K + ((int64_t)j * hkv + hk) * d;
+                double dot = 0.0;
+                for (int32_t k = 0; k < d; ++k) dot += qv[k] * kj[k];
+                p[j] = c->scale * dot;
+                if (p[j] > m) m = p[j];
+            }
+            double l = 0.0;
+            for (int32_t j = 0; j <= i; ++j) l += exp(p[j] - m);
+            double D = 0.0;
+            for (int32_t j = 0; j <= i; ++j) {
+                p[j] = exp(p[j] - m) / l;
+                const double* vj = V + ((int64_t)j * hkv + hk) * d;
+                double dp = 0.0;
+                for (int32_t k = 0; k < d; ++k) dp += dov[k] * vj[k];
+                ds[j] = dp;
+                D += p[j] * dp;
+            }
+            double* dqi = c->dq + (row * hq_n + h) * d;
+            for (int32_t k = 0; k < d; ++k) dqi[k] = 0.0;
+            for (int32_t j = 0; j <= i; ++j) {
+                ds[j] = p[j] * (ds[j] - D);
+                const double* kj = K + ((int64_t)j * hkv + hk) * d;
+                double* dkj = c->dk + ((r0 + j) * hkv + hk) * d;
+                double* dvj = c->dv + ((r0 + j) * hkv + hk) * d;
+                for (int32_t k = 0; k < d; ++k) {
+                    dqi[k] += c->scale * ds[j] * kj[k];
+                    dkj[k] += c->scale * ds[j] * qv[k];
+                    dvj[k] += p[j] * dov[k];
+                }
+            }
+        }
+    }
+}
+
+int orc_prefill_backward(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                         const int32_t* block_table, int32_t layer, int32_t batch,
+                         const int32_t* cu_seqlens, const int32_t* slots, float scale,
+                         const uint16_t* dout, double* dq, double* dk, double* dv, int32_t nthreads) {
+    if (!check_batch(g, batch, cu_seqlens, slots, layer) || !pool || !block_table || !dq || !dk || !dv)
+        return ORC_BAD_ARG;
+    const int64_t T = cu_seqlens[batch];
+    if (T > 0 && (!q || !dout)) return ORC_BAD_ARG;
+    int32_t* lens = (int32_t*)malloc(sizeof(int32_t) * (size_t)(batch + 1));
+    double** K = (double**)calloc((size_t)batch + 1, sizeof(double*));
+    double** V = (double**)calloc((size_t)batch + 1, sizeof(double*));
+    if (!lens || !K || !V) {
+        free(lens); free(K); free(V);
+        return ORC_BAD_ARG;
+    }
+    int32_t nmax = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        lens[b] = cu_seqlens[b + 1] - cu_seqlens[b];
+        if (lens[b] > nmax) nmax = lens[b];
+    }
+    const int64_t kv = kv_dim(g);
+    for (int64_t x = 0; x < T * g->num_q_heads * g->head_dim; ++x) dq[x] = 0.0;
+    for (int64_t x = 0; x < T * kv; ++x) dk[x] = dv[x] = 0.0;
+    int st = gather_all(g, pool, block_table, layer, batch, lens, slots, NULL, K, V);
+    if (st == ORC_OK) {
+        backward_ctx c = {g, q, dout, cu_seqlens, (double)scale, K, V, dq, dk, dv, batch};
+        run_items(backward_item, &c, (int64_t)batch * g->num_kv_heads, 2 * (int64_t)g->head_dim + 2 * nmax,
+                  nthreads);
+    }
+    free_all(batch, K, V);
+    free(lens);
+    return st;
+}
+
 /* -------------------------------------------------------------- decode */
 
 typedef struct {

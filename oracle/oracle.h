@@ -153,6 +153,17 @@ int orc_prefill_cached_rows(const orc_geom* g, const uint16_t* q, const uint8_t*
                             const int32_t* slots, float scale, int64_t nsamp, const int64_t* rows,
                             const int32_t* heads, double* o, double* lse, int32_t nthreads);
 
+/* Gradients of the causal prefill (orc_prefill's definition) with respect to
+ * q and to the K/V rows it reads, given the output gradient dout[T][Hq][d]
+ * (bf16 bits): dq[T][Hq][d], and dk, dv[T][Hkv][d] for the prompt tokens in
+ * packed row order, kv head h of row t holding the sum over the q heads that
+ * read it [FA2 "4. MQA · GQA 지원"].  fp64, from the chain rule through the
+ * softmax with p recomputed from the scores [FA2, 전체 흐름]. */
+int orc_prefill_backward(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                         const int32_t* block_table, int32_t layer, int32_t batch,
+                         const int32_t* cu_seqlens, const int32_t* slots, float scale,
+                         const uint16_t* dout, double* dq, double* dk, double* dv, int32_t nthreads);
+
 /* Single-query decode [TV6 "논리 블록 → 물리 블록 → 바이트 주소"]: query b
  * (q[B][Hq][d]) attends keys 0..seq_lens[b]-1 of slots[b]; the length
  * includes the token just written.  seq_len 0 gives O = 0, L = -inf.

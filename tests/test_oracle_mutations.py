@@ -10,6 +10,7 @@ import subprocess
 import pytest
 
 import oracle
+from tests import test_oracle_backward_pins as bpins
 from tests import test_oracle_chunked_pins as cpins
 from tests import test_oracle_pages_pins as ppins
 from tests import test_oracle_rope_pins as rpins
@@ -45,6 +46,11 @@ MUTANTS = {
                           "        for (int32_t b = batch - 1; b >= 0; --b) {\n            const int32_t slot = slots[b], len = seq_lens[b];"),
     "release_keeps_entry": ("                free_pages[top++] = *e; /* push_back */\n                *e = -1;",
                             "                free_pages[top++] = *e; /* push_back */"),
+    "bwd_D_dropped": ("ds[j] = p[j] * (ds[j] - D);", "ds[j] = p[j] * ds[j];"),
+    "bwd_dk_unscaled": ("dkj[k] += c->scale * ds[j] * qv[k];", "dkj[k] += ds[j] * qv[k];"),
+    "bwd_dv_uses_ds": ("dvj[k] += p[j] * dov[k];", "dvj[k] += ds[j] * dov[k];"),
+    "bwd_first_head_only": ("    for (int32_t r = 0; r < group; ++r) {\n        const int32_t h = hk * group + r;\n        for (int32_t i = 0; i < n; ++i) {",
+                            "    for (int32_t r = 0; r < 1; ++r) {\n        const int32_t h = hk * group + r;\n        for (int32_t i = 0; i < n; ++i) {"),
     "max_not_subtracted": ("for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m);",
                            "for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m) * (1 + 1e-9 * m);"),
 }
@@ -68,6 +74,8 @@ PIN_TESTS = [
     lambda gd: rpins.test_matches_torch_fp32_ops_byte_for_byte(),
     lambda gd: ppins.test_worked_example(gd),
     lambda gd: ppins.test_decode_takes_a_page_only_at_a_new_block(),
+    lambda gd: bpins.test_matches_torch_autograd(8, 2, 64, [40, 17]),
+    lambda gd: bpins.test_identities(),
 ]
 
 
