@@ -17,6 +17,8 @@ decode's 4 d Hq n).  The line also carries:
                   against the measured HBM copy bandwidth;
   chunked      -- pa_prefill_cached: 4 x 2048-query chunks after 6144 cached
                   tokens, exact-causal TFLOP/s against the same bf16 peak;
+  backward     -- pa_prefill_backward on the long prompt (4 x 8192, d 64):
+                  2.5 x the exact causal count, TFLOP/s against that peak;
   e2e          -- the same metric through the C ABI with host buffers: pinned
                   H2D of the step's inputs and D2H of its outputs inside the
                   timed region;
@@ -56,7 +58,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time (10-30 s)")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "chunked", "scatter", "pages"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "chunked", "scatter", "pages", "backward"], default="all",
                     help="profiling aid: run only the main (prefill) step or only the decode step")
     ap.add_argument("--batch", type=int, default=4, help="prefill sequences (profiling aid)")
     ap.add_argument("--seqlen", type=int, default=8192, help="prefill length (profiling aid)")
@@ -296,6 +298,48 @@ class ChunkedStep:
             ev[0].record()
         pa.pa_prefill_cached(self.g, d["q"], self.pool, d["bt"], 0, d["cu"], d["pre"], d["slots"], self.chunk,
                              c.scale, self.o, self.lse, self.err)
+        if ev is not None:
+            ev[1].record()
+
+
+class BackwardStep:
+    """Gradients of the long-prompt prefill (4 x 8192 tokens, 32 q / 8 kv heads,
+    d 64): the forward runs once to give o and lse; a step is one
+    pa_prefill_backward (D = do . o, then the column-block kernel)."""
+
+    def __init__(self, torch, pa, W, seed=1007, batch=4, seqlen=8192):
+        self.torch, self.pa = torch, pa
+        case = W.c4_long("d64", seed=seed, batch=batch, seqlen=seqlen)
+        self.case, self.geom = case, case.geom
+        self.g = pa.geom(*self.geom.as_tuple())
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        w = case.writes[0]
+        self.d = {"q": dev(case.q), "bt": dev(case.block_table), "cu": dev(case.cu_seqlens), "slots": dev(case.slots)}
+        self.pool = torch.empty(self.geom.pool_bytes, dtype=torch.uint8, device="cuda")
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pa.pa_write_kv(self.g, self.pool, self.d["bt"], 0, dev(w.tok_slot), dev(w.tok_pos), dev(w.k), dev(w.v),
+                       self.err)
+        T, Hq, Hkv, D = case.total_tokens, self.geom.num_q_heads, self.geom.num_kv_heads, self.geom.head_dim
+        self.o = torch.empty((T, Hq, D), dtype=torch.int16, device="cuda")
+        self.lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+        pa.pa_prefill(self.g, self.d["q"], self.pool, self.d["bt"], 0, self.d["cu"], self.d["slots"], case.max_len,
+                      case.scale, self.o, self.lse, self.err)
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed)
+        self.dout = torch.randn((T, Hq, D), generator=gen, device="cuda").to(torch.bfloat16)
+        self.delta = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+        self.dq = torch.empty((T, Hq, D), dtype=torch.float32, device="cuda")
+        self.dk = torch.empty((T, Hkv, D), dtype=torch.float32, device="cuda")
+        self.dv = torch.empty((T, Hkv, D), dtype=torch.float32, device="cuda")
+        # 5 products of 2 d flops per (query, key) pair on or below the diagonal: 2.5 x the forward's count
+        self.flops = float(10.0 * D * Hq * np.sum(case.lens.astype(np.float64) * (case.lens + 1) / 2))
+
+    def run(self, ev=None):
+        pa, c, d = self.pa, self.case, self.d
+        if ev is not None:
+            ev[0].record()
+        pa.pa_prefill_backward(self.g, d["q"], self.pool, d["bt"], 0, d["cu"], d["slots"], c.max_len, c.scale,
+                               self.o, self.lse, self.dout, self.delta, self.dq, self.dk, self.dv, self.err)
         if ev is not None:
             ev[1].record()
 
@@ -689,6 +733,30 @@ def main():
                                           "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": s_avg * 1e3}}
         del sstep
 
+    backward = None
+    if args.only in ("all", "backward"):
+        # ----------------------------------------- FA2 backward over the pages (f4)
+        bstep = BackwardStep(torch, pa, W)
+        bsteps = max(10, args.steps // 4)
+        b_s, bk_s = timed(torch, lambda ev: bstep.run(ev=ev), bsteps, args.warmup, flush, dist)
+        torch.cuda.synchronize()
+        if int(bstep.err.item()) != 0:
+            raise SystemExit("device error in backward steps: %s" % pa.pa_status_string(int(bstep.err.item())))
+        b_avg = float(np.mean(bk_s))
+        b_rate, b_total, _ = job_rate(torch, dist, bstep.flops * bsteps, float(np.sum(b_s)))
+        bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        b_ach = bstep.flops / b_avg / 1e12
+        backward = {"metric": "prefill backward TFLOP/s (4 x 8192 tokens, 32 q / 8 kv heads, d 64; "
+                              "exact causal count x 2.5)",
+                    "value": b_rate / 1e12, "unit": "TFLOP/s", "ms_per_step": b_total / bsteps * 1e3,
+                    "steps": bsteps,
+                    "roofline": {"bound": "tensor", "achieved": b_ach, "peak": bf16_peak, "unit": "TFLOP/s",
+                                 "frac": b_ach / bf16_peak, "traffic": profiled_traffic("backward_d64"),
+                                 "kernel": "bwd_prep_kernel<64> + bwd_main_kernel<64>",
+                                 "peak_source": "%s bf16_tflops (burst)" % peak_src,
+                                 "algorithmic_flops_per_launch": bstep.flops, "avg_launch_ms": b_avg * 1e3}}
+        del bstep
+
     pages = None
     if args.only in ("all", "pages"):
         # ----------------------------------- page lifetime on the device (f3)
@@ -730,7 +798,7 @@ def main():
 
     if rank == 0 and step is None:
         print(json.dumps({"metric": "%s only (profiling aid)" % args.only, "decode": decode, "chunked": chunked,
-                          "scatter": scatter, "pages": pages, "clocks": clk}), flush=True)
+                          "scatter": scatter, "pages": pages, "backward": backward, "clocks": clk}), flush=True)
     elif rank == 0:
         line = {
             "metric": METRIC,
@@ -744,6 +812,7 @@ def main():
             "chunked": chunked,
             "scatter": scatter,
             "pages": pages,
+            "backward": backward,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,

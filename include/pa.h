@@ -189,6 +189,38 @@ pa_status pa_prefill_cached(const pa_geom* geom, const void* q, const void* pool
                             pa_stream_t stream);
 
 /*
+ * pa_prefill_backward -- gradients of pa_prefill's output with respect to q
+ * and to the K / V rows it read from the pages (training only).
+ * Definition: with s_ij = scale <q_i, k_j> (j <= i), p_ij = e^(s_ij - L_i)
+ * recomputed from the stored L = lse (FlashAttention-2 explainer, "전체
+ * 흐름": the backward rebuilds P from L), do = dout and o the forward output:
+ *   D_i = <do_i, o_i>,  dp_ij = <do_i, v_j>,  ds_ij = p_ij (dp_ij - D_i),
+ *   dv_j = sum_i p_ij do_i,  dk_j = scale sum_i ds_ij q_i,  dq_i = scale sum_j ds_ij k_j,
+ * with dk, dv summed over the q heads of each kv head's group ("4. MQA · GQA
+ * 지원").  Work is split by key blocks, dq contributions are added atomically
+ * ("2. 시퀀스 길이 방향으로도 병렬화", item 4), so dq's low bits vary from run
+ * to run; dk and dv do not.
+ * Arguments: q, pool, block_table, layer, batch, cu_seqlens, slots,
+ * max_seqlen, total_tokens, scale: exactly those of the pa_prefill call whose
+ * gradients are wanted (the pages must still hold the same K/V).  o: device
+ * bf16 [total_tokens][Hq][d] and lse: device fp32 [total_tokens][Hq], that
+ * call's outputs.  dout: device bf16 [total_tokens][Hq][d].  delta: device fp32
+ * [total_tokens][Hq] workspace (overwritten with D).  dq: device fp32
+ * [total_tokens][Hq][d], set to zero first (every row).  dk, dv: device fp32
+ * [total_tokens][Hkv][d], row t is the gradient of the K / V row written for
+ * token t; rows not covered by cu_seqlens are not written.  q, o, dout, dq,
+ * dk, dv and pool 16-byte aligned; lse, delta 4-byte aligned.  Requires d in
+ * {64, 128} and max_seqlen <= 4194240.  Bad lengths, slots or table entries
+ * set PA_ERR_BAD_BLOCK (the gradients of that sequence are then unspecified).
+ */
+pa_status pa_prefill_backward(const pa_geom* geom, const void* q, const void* pool,
+                              const int32_t* block_table, int32_t layer, int32_t batch,
+                              const int32_t* cu_seqlens, const int32_t* slots, int32_t max_seqlen,
+                              int32_t total_tokens, float scale, const void* o, const float* lse,
+                              const void* dout, float* delta, float* dq, float* dk, float* dv,
+                              int32_t* err_flag, pa_stream_t stream);
+
+/*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
  * up to `batch` sequences of up to `max_seq_len` tokens.  Depends only on the
  * geometry and these two numbers (not on the device).  0 for invalid input.

@@ -134,6 +134,31 @@ PA_API pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool
                              max_seqlen, total_tokens, scale, o, lse, err_flag, stream);
 }
 
+PA_API pa_status pa_prefill_backward(const pa_geom* geom, const void* q, const void* pool,
+                                     const int32_t* block_table, int32_t layer, int32_t batch,
+                                     const int32_t* cu_seqlens, const int32_t* slots, int32_t max_seqlen,
+                                     int32_t total_tokens, float scale, const void* o, const float* lse,
+                                     const void* dout, float* delta, float* dq, float* dk, float* dv,
+                                     int32_t* err_flag, pa_stream_t stream) {
+    if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= geom->n_layers) return PA_ERR_INVALID_ARG;
+    if (batch < 0 || max_seqlen < 0 || total_tokens < 0 || !std::isfinite(scale) || !(scale > 0.f))
+        return PA_ERR_INVALID_ARG;
+    if (geom->head_dim != 64 && geom->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (total_tokens == 0) return PA_OK;
+    if (!q || !pool || !o || !lse || !dout || !delta || !dq || !dk || !dv || !err_flag)
+        return PA_ERR_INVALID_ARG;
+    if (batch > 0 && (!block_table || !cu_seqlens || !slots)) return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv) || !aligned16(pool) || (reinterpret_cast<uintptr_t>(lse) & 3) ||
+        (reinterpret_cast<uintptr_t>(delta) & 3))
+        return PA_ERR_INVALID_ARG;
+    if (max_seqlen > 64 * 65535) return PA_ERR_UNSUPPORTED;
+    return cuda_status(pa::launch_prefill_backward(kgeom(geom), q, pool, block_table, layer, batch, cu_seqlens,
+                                                   slots, max_seqlen, total_tokens, scale, o, lse, dout, delta,
+                                                   dq, dk, dv, err_flag, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 PA_API size_t pa_decode_workspace_size(const pa_geom* geom, int32_t batch, int32_t max_seq_len) {
     if (!geom_valid(geom) || batch < 0 || max_seq_len < 0) return 0;
     return pa::decode_workspace_bytes(kgeom(geom), batch, max_seq_len);

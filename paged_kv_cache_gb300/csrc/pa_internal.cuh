@@ -533,6 +533,11 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool,
 
 size_t decode_workspace_bytes(const KGeom& g, int batch, int max_seq_len);
 bool decode_supported(const KGeom& g);
+cudaError_t launch_prefill_backward(const KGeom& g, const void* q, const void* pool, const int32_t* bt,
+                                    int layer, int batch, const int32_t* cu, const int32_t* slots,
+                                    int max_seqlen, int total_tokens, float scale, const void* o,
+                                    const float* lse, const void* dout, float* delta, float* dq, float* dk,
+                                    float* dv, int32_t* err, cudaStream_t stream);
 cudaError_t launch_decode(const KGeom& g, const void* q, const void* pool,
                           const int32_t* block_table, int layer, int batch,
                           const int32_t* seq_lens, const int32_t* slots, int max_seq_len,
