@@ -97,6 +97,15 @@ def test_validation_without_gpu(lib):
                               NULL, NULL, NULL, NULL) == pa.PA_ERR_INVALID_ARG
         assert lib.pa_decode(C.byref(g), NULL, NULL, NULL, 0, 1, NULL, NULL, 4, C.c_float(bad), NULL, NULL,
                              NULL, 0, NULL, NULL) == pa.PA_ERR_INVALID_ARG
+    # backward: no rows is a no-op; bad scale, head dim, pointers and alignment are refused
+    bw = lambda gg, T, sc, ptr=NULL, lse=NULL: lib.pa_prefill_backward(
+        C.byref(gg), ptr, ptr, ptr, 0, 1, ptr, ptr, 4, T, C.c_float(sc), ptr, lse, ptr, lse, ptr, ptr, ptr, ptr, NULL)
+    assert bw(g, 0, 0.1) == pa.PA_OK
+    assert bw(g, 4, 0.0) == pa.PA_ERR_INVALID_ARG
+    assert bw(g96, 4, 0.1) == pa.PA_ERR_UNSUPPORTED
+    assert bw(g, 4, 0.1) == pa.PA_ERR_INVALID_ARG                  # null pointers
+    assert bw(g, 4, 0.1, ptr=24, lse=16) == pa.PA_ERR_INVALID_ARG  # 8-byte aligned tensors
+    assert bw(g, 4, 0.1, ptr=32, lse=18) == pa.PA_ERR_INVALID_ARG  # misaligned fp32 rows
     # decode: unsupported group size 3, too-small workspace
     g3 = pa.geom(6, 2, 64, 1, 1, 4, 8)
     assert lib.pa_decode(C.byref(g3), NULL, NULL, NULL, 0, 1, NULL, NULL, 4, C.c_float(0.1), NULL, NULL,
