@@ -309,8 +309,10 @@ class BackwardStep:
 
     def __init__(self, torch, pa, W, seed=1007, batch=4, seqlen=8192):
         self.torch, self.pa = torch, pa
-        case = W.c4_long("d64", seed=seed, batch=batch, seqlen=seqlen)
-        self.case, self.geom = case, case.geom
+        pages = (seqlen + 15) // 16
+        geom = W.Geometry(32, 8, 64, 1, batch, pages, batch * pages + 64)
+        case = W.make_prefill_case("bwd", geom, [seqlen] * batch, seed)
+        self.case, self.geom = case, geom
         self.g = pa.geom(*self.geom.as_tuple())
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
         w = case.writes[0]
@@ -736,7 +738,7 @@ def main():
     backward = None
     if args.only in ("all", "backward"):
         # ----------------------------------------- FA2 backward over the pages (f4)
-        bstep = BackwardStep(torch, pa, W)
+        bstep = BackwardStep(torch, pa, W, batch=args.batch, seqlen=args.seqlen)
         bsteps = max(10, args.steps // 4)
         b_s, bk_s = timed(torch, lambda ev: bstep.run(ev=ev), bsteps, args.warmup, flush, dist)
         torch.cuda.synchronize()
