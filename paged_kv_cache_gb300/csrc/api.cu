@@ -154,7 +154,9 @@ PA_API pa_status pa_prefill_backward(const pa_geom* geom, const void* q, const v
         (reinterpret_cast<uintptr_t>(delta) & 3))
         return PA_ERR_INVALID_ARG;
     if (max_seqlen > 64 * 65535) return PA_ERR_UNSUPPORTED;
-    return cuda_status(pa::launch_prefill_backward(kgeom(geom), q, pool, block_table, layer, batch, cu_seqlens,
+    const pa::KGeom kg = kgeom(geom);
+    if (kg.nblocks * 32 >= (1ll << 31)) return PA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+    return cuda_status(pa::launch_prefill_backward(kg, q, pool, block_table, layer, batch, cu_seqlens,
                                                    slots, max_seqlen, total_tokens, scale, o, lse, dout, delta,
                                                    dq, dk, dv, err_flag, reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -14,7 +14,10 @@
 // (D_i = sum_j p_ij dp_ij = do_i . o_i, since o_i = sum_j p_ij v_j.)
 //
 // Two kernels.  bwd_prep: D for every (row, q head) from the bf16 o and do,
-// and dq set to zero.  bwd_main: one CTA of four warps per (64-key block,
+// and dq set to zero.  Then, for head dim 64, the tensor-core kernel of
+// backward_tc.cu; for head dim 128 (whose dK, dV and dQ accumulators do not
+// fit tensor memory beside double-buffered S^T and dP^T) bwd_main here: one
+// CTA of four warps per (64-key block,
 // sequence, kv head).  It stages the block's K and V rows from the pages once,
 // keeps dK and dV for its 64 keys in registers, and walks every q head of the
 // group and every 64-row query block at or after the diagonal.  Each warp owns
@@ -375,13 +378,18 @@ cudaError_t launch_backward_d(const BwdParams& p, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.batch == 0 || p.max_seqlen == 0) return cudaSuccess;
-    using C = BwdCfg<D>;
-    e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(p.batch * p.g.hkv),
-                    static_cast<unsigned>((p.max_seqlen + kBwdRows - 1) / kBwdRows));
-    bwd_main_kernel<D><<<grid, kBwdThreads, C::SMEM, stream>>>(p);
-    return cudaGetLastError();
+    if constexpr (D == 64)
+        return launch_backward_tc(p.g, p.q, p.pool, p.bt, p.layer, p.batch, p.cu, p.slots, p.max_seqlen,
+                                  p.total_tokens, p.scale, p.lse, p.dout, p.delta, p.dq, p.dk, p.dv, p.err, stream);
+    else {
+        using C = BwdCfg<D>;
+        e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        const dim3 grid(static_cast<unsigned>(p.batch * p.g.hkv),
+                        static_cast<unsigned>((p.max_seqlen + kBwdRows - 1) / kBwdRows));
+        bwd_main_kernel<D><<<grid, kBwdThreads, C::SMEM, stream>>>(p);
+        return cudaGetLastError();
+    }
 }
 
 }  // namespace
@@ -412,6 +420,9 @@ cudaError_t launch_prefill_backward(const KGeom& g, const void* q, const void* p
     p.dk = dk;
     p.dv = dv;
     p.err = err;
+    // d 64: the tensor-core kernel (backward_tc.cu); d 128 (its dK, dV and dQ
+    // accumulators do not fit tensor memory beside double-buffered S and dP):
+    // the mma.sync kernel here
     if (g.d == 64) return launch_backward_d<64>(p, stream);
     return launch_backward_d<128>(p, stream);
 }

@@ -1,0 +1,566 @@
+// backward_tc.cu -- the column-block kernel of the prefill backward on the
+// sm_103a tensor cores (tcgen05.mma, accumulators in tensor memory, operands
+// staged by TMA), head dim 64.
+//
+// Same arithmetic as bwd_main_kernel (FlashAttention-2 explainer, "전체
+// 흐름": P rebuilt from L; "2. 시퀀스 길이 방향으로도 병렬화" item 4: one
+// thread block per key block, dQ added atomically; "4. MQA · GQA 지원": dK, dV
+// summed over the group):
+//   S^T = K Q^T, dP^T = V dO^T, P^T = e^(scale S^T - L), dS^T = P^T (dP^T - D),
+//   dV += P^T dO, dK += dS^T Q, dQ += dS K.
+//
+// One CTA per (128-key block, sequence, kv head); the key block's K and V stay
+// in shared memory and its dK, dV accumulate in tensor memory over every q head
+// of the group and every 64-row query block at or after the diagonal.
+//  * warp 0 (producer): K, V once (8 pages each, rows through the block table,
+//    pages past the end read at an out-of-range row = zeros); then per query
+//    block the Q and dO tiles by TMA and L, D by plain loads, into 4 stages.
+//  * warp 1 (MMA issue, elected lane): S^T and dP^T (M 128 keys, N 64 rows,
+//    K 64 dims, both operands K-major) into one of two TMEM buffers; once the
+//    elementwise warps hand back P^T and dS^T (bf16, in TMEM over the first
+//    16 columns of each 32-column half), dV += P^T dO and dK += dS^T Q (A from
+//    TMEM, B = the same Q / dO tiles read MN-major); after every second query
+//    block, dQ = dS K for the pair (M 128 rows, N 64 dims, K 128 keys; dS from
+//    shared memory MN-major, K read MN-major).  S^T of the next block is
+//    issued before dV / dK of this one, so the tensor core works while the
+//    elementwise warps run.
+//  * warps 2..9 (elementwise): thread = key (TMEM lane), two warps per lane
+//    quarter, 32 query rows each.  Mask j <= i < n, P^T, dS^T; P^T and dS^T to
+//    TMEM, dS^T also to shared memory (key rows of 64 query rows, 128-byte
+//    swizzle) for the dQ product.  Rows of Q / dO past the sequence and K rows
+//    past it are zeroed in shared memory first (masked weights are exactly 0,
+//    0 x NaN is not).
+//  * warps 10..13 (dQ epilogue): thread = query row; dQ of a pair from TMEM,
+//    times scale, into a swizzled fp32 staging tile, then one TMA reduce-add
+//    per 32 columns into dq (rows past the sequence add zeros; rows past the
+//    tensor are clipped).  At the end they write dK * scale and dV.
+// TMEM: S^T 2 x 64 columns, dP^T 2 x 64, dV 64, dK 64, dQ 2 x 64 = 512.
+// Every wait is bounded; on a timeout the CTA records PA_ERR_TIMEOUT, drains
+// its copies and products in flight and frees its tensor memory.
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kKeys = 128;        // keys per CTA: TMEM lanes of the key-side products
+constexpr int kRowsIt = 64;       // query rows per iteration
+constexpr int kNst = 4;           // Q / dO / L / D stages
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kEwWarp0 = 2;       // 8 elementwise warps
+constexpr int kEpiWarp0 = 10;     // 4 dQ epilogue warps
+constexpr int kThreads = 14 * 32;
+
+constexpr int kTileKV = kKeys * 128;    // 128 keys x 64 dims bf16, 128-byte rows
+constexpr int kTileQ = kRowsIt * 128;   // 64 rows x 64 dims bf16
+constexpr int kDsHalf = kKeys * 128;    // dS^T of 64 query rows for 128 keys
+constexpr int kDsBuf = 2 * kDsHalf;     // one pair of query blocks
+constexpr int kDqBox = 128 * 128;       // 128 rows x 32 fp32
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + kTileKV;
+constexpr int OFF_Q = OFF_V + kTileKV;           // [kNst]
+constexpr int OFF_DO = OFF_Q + kNst * kTileQ;    // [kNst]
+constexpr int OFF_DS = OFF_DO + kNst * kTileQ;   // [2]
+constexpr int OFF_DQ = OFF_DS + 2 * kDsBuf;      // 2 boxes
+constexpr int OFF_LD = OFF_DQ + 2 * kDqBox;      // [kNst] x (64 L log2e, 64 D) fp32
+constexpr int OFF_BAR = OFF_LD + kNst * 2 * kRowsIt * 4;
+constexpr int SMEM = 1024 + OFF_BAR + 256;
+static_assert(SMEM <= 227 * 1024, "shared memory");
+
+constexpr uint32_t COL_S = 0;     // [2] x 64
+constexpr uint32_t COL_DP = 128;  // [2] x 64
+constexpr uint32_t COL_DV = 256;
+constexpr uint32_t COL_DK = 320;
+constexpr uint32_t COL_DQ = 384;  // [2] x 64
+constexpr uint32_t kTmemCols = 512;
+
+struct BwdTcParams {
+    KGeom g;
+    const int32_t* bt;
+    int layer;
+    const int32_t* cu;
+    const int32_t* slots;
+    int max_seqlen;
+    int total_tokens;
+    const float* lse;
+    const float* delta;
+    float scale;
+    float scale_log2;
+    float* dk;
+    float* dv;
+    int32_t* err;
+};
+
+// Columns of the bf16 P^T (or dS^T) of query rows 16 ks .. 16 ks + 15 within a
+// 64-column buffer: each 32-row half keeps its 16 packed columns at its start.
+__device__ __forceinline__ uint32_t packed_col(int ks) { return 32u * (ks >> 1) + 8u * (ks & 1); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_v4f(uint32_t saddr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier of the four epilogue warps that also ANDs a flag over their threads,
+// so that all four leave a loop together.
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int x, int y, uint32_t ssrc) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(ssrc)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Zeroes 128-byte rows [r0, r1) of a tile (the swizzle only permutes 16-byte
+// chunks within a row), spread over `nthr` threads.
+__device__ __forceinline__ void zero_rows(uint32_t tile, int r0, int r1, int t, int nthr) {
+    for (int c = t; c < (r1 - r0) * 8; c += nthr) st_shared_v4(tile + (r0 + c / 8) * 128 + (c % 8) * 16, 0, 0, 0, 0);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap domap,
+              const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap dqmap,
+              const BwdTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sb = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* kv_full = bars;              // 1
+    uint64_t* q_full = bars + 1;           // [kNst]
+    uint64_t* q_empty = bars + 5;          // [kNst]
+    uint64_t* s_full = bars + 9;           // [2]
+    uint64_t* p_ready = bars + 11;         // [2]
+    uint64_t* ds_empty = bars + 13;        // [2]
+    uint64_t* dq_full = bars + 15;         // [2]
+    uint64_t* dq_empty = bars + 17;        // [2]
+    uint64_t* kv_done = bars + 19;         // 1: last dV / dK product done
+    uint64_t* mma_done = bars + 20;        // 1: every product done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 25);
+    float* sLD = reinterpret_cast<float*>(smem + OFF_LD);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const KGeom& g = p.g;
+    const int b = blockIdx.x / g.hkv, hk = blockIdx.x % g.hkv;
+    const int jb = blockIdx.y;
+    const int cu0 = p.cu[b], cu1 = p.cu[b + 1];
+    const int n = cu1 - cu0;
+    const bool bad_len = cu0 < 0 || n < 0 || cu1 > p.total_tokens || n > p.max_seqlen ||
+                         n > g.maxb * kBlockTokens;
+    if (jb == 0 && hk == 0 && tid == 0 && bad_len) set_error(p.err, PA_ERR_BAD_BLOCK);
+    if (bad_len || jb * kKeys >= n) return;
+    const int slot = p.slots[b];
+    if (slot < 0 || slot >= g.num_slots) {
+        if (jb == 0 && hk == 0 && tid == 0) set_error(p.err, PA_ERR_BAD_BLOCK);
+        return;
+    }
+    const int group = g.group;
+    const int nph = (n + 2 * kRowsIt - 1) / (2 * kRowsIt) - jb;  // query-block pairs per head
+    const int n_it = group * 2 * nph;                            // iterations: (head, pair, half)
+    const int n_pairs = group * nph;
+
+    if (tid == 0) {
+        mbar_init(kv_full, 1);
+        for (int s = 0; s < kNst; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_ready[x], 8 * 32);
+            mbar_init(&ds_empty[x], 1);
+            mbar_init(&dq_full[x], 1);
+            mbar_init(&dq_empty[x], 4 * 32);
+        }
+        mbar_init(kv_done, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        const long long tbase = (static_cast<long long>(slot) * g.n_layers + p.layer) * g.maxb;
+        const int pages_b = (n + kBlockTokens - 1) / kBlockTokens;
+        const int oob_row = static_cast<int>(g.nblocks * 32);
+        const int lp = jb * (kKeys / kBlockTokens) + lane;
+        int row = -1;
+        if (lane < kKeys / kBlockTokens && lp < pages_b) {
+            const int e = __ldg(p.bt + tbase + lp);
+            if (e >= 0 && e < g.nblocks)
+                row = e * 32;
+            else
+                set_error(p.err, PA_ERR_BAD_BLOCK);
+        }
+        if (lane == 0) {
+            prefetch_tensor_map(&qmap);
+            prefetch_tensor_map(&domap);
+            prefetch_tensor_map(&kvmap);
+            mbar_arrive_expect_tx(kv_full, 2 * kTileKV);
+        }
+#pragma unroll
+        for (int k = 0; k < kKeys / kBlockTokens; ++k) {
+            const int rr = __shfl_sync(0xffffffffu, row, k);
+            if (lane == 0) {
+                const int y = rr < 0 ? oob_row : rr;
+                tma_load_2d(smem + OFF_K + k * 2048, &kvmap, hk * 64, y, kv_full);
+                tma_load_2d(smem + OFF_V + k * 2048, &kvmap, hk * 64, y + 16, kv_full);
+            }
+        }
+        int issued = 0;
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it % kNst;
+            if (it >= kNst &&
+                !__all_sync(0xffffffffu, mbar_wait(&q_empty[s], ((it / kNst) - 1) & 1, abort_flag, p.err)))
+                break;
+            const int pp = it >> 1;
+            const int h = hk * group + pp / nph;
+            const int ib = 2 * (jb + pp % nph) + (it & 1);
+            float* ld = sLD + s * 2 * kRowsIt;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const int r = lane + 32 * x;
+                const int i = ib * kRowsIt + r;
+                float l = 0.f, dd = 0.f;
+                if (i < n) {
+                    const long long off = static_cast<long long>(cu0 + i) * g.hq + h;
+                    l = __ldg(p.lse + off) * kLog2e;
+                    dd = __ldg(p.delta + off);
+                }
+                ld[r] = l;
+                ld[kRowsIt + r] = dd;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&q_full[s], 2 * kTileQ);
+                tma_load_2d(smem + OFF_Q + s * kTileQ, &qmap, h * 64, cu0 + ib * kRowsIt, &q_full[s]);
+                tma_load_2d(smem + OFF_DO + s * kTileQ, &domap, h * 64, cu0 + ib * kRowsIt, &q_full[s]);
+            }
+            ++issued;
+        }
+        if (lane == 0) {  // every copy issued has landed before the CTA leaves
+            mbar_drain(kv_full, 0);
+            for (int it = issued > kNst ? issued - kNst : 0; it < issued; ++it)
+                mbar_drain(&q_full[it % kNst], (it / kNst) & 1);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issue
+        constexpr uint32_t idesc_t = umma_idesc_bf16(128, 64, false);        // S^T, dP^T
+        constexpr uint32_t idesc_kv = umma_idesc_bf16(128, 64, true);        // dV, dK (A from TMEM)
+        constexpr uint32_t idesc_q = umma_idesc_bf16(128, 64, true, true);   // dQ
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err));
+        };
+        const uint32_t sK = sb + OFF_K, sV = sb + OFF_V;
+        auto issue_sdp = [&](int it) {
+            const int s = it % kNst, x = it & 1;
+            const uint32_t sQ = sb + OFF_Q + s * kTileQ, sO = sb + OFF_DO + s * kTileQ;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_ss_elect(tmem + COL_S + 64 * x, umma_sdesc_sw128(sK + ks * 32, 16, 1024),
+                              umma_sdesc_sw128(sQ + ks * 32, 16, 1024), idesc_t, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_ss_elect(tmem + COL_DP + 64 * x, umma_sdesc_sw128(sV + ks * 32, 16, 1024),
+                              umma_sdesc_sw128(sO + ks * 32, 16, 1024), idesc_t, ks > 0 ? 1u : 0u);
+            umma_commit_elect(&s_full[x]);
+        };
+        bool ok = wait_all(kv_full, 0) && wait_all(&q_full[0], 0);
+        if (ok) {
+            tc_fence_after_sync();
+            issue_sdp(0);
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int s = it % kNst, x = it & 1;
+            if (it + 1 < n_it) {
+                if (!wait_all(&q_full[(it + 1) % kNst], ((it + 1) / kNst) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                issue_sdp(it + 1);
+            }
+            if (!wait_all(&p_ready[x], (it >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t sQ = sb + OFF_Q + s * kTileQ, sO = sb + OFF_DO + s * kTileQ;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_ts_elect(tmem + COL_DV, tmem + COL_S + 64 * x + packed_col(ks),
+                              umma_sdesc_sw128(sO + ks * 2048, 1024, 1024), idesc_kv, (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_ts_elect(tmem + COL_DK, tmem + COL_DP + 64 * x + packed_col(ks),
+                              umma_sdesc_sw128(sQ + ks * 2048, 1024, 1024), idesc_kv, (it > 0 || ks > 0) ? 1u : 0u);
+            umma_commit_elect(&q_empty[s]);
+            if (it + 1 == n_it) umma_commit_elect(kv_done);
+            if (it & 1) {
+                const int pp = it >> 1, y = pp & 1;
+                if (pp >= 2 && !wait_all(&dq_empty[y], ((pp >> 1) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sD = sb + OFF_DS + y * kDsBuf;
+#pragma unroll
+                for (int ks = 0; ks < kKeys / 16; ++ks)
+                    umma_ss_elect(tmem + COL_DQ + 64 * y, umma_sdesc_sw128(sD + ks * 2048, kDsHalf, 1024),
+                                  umma_sdesc_sw128(sK + ks * 2048, 1024, 1024), idesc_q, ks > 0 ? 1u : 0u);
+                umma_commit_elect(&dq_full[y]);
+                umma_commit_elect(&ds_empty[y]);
+            }
+        }
+        umma_commit_elect(mma_done);
+        mbar_drain(mma_done, 0);
+        __syncwarp();
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------------ elementwise
+        const int ew = warp - kEwWarp0;          // 0..7
+        const int half = ew >> 2;                // query rows 32 half .. 32 half + 31 of a block
+        const int kq = (warp & 3) * 32 + lane;   // key within the block = TMEM lane
+        const int key = jb * kKeys + kq;
+        const uint32_t lane_addr = tmem + tmem_lane_base(warp);
+        const int et = ew * 32 + lane;           // 0..255
+        bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort_flag, p.err));
+        if (ok && (jb + 1) * kKeys > n) {  // K rows past the sequence: zero (dQ reads them)
+            zero_rows(sb + OFF_K, n - jb * kKeys, kKeys, et, 256);
+            fence_proxy_async_smem();
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int s = it % kNst, x = it & 1, pp = it >> 1;
+            const int ib = 2 * (jb + pp % nph) + (it & 1);
+            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[x], (it >> 1) & 1, abort_flag, p.err)) ||
+                !__all_sync(0xffffffffu, mbar_wait(&q_full[s], (it / kNst) & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            uint32_t sv[32], dv[32];
+            tmem_ld_x32_nowait(lane_addr + COL_S + 64 * x + 32 * half, sv);
+            tmem_ld_x32_nowait(lane_addr + COL_DP + 64 * x + 32 * half, dv);
+            if ((ib + 1) * kRowsIt > n) {  // Q / dO rows past the sequence: zero (dK, dV read them)
+                const int r0 = max(0, n - ib * kRowsIt);
+                zero_rows(sb + OFF_Q + s * kTileQ, r0, kRowsIt, et, 256);
+                zero_rows(sb + OFF_DO + s * kTileQ, r0, kRowsIt, et, 256);
+            }
+            const float* ls = sLD + s * 2 * kRowsIt + 32 * half;
+            const float* ds_ = ls + kRowsIt;
+            const int row0 = ib * kRowsIt + 32 * half;
+            tmem_wait_ld_dep(sv);
+            tmem_wait_ld_dep(dv);
+            uint32_t pk[16], dk[16];
+            const bool full = key <= row0 && row0 + 31 < n;  // no element masked (warp-uniform for most blocks)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, -ls[e]));
+                float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -ls[e + 1]));
+                float d0 = p0 * (__uint_as_float(dv[e]) - ds_[e]);
+                float d1 = p1 * (__uint_as_float(dv[e + 1]) - ds_[e + 1]);
+                if (!full) {
+                    const bool v0 = key <= row0 + e && row0 + e < n;
+                    const bool v1 = key <= row0 + e + 1 && row0 + e + 1 < n;
+                    p0 = v0 ? p0 : 0.f;
+                    d0 = v0 ? d0 : 0.f;
+                    p1 = v1 ? p1 : 0.f;
+                    d1 = v1 ? d1 : 0.f;
+                }
+                pk[e >> 1] = pack_bf16x2(p0, p1);
+                dk[e >> 1] = pack_bf16x2(d0, d1);
+            }
+            tmem_st_x16_nowait(lane_addr + COL_S + 64 * x + 32 * half, pk);
+            tmem_st_x16_nowait(lane_addr + COL_DP + 64 * x + 32 * half, dk);
+            // dS^T rows of this key into the pair's dQ operand: query rows 64 (it & 1) + 32 half + ..
+            if ((it & 1) == 0 && pp >= 2 &&
+                !__all_sync(0xffffffffu, mbar_wait(&ds_empty[pp & 1], ((pp >> 1) - 1) & 1, abort_flag, p.err))) {
+                tmem_wait_st();
+                ok = false;
+                break;
+            }
+            const uint32_t drow = sb + OFF_DS + (pp & 1) * kDsBuf + (it & 1) * kDsHalf + kq * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                st_shared_v4(drow + (((4 * half + c) ^ (kq & 7)) * 16), dk[4 * c], dk[4 * c + 1], dk[4 * c + 2],
+                             dk[4 * c + 3]);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            fence_proxy_async_smem();
+            mbar_arrive(&p_ready[x]);
+        }
+    } else {
+        // ------------------------------------------------------------ dQ epilogue, then dK / dV
+        const int r = (warp & 3) * 32 + lane;   // query row within a pair = TMEM lane
+        const uint32_t lane_addr = tmem + tmem_lane_base(warp);
+        const bool leader = warp == kEpiWarp0 && lane == 0;
+        bool ok = true;
+        for (int pp = 0; ok && pp < n_pairs; ++pp) {
+            const int y = pp & 1;
+            if (!epi_all(mbar_wait(&dq_full[y], (pp >> 1) & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            uint32_t v[32], w[32];
+            tmem_ld_x32_nowait(lane_addr + COL_DQ + 64 * y, v);
+            tmem_ld_x32_nowait(lane_addr + COL_DQ + 64 * y + 32, w);
+            tmem_wait_ld_dep(v);
+            tmem_wait_ld_dep(w);
+            tc_fence_before_sync();
+            mbar_arrive(&dq_empty[y]);
+            if (leader) bulk_wait_read0();  // the previous pair's reduce has read the staging tile
+            epi_barrier();
+            const uint32_t row_addr = sb + OFF_DQ + r * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint32_t pos = ((ch ^ (r & 7)) * 16);
+                st_shared_v4f(row_addr + pos, p.scale * __uint_as_float(v[4 * ch]),
+                              p.scale * __uint_as_float(v[4 * ch + 1]), p.scale * __uint_as_float(v[4 * ch + 2]),
+                              p.scale * __uint_as_float(v[4 * ch + 3]));
+                st_shared_v4f(row_addr + kDqBox + pos, p.scale * __uint_as_float(w[4 * ch]),
+                              p.scale * __uint_as_float(w[4 * ch + 1]), p.scale * __uint_as_float(w[4 * ch + 2]),
+                              p.scale * __uint_as_float(w[4 * ch + 3]));
+            }
+            fence_proxy_async_smem();
+            epi_barrier();
+            if (leader) {
+                const int h = hk * group + pp / nph;
+                const int y0 = cu0 + (jb + pp % nph) * 2 * kRowsIt;
+                tma_reduce_add_2d(&dqmap, h * 64, y0, sb + OFF_DQ);
+                tma_reduce_add_2d(&dqmap, h * 64 + 32, y0, sb + OFF_DQ + kDqBox);
+                bulk_commit();
+            }
+        }
+        if (leader) bulk_wait0();
+        if (ok && __all_sync(0xffffffffu, mbar_wait(kv_done, 0, abort_flag, p.err))) {
+            tc_fence_after_sync();
+            const int j = jb * kKeys + r;
+            uint32_t a[32], c[32];
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                tmem_ld_x32_nowait(lane_addr + COL_DK + 32 * part, a);
+                tmem_ld_x32_nowait(lane_addr + COL_DV + 32 * part, c);
+                tmem_wait_ld_dep(a);
+                tmem_wait_ld_dep(c);
+                if (j < n) {
+                    const long long off = (static_cast<long long>(cu0 + j) * g.hkv + hk) * 64 + 32 * part;
+                    float4* dkr = reinterpret_cast<float4*>(p.dk + off);
+                    float4* dvr = reinterpret_cast<float4*>(p.dv + off);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        dkr[q] = make_float4(p.scale * __uint_as_float(a[4 * q]), p.scale * __uint_as_float(a[4 * q + 1]),
+                                             p.scale * __uint_as_float(a[4 * q + 2]),
+                                             p.scale * __uint_as_float(a[4 * q + 3]));
+                        dvr[q] = make_float4(__uint_as_float(c[4 * q]), __uint_as_float(c[4 * q + 1]),
+                                             __uint_as_float(c[4 * q + 2]), __uint_as_float(c[4 * q + 3]));
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2D tensor [rows][cols] (row pitch in bytes), box {box_cols, box_rows},
+// 128-byte swizzle, zero fill out of range.
+bool encode(CUtensorMap* map, CUtensorMapDataType type, const void* base, unsigned long long cols,
+            unsigned long long rows, unsigned long long pitch, unsigned box_cols, unsigned box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_backward_tc(const KGeom& g, const void* q, const void* pool, const int32_t* bt, int layer,
+                               int batch, const int32_t* cu, const int32_t* slots, int max_seqlen, int total_tokens,
+                               float scale, const float* lse, const void* dout, const float* delta, float* dq,
+                               float* dk, float* dv, int32_t* err, cudaStream_t stream) {
+    CUtensorMap qmap, domap, kvmap, dqmap;
+    const unsigned long long qcols = static_cast<unsigned long long>(g.hq) * 64;
+    if (!encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, qcols, total_tokens, qcols * 2, 64, kRowsIt) ||
+        !encode(&domap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dout, qcols, total_tokens, qcols * 2, 64, kRowsIt) ||
+        !encode(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool, g.kv_dim, static_cast<unsigned long long>(g.nblocks) * 32,
+                static_cast<unsigned long long>(g.kv_dim) * 2, 64, kBlockTokens) ||
+        !encode(&dqmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dq, qcols, total_tokens, qcols * 4, 32, 2 * kRowsIt))
+        return cudaErrorInvalidValue;
+    BwdTcParams p;
+    p.g = g;
+    p.bt = bt;
+    p.layer = layer;
+    p.cu = cu;
+    p.slots = slots;
+    p.max_seqlen = max_seqlen;
+    p.total_tokens = total_tokens;
+    p.lse = lse;
+    p.delta = delta;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.dk = dk;
+    p.dv = dv;
+    p.err = err;
+    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(batch * g.hkv), static_cast<unsigned>((max_seqlen + kKeys - 1) / kKeys));
+    bwd_tc_kernel<<<grid, kThreads, SMEM, stream>>>(qmap, domap, kvmap, dqmap, p);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

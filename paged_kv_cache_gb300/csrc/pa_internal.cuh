@@ -287,11 +287,12 @@ __device__ __forceinline__ void mbar_arrive_elect(uint64_t* bar) {
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D,
-// A K-major, B K-major (b_mn_major = false) or MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool b_mn_major) {
+// A and B K-major or MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool b_mn_major, bool a_mn_major = false) {
     return (1u << 4)                                   // D format: f32
            | (1u << 7)                                 // A format: bf16
            | (1u << 10)                                // B format: bf16
+           | ((a_mn_major ? 1u : 0u) << 15)            // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
@@ -538,6 +539,10 @@ cudaError_t launch_prefill_backward(const KGeom& g, const void* q, const void* p
                                     int max_seqlen, int total_tokens, float scale, const void* o,
                                     const float* lse, const void* dout, float* delta, float* dq, float* dk,
                                     float* dv, int32_t* err, cudaStream_t stream);
+cudaError_t launch_backward_tc(const KGeom& g, const void* q, const void* pool, const int32_t* bt, int layer,
+                               int batch, const int32_t* cu, const int32_t* slots, int max_seqlen, int total_tokens,
+                               float scale, const float* lse, const void* dout, const float* delta, float* dq,
+                               float* dk, float* dv, int32_t* err, cudaStream_t stream);
 cudaError_t launch_decode(const KGeom& g, const void* q, const void* pool,
                           const int32_t* block_table, int layer, int batch,
                           const int32_t* seq_lens, const int32_t* slots, int max_seq_len,
