@@ -329,7 +329,7 @@ class BackwardStep:
         gen = torch.Generator(device="cuda")
         gen.manual_seed(seed)
         self.dout = torch.randn((T, Hq, D), generator=gen, device="cuda").to(torch.bfloat16)
-        self.delta = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+        self.delta = torch.empty((2, T, Hq), dtype=torch.float32, device="cuda")
         self.dq = torch.empty((T, Hq, D), dtype=torch.float32, device="cuda")
         self.dk = torch.empty((T, Hkv, D), dtype=torch.float32, device="cuda")
         self.dv = torch.empty((T, Hkv, D), dtype=torch.float32, device="cuda")

@@ -205,7 +205,7 @@ pa_status pa_prefill_cached(const pa_geom* geom, const void* q, const void* pool
  * gradients are wanted (the pages must still hold the same K/V).  o: device
  * bf16 [total_tokens][Hq][d] and lse: device fp32 [total_tokens][Hq], that
  * call's outputs.  dout: device bf16 [total_tokens][Hq][d].  delta: device fp32
- * [total_tokens][Hq] workspace (overwritten with D).  dq: device fp32
+ * workspace of 2 * total_tokens * Hq floats (overwritten: -L log2 e, then -D).  dq: device fp32
  * [total_tokens][Hq][d], set to zero first (every row).  dk, dv: device fp32
  * [total_tokens][Hkv][d], row t is the gradient of the K / V row written for
  * token t; rows not covered by cu_seqlens are not written.  q, o, dout, dq,

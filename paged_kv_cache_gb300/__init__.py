@@ -195,7 +195,7 @@ def pa_prefill_backward(g, q, pool, block_table, layer, cu_seqlens, slots, max_s
                         delta, dq, dk, dv, err_flag, stream=None, batch=None, total_tokens=None):
     """Gradients dq [T][Hq][d], dk / dv [T][Hkv][d] (fp32) of the causal prefill
     for the output gradient dout, from the forward's o and lse; delta is an fp32
-    [T][Hq] workspace."""
+    workspace of 2 * T * Hq floats."""
     batch = int(cu_seqlens.shape[0]) - 1 if batch is None else int(batch)
     total = int(q.shape[0]) if total_tokens is None else int(total_tokens)
     _check("pa_prefill_backward", lib().pa_prefill_backward(

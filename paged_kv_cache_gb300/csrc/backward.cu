@@ -66,7 +66,8 @@ struct BwdParams {
     const uint16_t* o;
     const float* lse;
     const uint16_t* dout;
-    float* delta;
+    float* delta;        // workspace: [2][total_tokens][hq], -L log2 e then -D
+    long long ws_half;   // total_tokens * hq
     float scale;
     float scale_log2;
     float* dq;
@@ -94,12 +95,15 @@ __device__ __forceinline__ void st_shared_u32(uint32_t saddr, uint32_t v) {
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
 }
 
-// D_i = do_i . o_i per (row, q head), fp32 from the bf16 values; dq = 0.
-// D / 8 consecutive threads share one (row, head): 16 bytes of o and do each.
+// Per (row, q head): D_i = do_i . o_i in fp32 from the bf16 values, stored
+// as the two terms the main kernels add, ws[0][row][h] = -L_i log2 e and
+// ws[1][row][h] = -D_i; dq = 0.  D / 8 consecutive threads share one (row,
+// head): 16 bytes of o and do each.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o,
                                                        const uint16_t* __restrict__ dout,
-                                                       float* __restrict__ delta, float* __restrict__ dq,
+                                                       const float* __restrict__ lse,
+                                                       float* __restrict__ ws, float* __restrict__ dq,
                                                        long long pairs) {
     constexpr int PER = D / 8;
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -124,7 +128,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
     }
 #pragma unroll
     for (int s = PER / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (live && part == 0) delta[pair] = acc;
+    if (live && part == 0) {
+        ws[pair] = -__ldg(lse + pair) * kLog2e;
+        ws[pairs + pair] = -acc;
+    }
 }
 
 template <int D>
@@ -201,8 +208,8 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_main_kernel(const BwdParams p
             const uint32_t so = static_cast<uint32_t>((st * kBwdRows + tid) * 4);
             if (i < n) {
                 const long long off = static_cast<long long>(cu0 + i) * p.g.hq + h;
-                cp_async4(sbase + C::L_OFF + so, p.lse + off);
-                cp_async4(sbase + C::DD_OFF + so, p.delta + off);
+                cp_async4(sbase + C::L_OFF + so, p.delta + off);
+                cp_async4(sbase + C::DD_OFF + so, p.delta + p.ws_half + off);
             } else {
                 st_shared_f32(sbase + C::L_OFF + so, 0.f);
                 st_shared_f32(sbase + C::DD_OFF + so, 0.f);
@@ -266,22 +273,23 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_main_kernel(const BwdParams p
             }
         }
 
-        // P^T = e^(scale s - L) on j <= i < n, else 0; dS^T = P^T (dP^T - D).
+        // P^T = e^(scale s - L) on j <= i < n, else 0; dS^T = P^T (dP^T - D)
+        // (shared memory holds -L log2 e and -D).
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int col = 8 * t + 2 * (lane & 3) + e;
                 const int i = ib * kBwdRows + col;
-                const float lsc = l_s[col] * kLog2e;
-                const float dd = d_s[col];
+                const float nl = l_s[col];
+                const float nd = d_s[col];
                 const bool in_seq = i < n;
-                const float p0 = (in_seq && key0 <= i) ? ex2_approx(fmaf(s[t][e], p.scale_log2, -lsc)) : 0.f;
-                const float p1 = (in_seq && key0 + 8 <= i) ? ex2_approx(fmaf(s[t][2 + e], p.scale_log2, -lsc)) : 0.f;
+                const float p0 = (in_seq && key0 <= i) ? ex2_approx(fmaf(s[t][e], p.scale_log2, nl)) : 0.f;
+                const float p1 = (in_seq && key0 + 8 <= i) ? ex2_approx(fmaf(s[t][2 + e], p.scale_log2, nl)) : 0.f;
                 s[t][e] = p0;
                 s[t][2 + e] = p1;
-                dp[t][e] = p0 * (dp[t][e] - dd);
-                dp[t][2 + e] = p1 * (dp[t][2 + e] - dd);
+                dp[t][e] = p0 * (dp[t][e] + nd);
+                dp[t][2 + e] = p1 * (dp[t][2 + e] + nd);
             }
         }
 
@@ -374,13 +382,13 @@ cudaError_t launch_backward_d(const BwdParams& p, cudaStream_t stream) {
     const long long threads = pairs * (D / 8);
     const int prep_block = 256;
     bwd_prep_kernel<D><<<static_cast<unsigned>((threads + prep_block - 1) / prep_block), prep_block, 0, stream>>>(
-        p.o, p.dout, p.delta, p.dq, pairs);
+        p.o, p.dout, p.lse, p.delta, p.dq, pairs);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.batch == 0 || p.max_seqlen == 0) return cudaSuccess;
     if constexpr (D == 64)
         return launch_backward_tc(p.g, p.q, p.pool, p.bt, p.layer, p.batch, p.cu, p.slots, p.max_seqlen,
-                                  p.total_tokens, p.scale, p.lse, p.dout, p.delta, p.dq, p.dk, p.dv, p.err, stream);
+                                  p.total_tokens, p.scale, p.dout, p.delta, p.dq, p.dk, p.dv, p.err, stream);
     else {
         using C = BwdCfg<D>;
         e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -414,6 +422,7 @@ cudaError_t launch_prefill_backward(const KGeom& g, const void* q, const void* p
     p.lse = lse;
     p.dout = static_cast<const uint16_t*>(dout);
     p.delta = delta;
+    p.ws_half = static_cast<long long>(total_tokens) * g.hq;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.dq = dq;

@@ -14,23 +14,24 @@
 // of the group and every 64-row query block at or after the diagonal.
 //  * warp 0 (producer): K, V once (8 pages each, rows through the block table,
 //    pages past the end read at an out-of-range row = zeros); then per query
-//    block the Q and dO tiles by TMA and L, D by plain loads, into 4 stages.
+//    block the Q and dO tiles by TMA and -L log2 e, -D (from the prep kernel's
+//    workspace) by cp.async, all completing on one mbarrier, into 5 stages.
 //  * warp 1 (MMA issue, elected lane): S^T and dP^T (M 128 keys, N 64 rows,
 //    K 64 dims, both operands K-major) into one of two TMEM buffers; once the
 //    elementwise warps hand back P^T and dS^T (bf16, in TMEM over the first
-//    16 columns of each 32-column half), dV += P^T dO and dK += dS^T Q (A from
+//    8 columns of each 16-column quarter), dV += P^T dO and dK += dS^T Q (A from
 //    TMEM, B = the same Q / dO tiles read MN-major); after every second query
 //    block, dQ = dS K for the pair (M 128 rows, N 64 dims, K 128 keys; dS from
 //    shared memory MN-major, K read MN-major).  S^T of the next block is
 //    issued before dV / dK of this one, so the tensor core works while the
 //    elementwise warps run.
-//  * warps 2..9 (elementwise): thread = key (TMEM lane), two warps per lane
-//    quarter, 32 query rows each.  Mask j <= i < n, P^T, dS^T; P^T and dS^T to
+//  * warps 2..17 (elementwise): thread = key (TMEM lane), four warps per lane
+//    quarter, 16 query rows each.  Mask j <= i < n, P^T, dS^T; P^T and dS^T to
 //    TMEM, dS^T also to shared memory (key rows of 64 query rows, 128-byte
 //    swizzle) for the dQ product.  Rows of Q / dO past the sequence and K rows
 //    past it are zeroed in shared memory first (masked weights are exactly 0,
 //    0 x NaN is not).
-//  * warps 10..13 (dQ epilogue): thread = query row; dQ of a pair from TMEM,
+//  * warps 18..21 (dQ epilogue): thread = query row; dQ of a pair from TMEM,
 //    times scale, into a swizzled fp32 staging tile, then one TMA reduce-add
 //    per 32 columns into dq (rows past the sequence add zeros; rows past the
 //    tensor are clipped).  At the end they write dK * scale and dV.
@@ -44,12 +45,13 @@ namespace {
 
 constexpr int kKeys = 128;        // keys per CTA: TMEM lanes of the key-side products
 constexpr int kRowsIt = 64;       // query rows per iteration
-constexpr int kNst = 4;           // Q / dO / L / D stages
+constexpr int kNst = 5;           // Q / dO / L / D stages
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kEwWarp0 = 2;       // 8 elementwise warps
-constexpr int kEpiWarp0 = 10;     // 4 dQ epilogue warps
-constexpr int kThreads = 14 * 32;
+constexpr int kEwWarp0 = 2;       // 16 elementwise warps
+constexpr int kEwWarps = 16;
+constexpr int kEpiWarp0 = kEwWarp0 + kEwWarps;  // 4 dQ epilogue warps
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 
 constexpr int kTileKV = kKeys * 128;    // 128 keys x 64 dims bf16, 128-byte rows
 constexpr int kTileQ = kRowsIt * 128;   // 64 rows x 64 dims bf16
@@ -62,9 +64,9 @@ constexpr int OFF_Q = OFF_V + kTileKV;           // [kNst]
 constexpr int OFF_DO = OFF_Q + kNst * kTileQ;    // [kNst]
 constexpr int OFF_DS = OFF_DO + kNst * kTileQ;   // [2]
 constexpr int OFF_DQ = OFF_DS + 2 * kDsBuf;      // 2 boxes
-constexpr int OFF_LD = OFF_DQ + 2 * kDqBox;      // [kNst] x (64 L log2e, 64 D) fp32
+constexpr int OFF_LD = OFF_DQ + 2 * kDqBox;      // [kNst] x (64 -L log2e, 64 -D) fp32
 constexpr int OFF_BAR = OFF_LD + kNst * 2 * kRowsIt * 4;
-constexpr int SMEM = 1024 + OFF_BAR + 256;
+constexpr int SMEM = 1024 + OFF_BAR + 512;
 static_assert(SMEM <= 227 * 1024, "shared memory");
 
 constexpr uint32_t COL_S = 0;     // [2] x 64
@@ -82,8 +84,8 @@ struct BwdTcParams {
     const int32_t* slots;
     int max_seqlen;
     int total_tokens;
-    const float* lse;
-    const float* delta;
+    const float* ws;        // [2][total_tokens][hq]: -L log2 e, -D
+    long long ws_half;
     float scale;
     float scale_log2;
     float* dk;
@@ -92,8 +94,8 @@ struct BwdTcParams {
 };
 
 // Columns of the bf16 P^T (or dS^T) of query rows 16 ks .. 16 ks + 15 within a
-// 64-column buffer: each 32-row half keeps its 16 packed columns at its start.
-__device__ __forceinline__ uint32_t packed_col(int ks) { return 32u * (ks >> 1) + 8u * (ks & 1); }
+// 64-column buffer: each 16-row quarter keeps its 8 packed columns at its start.
+__device__ __forceinline__ uint32_t packed_col(int ks) { return 16u * ks; }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d)
@@ -126,6 +128,15 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int x,
         "r"(x), "r"(y), "r"(ssrc)
         : "memory");
 }
+// 4 bytes global -> shared, zero-filled when `bytes` is 0 (nothing is read then).
+__device__ __forceinline__ void cp_async4_zfill(uint32_t sdst, const float* gsrc, uint32_t bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(sdst), "l"(gsrc), "r"(bytes) : "memory");
+}
+// Arrives on `bar` once every cp.async this thread issued so far has landed
+// (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -146,17 +157,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
     const uint32_t sb = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* kv_full = bars;              // 1
-    uint64_t* q_full = bars + 1;           // [kNst]
-    uint64_t* q_empty = bars + 5;          // [kNst]
-    uint64_t* s_full = bars + 9;           // [2]
-    uint64_t* p_ready = bars + 11;         // [2]
-    uint64_t* ds_empty = bars + 13;        // [2]
-    uint64_t* dq_full = bars + 15;         // [2]
-    uint64_t* dq_empty = bars + 17;        // [2]
-    uint64_t* kv_done = bars + 19;         // 1: last dV / dK product done
-    uint64_t* mma_done = bars + 20;        // 1: every product done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 25);
+    uint64_t* q_full = kv_full + 1;        // [kNst]
+    uint64_t* q_empty = q_full + kNst;     // [kNst]
+    uint64_t* s_full = q_empty + kNst;     // [2]
+    uint64_t* p_ready = s_full + 2;        // [2]
+    uint64_t* ds_empty = p_ready + 2;      // [2]
+    uint64_t* dq_full = ds_empty + 2;      // [2]
+    uint64_t* dq_empty = dq_full + 2;      // [2]
+    uint64_t* kv_done = dq_empty + 2;      // 1: last dV / dK product done
+    uint64_t* mma_done = kv_done + 1;      // 1: every product done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_done + 2);
     float* sLD = reinterpret_cast<float*>(smem + OFF_LD);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -182,12 +193,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
     if (tid == 0) {
         mbar_init(kv_full, 1);
         for (int s = 0; s < kNst; ++s) {
-            mbar_init(&q_full[s], 1);
+            mbar_init(&q_full[s], 1 + 32);  // expect_tx arrival + one cp.async arrival per producer lane
             mbar_init(&q_empty[s], 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
-            mbar_init(&p_ready[x], 8 * 32);
+            mbar_init(&p_ready[x], kEwWarps * 32);
             mbar_init(&ds_empty[x], 1);
             mbar_init(&dq_full[x], 1);
             mbar_init(&dq_empty[x], 4 * 32);
@@ -244,21 +255,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
             const int pp = it >> 1;
             const int h = hk * group + pp / nph;
             const int ib = 2 * (jb + pp % nph) + (it & 1);
-            float* ld = sLD + s * 2 * kRowsIt;
+            const uint32_t ld = sb + OFF_LD + s * 2 * kRowsIt * 4;
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
                 const int r = lane + 32 * x;
                 const int i = ib * kRowsIt + r;
-                float l = 0.f, dd = 0.f;
-                if (i < n) {
-                    const long long off = static_cast<long long>(cu0 + i) * g.hq + h;
-                    l = __ldg(p.lse + off) * kLog2e;
-                    dd = __ldg(p.delta + off);
-                }
-                ld[r] = l;
-                ld[kRowsIt + r] = dd;
+                const float* src = p.ws + (i < n ? static_cast<long long>(cu0 + i) * g.hq + h : 0);
+                const uint32_t bytes = i < n ? 4u : 0u;
+                cp_async4_zfill(ld + r * 4, src, bytes);
+                cp_async4_zfill(ld + (kRowsIt + r) * 4, src + p.ws_half, bytes);
             }
-            __syncwarp();
+            cp_async_arrive_noinc(&q_full[s]);
             if (lane == 0) {
                 mbar_arrive_expect_tx(&q_full[s], 2 * kTileQ);
                 tma_load_2d(smem + OFF_Q + s * kTileQ, &qmap, h * 64, cu0 + ib * kRowsIt, &q_full[s]);
@@ -345,15 +352,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------------ elementwise
-        const int ew = warp - kEwWarp0;          // 0..7
-        const int half = ew >> 2;                // query rows 32 half .. 32 half + 31 of a block
+        const int ew = warp - kEwWarp0;          // 0..15
+        const int grp = ew >> 2;                 // query rows 16 grp .. 16 grp + 15 of a block
         const int kq = (warp & 3) * 32 + lane;   // key within the block = TMEM lane
         const int key = jb * kKeys + kq;
         const uint32_t lane_addr = tmem + tmem_lane_base(warp);
-        const int et = ew * 32 + lane;           // 0..255
+        const int et = ew * 32 + lane;           // 0 .. 511
+        constexpr int kEt = kEwWarps * 32;
+        const float sc = p.scale_log2;
         bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort_flag, p.err));
         if (ok && (jb + 1) * kKeys > n) {  // K rows past the sequence: zero (dQ reads them)
-            zero_rows(sb + OFF_K, n - jb * kKeys, kKeys, et, 256);
+            zero_rows(sb + OFF_K, n - jb * kKeys, kKeys, et, kEt);
             fence_proxy_async_smem();
         }
         for (int it = 0; ok && it < n_it; ++it) {
@@ -365,27 +374,35 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
                 break;
             }
             tc_fence_after_sync();
-            uint32_t sv[32], dv[32];
-            tmem_ld_x32_nowait(lane_addr + COL_S + 64 * x + 32 * half, sv);
-            tmem_ld_x32_nowait(lane_addr + COL_DP + 64 * x + 32 * half, dv);
+            uint32_t sv[16], dv[16];
+            tmem_ld_x16_nowait(lane_addr + COL_S + 64 * x + 16 * grp, sv);
+            tmem_ld_x16_nowait(lane_addr + COL_DP + 64 * x + 16 * grp, dv);
             if ((ib + 1) * kRowsIt > n) {  // Q / dO rows past the sequence: zero (dK, dV read them)
                 const int r0 = max(0, n - ib * kRowsIt);
-                zero_rows(sb + OFF_Q + s * kTileQ, r0, kRowsIt, et, 256);
-                zero_rows(sb + OFF_DO + s * kTileQ, r0, kRowsIt, et, 256);
+                zero_rows(sb + OFF_Q + s * kTileQ, r0, kRowsIt, et, kEt);
+                zero_rows(sb + OFF_DO + s * kTileQ, r0, kRowsIt, et, kEt);
             }
-            const float* ls = sLD + s * 2 * kRowsIt + 32 * half;
-            const float* ds_ = ls + kRowsIt;
-            const int row0 = ib * kRowsIt + 32 * half;
+            const float4* nl4 = reinterpret_cast<const float4*>(sLD + s * 2 * kRowsIt + 16 * grp);
+            const float4* nd4 = reinterpret_cast<const float4*>(sLD + s * 2 * kRowsIt + kRowsIt + 16 * grp);
+            float nl[16], nd[16];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const float4 a = nl4[v], c = nd4[v];
+                nl[4 * v] = a.x; nl[4 * v + 1] = a.y; nl[4 * v + 2] = a.z; nl[4 * v + 3] = a.w;
+                nd[4 * v] = c.x; nd[4 * v + 1] = c.y; nd[4 * v + 2] = c.z; nd[4 * v + 3] = c.w;
+            }
+            const int row0 = ib * kRowsIt + 16 * grp;
             tmem_wait_ld_dep(sv);
             tmem_wait_ld_dep(dv);
-            uint32_t pk[16], dk[16];
-            const bool full = key <= row0 && row0 + 31 < n;  // no element masked (warp-uniform for most blocks)
+            uint32_t pk[8], dk[8];
+            const bool full = key <= row0 && row0 + 15 < n;  // no element masked (warp-uniform off the diagonal)
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, -ls[e]));
-                float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -ls[e + 1]));
-                float d0 = p0 * (__uint_as_float(dv[e]) - ds_[e]);
-                float d1 = p1 * (__uint_as_float(dv[e + 1]) - ds_[e + 1]);
+            for (int e = 0; e < 16; e += 2) {
+                float x0, x1, t0, t1, d0, d1;
+                ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sc, sc, nl[e], nl[e + 1]);
+                float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                fadd2(t0, t1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), nd[e], nd[e + 1]);
+                fmul2(d0, d1, p0, p1, t0, t1);
                 if (!full) {
                     const bool v0 = key <= row0 + e && row0 + e < n;
                     const bool v1 = key <= row0 + e + 1 && row0 + e + 1 < n;
@@ -397,9 +414,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
                 pk[e >> 1] = pack_bf16x2(p0, p1);
                 dk[e >> 1] = pack_bf16x2(d0, d1);
             }
-            tmem_st_x16_nowait(lane_addr + COL_S + 64 * x + 32 * half, pk);
-            tmem_st_x16_nowait(lane_addr + COL_DP + 64 * x + 32 * half, dk);
-            // dS^T rows of this key into the pair's dQ operand: query rows 64 (it & 1) + 32 half + ..
+            tmem_st_x8_nowait(lane_addr + COL_S + 64 * x + 16 * grp, pk);
+            tmem_st_x8_nowait(lane_addr + COL_DP + 64 * x + 16 * grp, dk);
+            // dS^T of this key into the pair's dQ operand: query rows 64 (it & 1) + 16 grp + ..
             if ((it & 1) == 0 && pp >= 2 &&
                 !__all_sync(0xffffffffu, mbar_wait(&ds_empty[pp & 1], ((pp >> 1) - 1) & 1, abort_flag, p.err))) {
                 tmem_wait_st();
@@ -408,8 +425,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
             }
             const uint32_t drow = sb + OFF_DS + (pp & 1) * kDsBuf + (it & 1) * kDsHalf + kq * 128;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                st_shared_v4(drow + (((4 * half + c) ^ (kq & 7)) * 16), dk[4 * c], dk[4 * c + 1], dk[4 * c + 2],
+            for (int c = 0; c < 2; ++c)
+                st_shared_v4(drow + (((2 * grp + c) ^ (kq & 7)) * 16), dk[4 * c], dk[4 * c + 1], dk[4 * c + 2],
                              dk[4 * c + 3]);
             tmem_wait_st();
             tc_fence_before_sync();
@@ -429,26 +446,21 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
                 break;
             }
             tc_fence_after_sync();
-            uint32_t v[32], w[32];
-            tmem_ld_x32_nowait(lane_addr + COL_DQ + 64 * y, v);
-            tmem_ld_x32_nowait(lane_addr + COL_DQ + 64 * y + 32, w);
-            tmem_wait_ld_dep(v);
-            tmem_wait_ld_dep(w);
-            tc_fence_before_sync();
-            mbar_arrive(&dq_empty[y]);
             if (leader) bulk_wait_read0();  // the previous pair's reduce has read the staging tile
             epi_barrier();
             const uint32_t row_addr = sb + OFF_DQ + r * 128;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const uint32_t pos = ((ch ^ (r & 7)) * 16);
-                st_shared_v4f(row_addr + pos, p.scale * __uint_as_float(v[4 * ch]),
-                              p.scale * __uint_as_float(v[4 * ch + 1]), p.scale * __uint_as_float(v[4 * ch + 2]),
-                              p.scale * __uint_as_float(v[4 * ch + 3]));
-                st_shared_v4f(row_addr + kDqBox + pos, p.scale * __uint_as_float(w[4 * ch]),
-                              p.scale * __uint_as_float(w[4 * ch + 1]), p.scale * __uint_as_float(w[4 * ch + 2]),
-                              p.scale * __uint_as_float(w[4 * ch + 3]));
+            for (int part = 0; part < 2; ++part) {
+                uint32_t v[32];
+                tmem_ld_x32(lane_addr + COL_DQ + 64 * y + 32 * part, v);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    st_shared_v4f(row_addr + part * kDqBox + ((ch ^ (r & 7)) * 16), p.scale * __uint_as_float(v[4 * ch]),
+                                  p.scale * __uint_as_float(v[4 * ch + 1]), p.scale * __uint_as_float(v[4 * ch + 2]),
+                                  p.scale * __uint_as_float(v[4 * ch + 3]));
             }
+            tc_fence_before_sync();
+            mbar_arrive(&dq_empty[y]);
             fence_proxy_async_smem();
             epi_barrier();
             if (leader) {
@@ -531,8 +543,8 @@ bool encode(CUtensorMap* map, CUtensorMapDataType type, const void* base, unsign
 
 cudaError_t launch_backward_tc(const KGeom& g, const void* q, const void* pool, const int32_t* bt, int layer,
                                int batch, const int32_t* cu, const int32_t* slots, int max_seqlen, int total_tokens,
-                               float scale, const float* lse, const void* dout, const float* delta, float* dq,
-                               float* dk, float* dv, int32_t* err, cudaStream_t stream) {
+                               float scale, const void* dout, const float* ws, float* dq, float* dk, float* dv,
+                               int32_t* err, cudaStream_t stream) {
     CUtensorMap qmap, domap, kvmap, dqmap;
     const unsigned long long qcols = static_cast<unsigned long long>(g.hq) * 64;
     if (!encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, qcols, total_tokens, qcols * 2, 64, kRowsIt) ||
@@ -549,8 +561,8 @@ cudaError_t launch_backward_tc(const KGeom& g, const void* q, const void* pool, 
     p.slots = slots;
     p.max_seqlen = max_seqlen;
     p.total_tokens = total_tokens;
-    p.lse = lse;
-    p.delta = delta;
+    p.ws = ws;
+    p.ws_half = static_cast<long long>(total_tokens) * g.hq;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.dk = dk;

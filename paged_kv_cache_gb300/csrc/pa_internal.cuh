@@ -489,6 +489,15 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a2, b2, d2;\n\t"
+        "mov.b64 a2, {%2, %3};\n\t"
+        "mov.b64 b2, {%4, %5};\n\t"
+        "mul.rn.f32x2 d2, a2, b2;\n\t"
+        "mov.b64 {%0, %1}, d2;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
 __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
     asm("{\n\t.reg .b64 a2, b2, d2;\n\t"
         "mov.b64 a2, {%2, %3};\n\t"
@@ -541,8 +550,8 @@ cudaError_t launch_prefill_backward(const KGeom& g, const void* q, const void* p
                                     float* dv, int32_t* err, cudaStream_t stream);
 cudaError_t launch_backward_tc(const KGeom& g, const void* q, const void* pool, const int32_t* bt, int layer,
                                int batch, const int32_t* cu, const int32_t* slots, int max_seqlen, int total_tokens,
-                               float scale, const float* lse, const void* dout, const float* delta, float* dq,
-                               float* dk, float* dv, int32_t* err, cudaStream_t stream);
+                               float scale, const void* dout, const float* ws, float* dq, float* dk, float* dv,
+                               int32_t* err, cudaStream_t stream);
 cudaError_t launch_decode(const KGeom& g, const void* q, const void* pool,
                           const int32_t* block_table, int layer, int batch,
                           const int32_t* seq_lens, const int32_t* slots, int max_seq_len,

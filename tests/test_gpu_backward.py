@@ -36,7 +36,7 @@ def gpu_forward_backward(case, pool, bt, dout):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     cu, slots = H.to_dev(case.cu_seqlens), H.to_dev(case.slots)
     H.pa.pa_prefill(g, q, pool, bt, case.layer, cu, slots, case.max_len, case.scale, o, lse, err)
-    delta = torch.empty((T, hq), dtype=torch.float32, device="cuda")
+    delta = torch.empty((2, T, hq), dtype=torch.float32, device="cuda")
     dq = torch.full((T, hq, d), float("nan"), dtype=torch.float32, device="cuda")
     dk = torch.full((T, hkv, d), float("nan"), dtype=torch.float32, device="cuda")
     dv = torch.full((T, hkv, d), float("nan"), dtype=torch.float32, device="cuda")
@@ -112,7 +112,7 @@ def test_rows_outside_the_batch():
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     cu, slots = H.to_dev(case.cu_seqlens), H.to_dev(case.slots)
     H.pa.pa_prefill(g, q, pool, bt, 0, cu, slots, case.max_len, case.scale, o, lse, err)
-    delta = torch.empty((T, 8), dtype=torch.float32, device="cuda")
+    delta = torch.empty((2, T, 8), dtype=torch.float32, device="cuda")
     dq = torch.full((T, 8, 64), 7.0, dtype=torch.float32, device="cuda")
     dk = torch.full((T, 2, 64), 7.0, dtype=torch.float32, device="cuda")
     dv = torch.full((T, 2, 64), 7.0, dtype=torch.float32, device="cuda")
