@@ -78,10 +78,14 @@ def load_peaks():
 
 
 def kernel_source_hash():
+    """Hash of every CUDA source of the library (a traffic figure taken on other
+    sources is not reported)."""
     h = hashlib.sha256()
-    for name in ("prefill.cu", "decode.cu", "write_kv.cu", "pa_internal.cuh"):
-        with open(os.path.join(ROOT, "paged_kv_cache_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    csrc = os.path.join(ROOT, "paged_kv_cache_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 
