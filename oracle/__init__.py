@@ -73,6 +73,10 @@ def lib():
         L.orc_prefill_backward.restype = C.c_int
         L.orc_prefill_backward.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, C.c_float, _P,
                                            _P, _P, _P, C.c_int32]
+        L.orc_prefill_backward_rows.restype = C.c_int
+        L.orc_prefill_backward_rows.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P,
+                                                C.c_float, _P, C.c_int64, _P, _P, _P, C.c_int64, _P, _P, _P, _P,
+                                                C.c_int32]
         L.orc_decode.restype = C.c_int
         L.orc_decode.argtypes = [C.POINTER(Geom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P,
                                  C.c_float, _P, _P, C.c_int32]
@@ -278,6 +282,27 @@ def prefill_backward(g, q, pool, block_table, layer, cu_seqlens, slots, scale, d
     st = lib().orc_prefill_backward(C.byref(g), _ptr(q), _ptr(pool), _ptr(_c(block_table, np.int32)), layer,
                                     cu.shape[0] - 1, _ptr(cu), _ptr(sl), C.c_float(scale), _ptr(do), _ptr(dq),
                                     _ptr(dk), _ptr(dv), nthreads)
+    return int(st), dq, dk, dv
+
+
+def prefill_backward_rows(g, q, pool, block_table, layer, cu_seqlens, slots, scale, dout, q_rows, q_heads,
+                          k_rows, k_heads, nthreads=0):
+    """prefill_backward at sampled outputs: (status, dq[len(q_rows)][d] of (q_rows, q_heads),
+    dk, dv [len(k_rows)][d] of (k_rows, kv heads k_heads)), float64, equal to the full call's entries."""
+    cu = _c(cu_seqlens, np.int32)
+    qr = _c(q_rows, np.int64)
+    qh = _c(q_heads, np.int32)
+    kr = _c(k_rows, np.int64)
+    kh = _c(k_heads, np.int32)
+    d = g.head_dim
+    dq = np.zeros((qr.shape[0], d), np.float64)
+    dk = np.zeros((kr.shape[0], d), np.float64)
+    dv = np.zeros_like(dk)
+    st = lib().orc_prefill_backward_rows(C.byref(g), _ptr(_c(q, np.uint16)), _ptr(pool),
+                                         _ptr(_c(block_table, np.int32)), layer, cu.shape[0] - 1, _ptr(cu),
+                                         _ptr(_c(slots, np.int32)), C.c_float(scale), _ptr(_c(dout, np.uint16)),
+                                         qr.shape[0], _ptr(qr), _ptr(qh), _ptr(dq), kr.shape[0], _ptr(kr), _ptr(kh),
+                                         _ptr(dk), _ptr(dv), nthreads)
     return int(st), dq, dk, dv
 
 

@@ -630,6 +630,58 @@ typedef struct {
     int32_t batch;
 } backward_ctx;
 
+/* One query row i of sequence b, q head h: the scores s_j = scale q_i . k_j
+ * (j <= i), m = max_j s_j, l = sum_j e^(s_j - m), p_j = e^(s_j - m) / l,
+ * dp_j = do_i . v_j, D = sum_j p_j dp_j and ds_j = p_j (dp_j - D), with p
+ * recomputed from the scores as the FA2 backward recomputes it from the stored
+ * L [FA2, 전체 흐름: "L로 P 재계산"].  Fills qv, dov (the row's q and do),
+ * p[0..i], ds[0..i]; returns m, l, D; dq_i = scale sum_j ds_j k_j into dqi
+ * when it is not NULL. */
+static void backward_row(const backward_ctx* c, int32_t b, int32_t h, int32_t i, double* qv,
+                         double* dov, double* p, double* ds, double* m_out, double* l_out,
+                         double* D_out, double* dqi) {
+    const orc_geom* g = c->g;
+    const int32_t hq_n = g->num_q_heads, hkv = g->num_kv_heads, d = g->head_dim;
+    const int32_t hk = h / (hq_n / hkv);
+    const int64_t row = c->cu[b] + i;
+    const double* K = c->K[b];
+    const double* V = c->V[b];
+    for (int32_t k = 0; k < d; ++k) {
+        qv[k] = bf16_to_double(c->q[(row * hq_n + h) * d + k]);
+        dov[k] = bf16_to_double(c->dout[(row * hq_n + h) * d + k]);
+    }
+    double m = -INFINITY;
+    for (int32_t j = 0; j <= i; ++j) {
+        const double* kj = K + ((int64_t)j * hkv + hk) * d;
+        double dot = 0.0;
+        for (int32_t k = 0; k < d; ++k) dot += qv[k] * kj[k];
+        p[j] = c->scale * dot;
+        if (p[j] > m) m = p[j];
+    }
+    double l = 0.0;
+    for (int32_t j = 0; j <= i; ++j) l += exp(p[j] - m);
+    double D = 0.0;
+    for (int32_t j = 0; j <= i; ++j) {
+        p[j] = exp(p[j] - m) / l;
+        const double* vj = V + ((int64_t)j * hkv + hk) * d;
+        double dp = 0.0;
+        for (int32_t k = 0; k < d; ++k) dp += dov[k] * vj[k];
+        ds[j] = dp;
+        D += p[j] * dp;
+    }
+    for (int32_t j = 0; j <= i; ++j) ds[j] = p[j] * (ds[j] - D);
+    if (dqi) {
+        for (int32_t k = 0; k < d; ++k) dqi[k] = 0.0;
+        for (int32_t j = 0; j <= i; ++j) {
+            const double* kj = K + ((int64_t)j * hkv + hk) * d;
+            for (int32_t k = 0; k < d; ++k) dqi[k] += c->scale * ds[j] * kj[k];
+        }
+    }
+    *m_out = m;
+    *l_out = l;
+    *D_out = D;
+}
+
 /* Gradients of the causal prefill of sequence b for the q heads of kv head hk
  * (one work item: it alone writes these dQ rows and these dK / dV rows).  The
  * definition, by the chain rule through o_i = sum_j p_ij v_j and the softmax
@@ -638,9 +690,7 @@ typedef struct {
  *   D_i   = sum_j p_ij dp_ij         ds_ij = p_ij (dp_ij - D_i)
  *   dq_i  = scale sum_j ds_ij k_j    dk_j += scale sum_i ds_ij q_i
  * with dk, dv summed over the q heads that read kv head hk [FA2 "4. MQA · GQA
- * 지원": the gradients of the implicitly repeated heads are added]; p is
- * recomputed here from the scores, as the FA2 backward recomputes it from the
- * stored L [FA2, 전체 흐름: "L로 P 재계산"]. */
+ * 지원": the gradients of the implicitly repeated heads are added]. */
 static void backward_item(void* ctx, int64_t item, double* scratch) {
     const backward_ctx* c = (const backward_ctx*)ctx;
     const orc_geom* g = c->g;
@@ -649,8 +699,6 @@ static void backward_item(void* ctx, int64_t item, double* scratch) {
     const int32_t b = (int32_t)(item / hkv), hk = (int32_t)(item % hkv);
     const int64_t r0 = c->cu[b];
     const int32_t n = c->cu[b + 1] - c->cu[b];
-    const double* K = c->K[b];
-    const double* V = c->V[b];
     double* qv = scratch;        /* d */
     double* dov = qv + d;        /* d */
     double* p = dov + d;         /* n */
@@ -658,39 +706,12 @@ static void backward_item(void* ctx, int64_t item, double* scratch) {
     for (int32_t r = 0; r < group; ++r) {
         const int32_t h = hk * group + r;
         for (int32_t i = 0; i < n; ++i) {
-            const int64_t row = r0 + i;
-            for (int32_t k = 0; k < d; ++k) {
-                qv[k] = bf16_to_double(c->q[(row * hq_n + h) * d + k]);
-                dov[k] = bf16_to_double(c->dout[(row * hq_n + h) * d + k]);
-            }
-            double m = -INFINITY;
+            double m, l, D;
+            backward_row(c, b, h, i, qv, dov, p, ds, &m, &l, &D, c->dq + ((r0 + i) * hq_n + h) * d);
             for (int32_t j = 0; j <= i; ++j) {
-                const double* kj = K + ((int64_t)j * hkv + hk) * d;
-                double dot = 0.0;
-                for (int32_t k = 0; k < d; ++k) dot += qv[k] * kj[k];
-                p[j] = c->scale * dot;
-                if (p[j] > m) m = p[j];
-            }
-            double l = 0.0;
-            for (int32_t j = 0; j <= i; ++j) l += exp(p[j] - m);
-            double D = 0.0;
-            for (int32_t j = 0; j <= i; ++j) {
-                p[j] = exp(p[j] - m) / l;
-                const double* vj = V + ((int64_t)j * hkv + hk) * d;
-                double dp = 0.0;
-                for (int32_t k = 0; k < d; ++k) dp += dov[k] * vj[k];
-                ds[j] = dp;
-                D += p[j] * dp;
-            }
-            double* dqi = c->dq + (row * hq_n + h) * d;
-            for (int32_t k = 0; k < d; ++k) dqi[k] = 0.0;
-            for (int32_t j = 0; j <= i; ++j) {
-                ds[j] = p[j] * (ds[j] - D);
-                const double* kj = K + ((int64_t)j * hkv + hk) * d;
                 double* dkj = c->dk + ((r0 + j) * hkv + hk) * d;
                 double* dvj = c->dv + ((r0 + j) * hkv + hk) * d;
                 for (int32_t k = 0; k < d; ++k) {
-                    dqi[k] += c->scale * ds[j] * kj[k];
                     dkj[k] += c->scale * ds[j] * qv[k];
                     dvj[k] += p[j] * dov[k];
                 }
@@ -730,6 +751,212 @@ int orc_prefill_backward(const orc_geom* g, const uint16_t* q, const uint8_t* po
     }
     free_all(batch, K, V);
     free(lens);
+    return st;
+}
+
+/* ------------------------------------------------ backward at sampled rows */
+
+typedef struct {
+    backward_ctx base;
+    int32_t n_pairs;            /* (sequence, q head) pairs whose row statistics are needed */
+    const int32_t* pair_b;
+    const int32_t* pair_h;
+    const int64_t* pair_first;  /* first stats item of each pair; [n_pairs + 1] */
+    double** stats;             /* per pair: m, l, D of every row, [3 n] */
+    int64_t n_q;
+    const int64_t* q_rows;
+    const int32_t* q_heads;
+    double* dq;                 /* [n_q][d] */
+    const int64_t* k_rows;
+    const int32_t* k_heads;
+    const int32_t* k_pair0;     /* stats pair of (sequence of k row, first q head of its group) */
+    double* dk;                 /* [n_k][d] */
+    double* dv;
+} backward_rows_ctx;
+
+static void backward_stats_item(void* ctx, int64_t item, double* scratch) {
+    const backward_rows_ctx* c = (const backward_rows_ctx*)ctx;
+    int32_t k = 0;
+    while (item >= c->pair_first[k + 1]) ++k;
+    const int32_t i = (int32_t)(item - c->pair_first[k]);
+    const int32_t d = c->base.g->head_dim;
+    const int32_t n = c->base.cu[c->pair_b[k] + 1] - c->base.cu[c->pair_b[k]];
+    double* st = c->stats[k] + 3 * (int64_t)i;
+    backward_row(&c->base, c->pair_b[k], c->pair_h[k], i, scratch, scratch + d, scratch + 2 * d,
+                 scratch + 2 * d + n, &st[0], &st[1], &st[2], NULL);
+}
+
+/* Sample s < n_q: dq of (row, q head), the row computation of
+ * orc_prefill_backward.  Sample n_q + t: dk, dv of key row k_rows[t], kv head
+ * k_heads[t]: the terms of orc_prefill_backward's sums that land on that key,
+ * in its order (q heads of the group, then query rows i >= j), each p_ij and
+ * ds_ij rebuilt from row i's m, l and D as that row computes them. */
+static void backward_sample_item(void* ctx, int64_t item, double* scratch) {
+    const backward_rows_ctx* c = (const backward_rows_ctx*)ctx;
+    const backward_ctx* bc = &c->base;
+    const orc_geom* g = bc->g;
+    const int32_t hq_n = g->num_q_heads, hkv = g->num_kv_heads, d = g->head_dim;
+    const int32_t group = hq_n / hkv;
+    if (item < c->n_q) {
+        const int64_t row = c->q_rows[item];
+        const int32_t b = seq_of_row(bc->cu, bc->batch, row);
+        const int32_t n = bc->cu[b + 1] - bc->cu[b];
+        double m, l, D;
+        backward_row(bc, b, c->q_heads[item], (int32_t)(row - bc->cu[b]), scratch, scratch + d,
+                     scratch + 2 * d, scratch + 2 * d + n, &m, &l, &D, c->dq + item * d);
+        return;
+    }
+    const int64_t t = item - c->n_q;
+    const int64_t row = c->k_rows[t];
+    const int32_t hk = c->k_heads[t];
+    const int32_t b = seq_of_row(bc->cu, bc->batch, row);
+    const int64_t r0 = bc->cu[b];
+    const int32_t n = bc->cu[b + 1] - bc->cu[b];
+    const int32_t j = (int32_t)(row - r0);
+    const double* kj = bc->K[b] + ((int64_t)j * hkv + hk) * d;
+    const double* vj = bc->V[b] + ((int64_t)j * hkv + hk) * d;
+    double* dkj = c->dk + t * d;
+    double* dvj = c->dv + t * d;
+    double* qv = scratch;
+    double* dov = scratch + d;
+    for (int32_t k = 0; k < d; ++k) dkj[k] = dvj[k] = 0.0;
+    for (int32_t r = 0; r < group; ++r) {
+        const int32_t h = hk * group + r;
+        const double* st = c->stats[c->k_pair0[t] + r];
+        for (int32_t i = j; i < n; ++i) {
+            const int64_t qrow = r0 + i;
+            for (int32_t k = 0; k < d; ++k) {
+                qv[k] = bf16_to_double(bc->q[(qrow * hq_n + h) * d + k]);
+                dov[k] = bf16_to_double(bc->dout[(qrow * hq_n + h) * d + k]);
+            }
+            double dot = 0.0;
+            for (int32_t k = 0; k < d; ++k) dot += qv[k] * kj[k];
+            const double pij = exp(bc->scale * dot - st[3 * i]) / st[3 * i + 1];
+            double dp = 0.0;
+            for (int32_t k = 0; k < d; ++k) dp += dov[k] * vj[k];
+            const double dsij = pij * (dp - st[3 * i + 2]);
+            for (int32_t k = 0; k < d; ++k) {
+                dkj[k] += bc->scale * dsij * qv[k];
+                dvj[k] += pij * dov[k];
+            }
+        }
+    }
+}
+
+int orc_prefill_backward_rows(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                              const int32_t* block_table, int32_t layer, int32_t batch,
+                              const int32_t* cu_seqlens, const int32_t* slots, float scale,
+                              const uint16_t* dout, int64_t n_q, const int64_t* q_rows,
+                              const int32_t* q_heads, double* dq, int64_t n_k, const int64_t* k_rows,
+                              const int32_t* k_heads, double* dk, double* dv, int32_t nthreads) {
+    if (!check_batch(g, batch, cu_seqlens, slots, layer) || !pool || !block_table || n_q < 0 || n_k < 0)
+        return ORC_BAD_ARG;
+    if ((n_q > 0 && (!q_rows || !q_heads || !dq)) || (n_k > 0 && (!k_rows || !k_heads || !dk || !dv)))
+        return ORC_BAD_ARG;
+    const int64_t T = cu_seqlens[batch];
+    if (T > 0 && (!q || !dout)) return ORC_BAD_ARG;
+    const int32_t hq_n = g->num_q_heads, hkv = g->num_kv_heads, group = hq_n / hkv;
+    int st = ORC_OK;
+    int32_t* lens = (int32_t*)malloc(sizeof(int32_t) * (size_t)(batch + 1));
+    char* need = (char*)calloc((size_t)batch + 1, 1);
+    int32_t* pair_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)((int64_t)batch * hq_n + 1));
+    int32_t* pair_b = (int32_t*)malloc(sizeof(int32_t) * (size_t)((int64_t)batch * hq_n + 1));
+    int32_t* pair_h = (int32_t*)malloc(sizeof(int32_t) * (size_t)((int64_t)batch * hq_n + 1));
+    int64_t* pair_first = (int64_t*)malloc(sizeof(int64_t) * (size_t)((int64_t)batch * hq_n + 2));
+    int32_t* k_pair0 = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_k + 1));
+    double** stats = (double**)calloc((size_t)((int64_t)batch * hq_n + 1), sizeof(double*));
+    double** K = (double**)calloc((size_t)batch + 1, sizeof(double*));
+    double** V = (double**)calloc((size_t)batch + 1, sizeof(double*));
+    if (!lens || !need || !pair_of || !pair_b || !pair_h || !pair_first || !k_pair0 || !stats || !K || !V) {
+        st = ORC_BAD_ARG;
+        goto done;
+    }
+    int32_t nmax = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        lens[b] = cu_seqlens[b + 1] - cu_seqlens[b];
+        if (lens[b] > nmax) nmax = lens[b];
+    }
+    for (int64_t x = 0; x < (int64_t)batch * hq_n; ++x) pair_of[x] = -1;
+    for (int64_t s = 0; s < n_q; ++s) {
+        const int32_t b = (q_rows[s] >= 0 && q_rows[s] < T) ? seq_of_row(cu_seqlens, batch, q_rows[s]) : -1;
+        if (b < 0 || q_heads[s] < 0 || q_heads[s] >= hq_n) st = ORC_BAD_ARG;
+        else need[b] = 1;
+    }
+    int32_t n_pairs = 0;
+    for (int64_t t = 0; t < n_k && st == ORC_OK; ++t) {
+        const int32_t b = (k_rows[t] >= 0 && k_rows[t] < T) ? seq_of_row(cu_seqlens, batch, k_rows[t]) : -1;
+        if (b < 0 || k_heads[t] < 0 || k_heads[t] >= hkv) {
+            st = ORC_BAD_ARG;
+            break;
+        }
+        need[b] = 1;
+        /* the group's q heads get consecutive pair numbers */
+        const int64_t key = (int64_t)b * hq_n + (int64_t)k_heads[t] * group;
+        if (pair_of[key] < 0) {
+            for (int32_t r = 0; r < group; ++r) {
+                pair_of[key + r] = n_pairs;
+                pair_b[n_pairs] = b;
+                pair_h[n_pairs] = k_heads[t] * group + r;
+                ++n_pairs;
+            }
+        }
+        k_pair0[t] = pair_of[key];
+    }
+    if (st == ORC_OK) st = gather_all(g, pool, block_table, layer, batch, lens, slots, need, K, V);
+    if (st == ORC_OK) {
+        pair_first[0] = 0;
+        for (int32_t k = 0; k < n_pairs; ++k) {
+            const int32_t n = lens[pair_b[k]];
+            pair_first[k + 1] = pair_first[k] + n;
+            stats[k] = (double*)malloc(sizeof(double) * (size_t)(3 * (int64_t)n + 1));
+            if (!stats[k]) st = ORC_BAD_ARG;
+        }
+    }
+    if (st == ORC_OK) {
+        backward_rows_ctx c;
+        memset(&c, 0, sizeof(c));
+        c.base.g = g;
+        c.base.q = q;
+        c.base.dout = dout;
+        c.base.cu = cu_seqlens;
+        c.base.scale = (double)scale;
+        c.base.K = K;
+        c.base.V = V;
+        c.base.batch = batch;
+        c.n_pairs = n_pairs;
+        c.pair_b = pair_b;
+        c.pair_h = pair_h;
+        c.pair_first = pair_first;
+        c.stats = stats;
+        c.n_q = n_q;
+        c.q_rows = q_rows;
+        c.q_heads = q_heads;
+        c.dq = dq;
+        c.k_rows = k_rows;
+        c.k_heads = k_heads;
+        c.k_pair0 = k_pair0;
+        c.dk = dk;
+        c.dv = dv;
+        const int64_t scratch = 2 * (int64_t)g->head_dim + 2 * (int64_t)nmax;
+        if (n_pairs > 0) run_items(backward_stats_item, &c, pair_first[n_pairs], scratch, nthreads);
+        run_items(backward_sample_item, &c, n_q + n_k, scratch, nthreads);
+    }
+done:
+    if (stats)
+        for (int64_t k = 0; k < (int64_t)batch * hq_n; ++k) free(stats[k]);
+    free(stats);
+    if (K && V) free_all(batch, K, V);
+    else {
+        free(K);
+        free(V);
+    }
+    free(lens);
+    free(need);
+    free(pair_of);
+    free(pair_b);
+    free(pair_h);
+    free(pair_first);
+    free(k_pair0);
     return st;
 }
 

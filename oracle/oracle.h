@@ -164,6 +164,18 @@ int orc_prefill_backward(const orc_geom* g, const uint16_t* q, const uint8_t* po
                          const int32_t* cu_seqlens, const int32_t* slots, float scale,
                          const uint16_t* dout, double* dq, double* dk, double* dv, int32_t nthreads);
 
+/* orc_prefill_backward at sampled outputs: dq[s] = dq of (q_rows[s],
+ * q_heads[s]) for s < n_q, and dk[t], dv[t] = dk, dv of (k_rows[t], kv head
+ * k_heads[t]) for t < n_k (rows in packed order), equal bit for bit to the
+ * full call's entries; each row's statistics are computed once per (sequence,
+ * q head) that a k sample needs. */
+int orc_prefill_backward_rows(const orc_geom* g, const uint16_t* q, const uint8_t* pool,
+                              const int32_t* block_table, int32_t layer, int32_t batch,
+                              const int32_t* cu_seqlens, const int32_t* slots, float scale,
+                              const uint16_t* dout, int64_t n_q, const int64_t* q_rows,
+                              const int32_t* q_heads, double* dq, int64_t n_k, const int64_t* k_rows,
+                              const int32_t* k_heads, double* dk, double* dv, int32_t nthreads);
+
 /* Single-query decode [TV6 "논리 블록 → 물리 블록 → 바이트 주소"]: query b
  * (q[B][Hq][d]) attends keys 0..seq_lens[b]-1 of slots[b]; the length
  * includes the token just written.  seq_len 0 gives O = 0, L = -inf.

@@ -176,3 +176,37 @@ def test_identities_at_long_prompt_size():
         rhs = (k[rows] * dk[rows].astype(np.float64)).sum(axis=(0, 2))
         mag = (np.abs(q[rows].reshape(-1, 8, 4, 64) * dq[rows].reshape(-1, 8, 4, 64))).sum(axis=(0, 2, 3))
         assert np.all(np.abs(lhs - rhs) <= 1e-3 * mag + 1e-6), (lhs, rhs, mag)
+
+
+def test_bench_size_sampled_rows():
+    """The bench's backward workload in its launch configuration: 4 prompts of
+    8192 tokens, 32 q / 8 kv heads, d 64, shuffled pages.  dq at 48 sampled
+    (row, q head) pairs and dk, dv at 12 sampled (key row, kv head) pairs of
+    two (sequence, kv head) units against the oracle's sampled backward (the
+    full backward's entries, computed one by one)."""
+    B, n = 4, 8192
+    pages = n // 16
+    geom = W.Geometry(32, 8, 64, 1, B, pages, B * pages + 64)
+    case = W.make_prefill_case("bwd", geom, [n] * B, 1007)
+    dout = W.normal_bf16(np.random.default_rng(1008), case.q.shape)
+    pool, bt, werr = H.gpu_setup(case)
+    assert werr == 0
+    dq, dk, dv, err = gpu_forward_backward(case, pool, bt, dout)
+    assert err == 0
+    rng = np.random.default_rng(5)
+    starts = np.arange(B) * n
+    q_rows = np.concatenate([starts, starts + n - 1, starts + 127, starts + 128, rng.integers(0, B * n, 32)])
+    q_heads = rng.integers(0, 32, q_rows.shape[0]).astype(np.int32)
+    units = [(0, 3), (3, 6)]  # (sequence, kv head)
+    k_rows, k_heads = [], []
+    for b, hk in units:
+        for j in (0, 127, 128, n - 1, int(rng.integers(0, n)), int(rng.integers(0, n))):
+            k_rows.append(b * n + j)
+            k_heads.append(hk)
+    st, rq, rk, rv = oracle.prefill_backward_rows(
+        H.oracle_geom(case), case.q, H.oracle_pool(case), case.block_table, 0, case.cu_seqlens, case.slots,
+        case.scale, dout, q_rows, q_heads, np.array(k_rows), np.array(k_heads))
+    assert st == 0
+    assert_grad_close(dq[q_rows, q_heads], rq, "dq sampled, 4 x 8192")
+    assert_grad_close(dk[k_rows, k_heads], rk, "dk sampled, 4 x 8192")
+    assert_grad_close(dv[k_rows, k_heads], rv, "dv sampled, 4 x 8192")

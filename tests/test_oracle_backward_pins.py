@@ -129,3 +129,33 @@ def test_identities():
         sv = dv[cu[b]:cu[b + 1]].sum(axis=0)
         want = do[cu[b]:cu[b + 1]].reshape(-1, 2, 4, 64).sum(axis=(0, 2))
         np.testing.assert_allclose(sv, want, rtol=1e-11, atol=1e-10)
+
+
+@pytest.mark.parametrize("hq,hkv,d,lens", [
+    (8, 2, 64, [40, 17, 1]),
+    (6, 1, 64, [29, 33]),     # MQA, a group of 6
+    (4, 2, 128, [23, 9]),
+])
+def test_sampled_rows_equal_the_full_backward(hq, hkv, d, lens):
+    """prefill_backward_rows (dq of chosen (row, q head), dk / dv of chosen
+    (row, kv head)) is the full call's entries, bit for bit: the same
+    arithmetic in the same order."""
+    case, g, pool, dout = setup(hq, hkv, d, lens, seed=hq * 7 + d)
+    args = (g, case.q, pool, case.block_table, 0, case.cu_seqlens, case.slots, case.scale, dout)
+    st, dq, dk, dv = oracle.prefill_backward(*args)
+    assert st == 0
+    T = case.total_tokens
+    cu = case.cu_seqlens
+    rng = np.random.default_rng(hq + d)
+    q_rows = np.concatenate([[0, T - 1, cu[1] - 1, cu[1]], rng.integers(0, T, 12)]).astype(np.int64)
+    q_heads = rng.integers(0, hq, q_rows.shape[0]).astype(np.int32)
+    k_rows = np.concatenate([[0, T - 1, cu[1] - 1, cu[1]], rng.integers(0, T, 8)]).astype(np.int64)
+    k_heads = rng.integers(0, hkv, k_rows.shape[0]).astype(np.int32)
+    st2, sq, sk, sv = oracle.prefill_backward_rows(*args, q_rows, q_heads, k_rows, k_heads)
+    assert st2 == 0
+    np.testing.assert_array_equal(sq, dq[q_rows, q_heads])
+    np.testing.assert_array_equal(sk, dk[k_rows, k_heads])
+    np.testing.assert_array_equal(sv, dv[k_rows, k_heads])
+    # out-of-range samples are refused
+    assert oracle.prefill_backward_rows(*args, [T], [0], [], [])[0] != 0
+    assert oracle.prefill_backward_rows(*args, [], [], [0], [hkv])[0] != 0

@@ -51,6 +51,10 @@ MUTANTS = {
     "bwd_dv_uses_ds": ("dvj[k] += p[j] * dov[k];", "dvj[k] += ds[j] * dov[k];"),
     "bwd_first_head_only": ("    for (int32_t r = 0; r < group; ++r) {\n        const int32_t h = hk * group + r;\n        for (int32_t i = 0; i < n; ++i) {",
                             "    for (int32_t r = 0; r < 1; ++r) {\n        const int32_t h = hk * group + r;\n        for (int32_t i = 0; i < n; ++i) {"),
+    "bwd_rows_skips_diagonal": ("        for (int32_t i = j; i < n; ++i) {\n            const int64_t qrow = r0 + i;",
+                                "        for (int32_t i = j + 1; i < n; ++i) {\n            const int64_t qrow = r0 + i;"),
+    "bwd_rows_stats_of_next_row": ("const double pij = exp(bc->scale * dot - st[3 * i]) / st[3 * i + 1];",
+                                   "const double pij = exp(bc->scale * dot - st[3 * (i + (i + 1 < n))]) / st[3 * i + 1];"),
     "max_not_subtracted": ("for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m);",
                            "for (int32_t j = 0; j < n; ++j) l += exp(s[j] - m) * (1 + 1e-9 * m);"),
 }
@@ -76,6 +80,7 @@ PIN_TESTS = [
     lambda gd: ppins.test_decode_takes_a_page_only_at_a_new_block(),
     lambda gd: bpins.test_matches_torch_autograd(8, 2, 64, [40, 17]),
     lambda gd: bpins.test_identities(),
+    lambda gd: bpins.test_sampled_rows_equal_the_full_backward(8, 2, 64, [40, 17, 1]),
 ]
 
 
