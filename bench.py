@@ -20,8 +20,9 @@ decode's 4 d Hq n).  The line also carries:
   backward     -- pa_prefill_backward on the long prompt (4 x 8192, d 64):
                   2.5 x the exact causal count, TFLOP/s against that peak;
   e2e          -- the same metric through the C ABI with host buffers: pinned
-                  H2D of the step's inputs and D2H of its outputs inside the
-                  timed region;
+                  H2D of every step's inputs and D2H of its outputs inside the
+                  timed region, neighbouring steps' copies overlapping the
+                  compute (and, as "serial", without that overlap);
   cpu_baseline -- the fp64 CPU oracle timed on a bounded sample of the same
                   workload on this host's cores.
 N > 1 (torchrun): independent replicas, one per GPU, no collective on the
@@ -215,20 +216,25 @@ class PrefillStep:
         self.flops = self.flops_prefill + self.flops_decode
         self.launches = 5  # write, prefill, write, attend, merge
 
-    def run(self, d=None, ev=None):
+    def outputs(self):
+        """Fresh device output buffers (o, lse, decode o, decode lse)."""
+        return tuple(self.torch.empty_like(t) for t in (self.o, self.lse, self.dec_o, self.dec_lse))
+
+    def run(self, d=None, ev=None, out=None):
         pa, c = self.pa, self.case
         d = self.d if d is None else d
+        o, lse, dec_o, dec_lse = (self.o, self.lse, self.dec_o, self.dec_lse) if out is None else out
         pa.pa_write_kv(self.g, self.pool, d["bt"], 0, d["tok_slot"], d["tok_pos"], d["k"], d["v"], self.err)
         if ev is not None:
             ev[0].record()
-        pa.pa_prefill(self.g, d["q"], self.pool, d["bt"], 0, d["cu"], d["slots"], self.n, c.scale, self.o,
-                      self.lse, self.err)
+        pa.pa_prefill(self.g, d["q"], self.pool, d["bt"], 0, d["cu"], d["slots"], self.n, c.scale, o, lse,
+                      self.err)
         if ev is not None:
             ev[1].record()
         pa.pa_write_kv(self.g, self.pool, d["bt"], 0, d["new_slot"], d["new_pos"], d["new_k"], d["new_v"],
                        self.err)
         pa.pa_decode(self.g, d["dec_q"], self.pool, d["bt"], 0, d["dec_lens"], d["slots"], self.n + 1,
-                     c.scale, self.dec_o, self.dec_lse, self.ws, self.err)
+                     c.scale, dec_o, dec_lse, self.ws, self.err)
 
 
 class ScatterStep:
@@ -435,6 +441,85 @@ def timed(torch, fn, steps, warmup, flush, dist=None, kernel_events=True):
     step_s = [m[0].elapsed_time(m[1]) * 1e-3 for m in marks]
     kern_s = [m[2].elapsed_time(m[3]) * 1e-3 for m in marks] if kernel_events else []
     return step_s, kern_s
+
+
+def e2e_timing(torch, step, steps, warmup, flush, dist):
+    """The step through the C ABI with host buffers: every step copies its
+    inputs in from pinned host memory and its outputs (prefill o and lse,
+    decode o and lse) back out.  Two figures:
+      value  -- pipelined, as a serving loop runs: step s + 1's inputs are
+                copied in (copy stream) and step s - 1's outputs copied out
+                (another stream) while step s computes; double-buffered
+                device inputs and outputs; one timed region over all steps
+                (every step's copies inside it; the 201 MB of inputs per step
+                exceed L2, so no flush is needed between steps);
+      serial -- each step's copy-in, compute and copy-out back to back, L2
+                flushed between steps."""
+    pin = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in step.h.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d_in = [{k: torch.empty_like(v, device="cuda") for k, v in pin.items()} for _ in range(2)]
+    d_out = [step.outputs() for _ in range(2)]
+    h_out = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in d_out[0]) for _ in range(2)]
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    s_c = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    E = torch.cuda.Event
+    ev_in = [E(), E()]
+    ev_comp = [E(), E()]
+    ev_out = [E(), E()]
+
+    def one(s):
+        x = s % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_comp[x])  # the compute of step s - 2 is done with buffer x
+            for k, v in pin.items():
+                d_in[x][k].copy_(v, non_blocking=True)
+            ev_in[x].record(s_in)
+        s_c.wait_event(ev_in[x])
+        s_c.wait_event(ev_out[x])  # the outputs of step s - 2 have left buffer x
+        step.run(d=d_in[x], out=d_out[x])
+        ev_comp[x].record(s_c)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[x])
+            for hst, dv in zip(h_out[x], d_out[x]):
+                hst.copy_(dv, non_blocking=True)
+            ev_out[x].record(s_out)
+
+    for s in range(warmup):
+        one(s)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = E(enable_timing=True), E(enable_timing=True)
+    t0.record(s_c)
+    s_in.wait_stream(s_c)
+    s_out.wait_stream(s_c)
+    for s in range(steps):
+        one(warmup + s)
+    s_c.wait_stream(s_out)
+    s_c.wait_stream(s_in)
+    t1.record(s_c)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    total = t0.elapsed_time(t1) * 1e-3
+    rate, total_s, _ = job_rate(torch, dist, step.flops * steps, total)
+
+    def serial_step(ev):
+        for k, v in pin.items():
+            d_in[0][k].copy_(v, non_blocking=True)
+        step.run(d=d_in[0], out=d_out[0])
+        for hst, dv in zip(h_out[0], d_out[0]):
+            hst.copy_(dv, non_blocking=True)
+
+    es, _ = timed(torch, serial_step, steps, warmup, flush, dist, kernel_events=False)
+    s_rate, s_total, _ = job_rate(torch, dist, step.flops * steps, float(np.sum(es)))
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps, "ms_per_step": total_s / steps * 1e3,
+            "pipelining": "step s+1 copied in and step s-1 copied out while step s computes",
+            "serial": {"value": s_rate / 1e12, "unit": "TFLOP/s", "ms_per_step": s_total / steps * 1e3}}
 
 
 def _rank_device(dist):
@@ -771,29 +856,7 @@ def main():
 
     if step is not None and not args.no_e2e:
         # ------------------------------------------------------------ e2e
-        pin = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in step.h.items()}
-        o_host = torch.empty(step.o.shape, dtype=torch.int16).pin_memory()
-        lse_host = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
-        do_host = torch.empty(step.dec_o.shape, dtype=torch.int16).pin_memory()
-        dl_host = torch.empty(step.dec_lse.shape, dtype=torch.float32).pin_memory()
-        d_in = {k: torch.empty_like(v, device="cuda") for k, v in pin.items()}
-        h2d = sum(v.numel() * v.element_size() for v in pin.values())
-        d2h = sum(t.numel() * t.element_size() for t in (o_host, lse_host, do_host, dl_host))
-
-        def e2e_step(ev):
-            for k, v in pin.items():
-                d_in[k].copy_(v, non_blocking=True)
-            step.run(d=d_in)
-            o_host.copy_(step.o, non_blocking=True)
-            lse_host.copy_(step.lse, non_blocking=True)
-            do_host.copy_(step.dec_o, non_blocking=True)
-            dl_host.copy_(step.dec_lse, non_blocking=True)
-
-        e_steps = max(10, args.steps // 4)
-        es, _ = timed(torch, e2e_step, e_steps, args.warmup, flush, dist, kernel_events=False)
-        e_rate, e_total, _ = job_rate(torch, dist, step.flops * e_steps, float(np.sum(es)))
-        e2e = {"value": e_rate / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": e_steps}
+        e2e = e2e_timing(torch, step, max(10, args.steps // 4), args.warmup, flush, dist)
 
     # ------------------------------------------------------- CPU oracle
     cpu = None
