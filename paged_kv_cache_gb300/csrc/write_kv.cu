@@ -6,14 +6,18 @@
 // block_table[slot][layer][pos / 16] (jaehun.me tiny-vllm part 6, "블록 하나가
 // 담는 것: K 는 앞, V 는 V_OFFSET 뒤"; part 3, "Distributing K/V into paged
 // blocks").  The series issues one device-to-device memcpy per page per layer;
-// here one launch moves every row of the call: one thread per 16-byte chunk,
-// consecutive threads on consecutive chunks of a row, so reads of k_new/v_new
-// and writes of each 2*KV_DIM-byte row are fully coalesced 16-byte accesses.
+// here one launch moves every row of the call: each thread moves 64 bytes (4
+// chunks of 16) of one row, consecutive threads on consecutive chunks, so reads
+// of k_new/v_new and writes of each 2*KV_DIM-byte row are fully coalesced.
 #include "pa_internal.cuh"
 
 namespace pa {
 namespace {
 
+// CPT consecutive 16-byte chunks of one K or V row per thread (CPT divides the
+// row's chunk count).  The row's data is read before its page is looked up,
+// so the two global latencies overlap instead of adding up.
+template <int CPT>
 __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restrict__ pool,
                                                        const int32_t* __restrict__ block_table,
                                                        int layer, int n_tokens,
@@ -23,15 +27,23 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
                                                        const uint4* __restrict__ v_new,
                                                        int32_t* err) {
     const int chunks = g.kv_dim / 8;  // 16-byte chunks per K (or V) row
-    const long long total = static_cast<long long>(n_tokens) * 2 * chunks;
+    const int groups = chunks / CPT;  // threads per K (or V) row
+    const long long total = static_cast<long long>(n_tokens) * 2 * groups;
     const long long half_page = g.page_bytes / 2;  // V_OFFSET
     const long long row_bytes = static_cast<long long>(g.kv_dim) * 2;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long row = idx / (2 * chunks);
-        const int rem = static_cast<int>(idx - row * 2 * chunks);
-        const int is_v = rem >= chunks;
-        const int c = is_v ? rem - chunks : rem;
+        const long long row = idx / (2 * groups);
+        const int rem = static_cast<int>(idx - row * 2 * groups);
+        const int is_v = rem >= groups;
+        const int c = (is_v ? rem - groups : rem) * CPT;
+        const uint4* src = (is_v ? v_new : k_new) + row * chunks + c;
+        uint4 val[CPT];
+#pragma unroll
+        for (int x = 0; x < CPT; ++x)
+            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(val[x].x), "=r"(val[x].y), "=r"(val[x].z), "=r"(val[x].w)
+                         : "l"(src + x));
         const int slot = __ldg(tok_slot + row);
         const int pos = __ldg(tok_pos + row);
         long long blk = -1;
@@ -45,15 +57,10 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
             if (rem == 0) set_error(err, PA_ERR_BAD_BLOCK);
             continue;
         }
-        const uint4* src = (is_v ? v_new : k_new) + row * chunks + c;
-        uint4 val;
-        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                     : "l"(src));
-        uint8_t* dst = pool + blk * g.page_bytes + (is_v ? half_page : 0) +
-                       static_cast<long long>(pos % kBlockTokens) * row_bytes +
-                       static_cast<long long>(c) * 16;
-        *reinterpret_cast<uint4*>(dst) = val;
+        uint4* dst = reinterpret_cast<uint4*>(pool + blk * g.page_bytes + (is_v ? half_page : 0) +
+                                              static_cast<long long>(pos % kBlockTokens) * row_bytes) + c;
+#pragma unroll
+        for (int x = 0; x < CPT; ++x) dst[x] = val[x];
     }
 }
 
@@ -64,7 +71,8 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
 // with c, s from caller tables [max_pos][d/2] fp32.  Each product and sum is
 // rounded on its own (no FMA contraction), then to bf16 nearest-even.  Per
 // row, the first kv_dim/16 threads each take 8 pairs of one head (16 bytes of
-// each half, read and written whole), the next kv_dim/8 threads copy V.
+// each half, read and written whole), the next threads copy V, VPT 16-byte
+// chunks each.  Every thread reads its row's data before looking up the page.
 __device__ __forceinline__ void rope8(uint4& lo, uint4& hi, const float4 c0, const float4 c1, const float4 s0,
                                       const float4 s1) {
     const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
@@ -98,6 +106,7 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     return v;
 }
 
+template <int VPT>
 __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __restrict__ pool,
                                                             const int32_t* __restrict__ block_table, int layer,
                                                             int n_tokens, const int32_t* __restrict__ tok_slot,
@@ -108,8 +117,9 @@ __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __
                                                             const float* __restrict__ sin_tab, int max_pos,
                                                             int32_t* err) {
     const int kq = g.kv_dim / 16;  // K threads per row: 8 pairs each
-    const int vc = g.kv_dim / 8;   // V threads per row: one 16-byte chunk each
-    const int per_row = kq + vc;
+    const int vc = g.kv_dim / 8;   // 16-byte V chunks per row
+    const int vt = vc / VPT;       // V threads per row: VPT chunks each
+    const int per_row = kq + vt;
     const int hc = g.d / 16;       // pair chunks per head
     const long long total = static_cast<long long>(n_tokens) * per_row;
     const long long half_page = g.page_bytes / 2;  // V_OFFSET
@@ -118,6 +128,19 @@ __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const long long row = idx / per_row;
         const int rem = static_cast<int>(idx - row * per_row);
+        const bool is_k = rem < kq;
+        const int head = rem / hc, c = is_k ? rem % hc : rem - kq;
+        const long long e_lo = static_cast<long long>(head) * g.d + 8 * c;  // K: element index in the row
+        const long long e_hi = e_lo + g.d / 2;
+        // the row's data first: its latency overlaps the page lookup
+        uint4 lo, hi, vv[VPT];
+        if (is_k) {
+            lo = ld_stream(k_new + (row * g.kv_dim + e_lo) / 8);
+            hi = ld_stream(k_new + (row * g.kv_dim + e_hi) / 8);
+        } else {
+#pragma unroll
+            for (int x = 0; x < VPT; ++x) vv[x] = ld_stream(v_new + row * vc + c * VPT + x);
+        }
         const int slot = __ldg(tok_slot + row);
         const int pos = __ldg(tok_pos + row);
         long long blk = -1;
@@ -132,21 +155,16 @@ __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __
             continue;
         }
         uint8_t* dst_row = pool + blk * g.page_bytes + static_cast<long long>(pos % kBlockTokens) * row_bytes;
-        if (rem < kq) {
-            const int head = rem / hc, c = rem % hc;
-            const long long e_lo = static_cast<long long>(head) * g.d + 8 * c;  // element index in the row
-            const long long e_hi = e_lo + g.d / 2;
-            uint4 lo = ld_stream(k_new + (row * g.kv_dim + e_lo) / 8);
-            uint4 hi = ld_stream(k_new + (row * g.kv_dim + e_hi) / 8);
+        if (is_k) {
             const float4* ct = reinterpret_cast<const float4*>(cos_tab + static_cast<long long>(pos) * (g.d / 2) + 8 * c);
             const float4* st = reinterpret_cast<const float4*>(sin_tab + static_cast<long long>(pos) * (g.d / 2) + 8 * c);
             rope8(lo, hi, __ldg(ct), __ldg(ct + 1), __ldg(st), __ldg(st + 1));
             *reinterpret_cast<uint4*>(dst_row + e_lo * 2) = lo;
             *reinterpret_cast<uint4*>(dst_row + e_hi * 2) = hi;
         } else {
-            const int c = rem - kq;
-            *reinterpret_cast<uint4*>(dst_row + half_page + static_cast<long long>(c) * 16) =
-                ld_stream(v_new + row * vc + c);
+            uint4* dv = reinterpret_cast<uint4*>(dst_row + half_page) + c * VPT;
+#pragma unroll
+            for (int x = 0; x < VPT; ++x) dv[x] = vv[x];
         }
     }
 }
@@ -157,11 +175,13 @@ cudaError_t launch_write_kv_rope(const KGeom& g, void* pool, const int32_t* bloc
                                  int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,
                                  const void* k_new, const void* v_new, const float* cos_tab,
                                  const float* sin_tab, int max_pos, int32_t* err, cudaStream_t stream) {
-    const long long total = static_cast<long long>(n_tokens) * (g.kv_dim / 16 + g.kv_dim / 8);
+    const int vpt = (g.kv_dim / 8) % 4 == 0 ? 4 : 1;
+    const long long total = static_cast<long long>(n_tokens) * (g.kv_dim / 16 + g.kv_dim / 8 / vpt);
     const int threads = 256;
     long long blocks = (total + threads - 1) / threads;
     if (blocks > (1ll << 30)) blocks = 1ll << 30;  // grid-stride covers the rest
-    write_kv_rope_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+    auto kern = vpt == 4 ? write_kv_rope_kernel<4> : write_kv_rope_kernel<1>;
+    kern<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), cos_tab, sin_tab, max_pos, err);
     return cudaGetLastError();
@@ -171,13 +191,20 @@ cudaError_t launch_write_kv(const KGeom& g, void* pool, const int32_t* block_tab
                             int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,
                             const void* k_new, const void* v_new, int32_t* err,
                             cudaStream_t stream) {
-    const long long total = static_cast<long long>(n_tokens) * 2 * (g.kv_dim / 8);
+    const int chunks = g.kv_dim / 8;
+    const int cpt = chunks % 4 == 0 ? 4 : 1;
+    const long long total = static_cast<long long>(n_tokens) * 2 * (chunks / cpt);
     const int threads = 256;
     long long blocks = (total + threads - 1) / threads;
     if (blocks > (1ll << 30)) blocks = 1ll << 30;  // grid-stride covers the rest
-    write_kv_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), err);
+    if (cpt == 4)
+        write_kv_kernel<4><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+            g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
+            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), err);
+    else
+        write_kv_kernel<1><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+            g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
+            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), err);
     return cudaGetLastError();
 }
 

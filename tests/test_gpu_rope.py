@@ -79,3 +79,26 @@ def test_rope_write_then_prefill_matches_oracle():
     assert perr == 0
     ro, rl = H.oracle_prefill(case, ref)
     H.assert_close(o, l, ro, rl, H.max_abs_v(case), "rope write + prefill")
+
+
+@pytest.mark.parametrize("hq,hkv,d", [
+    (1, 1, 8),     # one 16-byte chunk per K or V row: one chunk per thread
+    (3, 3, 8),     # three chunks per row
+    (2, 1, 32),    # four chunks per row: four per thread
+    (1, 1, 16),    # RoPE with two V chunks per row
+])
+def test_narrow_rows_scatter_byte_exact(hq, hkv, d):
+    """Rows whose chunk count is not a multiple of four take the one-chunk
+    path of both scatters; the whole pool must still match the oracle."""
+    lens = [37, 5]
+    nb = sum((n + 15) // 16 for n in lens) + 4
+    geom = W.Geometry(hq, hkv, d, 2, len(lens), 8, nb)
+    case = W.make_prefill_case("narrow", geom, lens, seed=d + hkv, layers=(1,), pool_fill="nan")
+    pool, bt, werr = H.gpu_setup(case)
+    assert werr == 0
+    np.testing.assert_array_equal(pool.cpu().numpy(), H.oracle_pool(case))
+    if d % 16 == 0:
+        cos_t, sin_t = W.rope_tables(64, d)
+        got, ref, err, skipped = run_both(case, cos_t, sin_t)
+        assert err == 0 and skipped == 0
+        np.testing.assert_array_equal(got, ref)
