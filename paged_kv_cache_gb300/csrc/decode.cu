@@ -528,11 +528,110 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     if (lane == 0 && p.lse) p.lse[row] = S > 0.f ? M + lg2_approx(S) * kLn2 : -CUDART_INF_F;
 }
 
+// The same merge with one CTA per (sequence, q head): its 8 warps take the
+// partials in turn and add their sums through shared memory.  Used when the
+// batch has few (sequence, head) rows, so that long sequences, which the
+// attend grid splits into many pieces, do not leave one warp walking all of
+// them while most SMs idle.
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_split_kernel(const DecodeParams p) {
+    constexpr int PER = D / 32;
+    constexpr int W = kMergeThreads / 32;
+    __shared__ float red_m[W];
+    __shared__ float red_s[W];
+    __shared__ float red_o[W][D];
+    const KGeom& g = p.g;
+    const int b = blockIdx.x, hq = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int len = p.seq_lens[b];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long row = static_cast<long long>(b) * g.hq + hq;
+    if (len <= 0) {
+        if (warp == 0) {
+#pragma unroll
+            for (int e = 0; e < PER; ++e) p.o[row * D + lane * PER + e] = __float2bfloat16_rn(0.f);
+            if (lane == 0 && p.lse) p.lse[row] = -CUDART_INF_F;
+        }
+        return;
+    }
+    const int2 meta = *reinterpret_cast<const int2*>(p.ws + p.ws_meta + 8ll * b);
+    const long long G = p.attend_grid;
+    if (meta.x < 0 || meta.y >= G || meta.x > meta.y) {  // attend kernel gave up early
+        if (threadIdx.x == 0) set_error(p.err, PA_ERR_TIMEOUT);
+        return;
+    }
+    if (meta.x == meta.y) return;  // one unit: the attend kernel wrote the result
+    const long long T = *reinterpret_cast<const long long*>(p.ws);
+    const float* lse_part = reinterpret_cast<const float*>(p.ws + p.ws_lse);
+    const float* o_part = reinterpret_cast<const float*>(p.ws + p.ws_o);
+    auto has_pages = [&](long long cc) { return range_start(cc, T, G) != range_start(cc + 1, T, G); };
+
+    // 1. max of the partial L over the whole CTA
+    float M = -CUDART_INF_F;
+    for (long long cc = meta.x + threadIdx.x; cc <= meta.y; cc += kMergeThreads)
+        if (has_pages(cc)) M = fmaxf(M, lse_part[(b + cc) * g.hq + hq]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0) red_m[warp] = M;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, red_m[w]);
+
+    // 2. warp w sums partials meta.x + w, + W, ... (lanes over dims)
+    float acc[PER], S = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    if (M != -CUDART_INF_F) {
+#pragma unroll 4
+        for (long long cc = meta.x + warp; cc <= meta.y; cc += W) {
+            if (!has_pages(cc)) continue;
+            const float Lc = lse_part[(b + cc) * g.hq + hq];
+            const float wk = (Lc == -CUDART_INF_F) ? 0.f : ex2_approx((Lc - M) * kLog2e);
+            S += wk;
+            const float* src = o_part + ((b + cc) * g.hq + hq) * D + lane * PER;
+            if (PER == 2) {
+                const float2 v = *reinterpret_cast<const float2*>(src);
+                acc[0] = fmaf(wk, v.x, acc[0]);
+                acc[PER - 1] = fmaf(wk, v.y, acc[PER - 1]);
+            } else {
+                const float4 v = *reinterpret_cast<const float4*>(src);
+                acc[0] = fmaf(wk, v.x, acc[0]);
+                acc[1 % PER] = fmaf(wk, v.y, acc[1 % PER]);
+                acc[2 % PER] = fmaf(wk, v.z, acc[2 % PER]);
+                acc[3 % PER] = fmaf(wk, v.w, acc[3 % PER]);
+            }
+        }
+    }
+    if (lane == 0) red_s[warp] = S;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) red_o[warp][lane * PER + e] = acc[e];
+    __syncthreads();
+
+    // 3. the row
+    if (warp == 0) {
+        float St = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) St += red_s[w];
+        const float inv = St > 0.f ? 1.f / St : 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < W; ++w) a += red_o[w][lane * PER + e];
+            p.o[row * D + lane * PER + e] = __float2bfloat16_rn(a * inv);
+        }
+        if (lane == 0 && p.lse) p.lse[row] = St > 0.f ? M + lg2_approx(St) * kLn2 : -CUDART_INF_F;
+    }
+}
+
 template <int D>
 cudaError_t launch_merge(const DecodeParams& p, int batch, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(batch),
-                       static_cast<unsigned>((p.g.hq + kMergeHeadsPerCta - 1) / kMergeHeadsPerCta), 1);
+    // few (sequence, head) rows: a CTA per row; else a warp per row
+    const bool split = static_cast<long long>(batch) * p.g.hq <= 4ll * p.attend_grid;
+    cfg.gridDim = split ? dim3(static_cast<unsigned>(batch), static_cast<unsigned>(p.g.hq), 1)
+                        : dim3(static_cast<unsigned>(batch),
+                               static_cast<unsigned>((p.g.hq + kMergeHeadsPerCta - 1) / kMergeHeadsPerCta), 1);
     cfg.blockDim = dim3(kMergeThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -541,7 +640,8 @@ cudaError_t launch_merge(const DecodeParams& p, int batch, cudaStream_t stream) 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
+    return split ? cudaLaunchKernelEx(&cfg, decode_merge_split_kernel<D>, p)
+                 : cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
 }
 
 struct LaunchShape {
