@@ -13,7 +13,7 @@
 // the result is the pages' result exactly.
 //
 // One CTA of 1024 threads per call, one warp per (sequence, layer) item, its
-// lanes over consecutive logical blocks: the items' pages are counted, an
+// lanes over consecutive logical blocks (8 x 32 entries loaded at a time): the items' pages are counted, an
 // exclusive scan over the warps gives each item its place on the stack, and
 // the item's warp moves its pages in order (ballot and population count).
 // An allocation that gives old_lens (a decode step: a block or two per item)
@@ -65,15 +65,27 @@ __device__ __forceinline__ long long warps_exclusive_scan(long long v, long long
     return before;
 }
 
-// One warp walks the logical blocks [lo, hi) of a table row in order, 32 at a
-// time; `take` says whether an entry moves.  Returns the number that do.
+// A warp walks a table row kUnroll x 32 entries at a time: all the loads of a
+// stretch are issued before any of them is used, so a long row costs a few
+// memory latencies rather than one per 32 entries.
+constexpr int kUnroll = 8;
+
+// One warp walks the logical blocks [lo, hi) of a table row in order; `take`
+// says whether an entry moves.  Returns the number that do.
 template <typename Take>
 __device__ __forceinline__ int warp_count(const int32_t* row, int lo, int hi, Take take) {
     const int lane = threadIdx.x & 31;
     int n = 0;
-    for (int s0 = lo; s0 < hi; s0 += 32) {
-        const int lb = s0 + lane;
-        n += __popc(__ballot_sync(0xffffffffu, lb < hi && take(row[lb])));
+    for (int s0 = lo; s0 < hi; s0 += 32 * kUnroll) {
+        int32_t v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int lb = s0 + 32 * u + lane;
+            v[u] = lb < hi ? row[lb] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            n += __popc(__ballot_sync(0xffffffffu, s0 + 32 * u + lane < hi && take(v[u])));
     }
     return n;
 }
@@ -148,12 +160,21 @@ __global__ void __launch_bounds__(kThreads) alloc_pages_kernel(KGeom g, int32_t*
         long long total;
         long long r = base + warps_exclusive_scan(cnt, &total);
         if (it.row) {
-            for (int s0 = it.lo; s0 < it.hi; s0 += 32) {
-                const int lb = s0 + lane;
-                const bool take = lb < it.hi && it.row[lb] == -1;
-                const uint32_t m = __ballot_sync(0xffffffffu, take);
-                if (take) it.row[lb] = free_pages[top - 1 - (r + __popc(m & ((1u << lane) - 1u)))];
-                r += __popc(m);
+            for (int s0 = it.lo; s0 < it.hi; s0 += 32 * kUnroll) {
+                int32_t v[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int lb = s0 + 32 * u + lane;
+                    v[u] = lb < it.hi ? it.row[lb] : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int lb = s0 + 32 * u + lane;
+                    const bool take = lb < it.hi && v[u] == -1;
+                    const uint32_t m = __ballot_sync(0xffffffffu, take);
+                    if (take) it.row[lb] = free_pages[top - 1 - (r + __popc(m & ((1u << lane) - 1u)))];
+                    r += __popc(m);
+                }
             }
         }
         base += total;
@@ -296,16 +317,24 @@ __global__ void __launch_bounds__(kThreads) release_slots_kernel(KGeom g, int32_
         long long total;
         long long r = base + warps_exclusive_scan(cnt, &total);
         if (row) {
-            for (int s0 = 0; s0 < g.maxb; s0 += 32) {
-                const int lb = s0 + lane;
-                const int32_t e = lb < g.maxb ? row[lb] : -1;
-                const bool give = e != -1;
-                const uint32_t m = __ballot_sync(0xffffffffu, give);
-                if (give) {
-                    free_pages[top + r + __popc(m & ((1u << lane) - 1u))] = e;
-                    row[lb] = -1;
+            for (int s0 = 0; s0 < g.maxb; s0 += 32 * kUnroll) {
+                int32_t v[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int lb = s0 + 32 * u + lane;
+                    v[u] = lb < g.maxb ? row[lb] : -1;
                 }
-                r += __popc(m);
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int lb = s0 + 32 * u + lane;
+                    const bool give = v[u] != -1;
+                    const uint32_t m = __ballot_sync(0xffffffffu, give);
+                    if (give) {
+                        free_pages[top + r + __popc(m & ((1u << lane) - 1u))] = v[u];
+                        row[lb] = -1;
+                    }
+                    r += __popc(m);
+                }
             }
         }
         base += total;
