@@ -671,28 +671,11 @@ bool decode_shape(const KGeom& g, LaunchShape* s) {
     return true;
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
 // The pool as a 3D tensor {64 dims, pages*32 rows of 2*KV_DIM bytes,
 // KV_DIM/64 column blocks of 128 bytes}; one box {64, 16, KV_DIM/64} is a
 // half page (16 token rows, all heads).
 bool encode_pool_map(CUtensorMap* map, const KGeom& g, const void* pool) {
-    EncodeTiledFn fn = encode_fn();
+    EncodeTiledFn fn = tensor_map_encoder();
     if (!fn) return false;
     const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(g.nblocks) * 32, static_cast<cuuint64_t>(g.kv_dim / 64)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.kv_dim) * 2, 128};

@@ -518,6 +518,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLog2e = 1.442695040888963407f;
 
+// ------------------------------------------------------------ tensor maps
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (the library
+// links no driver stub); null if the driver does not provide it.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+
 // ------------------------------------------------------------ host entry
 
 // Kernel launchers (one per translation unit); return a cudaError_t.
