@@ -210,3 +210,21 @@ def test_bench_size_sampled_rows():
     assert_grad_close(dq[q_rows, q_heads], rq, "dq sampled, 4 x 8192")
     assert_grad_close(dk[k_rows, k_heads], rk, "dk sampled, 4 x 8192")
     assert_grad_close(dv[k_rows, k_heads], rv, "dv sampled, 4 x 8192")
+
+
+def test_bad_table_entry_reports_and_context_recovers():
+    """A table entry of the attended layer set to -1 where a page is needed:
+    the backward (both head dims) reports PA_ERR_BAD_BLOCK without faulting,
+    and the next call on the good table is correct."""
+    for hq, hkv, d in ((8, 2, 64), (8, 2, 128)):
+        case, dout = backward_case(hq, hkv, d, [90, 30], seed=41 + d, layers=(0,))
+        pool, bt, werr = H.gpu_setup(case)
+        assert werr == 0
+        bad = case.block_table.copy()
+        bad[case.slots[0], 0, 3] = -1
+        dq, dk, dv, err = gpu_forward_backward(case, pool, H.to_dev(bad), dout)
+        assert err == H.pa.PA_ERR_BAD_BLOCK
+        dq, dk, dv, err = gpu_forward_backward(case, pool, bt, dout)
+        assert err == 0
+        rq, rk, rv = oracle_backward(case, dout)
+        assert_grad_close(dk, rk, "dk after a bad table entry, d%d" % d)
