@@ -313,14 +313,14 @@ class ChunkedStep:
 
 
 class BackwardStep:
-    """Gradients of the long-prompt prefill (4 x 8192 tokens, 32 q / 8 kv heads,
-    d 64): the forward runs once to give o and lse; a step is one
-    pa_prefill_backward (D = do . o, then the column-block kernel)."""
+    """Gradients of the long-prompt prefill (4 x 8192 tokens; 32 q / 8 kv heads
+    at d 64, 16 / 4 at d 128): the forward runs once to give o and lse; a step
+    is one pa_prefill_backward (D = do . o, then the column-block kernel)."""
 
-    def __init__(self, torch, pa, W, seed=1007, batch=4, seqlen=8192):
+    def __init__(self, torch, pa, W, seed=1007, batch=4, seqlen=8192, heads=(32, 8, 64)):
         self.torch, self.pa = torch, pa
         pages = (seqlen + 15) // 16
-        geom = W.Geometry(32, 8, 64, 1, batch, pages, batch * pages + 64)
+        geom = W.Geometry(heads[0], heads[1], heads[2], 1, batch, pages, batch * pages + 64)
         case = W.make_prefill_case("bwd", geom, [seqlen] * batch, seed)
         self.case, self.geom = case, geom
         self.g = pa.geom(*self.geom.as_tuple())
@@ -827,26 +827,32 @@ def main():
     backward = None
     if args.only in ("all", "backward"):
         # ----------------------------------------- FA2 backward over the pages (f4)
-        bstep = BackwardStep(torch, pa, W, batch=args.batch, seqlen=args.seqlen)
-        bsteps = max(10, args.steps // 4)
-        b_s, bk_s = timed(torch, lambda ev: bstep.run(ev=ev), bsteps, args.warmup, flush, dist)
-        torch.cuda.synchronize()
-        if int(bstep.err.item()) != 0:
-            raise SystemExit("device error in backward steps: %s" % pa.pa_status_string(int(bstep.err.item())))
-        b_avg = float(np.mean(bk_s))
-        b_rate, b_total, _ = job_rate(torch, dist, bstep.flops * bsteps, float(np.sum(b_s)))
         bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        b_ach = bstep.flops / b_avg / 1e12
-        backward = {"metric": "prefill backward TFLOP/s (4 x 8192 tokens, 32 q / 8 kv heads, d 64; "
-                              "exact causal count x 2.5)",
-                    "value": b_rate / 1e12, "unit": "TFLOP/s", "ms_per_step": b_total / bsteps * 1e3,
-                    "steps": bsteps,
-                    "roofline": {"bound": "tensor", "achieved": b_ach, "peak": bf16_peak, "unit": "TFLOP/s",
-                                 "frac": b_ach / bf16_peak, "traffic": profiled_traffic("backward_d64"),
-                                 "kernel": "bwd_prep_kernel<64> + bwd_main_kernel<64>",
-                                 "peak_source": "%s bf16_tflops (burst)" % peak_src,
-                                 "algorithmic_flops_per_launch": bstep.flops, "avg_launch_ms": b_avg * 1e3}}
-        del bstep
+        for heads in ((32, 8, 64), (16, 4, 128)):
+            hq, hkv, hd = heads
+            bstep = BackwardStep(torch, pa, W, batch=args.batch, seqlen=args.seqlen, heads=heads)
+            bsteps = max(10, args.steps // 4)
+            b_s, bk_s = timed(torch, lambda ev: bstep.run(ev=ev), bsteps, args.warmup, flush, dist)
+            torch.cuda.synchronize()
+            if int(bstep.err.item()) != 0:
+                raise SystemExit("device error in backward steps: %s" % pa.pa_status_string(int(bstep.err.item())))
+            b_avg = float(np.mean(bk_s))
+            b_rate, b_total, _ = job_rate(torch, dist, bstep.flops * bsteps, float(np.sum(b_s)))
+            b_ach = bstep.flops / b_avg / 1e12
+            leg = {"metric": "prefill backward TFLOP/s (%d x %d tokens, %d q / %d kv heads, d %d; "
+                             "exact causal count x 2.5)" % (args.batch, args.seqlen, hq, hkv, hd),
+                   "value": b_rate / 1e12, "unit": "TFLOP/s", "ms_per_step": b_total / bsteps * 1e3,
+                   "steps": bsteps,
+                   "roofline": {"bound": "tensor", "achieved": b_ach, "peak": bf16_peak, "unit": "TFLOP/s",
+                                "frac": b_ach / bf16_peak, "traffic": profiled_traffic("backward_d%d" % hd),
+                                "kernel": "bwd_prep_kernel<%d> + bwd_tc_kernel<%d>" % (hd, hd),
+                                "peak_source": "%s bf16_tflops (burst)" % peak_src,
+                                "algorithmic_flops_per_launch": bstep.flops, "avg_launch_ms": b_avg * 1e3}}
+            if backward is None:
+                backward = leg
+            else:
+                backward["d%d" % hd] = leg
+            del bstep
 
     pages = None
     if args.only in ("all", "pages"):

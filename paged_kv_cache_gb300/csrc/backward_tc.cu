@@ -1,8 +1,8 @@
 // backward_tc.cu -- the column-block kernel of the prefill backward on the
 // sm_103a tensor cores (tcgen05.mma, accumulators in tensor memory, operands
-// staged by TMA), head dim 64.
+// staged by TMA), head dims 64 and 128.
 //
-// Same arithmetic as bwd_main_kernel (FlashAttention-2 explainer, "전체
+// The arithmetic (FlashAttention-2 explainer, "전체
 // 흐름": P rebuilt from L; "2. 시퀀스 길이 방향으로도 병렬화" item 4: one
 // thread block per key block, dQ added atomically; "4. MQA · GQA 지원": dK, dV
 // summed over the group):
@@ -15,16 +15,19 @@
 //  * warp 0 (producer): K, V once (8 pages each, rows through the block table,
 //    pages past the end read at an out-of-range row = zeros); then per query
 //    block the Q and dO tiles by TMA and -L log2 e, -D (from the prep kernel's
-//    workspace) by cp.async, all completing on one mbarrier, into 5 stages.
+//    workspace) by cp.async, all completing on one mbarrier, into 5 stages
+//    (2 at d 128).
 //  * warp 1 (MMA issue, elected lane): S^T and dP^T (M 128 keys, N 64 rows,
-//    K 64 dims, both operands K-major) into one of two TMEM buffers; once the
+//    K d dims, both operands K-major) into one of two TMEM buffers; once the
 //    elementwise warps hand back P^T and dS^T (bf16, in TMEM over the first
 //    8 columns of each 16-column quarter), dV += P^T dO and dK += dS^T Q (A from
-//    TMEM, B = the same Q / dO tiles read MN-major); after every second query
-//    block, dQ = dS K for the pair (M 128 rows, N 64 dims, K 128 keys; dS from
-//    shared memory MN-major, K read MN-major).  S^T of the next block is
-//    issued before dV / dK of this one, so the tensor core works while the
-//    elementwise warps run.
+//    TMEM, B = the same Q / dO tiles read MN-major, N = d); after every second
+//    query block, dQ = dS K for the pair (M 128 rows, N d, K 128 keys; dS from
+//    shared memory MN-major, K read MN-major).  At d 64 S^T of the next block
+//    is issued before dV / dK of this one, so the tensor core works while the
+//    elementwise warps run; at d 128, whose dV, dK and dQ take 384 columns,
+//    there is one S^T / dP^T buffer and one dQ buffer, and the next S^T
+//    follows dV / dK.
 //  * warps 2..17 (elementwise): thread = key (TMEM lane), four warps per lane
 //    quarter, 16 query rows each.  Mask j <= i < n, P^T, dS^T; P^T and dS^T to
 //    TMEM, dS^T also to shared memory (key rows of 64 query rows, 128-byte
@@ -35,7 +38,8 @@
 //    times scale, into a swizzled fp32 staging tile, then one TMA reduce-add
 //    per 32 columns into dq (rows past the sequence add zeros; rows past the
 //    tensor are clipped).  At the end they write dK * scale and dV.
-// TMEM: S^T 2 x 64 columns, dP^T 2 x 64, dV 64, dK 64, dQ 2 x 64 = 512.
+// TMEM, d 64: S^T 2 x 64 columns, dP^T 2 x 64, dQ 2 x 64, dV 64, dK 64;
+// d 128: S^T 64, dP^T 64, dQ 128, dV 128, dK 128 (512 either way).
 // Every wait is bounded; on a timeout the CTA records PA_ERR_TIMEOUT, drains
 // its copies and products in flight and frees its tensor memory.
 #include "pa_internal.cuh"
@@ -45,36 +49,45 @@ namespace {
 
 constexpr int kKeys = 128;        // keys per CTA: TMEM lanes of the key-side products
 constexpr int kRowsIt = 64;       // query rows per iteration
-constexpr int kNst = 5;           // Q / dO / L / D stages
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kEwWarp0 = 2;       // 16 elementwise warps
 constexpr int kEwWarps = 16;
 constexpr int kEpiWarp0 = kEwWarp0 + kEwWarps;  // 4 dQ epilogue warps
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
-
-constexpr int kTileKV = kKeys * 128;    // 128 keys x 64 dims bf16, 128-byte rows
-constexpr int kTileQ = kRowsIt * 128;   // 64 rows x 64 dims bf16
 constexpr int kDsHalf = kKeys * 128;    // dS^T of 64 query rows for 128 keys
 constexpr int kDsBuf = 2 * kDsHalf;     // one pair of query blocks
 constexpr int kDqBox = 128 * 128;       // 128 rows x 32 fp32
-constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + kTileKV;
-constexpr int OFF_Q = OFF_V + kTileKV;           // [kNst]
-constexpr int OFF_DO = OFF_Q + kNst * kTileQ;    // [kNst]
-constexpr int OFF_DS = OFF_DO + kNst * kTileQ;   // [2]
-constexpr int OFF_DQ = OFF_DS + 2 * kDsBuf;      // 2 boxes
-constexpr int OFF_LD = OFF_DQ + 2 * kDqBox;      // [kNst] x (64 -L log2e, 64 -D) fp32
-constexpr int OFF_BAR = OFF_LD + kNst * 2 * kRowsIt * 4;
-constexpr int SMEM = 1024 + OFF_BAR + 512;
-static_assert(SMEM <= 227 * 1024, "shared memory");
-
-constexpr uint32_t COL_S = 0;     // [2] x 64
-constexpr uint32_t COL_DP = 128;  // [2] x 64
-constexpr uint32_t COL_DV = 256;
-constexpr uint32_t COL_DK = 320;
-constexpr uint32_t COL_DQ = 384;  // [2] x 64
 constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct TcCfg {
+    static constexpr int KCH = D / 64;              // 64-dim chunks of a row (128-byte swizzle atoms)
+    static constexpr int NBUF = D == 64 ? 2 : 1;    // S^T / dP^T buffers in TMEM
+    static constexpr int NDQ = D == 64 ? 2 : 1;     // dQ buffers in TMEM
+    static constexpr int NST = D == 64 ? 5 : 2;     // Q / dO / L / D stages
+    static constexpr int DQ_BOXES = D == 64 ? 2 : 1;  // 32-column fp32 staging boxes
+    static constexpr int KV_CHUNK = kKeys * 128;    // one chunk of the K (or V) tile
+    static constexpr int TILE_KV = KCH * KV_CHUNK;
+    static constexpr int Q_CHUNK = kRowsIt * 128;   // one chunk of a Q (or dO) tile
+    static constexpr int TILE_Q = KCH * Q_CHUNK;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = TILE_KV;
+    static constexpr int OFF_Q = 2 * TILE_KV;                 // [NST]
+    static constexpr int OFF_DO = OFF_Q + NST * TILE_Q;       // [NST]
+    static constexpr int OFF_DS = OFF_DO + NST * TILE_Q;      // [2] pairs
+    static constexpr int OFF_DQ = OFF_DS + 2 * kDsBuf;        // DQ_BOXES boxes
+    static constexpr int OFF_LD = OFF_DQ + DQ_BOXES * kDqBox; // [NST] x (64 -L log2e, 64 -D) fp32
+    static constexpr int OFF_BAR = OFF_LD + NST * 2 * kRowsIt * 4;
+    static constexpr int SMEM = 1024 + OFF_BAR + 512;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static constexpr uint32_t COL_S = 0;                 // [NBUF] x 64
+    static constexpr uint32_t COL_DP = 64 * NBUF;        // [NBUF] x 64
+    static constexpr uint32_t COL_DQ = 128 * NBUF;       // [NDQ] x D
+    static constexpr uint32_t COL_DV = COL_DQ + NDQ * D;
+    static constexpr uint32_t COL_DK = COL_DV + D;
+    static_assert(COL_DK + D == kTmemCols, "tensor memory");
+};
 
 struct BwdTcParams {
     KGeom g;
@@ -147,10 +160,18 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int r0, int r1, int t, 
     for (int c = t; c < (r1 - r0) * 8; c += nthr) st_shared_v4(tile + (r0 + c / 8) * 128 + (c % 8) * 16, 0, 0, 0, 0);
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap domap,
               const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap dqmap,
               const BwdTcParams p) {
+    using C = TcCfg<D>;
+    constexpr int kNst = C::NST;
+    constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_Q = C::OFF_Q, OFF_DO = C::OFF_DO, OFF_DS = C::OFF_DS,
+                  OFF_DQ = C::OFF_DQ, OFF_LD = C::OFF_LD, OFF_BAR = C::OFF_BAR;
+    constexpr int kTileQ = C::TILE_Q;
+    constexpr uint32_t COL_S = C::COL_S, COL_DP = C::COL_DP, COL_DQ = C::COL_DQ, COL_DV = C::COL_DV,
+                       COL_DK = C::COL_DK;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -235,15 +256,18 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
             prefetch_tensor_map(&qmap);
             prefetch_tensor_map(&domap);
             prefetch_tensor_map(&kvmap);
-            mbar_arrive_expect_tx(kv_full, 2 * kTileKV);
+            mbar_arrive_expect_tx(kv_full, 2 * C::TILE_KV);
         }
 #pragma unroll
         for (int k = 0; k < kKeys / kBlockTokens; ++k) {
             const int rr = __shfl_sync(0xffffffffu, row, k);
             if (lane == 0) {
                 const int y = rr < 0 ? oob_row : rr;
-                tma_load_2d(smem + OFF_K + k * 2048, &kvmap, hk * 64, y, kv_full);
-                tma_load_2d(smem + OFF_V + k * 2048, &kvmap, hk * 64, y + 16, kv_full);
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c) {
+                    tma_load_2d(smem + OFF_K + c * C::KV_CHUNK + k * 2048, &kvmap, hk * D + 64 * c, y, kv_full);
+                    tma_load_2d(smem + OFF_V + c * C::KV_CHUNK + k * 2048, &kvmap, hk * D + 64 * c, y + 16, kv_full);
+                }
             }
         }
         int issued = 0;
@@ -268,8 +292,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
             cp_async_arrive_noinc(&q_full[s]);
             if (lane == 0) {
                 mbar_arrive_expect_tx(&q_full[s], 2 * kTileQ);
-                tma_load_2d(smem + OFF_Q + s * kTileQ, &qmap, h * 64, cu0 + ib * kRowsIt, &q_full[s]);
-                tma_load_2d(smem + OFF_DO + s * kTileQ, &domap, h * 64, cu0 + ib * kRowsIt, &q_full[s]);
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c) {
+                    tma_load_2d(smem + OFF_Q + s * kTileQ + c * C::Q_CHUNK, &qmap, h * D + 64 * c, cu0 + ib * kRowsIt,
+                                &q_full[s]);
+                    tma_load_2d(smem + OFF_DO + s * kTileQ + c * C::Q_CHUNK, &domap, h * D + 64 * c,
+                                cu0 + ib * kRowsIt, &q_full[s]);
+                }
             }
             ++issued;
         }
@@ -281,23 +310,27 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issue
         constexpr uint32_t idesc_t = umma_idesc_bf16(128, 64, false);        // S^T, dP^T
-        constexpr uint32_t idesc_kv = umma_idesc_bf16(128, 64, true);        // dV, dK (A from TMEM)
-        constexpr uint32_t idesc_q = umma_idesc_bf16(128, 64, true, true);   // dQ
+        constexpr uint32_t idesc_kv = umma_idesc_bf16(128, D, true);         // dV, dK (A from TMEM)
+        constexpr uint32_t idesc_q = umma_idesc_bf16(128, D, true, true);    // dQ
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err));
         };
         const uint32_t sK = sb + OFF_K, sV = sb + OFF_V;
         auto issue_sdp = [&](int it) {
-            const int s = it % kNst, x = it & 1;
+            const int s = it % kNst, x = it % C::NBUF;
             const uint32_t sQ = sb + OFF_Q + s * kTileQ, sO = sb + OFF_DO + s * kTileQ;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                umma_ss_elect(tmem + COL_S + 64 * x, umma_sdesc_sw128(sK + ks * 32, 16, 1024),
-                              umma_sdesc_sw128(sQ + ks * 32, 16, 1024), idesc_t, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks)
+                umma_ss_elect(tmem + COL_S + 64 * x,
+                              umma_sdesc_sw128(sK + (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32, 16, 1024),
+                              umma_sdesc_sw128(sQ + (ks >> 2) * C::Q_CHUNK + (ks & 3) * 32, 16, 1024), idesc_t,
+                              ks > 0 ? 1u : 0u);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                umma_ss_elect(tmem + COL_DP + 64 * x, umma_sdesc_sw128(sV + ks * 32, 16, 1024),
-                              umma_sdesc_sw128(sO + ks * 32, 16, 1024), idesc_t, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks)
+                umma_ss_elect(tmem + COL_DP + 64 * x,
+                              umma_sdesc_sw128(sV + (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32, 16, 1024),
+                              umma_sdesc_sw128(sO + (ks >> 2) * C::Q_CHUNK + (ks & 3) * 32, 16, 1024), idesc_t,
+                              ks > 0 ? 1u : 0u);
             umma_commit_elect(&s_full[x]);
         };
         bool ok = wait_all(kv_full, 0) && wait_all(&q_full[0], 0);
@@ -305,17 +338,22 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
             tc_fence_after_sync();
             issue_sdp(0);
         }
+        // the next block's S^T / dP^T: into the other buffer before this block's dV / dK
+        // (two buffers), or after them, over the P^T / dS^T they read (one buffer)
+        auto next_sdp = [&](int it) {
+            if (it + 1 >= n_it) return true;
+            if (!wait_all(&q_full[(it + 1) % kNst], ((it + 1) / kNst) & 1)) return false;
+            tc_fence_after_sync();
+            issue_sdp(it + 1);
+            return true;
+        };
         for (int it = 0; ok && it < n_it; ++it) {
-            const int s = it % kNst, x = it & 1;
-            if (it + 1 < n_it) {
-                if (!wait_all(&q_full[(it + 1) % kNst], ((it + 1) / kNst) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                issue_sdp(it + 1);
+            const int s = it % kNst, x = it % C::NBUF;
+            if (C::NBUF == 2 && !next_sdp(it)) {
+                ok = false;
+                break;
             }
-            if (!wait_all(&p_ready[x], (it >> 1) & 1)) {
+            if (!wait_all(&p_ready[x], (it / C::NBUF) & 1)) {
                 ok = false;
                 break;
             }
@@ -324,27 +362,33 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 umma_ts_elect(tmem + COL_DV, tmem + COL_S + 64 * x + packed_col(ks),
-                              umma_sdesc_sw128(sO + ks * 2048, 1024, 1024), idesc_kv, (it > 0 || ks > 0) ? 1u : 0u);
+                              umma_sdesc_sw128(sO + ks * 2048, C::Q_CHUNK, 1024), idesc_kv,
+                              (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 umma_ts_elect(tmem + COL_DK, tmem + COL_DP + 64 * x + packed_col(ks),
-                              umma_sdesc_sw128(sQ + ks * 2048, 1024, 1024), idesc_kv, (it > 0 || ks > 0) ? 1u : 0u);
+                              umma_sdesc_sw128(sQ + ks * 2048, C::Q_CHUNK, 1024), idesc_kv,
+                              (it > 0 || ks > 0) ? 1u : 0u);
             umma_commit_elect(&q_empty[s]);
             if (it + 1 == n_it) umma_commit_elect(kv_done);
+            if (C::NBUF == 1 && !next_sdp(it)) {
+                ok = false;
+                break;
+            }
             if (it & 1) {
-                const int pp = it >> 1, y = pp & 1;
-                if (pp >= 2 && !wait_all(&dq_empty[y], ((pp >> 1) - 1) & 1)) {
+                const int pp = it >> 1, y = pp % C::NDQ, dsb = pp & 1;
+                if (pp >= C::NDQ && !wait_all(&dq_empty[y], ((pp / C::NDQ) - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t sD = sb + OFF_DS + y * kDsBuf;
+                const uint32_t sD = sb + OFF_DS + dsb * kDsBuf;
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    umma_ss_elect(tmem + COL_DQ + 64 * y, umma_sdesc_sw128(sD + ks * 2048, kDsHalf, 1024),
-                                  umma_sdesc_sw128(sK + ks * 2048, 1024, 1024), idesc_q, ks > 0 ? 1u : 0u);
+                    umma_ss_elect(tmem + COL_DQ + D * y, umma_sdesc_sw128(sD + ks * 2048, kDsHalf, 1024),
+                                  umma_sdesc_sw128(sK + ks * 2048, C::KV_CHUNK, 1024), idesc_q, ks > 0 ? 1u : 0u);
                 umma_commit_elect(&dq_full[y]);
-                umma_commit_elect(&ds_empty[y]);
+                umma_commit_elect(&ds_empty[dsb]);
             }
         }
         umma_commit_elect(mma_done);
@@ -362,13 +406,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
         const float sc = p.scale_log2;
         bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort_flag, p.err));
         if (ok && (jb + 1) * kKeys > n) {  // K rows past the sequence: zero (dQ reads them)
-            zero_rows(sb + OFF_K, n - jb * kKeys, kKeys, et, kEt);
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c) zero_rows(sb + OFF_K + c * C::KV_CHUNK, n - jb * kKeys, kKeys, et, kEt);
             fence_proxy_async_smem();
         }
         for (int it = 0; ok && it < n_it; ++it) {
-            const int s = it % kNst, x = it & 1, pp = it >> 1;
+            const int s = it % kNst, x = it % C::NBUF, pp = it >> 1;
             const int ib = 2 * (jb + pp % nph) + (it & 1);
-            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[x], (it >> 1) & 1, abort_flag, p.err)) ||
+            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[x], (it / C::NBUF) & 1, abort_flag, p.err)) ||
                 !__all_sync(0xffffffffu, mbar_wait(&q_full[s], (it / kNst) & 1, abort_flag, p.err))) {
                 ok = false;
                 break;
@@ -379,8 +424,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
             tmem_ld_x16_nowait(lane_addr + COL_DP + 64 * x + 16 * grp, dv);
             if ((ib + 1) * kRowsIt > n) {  // Q / dO rows past the sequence: zero (dK, dV read them)
                 const int r0 = max(0, n - ib * kRowsIt);
-                zero_rows(sb + OFF_Q + s * kTileQ, r0, kRowsIt, et, kEt);
-                zero_rows(sb + OFF_DO + s * kTileQ, r0, kRowsIt, et, kEt);
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c) {
+                    zero_rows(sb + OFF_Q + s * kTileQ + c * C::Q_CHUNK, r0, kRowsIt, et, kEt);
+                    zero_rows(sb + OFF_DO + s * kTileQ + c * C::Q_CHUNK, r0, kRowsIt, et, kEt);
+                }
             }
             const float4* nl4 = reinterpret_cast<const float4*>(sLD + s * 2 * kRowsIt + 16 * grp);
             const float4* nd4 = reinterpret_cast<const float4*>(sLD + s * 2 * kRowsIt + kRowsIt + 16 * grp);
@@ -440,35 +488,42 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
         const bool leader = warp == kEpiWarp0 && lane == 0;
         bool ok = true;
         for (int pp = 0; ok && pp < n_pairs; ++pp) {
-            const int y = pp & 1;
-            if (!epi_all(mbar_wait(&dq_full[y], (pp >> 1) & 1, abort_flag, p.err))) {
+            const int y = pp % C::NDQ;
+            if (!epi_all(mbar_wait(&dq_full[y], (pp / C::NDQ) & 1, abort_flag, p.err))) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            if (leader) bulk_wait_read0();  // the previous pair's reduce has read the staging tile
-            epi_barrier();
+            const int h = hk * group + pp / nph;
+            const int y0 = cu0 + (jb + pp % nph) * 2 * kRowsIt;
             const uint32_t row_addr = sb + OFF_DQ + r * 128;
+            // D / 32 column groups of 32, staged DQ_BOXES at a time and each added by one reduce
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                uint32_t v[32];
-                tmem_ld_x32(lane_addr + COL_DQ + 64 * y + 32 * part, v);
+            for (int part0 = 0; part0 < D / 32; part0 += C::DQ_BOXES) {
+                if (leader) bulk_wait_read0();  // the previous reduce has read the staging tile
+                epi_barrier();
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    st_shared_v4f(row_addr + part * kDqBox + ((ch ^ (r & 7)) * 16), p.scale * __uint_as_float(v[4 * ch]),
-                                  p.scale * __uint_as_float(v[4 * ch + 1]), p.scale * __uint_as_float(v[4 * ch + 2]),
-                                  p.scale * __uint_as_float(v[4 * ch + 3]));
-            }
-            tc_fence_before_sync();
-            mbar_arrive(&dq_empty[y]);
-            fence_proxy_async_smem();
-            epi_barrier();
-            if (leader) {
-                const int h = hk * group + pp / nph;
-                const int y0 = cu0 + (jb + pp % nph) * 2 * kRowsIt;
-                tma_reduce_add_2d(&dqmap, h * 64, y0, sb + OFF_DQ);
-                tma_reduce_add_2d(&dqmap, h * 64 + 32, y0, sb + OFF_DQ + kDqBox);
-                bulk_commit();
+                for (int bx = 0; bx < C::DQ_BOXES; ++bx) {
+                    uint32_t v[32];
+                    tmem_ld_x32(lane_addr + COL_DQ + D * y + 32 * (part0 + bx), v);
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_v4f(row_addr + bx * kDqBox + ((ch ^ (r & 7)) * 16), p.scale * __uint_as_float(v[4 * ch]),
+                                      p.scale * __uint_as_float(v[4 * ch + 1]), p.scale * __uint_as_float(v[4 * ch + 2]),
+                                      p.scale * __uint_as_float(v[4 * ch + 3]));
+                }
+                if (part0 + C::DQ_BOXES >= D / 32) {  // dQ of this pair is out of tensor memory
+                    tc_fence_before_sync();
+                    mbar_arrive(&dq_empty[y]);
+                }
+                fence_proxy_async_smem();
+                epi_barrier();
+                if (leader) {
+#pragma unroll
+                    for (int bx = 0; bx < C::DQ_BOXES; ++bx)
+                        tma_reduce_add_2d(&dqmap, h * D + 32 * (part0 + bx), y0, sb + OFF_DQ + bx * kDqBox);
+                    bulk_commit();
+                }
             }
         }
         if (leader) bulk_wait0();
@@ -477,13 +532,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
             const int j = jb * kKeys + r;
             uint32_t a[32], c[32];
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
+            for (int part = 0; part < D / 32; ++part) {
                 tmem_ld_x32_nowait(lane_addr + COL_DK + 32 * part, a);
                 tmem_ld_x32_nowait(lane_addr + COL_DV + 32 * part, c);
                 tmem_wait_ld_dep(a);
                 tmem_wait_ld_dep(c);
                 if (j < n) {
-                    const long long off = (static_cast<long long>(cu0 + j) * g.hkv + hk) * 64 + 32 * part;
+                    const long long off = (static_cast<long long>(cu0 + j) * g.hkv + hk) * D + 32 * part;
                     float4* dkr = reinterpret_cast<float4*>(p.dk + off);
                     float4* dvr = reinterpret_cast<float4*>(p.dv + off);
 #pragma unroll
@@ -522,6 +577,17 @@ bool encode(CUtensorMap* map, CUtensorMapDataType type, const void* base, unsign
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int D>
+cudaError_t launch_tc(const CUtensorMap& qmap, const CUtensorMap& domap, const CUtensorMap& kvmap,
+                      const CUtensorMap& dqmap, const BwdTcParams& p, int batch, int max_seqlen, cudaStream_t stream) {
+    using C = TcCfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(batch * p.g.hkv), static_cast<unsigned>((max_seqlen + kKeys - 1) / kKeys));
+    bwd_tc_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(qmap, domap, kvmap, dqmap, p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_backward_tc(const KGeom& g, const void* q, const void* pool, const int32_t* bt, int layer,
@@ -529,7 +595,7 @@ cudaError_t launch_backward_tc(const KGeom& g, const void* q, const void* pool, 
                                float scale, const void* dout, const float* ws, float* dq, float* dk, float* dv,
                                int32_t* err, cudaStream_t stream) {
     CUtensorMap qmap, domap, kvmap, dqmap;
-    const unsigned long long qcols = static_cast<unsigned long long>(g.hq) * 64;
+    const unsigned long long qcols = static_cast<unsigned long long>(g.hq) * g.d;
     if (!encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, qcols, total_tokens, qcols * 2, 64, kRowsIt) ||
         !encode(&domap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dout, qcols, total_tokens, qcols * 2, 64, kRowsIt) ||
         !encode(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool, g.kv_dim, static_cast<unsigned long long>(g.nblocks) * 32,
@@ -551,11 +617,8 @@ cudaError_t launch_backward_tc(const KGeom& g, const void* q, const void* pool, 
     p.dk = dk;
     p.dv = dv;
     p.err = err;
-    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(batch * g.hkv), static_cast<unsigned>((max_seqlen + kKeys - 1) / kKeys));
-    bwd_tc_kernel<<<grid, kThreads, SMEM, stream>>>(qmap, domap, kvmap, dqmap, p);
-    return cudaGetLastError();
+    if (g.d == 64) return launch_tc<64>(qmap, domap, kvmap, dqmap, p, batch, max_seqlen, stream);
+    return launch_tc<128>(qmap, domap, kvmap, dqmap, p, batch, max_seqlen, stream);
 }
 
 }  // namespace pa
