@@ -357,15 +357,22 @@ class BackwardStep:
 
 
 class DecodeStep:
-    """The large mixed decode batch: 256 sequences, log-normal lengths, 4 GiB
-    pool; c-1 tokens preloaded, each step writes the token at c-1 and decodes c."""
+    """A decode batch: c-1 tokens preloaded, each step writes the token at c-1
+    and decodes c.  Default: the large mixed batch (256 sequences, log-normal
+    lengths, 4 GiB pool); small=True: 64 sequences, lengths uniform in
+    [128, 2048], 2 GiB pool."""
 
-    def __init__(self, torch, pa, W, seed=1004):
+    def __init__(self, torch, pa, W, seed=1004, small=False):
         self.torch, self.pa = torch, pa
-        lens = W.c5_lens(seed)
+        if small:
+            seed = 1002
+            lens = W.c3_lens(seed)
+            self.geom = W.Geometry(32, 8, 64, 1, lens.shape[0], 128, 65536)
+        else:
+            lens = W.c5_lens(seed)
+            self.geom = W.Geometry(32, 8, 64, 1, lens.shape[0], 1024, 131072)
         self.lens_np = lens
         B = lens.shape[0]
-        self.geom = W.Geometry(32, 8, 64, 1, B, 1024, 131072)
         rng = np.random.default_rng(seed + 1)
         table = W.empty_table(self.geom)
         free = W.FreeList(self.geom.num_blocks, rng)
@@ -776,6 +783,26 @@ def main():
                                "algorithmic_bytes_per_launch": dstep.kv_bytes,
                                "avg_launch_ms": dec_avg * 1e3}}
         del dstep
+        # the 64-sequence batch, lengths uniform in [128, 2048]: 143 MB of K/V per step
+        sstep = DecodeStep(torch, pa, W, small=True)
+        s_s, sk_s = timed(torch, lambda ev: sstep.run(ev=ev), dsteps, args.warmup, flush, dist)
+        torch.cuda.synchronize()
+        if int(sstep.err.item()) != 0:
+            raise SystemExit("device error in decode steps: %s" % pa.pa_status_string(int(sstep.err.item())))
+        s_avg = float(np.mean(sk_s))
+        s_gbs = sstep.kv_bytes / s_avg / 1e9
+        s_rate, s_total, _ = job_rate(torch, dist, sstep.kv_bytes * dsteps, float(np.sum(s_s)))
+        decode["batch64"] = {"metric": "decode KV-read GB/s (64 seqs, lengths uniform in [128, 2048], "
+                                       "write + decode per step)",
+                             "value": s_rate / 1e9, "unit": "GB/s", "ms_per_step": s_total / dsteps * 1e3,
+                             "kv_bytes_per_step": sstep.kv_bytes, "steps": dsteps,
+                             "roofline": {"bound": "hbm", "achieved": s_gbs, "peak": hbm_peak, "unit": "GB/s",
+                                          "frac": s_gbs / hbm_peak, "traffic": profiled_traffic("decode_c3"),
+                                          "kernel": "decode_attend_kernel<64> + decode_merge_kernel<64>",
+                                          "peak_source": "%s hbm_gbs" % peak_src,
+                                          "algorithmic_bytes_per_launch": sstep.kv_bytes,
+                                          "avg_launch_ms": s_avg * 1e3}}
+        del sstep
 
     chunked = None
     if args.only in ("all", "chunked"):

@@ -28,7 +28,7 @@
 //    128-byte lines (column block major, token minor) with the 128-byte
 //    swizzle, so the 16-byte pieces of 8 consecutive token rows sit in 8
 //    different bank groups.  The sequence's query row rides along at the start
-//    of a unit.  Two CTAs per SM, three stages each, keep enough bytes in
+//    of a unit.  Two CTAs per SM, two stages each, keep enough bytes in
 //    flight for HBM; the page is read front to back in two large requests.
 //  * Compute.  One consumer warp per KV head; the GQA group's query heads are
 //    the rows of a 16-row warp-level MMA (mma.sync m16n8k16, bf16 in, fp32
@@ -53,6 +53,11 @@ constexpr int kMaxGrid = 1024;
 constexpr int kSmemBudget = 112 * 1024;  // per CTA: two CTAs share an SM
 constexpr int kCtasPerSm = 2;
 constexpr int kMaxStages = 8;
+// Stages per CTA: two measured faster than three (256 mixed-length sequences
+// 160 -> 154 us, 64 sequences of 128..2048 tokens 43.3 -> 42.3 us): with 304
+// CTAs, two 32 KiB pages each already keep ~19 MB in flight, and fewer
+// requests queued in the memory system even out the CTAs' service.
+constexpr int kStagesWanted = 2;
 constexpr int kCtlBytes = 1024;  // barriers + control words, then the q slots, then the stages
 
 enum : int { kFirst = 1, kLast = 2, kWhole = 4, kSkip = 8 };
@@ -77,7 +82,6 @@ struct DecodeParams {
     __nv_bfloat16* o;
     float* lse;
     uint8_t* ws;
-    long long ws_meta;    // int2 [batch]: first and last CTA of each sequence
     long long ws_lse;     // float [nslots][hq]: partial L (natural log)
     long long ws_o;       // float [nslots][hq][d]: partial normalised outputs
     int32_t* err;
@@ -92,13 +96,13 @@ struct DecodeParams {
 __host__ __device__ inline long long align_up(long long x, long long a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-    long long meta, lse, o, total;
+    long long lse, o, total;
 };
 
 __host__ __device__ inline WsLayout ws_layout(int batch, long long nslots, int hq, int d) {
     WsLayout w;
-    w.meta = 256;  // [0, 256): header, total page count at offset 0
-    w.lse = align_up(w.meta + 8ll * batch, 256);
+    (void)batch;
+    w.lse = 0;
     w.o = align_up(w.lse + 4ll * nslots * hq, 256);
     w.total = align_up(w.o + 4ll * nslots * hq * d, 256);
     return w;
@@ -186,19 +190,23 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
     }
 
     // ---- this CTA's page range: total pages, then the sequence holding p_begin
+    // (the slots of the first blockDim sequences are loaded with their lengths,
+    // so that the first table row needs no further round trip)
     long long local = 0;
+    int my_slot = -1;
     for (int i = tid; i < p.batch; i += blockDim.x) {
         int len = p.seq_lens[i];
+        if (i == tid) my_slot = p.slots[i];
         if (len < 0) set_error(p.err, PA_ERR_BAD_BLOCK);
         local += pages_of(len);
     }
     const long long T = block_sum(local, red);
     const long long p_begin = T > 0 ? range_start(c, T, G) : 0;
     const long long p_end = T > 0 ? range_start(c + 1, T, G) : 0;
-    if (c == 0 && tid == 0) *reinterpret_cast<long long*>(p.ws) = T;
     if (tid == 0) {
         ctl[0] = -1;  // first sequence of the range
         ctl[1] = 0;   // its first flat page
+        ctl[2] = -1;  // its slot
     }
     __syncthreads();
     if (p_begin < p_end) {
@@ -212,6 +220,7 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
             if (pg > 0 && excl <= p_begin && p_begin < incl) {
                 ctl[0] = i;
                 ctl[1] = excl;
+                ctl[2] = base == 0 ? my_slot : p.slots[i];
             }
             carry += chunk_total;
             __syncthreads();
@@ -222,6 +231,7 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
     const long long n_pages = p_end - p_begin;
     const int b_first = static_cast<int>(ctl[0]);
     const long long sp_first = ctl[1];
+    const int slot_first = static_cast<int>(ctl[2]);
     if (n_pages <= 0 || b_first < 0) return;
 
 
@@ -231,24 +241,46 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
         long long sp = sp_first;  // flat index of page 0 of sequence b
         int len_b = p.seq_lens[b];
         int pages_b = pages_of(len_b);
-        int slot_b = p.slots[b];
+        int slot_b = slot_first;
         bool slot_ok = slot_b >= 0 && slot_b < g.num_slots;
         long long tbase = (static_cast<long long>(slot_ok ? slot_b : 0) * g.n_layers + p.layer) * g.maxb;
         long long win_base = -1;
         int win_val = -1;
+        // the first 32 table entries of the next sequence, loaded ahead so that
+        // crossing into it does not wait on the table (valid when nxt_b >= 0)
+        int nxt_b = -1, nxt_val = -1;
+        auto preload = [&](int bb) {
+            nxt_b = -1;
+            if (bb >= p.batch) return;
+            const int s2 = p.slots[bb];
+            const int pg2 = pages_of(p.seq_lens[bb]);
+            if (s2 < 0 || s2 >= g.num_slots || pg2 <= 0) return;
+            const long long tb2 = (static_cast<long long>(s2) * g.n_layers + p.layer) * g.maxb;
+            nxt_val = (lane < pg2 && lane < g.maxb) ? __ldg(p.bt + tb2 + lane) : -1;
+            nxt_b = bb;
+        };
+        if (sp + pages_b < p_end) preload(b + 1);  // the range goes past this sequence
         bool whole = false;
         long long k = 0;
         bool stop = false;
         for (long long pg = p_begin; pg < p_end; ++pg, ++k) {
-            while (pg >= sp + pages_b) {  // next sequence with pages
-                sp += pages_b;
-                ++b;
-                len_b = p.seq_lens[b];
-                pages_b = pages_of(len_b);
-                slot_b = p.slots[b];
-                slot_ok = slot_b >= 0 && slot_b < g.num_slots;
-                tbase = (static_cast<long long>(slot_ok ? slot_b : 0) * g.n_layers + p.layer) * g.maxb;
-                win_base = -1;
+            if (pg >= sp + pages_b) {
+                while (pg >= sp + pages_b) {  // next sequence with pages
+                    sp += pages_b;
+                    ++b;
+                    len_b = p.seq_lens[b];
+                    pages_b = pages_of(len_b);
+                    slot_b = p.slots[b];
+                    slot_ok = slot_b >= 0 && slot_b < g.num_slots;
+                    tbase = (static_cast<long long>(slot_ok ? slot_b : 0) * g.n_layers + p.layer) * g.maxb;
+                    win_base = -1;
+                }
+                if (b == nxt_b) {  // entries 0..31 of this sequence are already here
+                    win_base = 0;
+                    win_val = nxt_val;
+                }
+                nxt_b = -1;
+                if (sp + pages_b < p_end) preload(b + 1);
             }
             const long long lp = pg - sp;
             if (win_base < 0 || lp >= win_base + 32) {
@@ -273,12 +305,6 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
                 uint8_t* stage = stages + static_cast<long long>(st) * p.kv_stage_bytes;
                 uint8_t* qslot = qslots + st * p.qslot_bytes;
                 StageHeader* hdr = reinterpret_cast<StageHeader*>(qslot + p.q_bytes);
-                if (lp == 0) {  // this CTA holds the sequence's first page: record its CTA span
-                    int2 meta;
-                    meta.x = static_cast<int>(c);
-                    meta.y = static_cast<int>(owner_of(sp + pages_b - 1, T, G));
-                    *reinterpret_cast<int2*>(p.ws + p.ws_meta + 8ll * b) = meta;
-                }
                 if (bad) set_error(p.err, PA_ERR_BAD_BLOCK);
                 hdr->b = b;
                 hdr->ntok = bad ? 0 : ntok;
@@ -439,81 +465,150 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
     }
 }
 
+// The CTAs of the attend grid that hold sequence b, from the lengths and the
+// grid size alone (the same split the attend kernel makes): first and last
+// CTA, the page count T and whether the span is empty.  All threads of the
+// block call it; it reads only seq_lens.
+struct SeqSpan {
+    long long T, c0, c1;
+    int len;
+};
+
+__device__ SeqSpan seq_span(const DecodeParams& p, int b, long long G, long long* red) {
+    long long tot = 0, before = 0;
+    for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
+        const long long pg = pages_of(p.seq_lens[i]);
+        tot += pg;
+        if (i < b) before += pg;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        before += __shfl_xor_sync(0xffffffffu, before, off);
+    }
+    if (lane == 0) {
+        red[2 * warp] = tot;
+        red[2 * warp + 1] = before;
+    }
+    __syncthreads();
+    SeqSpan s;
+    s.T = 0;
+    long long sp = 0;
+    for (int w = 0; w < nw; ++w) {
+        s.T += red[2 * w];
+        sp += red[2 * w + 1];
+    }
+    s.len = p.seq_lens[b];
+    const int pages_b = pages_of(s.len);
+    s.c0 = pages_b > 0 ? owner_of(sp, s.T, G) : 0;
+    s.c1 = pages_b > 0 ? owner_of(sp + pages_b - 1, s.T, G) : 0;
+    return s;
+}
+
 // Merges the partial units of every split sequence; writes o = 0, lse = -inf
-// for empty sequences.  One CTA per (sequence, 8 q heads), one warp per head:
-// the lanes first take one partial each for the max and the weights of the
-// LSE rule, then run over the dims while the partial rows stream in.
-// Launched as a programmatic dependent of the attend kernel: everything the
-// attend kernel writes is read only after griddepcontrol.wait.
+// for empty sequences.  One CTA per (sequence, 8 q heads), one warp per head.
+// Launched as a programmatic dependent of the attend kernel: the span of the
+// sequence comes from the lengths before griddepcontrol.wait, and everything
+// the attend kernel writes is read after it, in one round of loads where the
+// sequence has at most kMergeBatch pieces: lane k takes piece k's L for the
+// max and the weights of the LSE rule while every lane loads its dims of the
+// pieces' rows.
 constexpr int kMergeHeadsPerCta = 8;
 constexpr int kMergeThreads = 32 * kMergeHeadsPerCta;
+constexpr int kMergeBatch = 8;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
     constexpr int PER = D / 32;  // dims per lane
+    __shared__ long long red[2 * (kMergeThreads / 32)];
     const KGeom& g = p.g;
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hq = blockIdx.y * kMergeHeadsPerCta + warp;
-    const int len = p.seq_lens[b];
+    const long long G = p.attend_grid;
+    const SeqSpan sp = seq_span(p, b, G, red);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (hq >= g.hq) return;
     const long long row = static_cast<long long>(b) * g.hq + hq;
-    if (len <= 0) {
+    if (sp.len <= 0) {
 #pragma unroll
         for (int e = 0; e < PER; ++e) p.o[row * D + lane * PER + e] = __float2bfloat16_rn(0.f);
         if (lane == 0 && p.lse) p.lse[row] = -CUDART_INF_F;
         return;
     }
-    const int2 meta = *reinterpret_cast<const int2*>(p.ws + p.ws_meta + 8ll * b);
-    const long long G = p.attend_grid;
-    if (meta.x < 0 || meta.y >= G || meta.x > meta.y) {  // attend kernel gave up early
-        if (lane == 0) set_error(p.err, PA_ERR_TIMEOUT);
-        return;
-    }
-    if (meta.x == meta.y) return;  // one unit: the attend kernel wrote the result
-    const long long T = *reinterpret_cast<const long long*>(p.ws);
+    if (sp.c0 == sp.c1) return;  // one unit: the attend kernel wrote the result
+    const long long T = sp.T;
+    const int P = static_cast<int>(sp.c1 - sp.c0 + 1);  // pieces
     const float* lse_part = reinterpret_cast<const float*>(p.ws + p.ws_lse);
     const float* o_part = reinterpret_cast<const float*>(p.ws + p.ws_o);
     // CTAs of the attend grid whose page range is empty wrote nothing
     auto has_pages = [&](long long cc) { return range_start(cc, T, G) != range_start(cc + 1, T, G); };
+    auto load_row = [&](long long cc, float* v) {
+        const float* src = o_part + ((b + cc) * g.hq + hq) * D + lane * PER;
+        if (PER == 2) {
+            const float2 x = *reinterpret_cast<const float2*>(src);
+            v[0] = x.x;
+            v[PER - 1] = x.y;
+        } else {
+            const float4 x = *reinterpret_cast<const float4*>(src);
+            v[0] = x.x;
+            v[1 % PER] = x.y;
+            v[2 % PER] = x.z;
+            v[3 % PER] = x.w;
+        }
+    };
 
-    // 1. max of the partial L (lanes over partials)
-    float M = -CUDART_INF_F;
-    for (long long cc = meta.x + lane; cc <= meta.y; cc += 32)
-        if (has_pages(cc)) M = fmaxf(M, lse_part[(b + cc) * g.hq + hq]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-
-    // 2. weighted sum (lanes over dims), 32 partials' weights at a time
     float acc[PER], S = 0.f;
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    if (M != -CUDART_INF_F) {
-        for (long long c0 = meta.x; c0 <= meta.y; c0 += 32) {
-            const long long mine = c0 + lane;
-            float w = 0.f;
-            if (mine <= meta.y && has_pages(mine)) {
-                const float Lc = lse_part[(b + mine) * g.hq + hq];
-                w = (Lc == -CUDART_INF_F) ? 0.f : ex2_approx((Lc - M) * kLog2e);
+    float M = -CUDART_INF_F;
+    if (P <= kMergeBatch) {
+        // every load at once: the pieces' rows, and lane k's L
+        float v[kMergeBatch][PER];
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k)
+            if (k < P) load_row(sp.c0 + k, v[k]);
+        const bool mine = lane < P && has_pages(sp.c0 + lane);
+        const float Lm = mine ? lse_part[(b + sp.c0 + lane) * g.hq + hq] : -CUDART_INF_F;
+        M = Lm;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float w = (M == -CUDART_INF_F || Lm == -CUDART_INF_F) ? 0.f : ex2_approx((Lm - M) * kLog2e);
+        S = w;
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+            if (k < P && wk != 0.f) {
+#pragma unroll
+                for (int e = 0; e < PER; ++e) acc[e] = fmaf(wk, v[k][e], acc[e]);
             }
-            S += w;
-            const int n = static_cast<int>(min(32ll, meta.y - c0 + 1));
+        }
+    } else {
+        // 1. max of the partial L (lanes over pieces)
+        for (long long cc = sp.c0 + lane; cc <= sp.c1; cc += 32)
+            if (has_pages(cc)) M = fmaxf(M, lse_part[(b + cc) * g.hq + hq]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        // 2. weighted sum (lanes over dims), 32 pieces' weights at a time
+        if (M != -CUDART_INF_F) {
+            for (long long c0 = sp.c0; c0 <= sp.c1; c0 += 32) {
+                const long long cm = c0 + lane;
+                float w = 0.f;
+                if (cm <= sp.c1 && has_pages(cm)) {
+                    const float Lc = lse_part[(b + cm) * g.hq + hq];
+                    w = (Lc == -CUDART_INF_F) ? 0.f : ex2_approx((Lc - M) * kLog2e);
+                }
+                S += w;
+                const int n = static_cast<int>(min(32ll, sp.c1 - c0 + 1));
 #pragma unroll 4
-            for (int k = 0; k < n; ++k) {
-                const float wk = __shfl_sync(0xffffffffu, w, k);
-                if (wk == 0.f) continue;
-                const float* src = o_part + ((b + c0 + k) * g.hq + hq) * D + lane * PER;
-                if (PER == 2) {
-                    const float2 v = *reinterpret_cast<const float2*>(src);
-                    acc[0] = fmaf(wk, v.x, acc[0]);
-                    acc[PER - 1] = fmaf(wk, v.y, acc[PER - 1]);
-                } else {
-                    const float4 v = *reinterpret_cast<const float4*>(src);
-                    acc[0] = fmaf(wk, v.x, acc[0]);
-                    acc[1 % PER] = fmaf(wk, v.y, acc[1 % PER]);
-                    acc[2 % PER] = fmaf(wk, v.z, acc[2 % PER]);
-                    acc[3 % PER] = fmaf(wk, v.w, acc[3 % PER]);
+                for (int k = 0; k < n; ++k) {
+                    const float wk = __shfl_sync(0xffffffffu, w, k);
+                    if (wk == 0.f) continue;
+                    float v[PER];
+                    load_row(c0 + k, v);
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) acc[e] = fmaf(wk, v[e], acc[e]);
                 }
             }
         }
@@ -537,16 +632,18 @@ template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_split_kernel(const DecodeParams p) {
     constexpr int PER = D / 32;
     constexpr int W = kMergeThreads / 32;
+    __shared__ long long red[2 * W];
     __shared__ float red_m[W];
     __shared__ float red_s[W];
     __shared__ float red_o[W][D];
     const KGeom& g = p.g;
     const int b = blockIdx.x, hq = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int len = p.seq_lens[b];
+    const long long G = p.attend_grid;
+    const SeqSpan sp = seq_span(p, b, G, red);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long row = static_cast<long long>(b) * g.hq + hq;
-    if (len <= 0) {
+    if (sp.len <= 0) {
         if (warp == 0) {
 #pragma unroll
             for (int e = 0; e < PER; ++e) p.o[row * D + lane * PER + e] = __float2bfloat16_rn(0.f);
@@ -554,21 +651,15 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_split_kernel(const
         }
         return;
     }
-    const int2 meta = *reinterpret_cast<const int2*>(p.ws + p.ws_meta + 8ll * b);
-    const long long G = p.attend_grid;
-    if (meta.x < 0 || meta.y >= G || meta.x > meta.y) {  // attend kernel gave up early
-        if (threadIdx.x == 0) set_error(p.err, PA_ERR_TIMEOUT);
-        return;
-    }
-    if (meta.x == meta.y) return;  // one unit: the attend kernel wrote the result
-    const long long T = *reinterpret_cast<const long long*>(p.ws);
+    if (sp.c0 == sp.c1) return;  // one unit: the attend kernel wrote the result
+    const long long T = sp.T;
     const float* lse_part = reinterpret_cast<const float*>(p.ws + p.ws_lse);
     const float* o_part = reinterpret_cast<const float*>(p.ws + p.ws_o);
     auto has_pages = [&](long long cc) { return range_start(cc, T, G) != range_start(cc + 1, T, G); };
 
     // 1. max of the partial L over the whole CTA
     float M = -CUDART_INF_F;
-    for (long long cc = meta.x + threadIdx.x; cc <= meta.y; cc += kMergeThreads)
+    for (long long cc = sp.c0 + threadIdx.x; cc <= sp.c1; cc += kMergeThreads)
         if (has_pages(cc)) M = fmaxf(M, lse_part[(b + cc) * g.hq + hq]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -577,13 +668,13 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_split_kernel(const
 #pragma unroll
     for (int w = 0; w < W; ++w) M = fmaxf(M, red_m[w]);
 
-    // 2. warp w sums partials meta.x + w, + W, ... (lanes over dims)
+    // 2. warp w sums partials sp.c0 + w, + W, ... (lanes over dims)
     float acc[PER], S = 0.f;
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
     if (M != -CUDART_INF_F) {
 #pragma unroll 4
-        for (long long cc = meta.x + warp; cc <= meta.y; cc += W) {
+        for (long long cc = sp.c0 + warp; cc <= sp.c1; cc += W) {
             if (!has_pages(cc)) continue;
             const float Lc = lse_part[(b + cc) * g.hq + hq];
             const float wk = (Lc == -CUDART_INF_F) ? 0.f : ex2_approx((Lc - M) * kLog2e);
@@ -659,7 +750,7 @@ bool decode_shape(const KGeom& g, LaunchShape* s) {
     s->kv_stage_bytes = static_cast<int>(g.page_bytes);
     if (s->kv_stage_bytes > 64 * 1024) return false;
     // 1024 B of slack to align the dynamic base, control words, q slots, stages
-    int nst = kMaxStages;
+    int nst = kStagesWanted;
     for (; nst >= 2; --nst) {
         const long long off = align_up(kCtlBytes + static_cast<long long>(nst) * s->qslot_bytes, 1024);
         if (1024 + off + static_cast<long long>(nst) * s->kv_stage_bytes <= kSmemBudget) break;
@@ -737,7 +828,6 @@ cudaError_t launch_decode(const KGeom& g, const void* q, const void* pool, const
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
     p.ws = static_cast<uint8_t*>(workspace);
-    p.ws_meta = w.meta;
     p.ws_lse = w.lse;
     p.ws_o = w.o;
     p.err = err;
