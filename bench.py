@@ -735,7 +735,7 @@ def main():
     peaks, peak_src = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
-    roofline = decode = e2e = None
+    roofline = decode = e2e = other_variant = None
     value = total_s = None
     step = None
     clk = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
@@ -760,6 +760,28 @@ def main():
                     "peak_source": "%s bf16_tflops (burst)" % peak_src,
                     "algorithmic_flops_per_launch": step.flops_prefill,
                     "avg_launch_ms": prefill_avg * 1e3}
+        # the other head-dim variant of the same long prefill (32 q / 8 kv heads at d 64,
+        # 16 / 4 at d 128; the same FLOPs), the same step, reported beside the main one
+        other = "d128" if args.variant == "d64" else "d64"
+        ostep = PrefillStep(torch, pa, W, other, batch=args.batch, seqlen=args.seqlen)
+        osteps = max(20, args.steps // 4)
+        ostep_s, opre_s = timed(torch, lambda ev: ostep.run(ev=ev), osteps, args.warmup, flush, dist)
+        torch.cuda.synchronize()
+        if int(ostep.err.item()) != 0:
+            raise SystemExit("device error during the %s steps: %s" % (other, pa.pa_status_string(int(ostep.err.item()))))
+        o_avg = float(np.mean(opre_s))
+        o_ach = ostep.flops_prefill / o_avg / 1e12
+        o_rate, o_total, _ = job_rate(torch, dist, ostep.flops * osteps, float(np.sum(ostep_s)))
+        other_variant = {
+            "metric": "causal prefill TFLOP/s, %s variant (%d q / %d kv heads), same step" % (
+                other, ostep.geom.num_q_heads, ostep.geom.num_kv_heads),
+            "value": o_rate / 1e12, "unit": "TFLOP/s", "ms_per_step": o_total / osteps * 1e3, "steps": osteps,
+            "roofline": {"bound": "tensor", "achieved": o_ach, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": o_ach / bf16_peak, "traffic": profiled_traffic("prefill_" + other),
+                         "kernel": "prefill_kernel<%d, %d>" % (ostep.geom.head_dim, prefill_heads_per_cta(ostep.geom)),
+                         "peak_source": "%s bf16_tflops (burst)" % peak_src,
+                         "algorithmic_flops_per_launch": ostep.flops_prefill, "avg_launch_ms": o_avg * 1e3}}
+        del ostep
 
     if args.only in ("all", "decode"):
         # -------------------------------------------------- decode (C5)
@@ -910,6 +932,7 @@ def main():
             "config": step_config(step.geom, step.case.batch, step.n, world),
             "gpu_launches": step.launches * args.steps,
             "roofline": roofline,
+            "prefill_" + ("d128" if args.variant == "d64" else "d64"): other_variant,
             "decode": decode,
             "chunked": chunked,
             "scatter": scatter,
