@@ -10,15 +10,20 @@ second (TFLOP/s; exact causal count 4 d Hq sum_b n_b (n_b + 1) / 2 plus the
 decode's 4 d Hq n).  The line also carries:
   roofline     -- the prefill kernel (the dominant launch) against the measured
                   dense bf16 peak;
+  prefill_d128 -- the same step at head dim 128 (16 q / 4 kv heads, the same
+                  FLOPs), its prefill against the same peak (prefill_d64 when
+                  --variant d128 is the main step);
   decode       -- decode KV-read GB/s on the large mixed-length batch (256
                   sequences, log-normal lengths, new-token write + decode per
-                  step) against the measured HBM copy bandwidth;
+                  step) against the measured HBM copy bandwidth; batch64: the
+                  same for 64 sequences of 128..2048 tokens;
   scatter      -- pa_write_kv and pa_write_kv_rope GB/s on the prompt rows
                   against the measured HBM copy bandwidth;
   chunked      -- pa_prefill_cached: 4 x 2048-query chunks after 6144 cached
                   tokens, exact-causal TFLOP/s against the same bf16 peak;
-  backward     -- pa_prefill_backward on the long prompt (4 x 8192, d 64):
-                  2.5 x the exact causal count, TFLOP/s against that peak;
+  backward     -- pa_prefill_backward on the long prompt (4 x 8192, d 64;
+                  d128: 16 q / 4 kv heads): 2.5 x the exact causal count,
+                  TFLOP/s against that peak;
   e2e          -- the same metric through the C ABI with host buffers: pinned
                   H2D of every step's inputs and D2H of its outputs inside the
                   timed region, neighbouring steps' copies overlapping the
