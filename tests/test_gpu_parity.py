@@ -173,8 +173,11 @@ def test_decode_ragged_lengths(hq, hkv, d):
 
 
 def test_decode_many_splits_and_tiny_batch():
-    """One long sequence split over every CTA, and lengths that leave CTAs empty."""
-    for lens in ([16384], [3], [1, 1], [40] * 3):
+    """One long sequence split over every CTA, and lengths that leave CTAs empty.
+    [16] * 63 + [16384] and [400] * 60 + [2500] * 4: 2048 (sequence, head) rows
+    take the warp-per-row merge; the long sequences' pieces (~290 and ~24) take
+    its general path, in several rounds and in one."""
+    for lens in ([16384], [3], [1, 1], [40] * 3, [16] * 63 + [16384], [400] * 60 + [2500] * 4):
         geom = W.Geometry(32, 8, 64, 1, len(lens), 1024, sum((n + 15) // 16 for n in lens) + 4)
         case = W.make_decode_case("splits", geom, lens, seed=len(lens), pool_fill="nan")
         pool, bt, werr = H.gpu_setup(case)
