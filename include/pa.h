@@ -1,10 +1,17 @@
 /*
  * pa.h -- C ABI of the paged-attention library (libpa.so) for GB300 (sm_103a).
  *
- * Exact causal grouped-query attention over a paged KV cache, in three calls:
- *   pa_write_kv  scatter new K/V rows into their pages,
- *   pa_prefill   causal prefill of a packed batch of prompts (tcgen05 / TMEM),
- *   pa_decode    one query per sequence over its whole cache (split-KV + LSE merge).
+ * Exact causal grouped-query attention over a paged KV cache.  The hot path:
+ *   pa_write_kv        scatter new K/V rows into their pages,
+ *   pa_prefill         causal prefill of a packed batch of prompts (tcgen05 / TMEM),
+ *   pa_decode          one query per sequence over its whole cache (split-KV + LSE merge).
+ * Around it:
+ *   pa_prefill_cached  prefill of query chunks over a cached prefix (chunked prefill),
+ *   pa_write_kv_rope   rotary embedding of K fused into the scatter,
+ *   pa_alloc_pages, pa_release_slots   page allocation on the device, table in place,
+ *   pa_prefill_backward  gradients of the prefill (tcgen05 / TMEM),
+ *   pa_decode_noalloc  pa_decode with the library's fixed scratch instead of a workspace,
+ *   pa_page_bytes, pa_decode_workspace_size, pa_status_string   sizes and messages.
  *
  * The problem statement follows these web pages (cited by title and section):
  *  - jaehun.me, "6. KV cache 를 16토큰 블록으로 쪼개기 -- block table 로 비연속 블록을
