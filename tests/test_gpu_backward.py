@@ -80,6 +80,7 @@ def oracle_backward(case, dout):
     (6, 1, 64, [129, 40]),           # MQA, a group of 6
     (16, 4, 128, [150, 64, 1]),      # head dim 128
     (8, 8, 128, [97]),
+    (8, 1, 128, [300, 129]),         # head dim 128, MQA: a group of 8, many query blocks per key block
 ])
 def test_backward_matches_oracle(hq, hkv, d, lens):
     case, dout = backward_case(hq, hkv, d, lens, seed=hq * 13 + d + len(lens))
@@ -178,15 +179,16 @@ def test_identities_at_long_prompt_size():
         assert np.all(np.abs(lhs - rhs) <= 1e-3 * mag + 1e-6), (lhs, rhs, mag)
 
 
-def test_bench_size_sampled_rows():
-    """The bench's backward workload in its launch configuration: 4 prompts of
-    8192 tokens, 32 q / 8 kv heads, d 64, shuffled pages.  dq at 48 sampled
-    (row, q head) pairs and dk, dv at 12 sampled (key row, kv head) pairs of
-    two (sequence, kv head) units against the oracle's sampled backward (the
-    full backward's entries, computed one by one)."""
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 64), (16, 4, 128)])
+def test_bench_size_sampled_rows(hq, hkv, d):
+    """The bench's backward workloads in their launch configuration: 4 prompts
+    of 8192 tokens, 32 q / 8 kv heads at d 64 and 16 / 4 at d 128, shuffled
+    pages.  dq at 48 sampled (row, q head) pairs and dk, dv at 12 sampled (key
+    row, kv head) pairs of two (sequence, kv head) units against the oracle's
+    sampled backward (the full backward's entries, computed one by one)."""
     B, n = 4, 8192
     pages = n // 16
-    geom = W.Geometry(32, 8, 64, 1, B, pages, B * pages + 64)
+    geom = W.Geometry(hq, hkv, d, 1, B, pages, B * pages + 64)
     case = W.make_prefill_case("bwd", geom, [n] * B, 1007)
     dout = W.normal_bf16(np.random.default_rng(1008), case.q.shape)
     pool, bt, werr = H.gpu_setup(case)
@@ -196,8 +198,8 @@ def test_bench_size_sampled_rows():
     rng = np.random.default_rng(5)
     starts = np.arange(B) * n
     q_rows = np.concatenate([starts, starts + n - 1, starts + 127, starts + 128, rng.integers(0, B * n, 32)])
-    q_heads = rng.integers(0, 32, q_rows.shape[0]).astype(np.int32)
-    units = [(0, 3), (3, 6)]  # (sequence, kv head)
+    q_heads = rng.integers(0, hq, q_rows.shape[0]).astype(np.int32)
+    units = [(0, 3), (3, hkv - 2)]  # (sequence, kv head)
     k_rows, k_heads = [], []
     for b, hk in units:
         for j in (0, 127, 128, n - 1, int(rng.integers(0, n)), int(rng.integers(0, n))):
@@ -207,9 +209,9 @@ def test_bench_size_sampled_rows():
         H.oracle_geom(case), case.q, H.oracle_pool(case), case.block_table, 0, case.cu_seqlens, case.slots,
         case.scale, dout, q_rows, q_heads, np.array(k_rows), np.array(k_heads))
     assert st == 0
-    assert_grad_close(dq[q_rows, q_heads], rq, "dq sampled, 4 x 8192")
-    assert_grad_close(dk[k_rows, k_heads], rk, "dk sampled, 4 x 8192")
-    assert_grad_close(dv[k_rows, k_heads], rv, "dv sampled, 4 x 8192")
+    assert_grad_close(dq[q_rows, q_heads], rq, "dq sampled, 4 x 8192, d%d" % d)
+    assert_grad_close(dk[k_rows, k_heads], rk, "dk sampled, 4 x 8192, d%d" % d)
+    assert_grad_close(dv[k_rows, k_heads], rv, "dv sampled, 4 x 8192, d%d" % d)
 
 
 def test_bad_table_entry_reports_and_context_recovers():
