@@ -6,16 +6,17 @@
 // block_table[slot][layer][pos / 16] (jaehun.me tiny-vllm part 6, "블록 하나가
 // 담는 것: K 는 앞, V 는 V_OFFSET 뒤"; part 3, "Distributing K/V into paged
 // blocks").  The series issues one device-to-device memcpy per page per layer;
-// here one launch moves every row of the call: each thread moves 64 bytes (4
-// chunks of 16) of one row, consecutive threads on consecutive chunks, so reads
-// of k_new/v_new and writes of each 2*KV_DIM-byte row are fully coalesced.
+// here one launch moves every row of the call: each thread moves 4 chunks of 16
+// bytes of one row, a row's threads taking consecutive chunks in each of 4
+// passes, so that every load and store instruction of a warp covers whole
+// contiguous 256-byte runs of k_new/v_new and of the page row.
 #include "pa_internal.cuh"
 
 namespace pa {
 namespace {
 
-// CPT consecutive 16-byte chunks of one K or V row per thread (CPT divides the
-// row's chunk count).  The row's data is read before its page is looked up,
+// CPT 16-byte chunks of one K or V row per thread, a row's chunks/CPT threads
+// apart (CPT divides the row's chunk count).  The row's data is read before its page is looked up,
 // so the two global latencies overlap instead of adding up.
 template <int CPT>
 __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restrict__ pool,
@@ -36,14 +37,14 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
         const long long row = idx / (2 * groups);
         const int rem = static_cast<int>(idx - row * 2 * groups);
         const int is_v = rem >= groups;
-        const int c = (is_v ? rem - groups : rem) * CPT;
+        const int c = is_v ? rem - groups : rem;  // chunks c, c + groups, c + 2 groups, ...
         const uint4* src = (is_v ? v_new : k_new) + row * chunks + c;
         uint4 val[CPT];
 #pragma unroll
         for (int x = 0; x < CPT; ++x)
             asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                          : "=r"(val[x].x), "=r"(val[x].y), "=r"(val[x].z), "=r"(val[x].w)
-                         : "l"(src + x));
+                         : "l"(src + x * groups));
         const int slot = __ldg(tok_slot + row);
         const int pos = __ldg(tok_pos + row);
         long long blk = -1;
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
         uint4* dst = reinterpret_cast<uint4*>(pool + blk * g.page_bytes + (is_v ? half_page : 0) +
                                               static_cast<long long>(pos % kBlockTokens) * row_bytes) + c;
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) dst[x] = val[x];
+        for (int x = 0; x < CPT; ++x) dst[x * groups] = val[x];
     }
 }
 
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
 // rounded on its own (no FMA contraction), then to bf16 nearest-even.  Per
 // row, the first kv_dim/16 threads each take 8 pairs of one head (16 bytes of
 // each half, read and written whole), the next threads copy V, VPT 16-byte
-// chunks each.  Every thread reads its row's data before looking up the page.
+// chunks each, a row's V threads taking consecutive chunks in each pass.  Every thread reads its row's data before looking up the page.
 __device__ __forceinline__ void rope8(uint4& lo, uint4& hi, const float4 c0, const float4 c1, const float4 s0,
                                       const float4 s1) {
     const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __
             hi = ld_stream(k_new + (row * g.kv_dim + e_hi) / 8);
         } else {
 #pragma unroll
-            for (int x = 0; x < VPT; ++x) vv[x] = ld_stream(v_new + row * vc + c * VPT + x);
+            for (int x = 0; x < VPT; ++x) vv[x] = ld_stream(v_new + row * vc + c + x * vt);
         }
         const int slot = __ldg(tok_slot + row);
         const int pos = __ldg(tok_pos + row);
@@ -162,9 +163,9 @@ __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __
             *reinterpret_cast<uint4*>(dst_row + e_lo * 2) = lo;
             *reinterpret_cast<uint4*>(dst_row + e_hi * 2) = hi;
         } else {
-            uint4* dv = reinterpret_cast<uint4*>(dst_row + half_page) + c * VPT;
+            uint4* dv = reinterpret_cast<uint4*>(dst_row + half_page) + c;
 #pragma unroll
-            for (int x = 0; x < VPT; ++x) dv[x] = vv[x];
+            for (int x = 0; x < VPT; ++x) dv[x * vt] = vv[x];
         }
     }
 }
