@@ -97,6 +97,7 @@ struct PrefillParams {
     int heads_per_cta;    // T
     float scale_log2;
     __nv_bfloat16* o;
+    bool o_32b;           // o is 32-byte aligned: rows go out in whole 32-byte sectors
     float* lse;
     int32_t* err;
 };
@@ -236,7 +237,17 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
         for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
             tmem_ld_x32(tO + 32 * c, ov);
-            if (store) {
+            if (store && p.o_32b) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    uint32_t v[8];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        v[w] = pack_bf16x2(__uint_as_float(ov[16 * e + 2 * w]) * inv,
+                                           __uint_as_float(ov[16 * e + 2 * w + 1]) * inv);
+                    st_global_v8(dst + 4 * c + 2 * e, v);
+                }
+            } else if (store) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     uint4 v;
@@ -536,6 +547,7 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, cons
     p.heads_per_cta = (g.group % 4 == 0 && tmax >= 4) ? 4 : (g.group % 2 == 0) ? 2 : 1;
     p.scale_log2 = scale * kLog2e;
     p.o = static_cast<__nv_bfloat16*>(o);
+    p.o_32b = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
     p.lse = lse;
     p.err = err;
     if (g.d == 64) {

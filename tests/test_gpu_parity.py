@@ -253,6 +253,24 @@ def test_output_may_alias_query():
     assert err == 0 and np.array_equal(o_ref, o_al) and np.array_equal(l_ref, l_al)
 
 
+def test_prefill_output_16_byte_aligned():
+    """o 16 bytes past a 32-byte boundary (the least alignment the call takes):
+    the rows go out in 16-byte stores instead of whole sectors, with the same
+    bytes as an aligned o."""
+    import torch
+    geom = W.Geometry(8, 2, 64, 1, 3, 32, 80)
+    pre = W.make_prefill_case("o16", geom, [200, 5, 129], seed=9, pool_fill="nan")
+    pool, bt, _ = H.gpu_setup(pre)
+    o_ref, l_ref, _ = H.gpu_prefill(pre, pool, bt)
+    T, hq, d = pre.total_tokens, geom.num_q_heads, geom.head_dim
+    flat = torch.zeros(T * hq * d + 8, dtype=torch.int16, device="cuda")
+    o16 = flat[8:].view(T, hq, d)
+    assert o16.data_ptr() % 32 == 16
+    o_al, l_al, err = H.gpu_prefill(pre, pool, bt, o=o16)
+    assert err == 0 and np.array_equal(o_ref, o_al) and np.array_equal(l_ref, l_al)
+    assert np.all(flat[:8].cpu().numpy() == 0)  # nothing written before o
+
+
 def test_bad_table_entries_report_and_recover():
     import torch
     geom = W.Geometry(8, 2, 64, 1, 2, 16, 40)
