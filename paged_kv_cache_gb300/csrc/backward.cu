@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
                                                        const uint16_t* __restrict__ dout,
                                                        const float* __restrict__ lse,
                                                        float* __restrict__ ws, float* __restrict__ dq,
-                                                       long long pairs) {
+                                                       long long pairs, bool dq_32b) {
     constexpr int PER = D / 8;
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long pair = t / PER;
@@ -49,9 +49,14 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
             acc = fmaf(bf16lo(ow[k]), bf16lo(gw[k]), acc);
             acc = fmaf(bf16hi(ow[k]), bf16hi(gw[k]), acc);
         }
-        float4* z = reinterpret_cast<float4*>(dq + off);
-        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (dq_32b) {  // one whole 32-byte sector
+            const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            st_global_v8(dq + off, zero);
+        } else {
+            float4* z = reinterpret_cast<float4*>(dq + off);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
 #pragma unroll
     for (int s = PER / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
@@ -74,10 +79,11 @@ cudaError_t launch_prefill_backward(const KGeom& g, const void* q, const void* p
     const unsigned prep_grid = static_cast<unsigned>((threads + prep_block - 1) / prep_block);
     const auto* o16 = static_cast<const uint16_t*>(o);
     const auto* do16 = static_cast<const uint16_t*>(dout);
+    const bool dq_32b = (reinterpret_cast<uintptr_t>(dq) & 31u) == 0;
     if (g.d == 64)
-        bwd_prep_kernel<64><<<prep_grid, prep_block, 0, stream>>>(o16, do16, lse, delta, dq, pairs);
+        bwd_prep_kernel<64><<<prep_grid, prep_block, 0, stream>>>(o16, do16, lse, delta, dq, pairs, dq_32b);
     else
-        bwd_prep_kernel<128><<<prep_grid, prep_block, 0, stream>>>(o16, do16, lse, delta, dq, pairs);
+        bwd_prep_kernel<128><<<prep_grid, prep_block, 0, stream>>>(o16, do16, lse, delta, dq, pairs, dq_32b);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (batch == 0 || max_seqlen == 0) return cudaSuccess;

@@ -103,6 +103,7 @@ struct BwdTcParams {
     float scale_log2;
     float* dk;
     float* dv;
+    bool kv_32b;            // dk and dv 32-byte aligned: rows go out in whole 32-byte sectors
     int32_t* err;
 };
 
@@ -537,7 +538,20 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
                 tmem_ld_x32_nowait(lane_addr + COL_DV + 32 * part, c);
                 tmem_wait_ld_dep(a);
                 tmem_wait_ld_dep(c);
-                if (j < n) {
+                if (j < n && p.kv_32b) {
+                    const long long off = (static_cast<long long>(cu0 + j) * g.hkv + hk) * D + 32 * part;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t vk[8], vv[8];
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            vk[w] = __float_as_uint(p.scale * __uint_as_float(a[8 * q + w]));
+                            vv[w] = c[8 * q + w];
+                        }
+                        st_global_v8(p.dk + off + 8 * q, vk);
+                        st_global_v8(p.dv + off + 8 * q, vv);
+                    }
+                } else if (j < n) {
                     const long long off = (static_cast<long long>(cu0 + j) * g.hkv + hk) * D + 32 * part;
                     float4* dkr = reinterpret_cast<float4*>(p.dk + off);
                     float4* dvr = reinterpret_cast<float4*>(p.dv + off);
@@ -616,6 +630,7 @@ cudaError_t launch_backward_tc(const KGeom& g, const void* q, const void* pool, 
     p.scale_log2 = scale * kLog2e;
     p.dk = dk;
     p.dv = dv;
+    p.kv_32b = ((reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 31u) == 0;
     p.err = err;
     if (g.d == 64) return launch_tc<64>(qmap, domap, kvmap, dqmap, p, batch, max_seqlen, stream);
     return launch_tc<128>(qmap, domap, kvmap, dqmap, p, batch, max_seqlen, stream);

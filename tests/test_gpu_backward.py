@@ -25,8 +25,9 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
-def gpu_forward_backward(case, pool, bt, dout):
-    """GPU pa_prefill then pa_prefill_backward; returns numpy (dq, dk, dv, err)."""
+def gpu_forward_backward(case, pool, bt, dout, offset16=False):
+    """GPU pa_prefill then pa_prefill_backward; returns numpy (dq, dk, dv, err).
+    offset16: dq, dk and dv start 16 bytes past a 32-byte boundary."""
     torch = H.torch_mod()
     g = H.pa_geom(case)
     T, hq, hkv, d = case.total_tokens, case.geom.num_q_heads, case.geom.num_kv_heads, case.geom.head_dim
@@ -37,9 +38,16 @@ def gpu_forward_backward(case, pool, bt, dout):
     cu, slots = H.to_dev(case.cu_seqlens), H.to_dev(case.slots)
     H.pa.pa_prefill(g, q, pool, bt, case.layer, cu, slots, case.max_len, case.scale, o, lse, err)
     delta = torch.empty((2, T, hq), dtype=torch.float32, device="cuda")
-    dq = torch.full((T, hq, d), float("nan"), dtype=torch.float32, device="cuda")
-    dk = torch.full((T, hkv, d), float("nan"), dtype=torch.float32, device="cuda")
-    dv = torch.full((T, hkv, d), float("nan"), dtype=torch.float32, device="cuda")
+    def out(shape):
+        if not offset16:
+            return torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+        n = int(np.prod(shape))
+        flat = torch.full((n + 4,), float("nan"), dtype=torch.float32, device="cuda")
+        view = flat[4:].view(shape)
+        assert view.data_ptr() % 32 == 16
+        return view
+
+    dq, dk, dv = out((T, hq, d)), out((T, hkv, d)), out((T, hkv, d))
     H.pa.pa_prefill_backward(g, q, pool, bt, case.layer, cu, slots, case.max_len, case.scale, o, lse,
                              H.to_dev(dout), delta, dq, dk, dv, err)
     torch.cuda.synchronize()
@@ -212,6 +220,23 @@ def test_bench_size_sampled_rows(hq, hkv, d):
     assert_grad_close(dq[q_rows, q_heads], rq, "dq sampled, 4 x 8192, d%d" % d)
     assert_grad_close(dk[k_rows, k_heads], rk, "dk sampled, 4 x 8192, d%d" % d)
     assert_grad_close(dv[k_rows, k_heads], rv, "dv sampled, 4 x 8192, d%d" % d)
+
+
+def test_outputs_16_byte_aligned():
+    """dq, dk and dv 16 bytes past a 32-byte boundary (the least alignment the
+    call takes): the rows go out in 16-byte stores instead of whole sectors;
+    dk and dv equal the aligned run's bit for bit (no atomics in them), dq
+    stays within the tolerance."""
+    for hq, hkv, d in ((8, 2, 64), (8, 2, 128)):
+        case, dout = backward_case(hq, hkv, d, [150, 40], seed=61 + d, layers=(0,))
+        pool, bt, werr = H.gpu_setup(case)
+        assert werr == 0
+        dq0, dk0, dv0, err0 = gpu_forward_backward(case, pool, bt, dout)
+        dq1, dk1, dv1, err1 = gpu_forward_backward(case, pool, bt, dout, offset16=True)
+        assert err0 == 0 and err1 == 0
+        assert np.array_equal(dk0, dk1) and np.array_equal(dv0, dv1)
+        rq, rk, rv = oracle_backward(case, dout)
+        assert_grad_close(dq1, rq, "dq at a 16-byte offset, d%d" % d)
 
 
 def test_bad_table_entry_reports_and_context_recovers():
