@@ -104,6 +104,25 @@ def test_shortage_and_bad_input_change_nothing():
     assert err == 0 and r == 6
 
 
+def test_release_refusals_change_nothing():
+    """A slot named twice, and a release whose pages would overflow the stack
+    (a page held by two slots: freed twice), change neither the table nor the
+    stack, on the device as in the oracle."""
+    geom = W.Geometry(8, 2, 64, 2, 4, 64, 30)
+    st = Pair(geom, seed=5)
+    r, err = st.alloc([0], [160])          # 2 layers x 10 blocks: 20 of the 30 pages
+    assert err == 0 and r == 20
+    r, err = st.release([0, 0])
+    assert r < 0 and err == H.pa.PA_ERR_BAD_BLOCK
+    # slot 1's rows name slot 0's pages too: releasing both pushes 40 pages onto 10
+    st.table[1] = st.table[0]
+    st.d_table[1] = st.d_table[0]
+    r, err = st.release([0, 1])
+    assert r < 0 and err == H.pa.PA_ERR_OUT_OF_PAGES
+    r, err = st.release([0])
+    assert err == 0
+
+
 def test_allocated_table_serves_the_attention_path():
     """Pages from the device allocator, then write + prefill against the oracle."""
     torch = H.torch_mod()
