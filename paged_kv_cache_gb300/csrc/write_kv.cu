@@ -6,10 +6,11 @@
 // block_table[slot][layer][pos / 16] (jaehun.me tiny-vllm part 6, "블록 하나가
 // 담는 것: K 는 앞, V 는 V_OFFSET 뒤"; part 3, "Distributing K/V into paged
 // blocks").  The series issues one device-to-device memcpy per page per layer;
-// here one launch moves every row of the call: each thread moves 4 chunks of 16
-// bytes of one row, a row's threads taking consecutive chunks in each of 4
-// passes, so that every load and store instruction of a warp covers whole
-// contiguous 256-byte runs of k_new/v_new and of the page row.
+// here one launch moves every row of the call: each thread moves 8 chunks of 16
+// bytes of one row (4 or 1 when the row's chunk count does not divide), a
+// row's threads taking consecutive chunks in each pass, so that every load and
+// store instruction of a warp covers whole contiguous runs of k_new/v_new and
+// of the page row.
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -193,12 +194,16 @@ cudaError_t launch_write_kv(const KGeom& g, void* pool, const int32_t* block_tab
                             const void* k_new, const void* v_new, int32_t* err,
                             cudaStream_t stream) {
     const int chunks = g.kv_dim / 8;
-    const int cpt = chunks % 4 == 0 ? 4 : 1;
+    const int cpt = chunks % 8 == 0 ? 8 : chunks % 4 == 0 ? 4 : 1;
     const long long total = static_cast<long long>(n_tokens) * 2 * (chunks / cpt);
     const int threads = 256;
     long long blocks = (total + threads - 1) / threads;
     if (blocks > (1ll << 30)) blocks = 1ll << 30;  // grid-stride covers the rest
-    if (cpt == 4)
+    if (cpt == 8)
+        write_kv_kernel<8><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+            g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
+            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), err);
+    else if (cpt == 4)
         write_kv_kernel<4><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
             g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
             static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), err);
