@@ -919,8 +919,8 @@ def main():
         e2e = e2e_timing(torch, step, max(10, args.steps // 4), args.warmup, flush, dist)
 
     # ------------------------------------------------------- CPU oracle
-    cpu = None
-    if rank == 0 and step is not None and not args.no_cpu_baseline:
+    cpu = None  # the oracle is timed on rank 0 of a single-GPU run only
+    if rank == 0 and world == 1 and step is not None and not args.no_cpu_baseline:
         flops, wall, threads, desc = oracle_sample(step.case, args.cpu_seconds)
         cpu = {"value": flops / wall / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": desc, "seconds": wall}
