@@ -175,7 +175,7 @@ class PrefillStep:
 
     def __init__(self, torch, pa, W, variant, seed=1003, batch=4, seqlen=8192):
         self.torch, self.pa = torch, pa
-        self.case = W.c4_long(variant, seed=seed, batch=batch, seqlen=seqlen)
+        self.case = W.long_prefill_case(variant, seed=seed, batch=batch, seqlen=seqlen)
         c = self.case
         geom = c.geom
         # one more page per sequence for the decoded token (position 8192)
@@ -250,7 +250,7 @@ class ScatterStep:
 
     def __init__(self, torch, pa, W, seed=1003):
         self.torch, self.pa = torch, pa
-        c = W.c4_long("d64", seed=seed)
+        c = W.long_prefill_case("d64", seed=seed)
         self.case, self.geom = c, c.geom
         self.g = pa.geom(*c.geom.as_tuple())
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
@@ -371,10 +371,10 @@ class DecodeStep:
         self.torch, self.pa = torch, pa
         if small:
             seed = 1002
-            lens = W.c3_lens(seed)
+            lens = W.uniform_decode_lens(seed)
             self.geom = W.Geometry(32, 8, 64, 1, lens.shape[0], 128, 65536)
         else:
-            lens = W.c5_lens(seed)
+            lens = W.lognormal_decode_lens(seed)
             self.geom = W.Geometry(32, 8, 64, 1, lens.shape[0], 1024, 131072)
         self.lens_np = lens
         B = lens.shape[0]
@@ -570,7 +570,7 @@ def page_lifetime_timing(torch, pa, W, warmup, reps=50):
     page), and the release of 64 slots; beside them, for context, the copy
     of the whole block table from pinned host memory that the pages' program
     makes after every change.  Latency-bound calls: microseconds per call."""
-    lens = W.c5_lens()
+    lens = W.lognormal_decode_lens()
     B, L = lens.shape[0], 16
     geom = W.Geometry(32, 8, 64, L, B, 1025, B * L * 1100)
     g = pa.geom(*geom.as_tuple())
@@ -672,7 +672,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     from paged_kv_cache_gb300 import workloads as W
-    case = W.c4_long(args.variant)
+    case = W.long_prefill_case(args.variant)
     per_step = min(5.0, max(0.5, 150.0 / max(1, args.steps + args.warmup)))
     import oracle
     g = oracle.geom(*case.geom.as_tuple())
@@ -789,7 +789,7 @@ def main():
         del ostep
 
     if args.only in ("all", "decode"):
-        # -------------------------------------------------- decode (C5)
+        # ------------------- decode (256 sequences, log-normal lengths)
         dstep = DecodeStep(torch, pa, W)
         dsteps = args.decode_steps or max(20, args.steps)
         dstep_s, dk_s = timed(torch, lambda ev: dstep.run(ev=ev), dsteps, args.warmup, flush, dist)
@@ -804,7 +804,7 @@ def main():
                   "value": d_rate / 1e9, "unit": "GB/s", "ms_per_step": d_total / dsteps * 1e3,
                   "kv_bytes_per_step": dstep.kv_bytes, "steps": dsteps,
                   "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
-                               "frac": dec_gbs / hbm_peak, "traffic": profiled_traffic("decode_c5"),
+                               "frac": dec_gbs / hbm_peak, "traffic": profiled_traffic("decode_256seq"),
                                "kernel": "decode_attend_kernel<64> + decode_merge_kernel<64>",
                                "peak_source": "%s hbm_gbs" % peak_src,
                                "algorithmic_bytes_per_launch": dstep.kv_bytes,
@@ -824,7 +824,7 @@ def main():
                              "value": s_rate / 1e9, "unit": "GB/s", "ms_per_step": s_total / dsteps * 1e3,
                              "kv_bytes_per_step": sstep.kv_bytes, "steps": dsteps,
                              "roofline": {"bound": "hbm", "achieved": s_gbs, "peak": hbm_peak, "unit": "GB/s",
-                                          "frac": s_gbs / hbm_peak, "traffic": profiled_traffic("decode_c3"),
+                                          "frac": s_gbs / hbm_peak, "traffic": profiled_traffic("decode_64seq"),
                                           "kernel": "decode_attend_kernel<64> + decode_merge_kernel<64>",
                                           "peak_source": "%s hbm_gbs" % peak_src,
                                           "algorithmic_bytes_per_launch": sstep.kv_bytes,

@@ -8,21 +8,22 @@ oracle's scatter (CPU), so the two sides never share a layout helper.
 
 The five named workloads follow the configurations the library is measured on:
 
-* ``c1_tiny``: 1 sequence of 40 tokens, 8 q heads / 2 kv heads, d 64, a pool
+* ``tiny_case``: 1 sequence of 40 tokens, 8 q heads / 2 kv heads, d 64, a pool
   of 16 pages, table = the first 3 entries of a seeded permutation; prefill
   of rows 0..39, then one token written at position 40 and a decode of 41.
-* ``c2_prefill``: Llama-3.2-1B attention shapes (32/8 heads, d 64), prompts of
+* ``llama_prefill_case``: Llama-3.2-1B attention shapes (32/8 heads, d 64), prompts of
   17 and 512 tokens, 2 GiB pool of 65536 pages, table [2][16][128], K/V written
   at layers 0 and 15.
-* ``c3_decode``: 64 sequences, lengths uniform in [128, 2048], fragmented pool
+* ``uniform_decode_case``: 64 sequences, lengths uniform in [128, 2048], fragmented pool
   of 65536 pages.
-* ``c4_long``: 4 x 8192 causal prefill, (32/8, d 64) or (16/4, d 128), 512
+* ``long_prefill_case``: 4 x 8192 causal prefill, (32/8, d 64) or (16/4, d 128), 512
   shuffled pages per sequence from a 65536-page pool.
-* ``c5_mixed``: 256 sequences, lengths round(LogNormal(ln 1024, 1.0)) clipped
+* ``lognormal_decode_case``: 256 sequences, lengths round(LogNormal(ln 1024, 1.0)) clipped
   to [1, 16384], 4 GiB pool of 131072 pages; c-1 tokens preloaded, then one
   new token written at position c-1 and a decode of length c.
 
-Seeds are 1000 + configuration index unless given.
+Default seeds: 1000 (tiny), 1001 (Llama prompts), 1002 (64-sequence decode),
+1003 (long prefill), 1004 (256-sequence decode).
 """
 from dataclasses import dataclass, field
 from typing import List, Optional
@@ -297,7 +298,7 @@ def make_decode_case(name, geom: Geometry, lens, seed: int, scale=None, layer=0,
 
 # -------------------------------------------------------- named workloads
 
-def c1_tiny(seed: int = 1000, pool_fill: str = "nan"):
+def tiny_case(seed: int = 1000, pool_fill: str = "nan"):
     """Returns (prefill_case, decode_case) sharing one table: 40-token prefill,
     then the token at position 40 and a decode of length 41."""
     geom = Geometry(8, 2, 64, 1, 1, 4, 16)
@@ -309,34 +310,34 @@ def c1_tiny(seed: int = 1000, pool_fill: str = "nan"):
     slots = np.array([0], np.int32)
     writes = prompt_writes(geom, rng, slots, lens, [0])
     q = normal_bf16(rng, (40, 8, 64))
-    pre = Case("c1_prefill", geom, 0.125, 0, slots, lens, table, writes, q, "prefill",
+    pre = Case("tiny_prefill", geom, 0.125, 0, slots, lens, table, writes, q, "prefill",
                pool_fill, seed)
     new = KVWrite(0, np.array([0], np.int32), np.array([40], np.int32),
                   normal_bf16(rng, (1, geom.kv_dim)), normal_bf16(rng, (1, geom.kv_dim)))
     qd = normal_bf16(rng, (1, 8, 64))
-    dec = Case("c1_decode", geom, 0.125, 0, slots, np.array([41], np.int32), table,
+    dec = Case("tiny_decode", geom, 0.125, 0, slots, np.array([41], np.int32), table,
                writes + [new], qd, "decode", pool_fill, seed)
     return pre, dec
 
 
-def c2_prefill(seed: int = 1001, pool_fill: str = "random", attend_layer: int = 15):
+def llama_prefill_case(seed: int = 1001, pool_fill: str = "random", attend_layer: int = 15):
     geom = Geometry(32, 8, 64, 16, 2, 128, 65536)
-    return make_prefill_case("c2_prefill", geom, [17, 512], seed, scale=0.125, layers=(0, 15),
+    return make_prefill_case("llama_prefill_case", geom, [17, 512], seed, scale=0.125, layers=(0, 15),
                              attend_layer=attend_layer, pool_fill=pool_fill)
 
 
-def c3_lens(seed: int = 1002, batch: int = 64):
+def uniform_decode_lens(seed: int = 1002, batch: int = 64):
     rng = np.random.default_rng(seed)
     return rng.integers(128, 2048, size=batch, endpoint=True).astype(np.int32)
 
 
-def c3_decode(seed: int = 1002, pool_fill: str = "random", batch: int = 64):
+def uniform_decode_case(seed: int = 1002, pool_fill: str = "random", batch: int = 64):
     geom = Geometry(32, 8, 64, 1, batch, 128, 65536)
-    return make_decode_case("c3_decode", geom, c3_lens(seed, batch), seed + 1, scale=0.125,
+    return make_decode_case("uniform_decode_case", geom, uniform_decode_lens(seed, batch), seed + 1, scale=0.125,
                             pool_fill=pool_fill)
 
 
-def c4_geometry(variant: str = "d64") -> Geometry:
+def long_prefill_geometry(variant: str = "d64") -> Geometry:
     if variant == "d64":
         return Geometry(32, 8, 64, 1, 4, 512, 65536)
     if variant == "d128":
@@ -344,20 +345,20 @@ def c4_geometry(variant: str = "d64") -> Geometry:
     raise ValueError(variant)
 
 
-def c4_long(variant: str = "d64", seed: int = 1003, pool_fill: str = "random", batch: int = 4,
+def long_prefill_case(variant: str = "d64", seed: int = 1003, pool_fill: str = "random", batch: int = 4,
             seqlen: int = 8192):
-    geom = c4_geometry(variant)
-    return make_prefill_case("c4_long_" + variant, geom, [seqlen] * batch, seed,
+    geom = long_prefill_geometry(variant)
+    return make_prefill_case("long_prefill_case_" + variant, geom, [seqlen] * batch, seed,
                              scale=1.0 / np.sqrt(geom.head_dim), layers=(0,), pool_fill=pool_fill)
 
 
-def c5_lens(seed: int = 1004, batch: int = 256):
+def lognormal_decode_lens(seed: int = 1004, batch: int = 256):
     rng = np.random.default_rng(seed)
     c = np.round(rng.lognormal(mean=np.log(1024.0), sigma=1.0, size=batch))
     return np.clip(c, 1, 16384).astype(np.int32)
 
 
-def c5_mixed(seed: int = 1004, pool_fill: str = "random", batch: int = 256):
+def lognormal_decode_case(seed: int = 1004, pool_fill: str = "random", batch: int = 256):
     geom = Geometry(32, 8, 64, 1, batch, 1024, 131072)
-    return make_decode_case("c5_mixed", geom, c5_lens(seed, batch), seed + 1, scale=0.125,
+    return make_decode_case("lognormal_decode_case", geom, lognormal_decode_lens(seed, batch), seed + 1, scale=0.125,
                             pool_fill=pool_fill)

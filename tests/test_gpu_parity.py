@@ -26,10 +26,10 @@ def _pool_equal(case, pool_dev, writes=None):
     return ref
 
 
-# ------------------------------------------------------------- C1 tiny
+# ------------------------------------------------------------- tiny (40 tokens)
 
-def test_c1_tiny_prefill_write_decode():
-    pre, dec = W.c1_tiny()
+def test_tiny_prefill_write_decode():
+    pre, dec = W.tiny_case()
     pool, bt, werr = H.gpu_setup(pre)
     assert werr == 0
     ref_pool = _pool_equal(pre, pool)
@@ -52,10 +52,10 @@ def test_c1_tiny_prefill_write_decode():
     H.assert_close(od[0], ld[0], op[40], lp_[40], H.max_abs_v(dec), "decode vs prefill row 40")
 
 
-# ------------------------------------------------------------ C2 llama
+# ------------------------------------------------ Llama-3.2-1B prompts
 
-def test_c2_llama_prefill_layers_0_and_15():
-    case = W.c2_prefill()
+def test_llama_prefill_layers_0_and_15():
+    case = W.llama_prefill_case()
     pool, bt, werr = H.gpu_setup(case)
     assert werr == 0
     ref_pool = _pool_equal(case, pool)
@@ -67,10 +67,10 @@ def test_c2_llama_prefill_layers_0_and_15():
         H.assert_close(o, l, ro, rl, H.max_abs_v(case), "c2 prefill layer %d" % layer)
 
 
-# ------------------------------------------------------------ C3 decode
+# ------------------------------------------- 64-sequence decode batch
 
-def test_c3_decode_batch():
-    case = W.c3_decode(pool_fill="nan")
+def test_uniform_decode_batch():
+    case = W.uniform_decode_case(pool_fill="nan")
     pool, bt, werr = H.gpu_setup(case)
     assert werr == 0
     ref_pool = _pool_equal(case, pool)
@@ -80,7 +80,7 @@ def test_c3_decode_batch():
     H.assert_close(o, l, ro, rl, H.max_abs_v(case), "c3 decode")
 
 
-# ------------------------------------------------------- C4 long prefill
+# --------------------------------------------- long prefill 4 x 8192
 
 def _sample_rows(case, rng, n_random=160):
     cu = case.cu_seqlens
@@ -101,8 +101,8 @@ def _sample_rows(case, rng, n_random=160):
 
 
 @pytest.mark.parametrize("variant", ["d64", "d128"])
-def test_c4_long_prefill_sampled(variant):
-    case = W.c4_long(variant)
+def test_long_prefill_sampled(variant):
+    case = W.long_prefill_case(variant)
     pool, bt, werr = H.gpu_setup(case)
     assert werr == 0
     o, l, err = H.gpu_prefill(case, pool, bt)
@@ -119,10 +119,10 @@ def test_c4_long_prefill_sampled(variant):
     H.assert_close(o[rows, heads], l[rows, heads], ro, rl, vmax, "c4 " + variant)
 
 
-# ------------------------------------------------------ C5 mixed decode
+# ------------------------------------ 256-sequence mixed decode batch
 
-def test_c5_mixed_decode_step():
-    case = W.c5_mixed(pool_fill="nan")
+def test_lognormal_decode_step():
+    case = W.lognormal_decode_case(pool_fill="nan")
     pool = H.device_pool(case)
     bt = H.to_dev(case.block_table)
     assert H.gpu_write(case, pool, bt, writes=case.writes[:-1]) == 0  # preload c-1 tokens

@@ -312,7 +312,7 @@ def test_page_permutation_invariance():
 
 
 def test_decode_equals_prefill_row():
-    pre, dec = W.c1_tiny()
+    pre, dec = W.tiny_case()
     g = oracle.geom(*pre.geom.as_tuple())
     pool = oracle_pool(dec)  # all 41 tokens written
     # prefill over all 41 tokens with the decode query placed at row 40

@@ -36,7 +36,7 @@ def _noalloc(case, pool, bt):
 
 def test_no_alloc_decode_matches_workspace_decode_twice():
     geom = W.Geometry(32, 8, 64, 1, 40, 160, 4000)
-    first = W.make_decode_case("noalloc_a", geom, W.c3_lens(1002, 40), seed=77, pool_fill="nan")
+    first = W.make_decode_case("noalloc_a", geom, W.uniform_decode_lens(1002, 40), seed=77, pool_fill="nan")
     second = W.make_decode_case("noalloc_b", geom, [0, 1, 17, 2048, 300] * 8, seed=78, pool_fill="nan")
     for case in (first, second):
         pool, bt, werr = H.gpu_setup(case)
