@@ -83,16 +83,34 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
-    """Hash of every CUDA source of the library (a traffic figure taken on other
-    sources is not reported)."""
+def kernel_source_hash(names=None):
+    """Hash of the library's CUDA sources: every .cu / .cuh file, or only the
+    files named (a traffic figure taken on other sources is not reported)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith((".cu", ".cuh")) and (names is None or name in names):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(f.read())
+    if names is not None:
+        with open(os.path.join(ROOT, "include", "pa.h"), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
+
+
+# The sources each profiled kernel is built from: its own file(s), the shared
+# device header and the C-ABI front end (pa.h is added by kernel_source_hash).
+TRAFFIC_SOURCES = {
+    "prefill": ("prefill.cu", "pa_internal.cuh", "api.cu"),
+    "chunked": ("prefill.cu", "pa_internal.cuh", "api.cu"),
+    "decode": ("decode.cu", "pa_internal.cuh", "api.cu"),
+    "backward": ("backward.cu", "backward_tc.cu", "pa_internal.cuh", "api.cu"),
+}
+
+
+def traffic_key(kernel_tag):
+    """Source hash a traffic row must carry: that of the tagged kernel's own sources."""
+    return kernel_source_hash(TRAFFIC_SOURCES[kernel_tag.split("_")[0]])
 
 
 def prefill_heads_per_cta(geom):
@@ -106,11 +124,11 @@ def prefill_heads_per_cta(geom):
 
 def profiled_traffic(kernel_tag):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current sources of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = traffic_key(kernel_tag)
     for line in open(path):
         m = re.match(r"\|\s*%s\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9.eE+]+)\s*\|" % re.escape(kernel_tag), line)
         if m and m.group(1) == want:

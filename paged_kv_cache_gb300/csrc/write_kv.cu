@@ -71,10 +71,14 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
 // and element i + d/2 form a pair turned by the angle of the row's position,
 //   x1' = x1 c - x2 s,   x2' = x1 s + x2 c,
 // with c, s from caller tables [max_pos][d/2] fp32.  Each product and sum is
-// rounded on its own (no FMA contraction), then to bf16 nearest-even.  Per
-// row, the first kv_dim/16 threads each take 8 pairs of one head (16 bytes of
-// each half, read and written whole), the next threads copy V, VPT 16-byte
-// chunks each, a row's V threads taking consecutive chunks in each pass.  Every thread reads its row's data before looking up the page.
+// rounded on its own (no FMA contraction), then to bf16 nearest-even.
+// Threads work on groups of kRopeRows rows: the group's K threads first (8
+// pairs, 16 bytes of each half, in each of KPT heads Hkv/KPT apart, which
+// share one angle row), then its V threads (VPT 16-byte chunks each, a row's
+// V threads taking consecutive chunks in each pass), so that a warp runs
+// either the rotation or the copy.
+// Every thread reads its row's data, then the position, then the page entry
+// and (K) the angle rows together, so that the latencies overlap.
 __device__ __forceinline__ void rope8(uint4& lo, uint4& hi, const float4 c0, const float4 c1, const float4 s0,
                                       const float4 s1) {
     const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
@@ -108,7 +112,9 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     return v;
 }
 
-template <int VPT>
+constexpr int kRopeRows = 8;  // rows per thread group of the RoPE scatter
+
+template <int KPT, int VPT>
 __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __restrict__ pool,
                                                             const int32_t* __restrict__ block_table, int layer,
                                                             int n_tokens, const int32_t* __restrict__ tok_slot,
@@ -118,51 +124,72 @@ __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __
                                                             const float* __restrict__ cos_tab,
                                                             const float* __restrict__ sin_tab, int max_pos,
                                                             int32_t* err) {
-    const int kq = g.kv_dim / 16;  // K threads per row: 8 pairs each
-    const int vc = g.kv_dim / 8;   // 16-byte V chunks per row
-    const int vt = vc / VPT;       // V threads per row: VPT chunks each
-    const int per_row = kq + vt;
-    const int hc = g.d / 16;       // pair chunks per head
-    const long long total = static_cast<long long>(n_tokens) * per_row;
+    const int hc = g.d / 16;            // pair chunks per head (8 pairs each)
+    const int kt = g.hkv / KPT * hc;    // K threads per row
+    const int vc = g.kv_dim / 8;        // 16-byte V chunks per row
+    const int vt = vc / VPT;            // V threads per row
+    const int k_threads = kRopeRows * kt;
+    const int per_group = k_threads + kRopeRows * vt;
+    const long long total = static_cast<long long>((n_tokens + kRopeRows - 1) / kRopeRows) * per_group;
     const long long half_page = g.page_bytes / 2;  // V_OFFSET
     const long long row_bytes = static_cast<long long>(g.kv_dim) * 2;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long row = idx / per_row;
-        const int rem = static_cast<int>(idx - row * per_row);
-        const bool is_k = rem < kq;
-        const int head = rem / hc, c = is_k ? rem % hc : rem - kq;
-        const long long e_lo = static_cast<long long>(head) * g.d + 8 * c;  // K: element index in the row
-        const long long e_hi = e_lo + g.d / 2;
-        // the row's data first: its latency overlaps the page lookup
-        uint4 lo, hi, vv[VPT];
+        const long long grp = idx / per_group;
+        const int rem = static_cast<int>(idx - grp * per_group);
+        const bool is_k = rem < k_threads;
+        const int local = is_k ? rem / kt : (rem - k_threads) / vt;
+        const int c = is_k ? rem % kt : (rem - k_threads) % vt;  // K: (first head, pair chunk); V: first chunk
+        const int c8 = 8 * (c % hc);                             // K: first pair element within the head
+        const long long row = grp * kRopeRows + local;
+        if (row >= n_tokens) continue;
+        // the row's data first: its latency overlaps the lookups
+        uint4 lo[KPT], hi[KPT], vv[VPT];
         if (is_k) {
-            lo = ld_stream(k_new + (row * g.kv_dim + e_lo) / 8);
-            hi = ld_stream(k_new + (row * g.kv_dim + e_hi) / 8);
+#pragma unroll
+            for (int x = 0; x < KPT; ++x) {
+                const long long e_lo = static_cast<long long>(c / hc + x * (g.hkv / KPT)) * g.d + c8;
+                lo[x] = ld_stream(k_new + (row * g.kv_dim + e_lo) / 8);
+                hi[x] = ld_stream(k_new + (row * g.kv_dim + e_lo + g.d / 2) / 8);
+            }
         } else {
 #pragma unroll
             for (int x = 0; x < VPT; ++x) vv[x] = ld_stream(v_new + row * vc + c + x * vt);
         }
         const int slot = __ldg(tok_slot + row);
         const int pos = __ldg(tok_pos + row);
+        const bool pos_ok = pos >= 0 && pos < max_pos && pos / kBlockTokens < g.maxb;
+        // the angle row is read beside the page entry, not after it
+        float4 cs[4];
+        if (is_k && pos_ok) {
+            const long long a = static_cast<long long>(pos) * (g.d / 2) + c8;
+            const float4* ct = reinterpret_cast<const float4*>(cos_tab + a);
+            const float4* st = reinterpret_cast<const float4*>(sin_tab + a);
+            cs[0] = __ldg(ct);
+            cs[1] = __ldg(ct + 1);
+            cs[2] = __ldg(st);
+            cs[3] = __ldg(st + 1);
+        }
         long long blk = -1;
-        if (slot >= 0 && slot < g.num_slots && pos >= 0 && pos < max_pos && pos / kBlockTokens < g.maxb) {
+        if (slot >= 0 && slot < g.num_slots && pos_ok) {
             const long long tidx =
                 (static_cast<long long>(slot) * g.n_layers + layer) * g.maxb + pos / kBlockTokens;
             const int e = __ldg(block_table + tidx);
             if (e >= 0 && e < g.nblocks) blk = e;
         }
         if (blk < 0) {
-            if (rem == 0) set_error(err, PA_ERR_BAD_BLOCK);
+            if (rem == local * kt) set_error(err, PA_ERR_BAD_BLOCK);  // the row's first K thread
             continue;
         }
         uint8_t* dst_row = pool + blk * g.page_bytes + static_cast<long long>(pos % kBlockTokens) * row_bytes;
         if (is_k) {
-            const float4* ct = reinterpret_cast<const float4*>(cos_tab + static_cast<long long>(pos) * (g.d / 2) + 8 * c);
-            const float4* st = reinterpret_cast<const float4*>(sin_tab + static_cast<long long>(pos) * (g.d / 2) + 8 * c);
-            rope8(lo, hi, __ldg(ct), __ldg(ct + 1), __ldg(st), __ldg(st + 1));
-            *reinterpret_cast<uint4*>(dst_row + e_lo * 2) = lo;
-            *reinterpret_cast<uint4*>(dst_row + e_hi * 2) = hi;
+#pragma unroll
+            for (int x = 0; x < KPT; ++x) {
+                const long long e_lo = static_cast<long long>(c / hc + x * (g.hkv / KPT)) * g.d + c8;
+                rope8(lo[x], hi[x], cs[0], cs[1], cs[2], cs[3]);
+                *reinterpret_cast<uint4*>(dst_row + e_lo * 2) = lo[x];
+                *reinterpret_cast<uint4*>(dst_row + (e_lo + g.d / 2) * 2) = hi[x];
+            }
         } else {
             uint4* dv = reinterpret_cast<uint4*>(dst_row + half_page) + c;
 #pragma unroll
@@ -177,12 +204,17 @@ cudaError_t launch_write_kv_rope(const KGeom& g, void* pool, const int32_t* bloc
                                  int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,
                                  const void* k_new, const void* v_new, const float* cos_tab,
                                  const float* sin_tab, int max_pos, int32_t* err, cudaStream_t stream) {
-    const int vpt = (g.kv_dim / 8) % 4 == 0 ? 4 : 1;
-    const long long total = static_cast<long long>(n_tokens) * (g.kv_dim / 16 + g.kv_dim / 8 / vpt);
+    // two heads' pairs and four V chunks per thread when the kv head count is
+    // even (d a multiple of 16 then makes the V chunk count a multiple of 4)
+    const bool wide = g.hkv % 2 == 0;
+    const int hc = g.d / 16;
+    const int per_group = wide ? kRopeRows * (g.hkv / 2 * hc + g.kv_dim / 32)
+                               : kRopeRows * (g.hkv * hc + g.kv_dim / 16);
+    const long long total = static_cast<long long>((n_tokens + kRopeRows - 1) / kRopeRows) * per_group;
     const int threads = 256;
     long long blocks = (total + threads - 1) / threads;
     if (blocks > (1ll << 30)) blocks = 1ll << 30;  // grid-stride covers the rest
-    auto kern = vpt == 4 ? write_kv_rope_kernel<4> : write_kv_rope_kernel<1>;
+    auto kern = wide ? write_kv_rope_kernel<2, 4> : write_kv_rope_kernel<1, 2>;
     kern<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), cos_tab, sin_tab, max_pos, err);
