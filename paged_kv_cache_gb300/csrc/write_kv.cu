@@ -206,15 +206,14 @@ cudaError_t launch_write_kv_rope(const KGeom& g, void* pool, const int32_t* bloc
                                  const float* sin_tab, int max_pos, int32_t* err, cudaStream_t stream) {
     // two heads' pairs and four V chunks per thread when the kv head count is
     // even (d a multiple of 16 then makes the V chunk count a multiple of 4)
-    const bool wide = g.hkv % 2 == 0;
+    const int kpt = g.hkv % 4 == 0 ? 4 : g.hkv % 2 == 0 ? 2 : 1;
     const int hc = g.d / 16;
-    const int per_group = wide ? kRopeRows * (g.hkv / 2 * hc + g.kv_dim / 32)
-                               : kRopeRows * (g.hkv * hc + g.kv_dim / 16);
+    const int per_group = kRopeRows * (g.hkv / kpt * hc + g.kv_dim / 8 / (2 * kpt));
     const long long total = static_cast<long long>((n_tokens + kRopeRows - 1) / kRopeRows) * per_group;
     const int threads = 256;
     long long blocks = (total + threads - 1) / threads;
     if (blocks > (1ll << 30)) blocks = 1ll << 30;  // grid-stride covers the rest
-    auto kern = wide ? write_kv_rope_kernel<2, 4> : write_kv_rope_kernel<1, 2>;
+    auto kern = kpt == 4 ? write_kv_rope_kernel<4, 8> : kpt == 2 ? write_kv_rope_kernel<2, 4> : write_kv_rope_kernel<1, 2>;
     kern<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), cos_tab, sin_tab, max_pos, err);

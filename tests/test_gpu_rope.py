@@ -37,6 +37,8 @@ def run_both(case, cos_t, sin_t, positions=None):
     (32, 8, 64, [17, 512]),     # the Llama-3.2-1B layout
     (16, 4, 128, [300, 45]),    # head dim 128
     (8, 1, 64, [1, 77, 16]),    # one kv head
+    (12, 6, 64, [33, 100]),     # two heads per K thread
+    (6, 3, 32, [50, 9]),        # odd kv head count: one head per K thread
 ])
 def test_rope_scatter_is_byte_exact(hq, hkv, d, lens):
     case = prompt_case(hq, hkv, d, lens, seed=hq + d)
