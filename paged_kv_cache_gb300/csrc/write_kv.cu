@@ -204,8 +204,9 @@ cudaError_t launch_write_kv_rope(const KGeom& g, void* pool, const int32_t* bloc
                                  int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,
                                  const void* k_new, const void* v_new, const float* cos_tab,
                                  const float* sin_tab, int max_pos, int32_t* err, cudaStream_t stream) {
-    // two heads' pairs and four V chunks per thread when the kv head count is
-    // even (d a multiple of 16 then makes the V chunk count a multiple of 4)
+    // KPT heads' pairs and 2 KPT V chunks per thread: KPT divides the kv head
+    // count, and d a multiple of 16 makes the V chunk count (2 Hkv d/16) a
+    // multiple of 2 KPT
     const int kpt = g.hkv % 4 == 0 ? 4 : g.hkv % 2 == 0 ? 2 : 1;
     const int hc = g.d / 16;
     const int per_group = kRopeRows * (g.hkv / kpt * hc + g.kv_dim / 8 / (2 * kpt));
