@@ -19,6 +19,9 @@ decode's 4 d Hq n).  The line also carries:
                   same for 64 sequences of 128..2048 tokens;
   scatter      -- pa_write_kv and pa_write_kv_rope GB/s on the prompt rows
                   against the measured HBM copy bandwidth;
+  llama_prompts -- pa_prefill of the Llama-3.2-1B-shaped prompts (17 and 512
+                  tokens, K/V scattered at layers 0 and 15): latency-bound,
+                  reported with its own oracle baseline;
   chunked      -- pa_prefill_cached: 4 x 2048-query chunks after 6144 cached
                   tokens, exact-causal TFLOP/s against the same bf16 peak;
   backward     -- pa_prefill_backward on the long prompt (4 x 8192, d 64;
@@ -29,7 +32,11 @@ decode's 4 d Hq n).  The line also carries:
                   timed region, neighbouring steps' copies overlapping the
                   compute (and, as "serial", without that overlap);
   cpu_baseline -- the fp64 CPU oracle timed on a bounded sample of the same
-                  workload on this host's cores.
+                  workload on this host's cores (and, inside the decode and
+                  llama_prompts legs, on samples of those workloads);
+  gates        -- last key of the line: each bar's fraction of its measured
+                  peak (prefill d 64 / d 128 against 0.55, the two decode
+                  batches against 0.75).
 N > 1 (torchrun): independent replicas, one per GPU, no collective on the
 data path ("weak" scaling); timing is the max over ranks.
 ``--impl reference`` times the CPU oracle itself as the reference arm.
@@ -64,7 +71,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time (10-30 s)")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "chunked", "scatter", "pages", "backward"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "llama", "decode", "chunked", "scatter", "pages", "backward"],
+                    default="all",
                     help="profiling aid: run only the main (prefill) step or only the decode step")
     ap.add_argument("--batch", type=int, default=4, help="prefill sequences (profiling aid)")
     ap.add_argument("--seqlen", type=int, default=8192, help="prefill length (profiling aid)")
@@ -105,6 +113,7 @@ TRAFFIC_SOURCES = {
     "chunked": ("prefill.cu", "pa_internal.cuh", "api.cu"),
     "decode": ("decode.cu", "pa_internal.cuh", "api.cu"),
     "backward": ("backward.cu", "backward_tc.cu", "pa_internal.cuh", "api.cu"),
+    "scatter": ("write_kv.cu", "pa_internal.cuh", "api.cu"),
 }
 
 
@@ -375,6 +384,40 @@ class BackwardStep:
             ev[0].record()
         pa.pa_prefill_backward(self.g, d["q"], self.pool, d["bt"], 0, d["cu"], d["slots"], c.max_len, c.scale,
                                self.o, self.lse, self.dout, self.delta, self.dq, self.dk, self.dv, self.err)
+        if ev is not None:
+            ev[1].record()
+
+
+class LlamaPromptStep:
+    """Prefill of the Llama-3.2-1B-shaped prompts (2 slots, 17 and 512 tokens,
+    32 q / 8 kv heads, d 64, 2 GiB pool, table [2][16][128]): a step scatters
+    both prompts' K/V at layers 0 and 15 and runs pa_prefill at layer 15.
+    Exact causal FLOPs 4 d Hq sum n (n + 1) / 2 = 1.077 GFLOP: a
+    latency-bound call, reported beside the long prefill, not against its bar."""
+
+    def __init__(self, torch, pa, W):
+        self.torch, self.pa = torch, pa
+        self.case = c = W.llama_prefill_case()
+        self.g = pa.geom(*c.geom.as_tuple())
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        self.d = {"q": dev(c.q), "bt": dev(c.block_table), "cu": dev(c.cu_seqlens), "slots": dev(c.slots)}
+        self.w = [(w.layer, dev(w.tok_slot), dev(w.tok_pos), dev(w.k), dev(w.v)) for w in c.writes]
+        self.pool = torch.empty(c.geom.pool_bytes, dtype=torch.uint8, device="cuda")
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        T, Hq, D = c.total_tokens, c.geom.num_q_heads, c.geom.head_dim
+        self.o = torch.empty((T, Hq, D), dtype=torch.int16, device="cuda")
+        self.lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+        self.flops = causal_flops(D, Hq, c.lens)
+        self.write_bytes = float(sum(w.k.size * 2 * 2 * 2 for w in c.writes))  # K and V, read and written
+
+    def run(self, ev=None):
+        pa, c, d = self.pa, self.case, self.d
+        for layer, ts, tp, k, v in self.w:
+            pa.pa_write_kv(self.g, self.pool, d["bt"], layer, ts, tp, k, v, self.err)
+        if ev is not None:
+            ev[0].record()
+        pa.pa_prefill(self.g, d["q"], self.pool, d["bt"], c.layer, d["cu"], d["slots"], c.max_len, c.scale,
+                      self.o, self.lse, self.err)
         if ev is not None:
             ev[1].record()
 
@@ -672,6 +715,69 @@ def oracle_sample(case, seconds, rng_seed=5):
     return flops, wall, threads, desc
 
 
+def oracle_decode_sample(lens, seconds, what, seed, budget_bytes=64 << 20):
+    """Times the oracle's decode (fp64, K/V gathered through the block table)
+    on the leading sequences of a decode batch -- their lengths, 32 q / 8 kv
+    heads, d 64, Q/K/V drawn from N(0, 1) in bf16, pages shuffled -- as many
+    as hold about budget_bytes of K/V, the call repeated until it has taken
+    about `seconds`.  Returns (KV bytes read, wall seconds, threads,
+    description)."""
+    import oracle
+    from paged_kv_cache_gb300 import workloads as W
+    kv_row = 2 * 8 * 64 * 2  # K and V rows of one token, bytes
+    k = 1
+    while k < lens.shape[0] and float(np.sum(lens[:k + 1].astype(np.float64))) * kv_row <= budget_bytes:
+        k += 1
+    sub = lens[:k]
+    pages = int(np.sum((sub.astype(np.int64) + 15) // 16))
+    geom = W.Geometry(32, 8, 64, 1, k, int(max(1, (int(sub.max()) + 15) // 16)), pages + 8)
+    case = W.make_decode_case("cpu_" + what, geom, sub, seed, scale=0.125, pool_fill="zero")
+    g = oracle.geom(*geom.as_tuple())
+    pool = W.initial_pool(geom, "zero", 0)
+    for w in case.writes:
+        oracle.write_kv(g, pool, case.block_table, w.layer, w.tok_slot, w.tok_pos, w.k, w.v)
+    run = lambda: oracle.decode(g, case.q, pool, case.block_table, 0, case.lens, case.slots, case.scale)[0]
+    t0 = time.perf_counter()
+    assert run() == 0
+    dt = time.perf_counter() - t0
+    reps = int(min(50, max(1, math.ceil(seconds / max(dt, 1e-3)))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        assert run() == 0
+    wall = time.perf_counter() - t0
+    nbytes = float(np.sum(sub.astype(np.float64))) * kv_row * reps
+    desc = ("decode of the first %d of the %d sequences (%.1f MB of K/V), %d calls, fp64 oracle, K/V gathered "
+            "through the block table, %d threads" % (k, lens.shape[0], nbytes / reps / 1e6, reps,
+                                                     oracle.default_threads()))
+    return nbytes, wall, oracle.default_threads(), desc
+
+
+def oracle_llama_sample(case, seconds):
+    """Times the oracle's whole prefill of the Llama-3.2-1B-shaped prompts
+    (17 and 512 tokens, every row and head), repeated until it has taken
+    about `seconds`.  Returns (FLOPs, wall seconds, threads, description)."""
+    import oracle
+    from paged_kv_cache_gb300 import workloads as W
+    g = oracle.geom(*case.geom.as_tuple())
+    pool = W.initial_pool(case.geom, "zero", 0)
+    for w in case.writes:
+        oracle.write_kv(g, pool, case.block_table, w.layer, w.tok_slot, w.tok_pos, w.k, w.v)
+    run = lambda: oracle.prefill(g, case.q, pool, case.block_table, case.layer, case.cu_seqlens, case.slots,
+                                 case.scale)[0]
+    t0 = time.perf_counter()
+    assert run() == 0
+    dt = time.perf_counter() - t0
+    reps = int(min(50, max(1, math.ceil(seconds / max(dt, 1e-3)))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        assert run() == 0
+    wall = time.perf_counter() - t0
+    flops = causal_flops(case.geom.head_dim, case.geom.num_q_heads, case.lens) * reps
+    desc = ("whole prefill of the prompts of 17 and 512 tokens (every row and q head), %d calls, fp64 oracle, "
+            "%d threads" % (reps, oracle.default_threads()))
+    return flops, wall, oracle.default_threads(), desc
+
+
 # ------------------------------------------------------------------- arms
 
 METRIC = "causal prefill TFLOP/s (exact causal count, step incl. KV write + decode)"
@@ -806,6 +912,30 @@ def main():
                          "algorithmic_flops_per_launch": ostep.flops_prefill, "avg_launch_ms": o_avg * 1e3}}
         del ostep
 
+    llama = None
+    if args.only in ("all", "llama"):
+        # ------------- Llama-3.2-1B-shaped prompts (17 and 512 tokens), layers 0 and 15
+        lstep = LlamaPromptStep(torch, pa, W)
+        lsteps = max(20, args.steps)
+        l_s, lk_s = timed(torch, lambda ev: lstep.run(ev=ev), lsteps, args.warmup, flush, dist)
+        torch.cuda.synchronize()
+        if int(lstep.err.item()) != 0:
+            raise SystemExit("device error in the Llama prompt steps: %s" % pa.pa_status_string(int(lstep.err.item())))
+        l_avg = float(np.mean(lk_s))
+        bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        l_rate, l_total, _ = job_rate(torch, dist, lstep.flops * lsteps, float(np.sum(lk_s)))
+        llama = {"metric": "causal prefill TFLOP/s of the Llama-3.2-1B-shaped prompts (17 and 512 tokens, "
+                           "32 q / 8 kv heads, d 64; K/V scattered at layers 0 and 15, prefill at 15); "
+                           "latency-bound, not the long-prefill bar",
+                 "value": l_rate / 1e12, "unit": "TFLOP/s", "steps": lsteps,
+                 "step_ms": float(np.mean(l_s)) * 1e3,
+                 "roofline": {"bound": "tensor", "achieved": lstep.flops / l_avg / 1e12, "peak": bf16_peak,
+                              "unit": "TFLOP/s", "frac": lstep.flops / l_avg / 1e12 / bf16_peak,
+                              "kernel": "prefill_kernel<64, 4>", "peak_source": "%s bf16_tflops (burst)" % peak_src,
+                              "algorithmic_flops_per_launch": lstep.flops, "avg_launch_ms": l_avg * 1e3}}
+        llama_case = lstep.case
+        del lstep
+
     if args.only in ("all", "decode"):
         # ------------------- decode (256 sequences, log-normal lengths)
         dstep = DecodeStep(torch, pa, W)
@@ -890,7 +1020,7 @@ def main():
             scatter[name] = {"value": s_rate / 1e9, "unit": "GB/s",
                              "roofline": {"bound": "hbm", "achieved": nbytes / s_avg / 1e9, "peak": hbm_peak,
                                           "unit": "GB/s", "frac": nbytes / s_avg / 1e9 / hbm_peak,
-                                          "traffic": None,
+                                          "traffic": profiled_traffic("scatter_" + name),
                                           "kernel": "write_kv_rope_kernel" if rope else "write_kv_kernel",
                                           "peak_source": "%s hbm_gbs" % peak_src,
                                           "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": s_avg * 1e3}}
@@ -942,9 +1072,22 @@ def main():
         flops, wall, threads, desc = oracle_sample(step.case, args.cpu_seconds)
         cpu = {"value": flops / wall / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": desc, "seconds": wall}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        side = max(2.0, args.cpu_seconds / 4)
+        if decode is not None:
+            for leg, lens, seed in ((decode, W.lognormal_decode_lens(), 1104),
+                                    (decode["batch64"], W.uniform_decode_lens(), 1102)):
+                nbytes, wall, threads, desc = oracle_decode_sample(lens, side, "decode", seed)
+                leg["cpu_baseline"] = {"value": nbytes / wall / 1e9, "unit": "GB/s", "cores": threads,
+                                       "kind": "oracle", "sample": desc, "seconds": wall}
+        if llama is not None:
+            flops, wall, threads, desc = oracle_llama_sample(llama_case, side)
+            llama["cpu_baseline"] = {"value": flops / wall / 1e12, "unit": "TFLOP/s", "cores": threads,
+                                     "kind": "oracle", "sample": desc, "seconds": wall}
 
     if rank == 0 and step is None:
-        print(json.dumps({"metric": "%s only (profiling aid)" % args.only, "decode": decode, "chunked": chunked,
+        print(json.dumps({"metric": "%s only (profiling aid)" % args.only, "llama_prompts": llama, "decode": decode,
+                          "chunked": chunked,
                           "scatter": scatter, "pages": pages, "backward": backward, "clocks": clk}), flush=True)
     elif rank == 0:
         line = {
@@ -966,6 +1109,18 @@ def main():
             "clocks": clk,
             "kernel_source": kernel_source_hash(),
         }
+        # the bars, compactly, at the very end of the line: each row's fraction
+        # of its measured peak beside the bar it is held to
+        gates = {"prefill_bar": 0.55, "decode_bar": 0.75,
+                 "prefill_" + args.variant: round(roofline["frac"], 4)}
+        if other_variant is not None:
+            gates["prefill_" + ("d128" if args.variant == "d64" else "d64")] = round(
+                other_variant["roofline"]["frac"], 4)
+        if decode is not None:
+            gates["decode_256seq"] = round(decode["roofline"]["frac"], 4)
+            gates["decode_64seq"] = round(decode["batch64"]["roofline"]["frac"], 4)
+        line["llama_prompts"] = llama
+        line["gates"] = gates
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

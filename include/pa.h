@@ -280,7 +280,13 @@ pa_status pa_decode(const pa_geom* geom, const void* q, const void* pool,
  *     PA_ERR_UNSUPPORTED before anything is enqueued (use pa_decode then).
  *   - Set-up: the first call on each device (with that device current) looks
  *     up the scratch array's device address; make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept for the life of the process: after
+ *     a cudaDeviceReset (or anything else that destroys and re-creates the
+ *     device's primary context) the kept address is stale, so do not call
+ *     pa_decode_noalloc on that device again in the same process.
+ *   - Checks: the arguments are checked exactly as pa_decode checks them
+ *     (same status codes, an empty batch is a no-op) before the size check
+ *     and the set-up.
  *   - Sharing: every call on a device uses the same scratch, which keeps the
  *     previous call's contents (nothing in it needs to start at zero).  Calls
  *     that can overlap on the GPU -- on different streams without ordering,
@@ -312,14 +318,19 @@ pa_status pa_decode_noalloc(const pa_geom* geom, const void* q, const void* pool
  * for 0).  All or nothing: if the stack holds fewer pages than needed, nothing
  * changes and *err_flag gets PA_ERR_OUT_OF_PAGES; an invalid slot or length
  * sets PA_ERR_BAD_BLOCK, also with nothing changed, as does a slot named
- * twice in one call (checked for slots below 65536).  slots, seq_lens: device
- * int32 [batch]; block_table: device, the layout of pa_write_kv.
+ * twice in one call.  slots, seq_lens: device int32 [batch]; block_table:
+ * device, the layout of pa_write_kv.  Both calls require geom->num_slots <=
+ * PA_PAGES_MAX_SLOTS (else PA_ERR_UNSUPPORTED before anything is enqueued):
+ * the kernels keep one bit per slot in shared memory to refuse a slot named
+ * twice.
  *
  * pa_release_slots -- every page held by slots[0 .. n-1], in every layer, goes
  * back on the stack in the same walking order and its entry becomes -1 (the
  * pages' slot-end loop).  Nothing changes (PA_ERR_OUT_OF_PAGES) if the stack
  * would grow past num_blocks, which means a page was freed twice.
  */
+#define PA_PAGES_MAX_SLOTS 65536
+
 pa_status pa_alloc_pages(const pa_geom* geom, int32_t* block_table, int32_t batch,
                          const int32_t* slots, const int32_t* old_lens, const int32_t* seq_lens,
                          int32_t* free_pages, int32_t* free_count, int32_t* err_flag,

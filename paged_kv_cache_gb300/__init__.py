@@ -39,6 +39,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libpa.so")
 EXPORTED = ("pa_page_bytes", "pa_write_kv", "pa_write_kv_rope", "pa_prefill", "pa_prefill_cached", "pa_prefill_backward", "pa_decode_workspace_size", "pa_decode",
             "pa_decode_noalloc", "pa_alloc_pages", "pa_release_slots", "pa_status_string")
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
+PA_PAGES_MAX_SLOTS = 65536
 
 
 class PaGeom(C.Structure):

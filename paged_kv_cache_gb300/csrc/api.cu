@@ -181,21 +181,39 @@ PA_API size_t pa_decode_workspace_size(const pa_geom* geom, int32_t batch, int32
     return pa::decode_workspace_bytes(kgeom(geom), batch, max_seq_len);
 }
 
+namespace pa {
+// Every check of pa_decode except those on the workspace, in the same order
+// (shared with pa_decode_noalloc); *no_work is set when the call has nothing
+// to enqueue (an empty batch) and the status is PA_OK.
+pa_status decode_args(const pa_geom* geom, const void* q, const void* pool, const int32_t* block_table,
+                      int32_t layer, int32_t batch, const int32_t* seq_lens, const int32_t* slots,
+                      int32_t max_seq_len, float scale, const void* o, const int32_t* err_flag, bool* no_work) {
+    *no_work = false;
+    if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= geom->n_layers) return PA_ERR_INVALID_ARG;
+    if (batch < 0 || max_seq_len < 0 || !std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
+    if (!decode_supported(kgeom(geom))) return PA_ERR_UNSUPPORTED;
+    if (batch == 0) {
+        *no_work = true;
+        return PA_OK;
+    }
+    if (!q || !pool || !block_table || !seq_lens || !slots || !o || !err_flag) return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o) || !aligned16(pool)) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+}  // namespace pa
+
 PA_API pa_status pa_decode(const pa_geom* geom, const void* q, const void* pool,
                            const int32_t* block_table, int32_t layer, int32_t batch,
                            const int32_t* seq_lens, const int32_t* slots, int32_t max_seq_len,
                            float scale, void* o, float* lse, void* workspace,
                            size_t workspace_bytes, int32_t* err_flag, pa_stream_t stream) {
-    if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
-    if (layer < 0 || layer >= geom->n_layers) return PA_ERR_INVALID_ARG;
-    if (batch < 0 || max_seq_len < 0 || !std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
+    bool no_work = false;
+    const pa_status st = pa::decode_args(geom, q, pool, block_table, layer, batch, seq_lens, slots, max_seq_len,
+                                         scale, o, err_flag, &no_work);
+    if (st != PA_OK || no_work) return st;
     const pa::KGeom g = kgeom(geom);
-    if (!pa::decode_supported(g)) return PA_ERR_UNSUPPORTED;
-    if (batch == 0) return PA_OK;
-    if (!q || !pool || !block_table || !seq_lens || !slots || !o || !workspace || !err_flag)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(o) || !aligned16(pool) || !aligned16(workspace))
-        return PA_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
     if (workspace_bytes < pa::decode_workspace_bytes(g, batch, max_seq_len))
         return PA_ERR_INVALID_ARG;
     return cuda_status(pa::launch_decode(g, q, pool, block_table, layer, batch, seq_lens, slots,
@@ -208,6 +226,7 @@ PA_API pa_status pa_alloc_pages(const pa_geom* geom, int32_t* block_table, int32
                                 int32_t* free_pages, int32_t* free_count, int32_t* err_flag,
                                 pa_stream_t stream) {
     if (!geom_valid(geom) || batch < 0) return PA_ERR_INVALID_ARG;
+    if (geom->num_slots > PA_PAGES_MAX_SLOTS) return PA_ERR_UNSUPPORTED;
     if (!block_table || !free_pages || !free_count || !err_flag) return PA_ERR_INVALID_ARG;
     if (batch > 0 && (!slots || !seq_lens)) return PA_ERR_INVALID_ARG;
     if (batch == 0) return PA_OK;
@@ -220,6 +239,7 @@ PA_API pa_status pa_release_slots(const pa_geom* geom, int32_t* block_table, int
                                   const int32_t* slots, int32_t* free_pages, int32_t* free_count,
                                   int32_t* err_flag, pa_stream_t stream) {
     if (!geom_valid(geom) || n < 0) return PA_ERR_INVALID_ARG;
+    if (geom->num_slots > PA_PAGES_MAX_SLOTS) return PA_ERR_UNSUPPORTED;
     if (!block_table || !free_pages || !free_count || !err_flag) return PA_ERR_INVALID_ARG;
     if (n > 0 && !slots) return PA_ERR_INVALID_ARG;
     if (n == 0) return PA_OK;

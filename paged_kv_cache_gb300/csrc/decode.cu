@@ -903,6 +903,12 @@ extern "C" __attribute__((visibility("default"))) pa_status pa_decode_noalloc(
     const pa_geom* geom, const void* q, const void* pool, const int32_t* block_table, int32_t layer,
     int32_t batch, const int32_t* seq_lens, const int32_t* slots, int32_t max_seq_len, float scale,
     void* o, float* lse, int32_t* err_flag, pa_stream_t stream) {
+    // the arguments are checked as pa_decode checks them before the scratch
+    // lookup (a runtime call), so a bad call returns the same status
+    bool no_work = false;
+    const pa_status st = pa::decode_args(geom, q, pool, block_table, layer, batch, seq_lens, slots, max_seq_len,
+                                         scale, o, err_flag, &no_work);
+    if (st != PA_OK || no_work) return st;
     if (pa_decode_workspace_size(geom, batch, max_seq_len) > pa::kStaticScratchBytes)
         return PA_ERR_UNSUPPORTED;
     void* scratch = nullptr;

@@ -456,7 +456,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Two floats -> packed bf16x2, round to nearest even; `lo` in the low half.
 // One 32-byte store (a whole sector); the address must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
@@ -464,6 +463,7 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
                  : "memory");
 }
 
+// Two floats -> packed bf16x2, round to nearest even; `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -558,6 +558,9 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool,
                            void* o, float* lse, int32_t* err, cudaStream_t stream);
 
 size_t decode_workspace_bytes(const KGeom& g, int batch, int max_seq_len);
+pa_status decode_args(const pa_geom* geom, const void* q, const void* pool, const int32_t* block_table,
+                      int32_t layer, int32_t batch, const int32_t* seq_lens, const int32_t* slots,
+                      int32_t max_seq_len, float scale, const void* o, const int32_t* err_flag, bool* no_work);
 bool decode_supported(const KGeom& g);
 cudaError_t launch_prefill_backward(const KGeom& g, const void* q, const void* pool, const int32_t* bt,
                                     int layer, int batch, const int32_t* cu, const int32_t* slots,

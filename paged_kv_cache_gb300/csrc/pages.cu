@@ -26,12 +26,14 @@ namespace pa {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kSlotBitmapWords = 2048;  // slots seen by a call: duplicates are refused (65536 slots)
+// One bit per slot a call names, so that a slot named twice is refused; the
+// C ABI refuses geometries with more slots than the bitmap covers.
+constexpr int kSlotBitmapWords = PA_PAGES_MAX_SLOTS / 32;
+static_assert(kSlotBitmapWords * 32 == PA_PAGES_MAX_SLOTS, "one bit per slot");
 
-// Marks slot as seen; returns true if it already was.  Slots past the bitmap
-// are not checked.
+// Marks slot (already checked to lie in [0, num_slots)) as seen; returns true
+// if it already was.
 __device__ __forceinline__ bool seen_before(uint32_t* bitmap, int slot) {
-    if (slot >= kSlotBitmapWords * 32) return false;
     const uint32_t bit = 1u << (slot & 31);
     return (atomicOr(&bitmap[slot >> 5], bit) & bit) != 0;
 }

@@ -114,6 +114,29 @@ def test_validation_without_gpu(lib):
                          NULL) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_decode(C.byref(g), NULL, NULL, NULL, 0, 0, NULL, NULL, 4, C.c_float(0.1), NULL, NULL,
                          NULL, 0, NULL, NULL) == pa.PA_OK  # empty batch
+    # the allocation-free decode answers the same way, before its scratch lookup (a CUDA call)
+    nd = lambda gg, layer, batch, sc, ptr=NULL: lib.pa_decode_noalloc(
+        gg, ptr, ptr, ptr, layer, batch, ptr, ptr, 64, C.c_float(sc), ptr, NULL, ptr, NULL)
+    assert nd(NULL, 0, 1, 0.1) == pa.PA_ERR_INVALID_ARG
+    assert nd(C.byref(g), 3, 1, 0.1) == pa.PA_ERR_INVALID_ARG      # layer out of range
+    assert nd(C.byref(g), 0, 1, 0.0) == pa.PA_ERR_INVALID_ARG      # scale
+    assert nd(C.byref(g3), 0, 1, 0.1) == pa.PA_ERR_UNSUPPORTED
+    assert nd(C.byref(g), 0, 0, 0.1) == pa.PA_OK                   # empty batch
+    assert nd(C.byref(g), 0, 1, 0.1) == pa.PA_ERR_INVALID_ARG      # null pointers
+    assert nd(C.byref(g), 0, 1, 0.1, ptr=24) == pa.PA_ERR_INVALID_ARG  # 8-byte aligned tensors
+
+
+def test_page_calls_refuse_more_slots_than_the_duplicate_check_covers(lib):
+    """The page kernels keep one shared-memory bit per slot to refuse a slot
+    named twice; a geometry with more slots is refused up front."""
+    NULL = None
+    big = pa.geom(8, 2, 64, 1, pa.PA_PAGES_MAX_SLOTS + 1, 4, 8)
+    ok = pa.geom(8, 2, 64, 1, pa.PA_PAGES_MAX_SLOTS, 4, 8)
+    assert lib.pa_alloc_pages(C.byref(big), 16, 1, 16, NULL, 16, 16, 16, 16, NULL) == pa.PA_ERR_UNSUPPORTED
+    assert lib.pa_release_slots(C.byref(big), 16, 1, 16, 16, 16, 16, NULL) == pa.PA_ERR_UNSUPPORTED
+    # at the limit the call goes on to its pointer checks (nothing enqueued here)
+    assert lib.pa_alloc_pages(C.byref(ok), NULL, 1, 16, NULL, 16, 16, 16, 16, NULL) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_release_slots(C.byref(ok), NULL, 1, 16, 16, 16, 16, NULL) == pa.PA_ERR_INVALID_ARG
 
 
 def test_missing_library_fails_loudly(tmp_path):

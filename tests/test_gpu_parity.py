@@ -101,7 +101,12 @@ def _sample_rows(case, rng, n_random=160):
 
 
 @pytest.mark.parametrize("variant", ["d64", "d128"])
-def test_long_prefill_sampled(variant):
+def test_long_prefill_sampled_and_one_whole_sequence(variant):
+    """The 4 x 8192 bench workload in the bench's launch configuration: every
+    output finite and bounded by max|V|; sampled (row, head) outputs of all
+    four sequences, and every (row, q head) output of the last sequence (all
+    64 row tiles x every head, so each tile position of the heaviest-first
+    grid and each head of each CTA's group is compared), against the oracle."""
     case = W.long_prefill_case(variant)
     pool, bt, werr = H.gpu_setup(case)
     assert werr == 0
@@ -117,6 +122,16 @@ def test_long_prefill_sampled(variant):
                                      case.cu_seqlens, case.slots, case.scale, rows, heads)
     assert st == 0
     H.assert_close(o[rows, heads], l[rows, heads], ro, rl, vmax, "c4 " + variant)
+    # every output of the last sequence
+    b = case.batch - 1
+    Hq = case.geom.num_q_heads
+    seq_rows = np.arange(case.cu_seqlens[b], case.cu_seqlens[b + 1], dtype=np.int64)
+    rows = np.repeat(seq_rows, Hq)
+    heads = np.tile(np.arange(Hq, dtype=np.int32), seq_rows.shape[0])
+    st, ro, rl = oracle.prefill_rows(H.oracle_geom(case), case.q, ref_pool, case.block_table, 0,
+                                     case.cu_seqlens, case.slots, case.scale, rows, heads)
+    assert st == 0
+    H.assert_close(o[rows, heads], l[rows, heads], ro, rl, vmax, "c4 %s, sequence %d, every output" % (variant, b))
 
 
 # ------------------------------------ 256-sequence mixed decode batch
@@ -365,7 +380,8 @@ def test_growing_scores_move_the_reference_max(kind):
 @pytest.mark.parametrize("kind", ["prefill", "decode"])
 def test_large_score_jump(kind):
     """Keys from position 300 on are 40x larger: the tile max jumps by far more
-    than 2^64 over the running max (the redo path of the prefill softmax)."""
+    than 2^64 over the running max: one large move of the reference max, whose
+rescale factor for l and O is tiny (it may flush to zero)."""
     geom = W.Geometry(8, 2, 64, 1, 2, 64, 80)
     lens = [520, 310]
     mk = W.make_prefill_case if kind == "prefill" else W.make_decode_case

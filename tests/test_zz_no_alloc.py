@@ -6,10 +6,11 @@ a serving loop that must not call cudaMalloc (it can synchronise the device)
 between steps.  pa_decode_noalloc keeps the split partials in a fixed scratch
 array inside the library instead.  This test calls it through the C ABI twice
 in a row, on two different batches, and checks each result against pa_decode
-with a caller workspace on the same inputs, at the parity tolerance of the
-other GPU tests.  It lives in its own file, collected last, and passes both in
-a fresh process (the first call does the per-device set-up) and after the
-other tests.
+with a caller workspace on the same inputs -- the same kernels with the same
+split, so bit for bit -- and against the CPU oracle at the parity tolerance
+of the other GPU tests.  It lives in its own file, collected last, and passes
+both in a fresh process (the first call does the per-device set-up) and after
+the other tests.
 """
 import numpy as np
 import pytest
@@ -41,10 +42,14 @@ def test_no_alloc_decode_matches_workspace_decode_twice():
     for case in (first, second):
         pool, bt, werr = H.gpu_setup(case)
         assert werr == 0
-        o_ref, l_ref, err_ref = H.gpu_decode(case, pool, bt)  # caller-provided workspace
+        o_ws, l_ws, err_ws = H.gpu_decode(case, pool, bt)  # caller-provided workspace
         o, l, err = _noalloc(case, pool, bt)
-        assert err_ref == 0 and err == 0
-        H.assert_close(o, l, o_ref, l_ref, H.max_abs_v(case), "noalloc " + case.name)
+        assert err_ws == 0 and err == 0
+        # the same kernels and the same split on the same inputs: identical bits
+        assert np.array_equal(o, o_ws), "noalloc %s: o differs from pa_decode" % case.name
+        assert np.array_equal(l, l_ws), "noalloc %s: lse differs from pa_decode" % case.name
+        ro, rl = H.oracle_decode(case, H.oracle_pool(case))
+        H.assert_close(o, l, ro, rl, H.max_abs_v(case), "noalloc " + case.name)
 
 
 def test_no_alloc_rejects_requests_beyond_the_scratch():
