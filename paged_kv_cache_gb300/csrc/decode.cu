@@ -510,13 +510,12 @@ __device__ SeqSpan seq_span(const DecodeParams& p, int b, long long G, long long
 // for empty sequences.  One CTA per (sequence, 8 q heads), one warp per head.
 // Launched as a programmatic dependent of the attend kernel: the span of the
 // sequence comes from the lengths before griddepcontrol.wait, and everything
-// the attend kernel writes is read after it, in one round of loads where the
-// sequence has at most kMergeBatch pieces: lane k takes piece k's L for the
-// max and the weights of the LSE rule while every lane loads its dims of the
-// pieces' rows.
+// the attend kernel writes is read after it, in one round of loads per
+// kMergeBatch pieces: lane k takes piece k's L for the max and the weights of
+// the LSE rule while every lane loads its dims of the pieces' rows.
 constexpr int kMergeHeadsPerCta = 8;
 constexpr int kMergeThreads = 32 * kMergeHeadsPerCta;
-constexpr int kMergeBatch = 8;
+constexpr int kMergeBatch = 16;  // pieces whose loads are all in flight at once
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
@@ -563,53 +562,37 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
     float M = -CUDART_INF_F;
-    if (P <= kMergeBatch) {
-        // every load at once: the pieces' rows, and lane k's L
-        float v[kMergeBatch][PER];
-#pragma unroll
-        for (int k = 0; k < kMergeBatch; ++k)
-            if (k < P) load_row(sp.c0 + k, v[k]);
-        const bool mine = lane < P && has_pages(sp.c0 + lane);
-        const float Lm = mine ? lse_part[(b + sp.c0 + lane) * g.hq + hq] : -CUDART_INF_F;
-        M = Lm;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        const float w = (M == -CUDART_INF_F || Lm == -CUDART_INF_F) ? 0.f : ex2_approx((Lm - M) * kLog2e);
-        S = w;
-#pragma unroll
-        for (int k = 0; k < kMergeBatch; ++k) {
-            const float wk = __shfl_sync(0xffffffffu, w, k);
-            if (k < P && wk != 0.f) {
-#pragma unroll
-                for (int e = 0; e < PER; ++e) acc[e] = fmaf(wk, v[k][e], acc[e]);
-            }
-        }
-    } else {
-        // 1. max of the partial L (lanes over pieces)
+    // Batches of kMergeBatch pieces, each in one round of loads: lane k takes
+    // piece k's L while every lane loads its dims of all the batch's rows.
+    // With more than one batch the max comes first, in a pass of its own.
+    const bool one_batch = P <= kMergeBatch;
+    if (!one_batch) {
         for (long long cc = sp.c0 + lane; cc <= sp.c1; cc += 32)
             if (has_pages(cc)) M = fmaxf(M, lse_part[(b + cc) * g.hq + hq]);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        // 2. weighted sum (lanes over dims), 32 pieces' weights at a time
-        if (M != -CUDART_INF_F) {
-            for (long long c0 = sp.c0; c0 <= sp.c1; c0 += 32) {
-                const long long cm = c0 + lane;
-                float w = 0.f;
-                if (cm <= sp.c1 && has_pages(cm)) {
-                    const float Lc = lse_part[(b + cm) * g.hq + hq];
-                    w = (Lc == -CUDART_INF_F) ? 0.f : ex2_approx((Lc - M) * kLog2e);
-                }
-                S += w;
-                const int n = static_cast<int>(min(32ll, sp.c1 - c0 + 1));
-#pragma unroll 4
-                for (int k = 0; k < n; ++k) {
-                    const float wk = __shfl_sync(0xffffffffu, w, k);
-                    if (wk == 0.f) continue;
-                    float v[PER];
-                    load_row(c0 + k, v);
+    }
+    for (long long c0 = sp.c0; c0 <= sp.c1; c0 += kMergeBatch) {
+        const int n = static_cast<int>(min(static_cast<long long>(kMergeBatch), sp.c1 - c0 + 1));
+        float v[kMergeBatch][PER];
 #pragma unroll
-                    for (int e = 0; e < PER; ++e) acc[e] = fmaf(wk, v[e], acc[e]);
-                }
+        for (int k = 0; k < kMergeBatch; ++k)
+            if (k < n) load_row(c0 + k, v[k]);
+        const bool mine = lane < n && has_pages(c0 + lane);
+        const float Lm = mine ? lse_part[(b + c0 + lane) * g.hq + hq] : -CUDART_INF_F;
+        if (one_batch) {
+            M = Lm;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        }
+        const float w = (M == -CUDART_INF_F || Lm == -CUDART_INF_F) ? 0.f : ex2_approx((Lm - M) * kLog2e);
+        S += w;
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+            if (k < n && wk != 0.f) {
+#pragma unroll
+                for (int e = 0; e < PER; ++e) acc[e] = fmaf(wk, v[k][e], acc[e]);
             }
         }
     }
