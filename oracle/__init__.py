@@ -46,6 +46,8 @@ def lib():
         L.orc_write_kv_rope.restype = C.c_int64
         L.orc_write_kv_rope.argtypes = [C.POINTER(Geom), _P, _P, C.c_int32, C.c_int64, _P, _P, _P, _P, _P, _P,
                                         C.c_int32]
+        L.orc_rope_q.restype = C.c_int
+        L.orc_rope_q.argtypes = [C.POINTER(Geom), _P, C.c_int32, _P, _P, _P, _P, C.c_int32, _P]
         L.orc_alloc_pages.restype = C.c_int64
         L.orc_alloc_pages.argtypes = [C.POINTER(Geom), _P, C.c_int32, _P, _P, _P, _P, _P]
         L.orc_release_slots.restype = C.c_int64
@@ -144,6 +146,35 @@ def write_kv_rope(g, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new, 
     r = lib().orc_write_kv_rope(C.byref(g), _ptr(pool), _ptr(bt), layer, n, _ptr(ts), _ptr(tp),
                                 _ptr(k), _ptr(v), _ptr(ct), _ptr(st), int(ct.shape[0]))
     return int(r)
+
+
+def rope_q(g, q, cu_seqlens, prefix_lens, cos_tab, sin_tab):
+    """Query rows rotated by RoPE at position prefix_lens[b] + i (prefix_lens
+    None: 0): (status, q_rot[T][Hq][d] bf16 bits)."""
+    cu = _c(cu_seqlens, np.int32)
+    pre = None if prefix_lens is None else _c(prefix_lens, np.int32)
+    q = _c(q, np.uint16)
+    ct, stab = _c(cos_tab, np.float32), _c(sin_tab, np.float32)
+    out = np.zeros_like(q)
+    st = lib().orc_rope_q(C.byref(g), _ptr(q), cu.shape[0] - 1, _ptr(cu), _ptr(pre), _ptr(ct), _ptr(stab),
+                          ct.shape[0], _ptr(out))
+    return int(st), out
+
+
+def prefill_rope(g, q, pool, block_table, layer, cu_seqlens, prefix_lens, slots, scale, cos_tab, sin_tab,
+                 rows=None, heads=None, nthreads=0):
+    """Prefill with RoPE on the queries: the rows rotated at their positions
+    (rope_q), then the causal prefill over the cached prefix (prefill_cached;
+    prefix_lens None: none) on the rotated rows, at every output or at the
+    sampled (row, head) pairs.  (status, O, L)."""
+    st, qr = rope_q(g, q, cu_seqlens, prefix_lens, cos_tab, sin_tab)
+    if st != OK:
+        return st, None, None
+    pre = np.zeros(len(cu_seqlens) - 1, np.int32) if prefix_lens is None else prefix_lens
+    if rows is None:
+        return prefill_cached(g, qr, pool, block_table, layer, cu_seqlens, pre, slots, scale, nthreads)
+    return prefill_cached_rows(g, qr, pool, block_table, layer, cu_seqlens, pre, slots, scale, rows, heads,
+                               nthreads)
 
 
 def alloc_pages(g, block_table, slots, seq_lens, free_pages, free_count, old_lens=None):

@@ -123,16 +123,17 @@ static float bf16_to_float(uint16_t h) {
     return f;
 }
 
-/* RoPE of one K row [TV3 "RoPE: a rotation that references a table"]: in each
- * kv head, element i and element i + d/2 form a pair rotated by the angle of
- * the token's position, read from caller tables cos/sin[pos][d/2]:
+/* RoPE of one row of `heads` heads (a K row: the kv heads; a query row: the
+ * q heads) [TV3 "RoPE: a rotation that references a table"]: in each head,
+ * element i and element i + d/2 form a pair rotated by the angle of the
+ * token's position, read from caller tables cos/sin[pos][d/2]:
  *   x1' = x1 c - x2 s,   x2' = x1 s + x2 c,
  * in fp32 with every product and sum rounded on its own (this file is built
  * as ISO C, so nothing is contracted into an FMA), then rounded to bf16. */
-static void rope_row(const orc_geom* g, const uint16_t* k, const float* cos_row, const float* sin_row,
-                     uint16_t* out) {
+static void rope_row(const orc_geom* g, int32_t heads, const uint16_t* k, const float* cos_row,
+                     const float* sin_row, uint16_t* out) {
     const int32_t d = g->head_dim, half = d / 2;
-    for (int32_t h = 0; h < g->num_kv_heads; ++h) {
+    for (int32_t h = 0; h < heads; ++h) {
         const uint16_t* x = k + (int64_t)h * d;
         uint16_t* y = out + (int64_t)h * d;
         for (int32_t i = 0; i < half; ++i) {
@@ -167,7 +168,7 @@ int64_t orc_write_kv_rope(const orc_geom* g, uint8_t* pool, const int32_t* block
             ++skipped;
             continue;
         }
-        rope_row(g, k_new + t * kv_dim(g), cos_tab + (int64_t)tok_pos[t] * half,
+        rope_row(g, g->num_kv_heads, k_new + t * kv_dim(g), cos_tab + (int64_t)tok_pos[t] * half,
                  sin_tab + (int64_t)tok_pos[t] * half, rot);
         int64_t token_in_block = tok_pos[t] % TOKENS_PER_BLOCK;
         uint8_t* k_dst = pool + blk * block_bytes(g) + token_in_block * row_bytes;
@@ -177,6 +178,30 @@ int64_t orc_write_kv_rope(const orc_geom* g, uint8_t* pool, const int32_t* block
     }
     free(rot);
     return skipped;
+}
+
+/* Query rows of a packed batch rotated at their positions [TV3 "RoPE: a
+ * rotation that references a table": the program rotates Q and K with the
+ * same kernel and tables before the scores].  The i-th query row of sequence
+ * b sits at position prefix[b] + i (prefix NULL: 0), the position its K row
+ * was written at; each of its q heads turns exactly as a kv head of K. */
+int orc_rope_q(const orc_geom* g, const uint16_t* q, int32_t batch, const int32_t* cu_seqlens,
+               const int32_t* prefix_lens, const float* cos_tab, const float* sin_tab, int32_t max_pos,
+               uint16_t* q_rot) {
+    if (!geom_ok(g) || batch < 0 || !cu_seqlens || max_pos < 0 || (g->head_dim & 1)) return ORC_BAD_ARG;
+    if (cu_seqlens[0] != 0) return ORC_BAD_ARG;
+    const int32_t half = g->head_dim / 2;
+    const int64_t row = (int64_t)g->num_q_heads * g->head_dim;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int32_t pre = prefix_lens ? prefix_lens[b] : 0;
+        if (cu_seqlens[b + 1] < cu_seqlens[b] || pre < 0) return ORC_BAD_ARG;
+        for (int64_t t = cu_seqlens[b]; t < cu_seqlens[b + 1]; ++t) {
+            const int64_t pos = (int64_t)pre + (t - cu_seqlens[b]);
+            if (pos >= max_pos || !q || !q_rot || !cos_tab || !sin_tab) return ORC_BAD_ARG;
+            rope_row(g, g->num_q_heads, q + t * row, cos_tab + pos * half, sin_tab + pos * half, q_rot + t * row);
+        }
+    }
+    return ORC_OK;
 }
 
 /* ------------------------------------------------------ page lifetime */

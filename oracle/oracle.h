@@ -90,6 +90,19 @@ int64_t orc_write_kv_rope(const orc_geom* g, uint8_t* pool, const int32_t* block
                           const int32_t* tok_pos, const uint16_t* k_new, const uint16_t* v_new,
                           const float* cos_tab, const float* sin_tab, int32_t max_pos);
 
+/* Query rows of a packed batch rotated by RoPE [TV3 "RoPE: a rotation that
+ * references a table": Q and K are rotated with the same tables before the
+ * scores].  The i-th query row of sequence b (rows cu_seqlens[b] ..
+ * cu_seqlens[b+1]-1 of q[T][Hq][d], bf16 bits) sits at position
+ * prefix_lens[b] + i (prefix_lens NULL: 0); each q head is rotated as
+ * orc_write_kv_rope rotates a kv head of K, then rounded to bf16.  Writes
+ * q_rot[T][Hq][d].  Returns ORC_OK, or ORC_BAD_ARG for a position >= max_pos
+ * or bad lengths.  RoPE-Q prefill = orc_rope_q, then orc_prefill_cached on
+ * q_rot. */
+int orc_rope_q(const orc_geom* g, const uint16_t* q, int32_t batch, const int32_t* cu_seqlens,
+               const int32_t* prefix_lens, const float* cos_tab, const float* sin_tab, int32_t max_pos,
+               uint16_t* q_rot);
+
 /* Gather the first n tokens of (slot, layer) into K[n][Hkv][d], V[n][Hkv][d]
  * (fp64) through the block table [TV6 address rule].  Returns ORC_OK or
  * ORC_BAD_BLOCK / ORC_BAD_ARG. */

@@ -14,6 +14,7 @@ from tests import test_oracle_backward_pins as bpins
 from tests import test_oracle_chunked_pins as cpins
 from tests import test_oracle_pages_pins as ppins
 from tests import test_oracle_rope_pins as rpins
+from tests import test_oracle_rope_q_pins as rqpins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "oracle.c")
@@ -36,9 +37,14 @@ MUTANTS = {
     "rope_signs_swapped": ("const float y1 = a - b, y2 = e + f;", "const float y1 = a + b, y2 = e - f;"),
     "rope_interleaved_pairs": ("const float x1 = bf16_to_float(x[i]), x2 = bf16_to_float(x[i + half]);",
                                "const float x1 = bf16_to_float(x[2 * i]), x2 = bf16_to_float(x[2 * i + 1]);"),
-    "rope_next_table_row": ("rope_row(g, k_new + t * kv_dim(g), cos_tab + (int64_t)tok_pos[t] * half,",
-                            "rope_row(g, k_new + t * kv_dim(g), cos_tab + (int64_t)(tok_pos[t] + 1 < max_pos ? tok_pos[t] + 1 : tok_pos[t]) * half,"),
+    "rope_next_table_row": ("rope_row(g, g->num_kv_heads, k_new + t * kv_dim(g), cos_tab + (int64_t)tok_pos[t] * half,",
+                            "rope_row(g, g->num_kv_heads, k_new + t * kv_dim(g), cos_tab + (int64_t)(tok_pos[t] + 1 < max_pos ? tok_pos[t] + 1 : tok_pos[t]) * half,"),
     "rope_truncating_round": ("u += 0x7FFFu + lsb;", "u += 0u * lsb;"),
+    "ropeq_position_without_prefix": ("const int64_t pos = (int64_t)pre + (t - cu_seqlens[b]);",
+                                      "const int64_t pos = (t - cu_seqlens[b]);"),
+    "ropeq_packed_row_as_position": ("const int64_t pos = (int64_t)pre + (t - cu_seqlens[b]);",
+                                     "const int64_t pos = (int64_t)pre + t;"),
+    "ropeq_kv_head_count": ("rope_row(g, g->num_q_heads, q + t * row,", "rope_row(g, g->num_kv_heads, q + t * row,"),
     "alloc_pop_order": ("*e = free_pages[--top]; /* pop_back */", "*e = free_pages[(--top) ^ 1]; /* pop_back */"),
     "alloc_last_block_missing": ("const int32_t hi = (len + TOKENS_PER_BLOCK - 1) / TOKENS_PER_BLOCK;",
                                  "const int32_t hi = len / TOKENS_PER_BLOCK;"),
@@ -76,6 +82,9 @@ PIN_TESTS = [
     lambda gd: rpins.test_worked_example_pairing(gd),
     lambda gd: rpins.test_special_angles(),
     lambda gd: rpins.test_matches_torch_fp32_ops_byte_for_byte(),
+    lambda gd: rqpins.test_identity_table_changes_nothing(),
+    lambda gd: rqpins.test_quarter_turns_by_position(8, 2, 64),
+    lambda gd: rqpins.test_prefill_rope_matches_library_sdpa_on_complex_turns(),
     lambda gd: ppins.test_worked_example(gd),
     lambda gd: ppins.test_decode_takes_a_page_only_at_a_new_block(),
     lambda gd: bpins.test_matches_torch_autograd(8, 2, 64, [40, 17]),
