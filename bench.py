@@ -19,6 +19,9 @@ decode's 4 d Hq n).  The line also carries:
                   same for 64 sequences of 128..2048 tokens;
   scatter      -- pa_write_kv and pa_write_kv_rope GB/s on the prompt rows
                   against the measured HBM copy bandwidth;
+  prefill_rope_q -- the main prefill with RoPE on the queries in the
+                  kernel's prologue (pa_prefill_rope), and its cost over the
+                  plain prefill;
   llama_prompts -- pa_prefill of the Llama-3.2-1B-shaped prompts (17 and 512
                   tokens, K/V scattered at layers 0 and 15): latency-bound,
                   reported with its own oracle baseline;
@@ -267,6 +270,32 @@ class PrefillStep:
                        self.err)
         pa.pa_decode(self.g, d["dec_q"], self.pool, d["bt"], 0, d["dec_lens"], d["slots"], self.n + 1,
                      c.scale, dec_o, dec_lse, self.ws, self.err)
+
+
+class RopePrefillStep:
+    """The main step's prompts with RoPE on both sides: the prompt K/V
+    scattered with K turned (pa_write_kv_rope), then pa_prefill_rope, which
+    turns every query row in the kernel's prologue (same FLOPs as the plain
+    prefill: the prologue is what it costs)."""
+
+    def __init__(self, torch, pa, W, step):
+        self.torch, self.pa, self.step = torch, pa, step
+        geom = step.case.geom
+        cos_t, sin_t = W.rope_tables(int(step.case.lens.max()) + 1, geom.head_dim)
+        self.cos = torch.from_numpy(cos_t).cuda()
+        self.sin = torch.from_numpy(sin_t).cuda()
+        self.flops = step.flops_prefill
+
+    def run(self, ev=None):
+        pa, st, c, d = self.pa, self.step, self.step.case, self.step.d
+        pa.pa_write_kv_rope(st.g, st.pool, d["bt"], 0, d["tok_slot"], d["tok_pos"], d["k"], d["v"], self.cos, self.sin,
+                            st.err)
+        if ev is not None:
+            ev[0].record()
+        pa.pa_prefill_rope(st.g, d["q"], st.pool, d["bt"], 0, d["cu"], None, d["slots"], st.n, c.scale, self.cos,
+                           self.sin, st.o, st.lse, st.err)
+        if ev is not None:
+            ev[1].record()
 
 
 class ScatterStep:
@@ -888,7 +917,7 @@ def main():
     peaks, peak_src = load_peaks()
     flush = L2Flush(torch)
 
-    roofline = decode = e2e = other_variant = None
+    roofline = decode = e2e = other_variant = rope_q = None
     value = total_s = None
     step = None
     clk = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
@@ -913,6 +942,26 @@ def main():
                     "peak_source": "%s bf16_tflops (burst)" % peak_src,
                     "algorithmic_flops_per_launch": step.flops_prefill,
                     "avg_launch_ms": prefill_avg * 1e3}
+        # the same prefill with RoPE on the queries in the kernel's prologue (K turned by the scatter)
+        rstep = RopePrefillStep(torch, pa, W, step)
+        rsteps = max(20, args.steps // 4)
+        _, rk_s = timed(torch, lambda ev: rstep.run(ev=ev), rsteps, args.warmup, flush, dist)
+        torch.cuda.synchronize()
+        if int(step.err.item()) != 0:
+            raise SystemExit("device error during the RoPE-Q steps: %s" % pa.pa_status_string(int(step.err.item())))
+        r_avg = float(np.mean(rk_s))
+        r_ach = rstep.flops / r_avg / 1e12
+        rope_q = {"metric": "causal prefill TFLOP/s with RoPE on the queries in the prologue (pa_prefill_rope; "
+                            "K turned by pa_write_kv_rope), same workload and FLOPs as the main prefill",
+                  "value": r_ach, "unit": "TFLOP/s", "steps": rsteps,
+                  "prologue_cost": r_avg / prefill_avg - 1.0,
+                  "roofline": {"bound": "tensor", "achieved": r_ach, "peak": bf16_peak, "unit": "TFLOP/s",
+                               "frac": r_ach / bf16_peak,
+                               "kernel": "prefill_kernel<%d, %d, rope>" % (step.geom.head_dim,
+                                                                           prefill_heads_per_cta(step.geom)),
+                               "peak_source": "%s bf16_tflops (burst)" % peak_src,
+                               "algorithmic_flops_per_launch": rstep.flops, "avg_launch_ms": r_avg * 1e3}}
+        del rstep
         # the other head-dim variant of the same long prefill (32 q / 8 kv heads at d 64,
         # 16 / 4 at d 128; the same FLOPs), the same step, reported beside the main one
         other = "d128" if args.variant == "d64" else "d64"
@@ -1123,6 +1172,7 @@ def main():
             "gpu_launches": step.launches * args.steps,
             "roofline": roofline,
             "prefill_" + ("d128" if args.variant == "d64" else "d64"): other_variant,
+            "prefill_rope_q": rope_q,
             "decode": decode,
             "chunked": chunked,
             "scatter": scatter,

@@ -8,6 +8,7 @@
  * Around it:
  *   pa_prefill_cached  prefill of query chunks over a cached prefix (chunked prefill),
  *   pa_write_kv_rope   rotary embedding of K fused into the scatter,
+ *   pa_prefill_rope    pa_prefill_cached with rotary embedding of Q in the kernel's prologue,
  *   pa_alloc_pages, pa_release_slots   page allocation on the device, table in place,
  *   pa_prefill_backward  gradients of the prefill (tcgen05 / TMEM),
  *   pa_decode_noalloc  pa_decode with the library's fixed scratch instead of a workspace,
@@ -194,6 +195,32 @@ pa_status pa_prefill_cached(const pa_geom* geom, const void* q, const void* pool
                             const int32_t* slots, int32_t max_seqlen, int32_t total_tokens,
                             float scale, void* o, float* lse, int32_t* err_flag,
                             pa_stream_t stream);
+
+/*
+ * pa_prefill_rope -- pa_prefill_cached with RoPE applied to the queries in the
+ * kernel's prologue (jaehun.me tiny-vllm part 3, "RoPE: a rotation that
+ * references a table": the program turns Q and K with the same tables before
+ * the scores; K turns on its way into the pages, pa_write_kv_rope).
+ * Definition: the i-th query row of sequence b sits at position
+ * prefix_lens[b] + i (prefix_lens NULL: 0), the position its K row was
+ * written at; in each q head, element k and element k + head_dim/2 turn by
+ * the angle of that position exactly as pa_write_kv_rope turns K (fp32, every
+ * product and sum rounded on its own, then bf16 nearest even), and the scores,
+ * softmax, o and lse are pa_prefill_cached's on the turned rows.  q itself is
+ * not modified; o may alias q.
+ * Arguments: as pa_prefill_cached, plus cos_table, sin_table: device fp32
+ * [max_pos][head_dim/2], 16-byte aligned (the tables given to
+ * pa_write_kv_rope).  max_pos >= 0 (else PA_ERR_INVALID_ARG).  A query row
+ * whose position is >= max_pos sets PA_ERR_BAD_BLOCK (its output is then
+ * unspecified).
+ */
+pa_status pa_prefill_rope(const pa_geom* geom, const void* q, const void* pool,
+                          const int32_t* block_table, int32_t layer, int32_t batch,
+                          const int32_t* cu_seqlens, const int32_t* prefix_lens,
+                          const int32_t* slots, int32_t max_seqlen, int32_t total_tokens,
+                          float scale, const float* cos_table, const float* sin_table,
+                          int32_t max_pos, void* o, float* lse, int32_t* err_flag,
+                          pa_stream_t stream);
 
 /*
  * pa_prefill_backward -- gradients of pa_prefill's output with respect to q

@@ -12,6 +12,7 @@ Calls (same names as the C ABI):
 * ``pa_write_kv_rope(geom, pool, block_table, layer, tok_slot, tok_pos, k_new, v_new, cos_table, sin_table, err_flag)``
 * ``pa_prefill(geom, q, pool, block_table, layer, cu_seqlens, slots, max_seqlen, scale, o, lse, err_flag)``
 * ``pa_prefill_cached(geom, q, pool, block_table, layer, cu_seqlens, prefix_lens, slots, max_seqlen, scale, o, lse, err_flag)``
+* ``pa_prefill_rope(geom, q, pool, block_table, layer, cu_seqlens, prefix_lens, slots, max_seqlen, scale, cos_table, sin_table, o, lse, err_flag)``
 * ``pa_prefill_backward(geom, q, pool, block_table, layer, cu_seqlens, slots, max_seqlen, scale, o, lse, dout, delta, dq, dk, dv, err_flag)``
 * ``pa_decode(geom, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse, workspace, err_flag)``
 * ``pa_decode_noalloc(geom, q, pool, block_table, layer, seq_lens, slots, max_seq_len, scale, o, lse, err_flag)``
@@ -36,7 +37,8 @@ PA_BLOCK_TOKENS = 16
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libpa.so")
-EXPORTED = ("pa_page_bytes", "pa_write_kv", "pa_write_kv_rope", "pa_prefill", "pa_prefill_cached", "pa_prefill_backward", "pa_decode_workspace_size", "pa_decode",
+EXPORTED = ("pa_page_bytes", "pa_write_kv", "pa_write_kv_rope", "pa_prefill", "pa_prefill_cached", "pa_prefill_rope",
+            "pa_prefill_backward", "pa_decode_workspace_size", "pa_decode",
             "pa_decode_noalloc", "pa_alloc_pages", "pa_release_slots", "pa_status_string")
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 PA_PAGES_MAX_SLOTS = 65536
@@ -88,6 +90,9 @@ def load_library(path: str = None):
     L.pa_prefill_cached.restype = C.c_int
     L.pa_prefill_cached.argtypes = [C.POINTER(PaGeom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, _P, C.c_int32,
                                     C.c_int32, C.c_float, _P, _P, _P, _P]
+    L.pa_prefill_rope.restype = C.c_int
+    L.pa_prefill_rope.argtypes = [C.POINTER(PaGeom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, _P, C.c_int32,
+                                  C.c_int32, C.c_float, _P, _P, C.c_int32, _P, _P, _P, _P]
     L.pa_decode_workspace_size.restype = C.c_size_t
     L.pa_prefill_backward.restype = C.c_int
     L.pa_prefill_backward.argtypes = [C.POINTER(PaGeom), _P, _P, _P, C.c_int32, C.c_int32, _P, _P, C.c_int32,
@@ -190,6 +195,18 @@ def pa_prefill_cached(g, q, pool, block_table, layer, cu_seqlens, prefix_lens, s
         C.byref(g), _ptr(q), _ptr(pool), _ptr(block_table), layer, batch, _ptr(cu_seqlens),
         _ptr(prefix_lens), _ptr(slots), int(max_seqlen), total, float(scale), _ptr(o), _ptr(lse),
         _ptr(err_flag), _stream(stream)))
+
+
+def pa_prefill_rope(g, q, pool, block_table, layer, cu_seqlens, prefix_lens, slots, max_seqlen, scale, cos_table,
+                    sin_table, o, lse, err_flag, stream=None, batch=None, total_tokens=None):
+    """pa_prefill_cached with RoPE on the queries (prefix_lens None: no prefix);
+    cos_table / sin_table: fp32 [max_pos][head_dim/2] CUDA tensors."""
+    batch = int(cu_seqlens.shape[0]) - 1 if batch is None else int(batch)
+    total = int(q.shape[0]) if total_tokens is None else int(total_tokens)
+    _check("pa_prefill_rope", lib().pa_prefill_rope(
+        C.byref(g), _ptr(q), _ptr(pool), _ptr(block_table), layer, batch, _ptr(cu_seqlens), _ptr(prefix_lens),
+        _ptr(slots), int(max_seqlen), total, float(scale), _ptr(cos_table), _ptr(sin_table), int(cos_table.shape[0]),
+        _ptr(o), _ptr(lse), _ptr(err_flag), _stream(stream)))
 
 
 def pa_prefill_backward(g, q, pool, block_table, layer, cu_seqlens, slots, max_seqlen, scale, o, lse, dout,

@@ -117,27 +117,63 @@ PA_API pa_status pa_write_kv_rope(const pa_geom* geom, void* pool, const int32_t
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+// The checks of pa_prefill_cached (shared with pa_prefill_rope); *no_work is
+// set when the call has nothing to enqueue and the status is PA_OK.
+pa_status prefill_args(const pa_geom* geom, const void* q, const void* pool, const int32_t* block_table,
+                       int32_t layer, int32_t batch, const int32_t* cu_seqlens, const int32_t* slots,
+                       int32_t max_seqlen, int32_t total_tokens, float scale, const void* o,
+                       const int32_t* err_flag, bool* no_work) {
+    *no_work = false;
+    if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= geom->n_layers) return PA_ERR_INVALID_ARG;
+    if (batch < 0 || max_seqlen < 0 || total_tokens < 0 || !std::isfinite(scale) || !(scale > 0.f))
+        return PA_ERR_INVALID_ARG;
+    if (geom->head_dim != 64 && geom->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (batch == 0 || total_tokens == 0 || max_seqlen == 0) {
+        *no_work = true;
+        return PA_OK;
+    }
+    if (!q || !pool || !block_table || !cu_seqlens || !slots || !o || !err_flag)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o) || !aligned16(pool)) return PA_ERR_INVALID_ARG;
+    // TMA coordinates are int32: pool rows (32 per page) and q rows must fit.
+    if (kgeom(geom).nblocks * 32 >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+}  // namespace
+
 PA_API pa_status pa_prefill_cached(const pa_geom* geom, const void* q, const void* pool,
                                    const int32_t* block_table, int32_t layer, int32_t batch,
                                    const int32_t* cu_seqlens, const int32_t* prefix_lens,
                                    const int32_t* slots, int32_t max_seqlen, int32_t total_tokens,
                                    float scale, void* o, float* lse, int32_t* err_flag,
                                    pa_stream_t stream) {
-    if (!geom_valid(geom)) return PA_ERR_INVALID_ARG;
-    if (layer < 0 || layer >= geom->n_layers) return PA_ERR_INVALID_ARG;
-    if (batch < 0 || max_seqlen < 0 || total_tokens < 0 || !std::isfinite(scale) || !(scale > 0.f))
-        return PA_ERR_INVALID_ARG;
-    if (geom->head_dim != 64 && geom->head_dim != 128) return PA_ERR_UNSUPPORTED;
-    if (batch == 0 || total_tokens == 0 || max_seqlen == 0) return PA_OK;
-    if (!q || !pool || !block_table || !cu_seqlens || !slots || !o || !err_flag)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(o) || !aligned16(pool)) return PA_ERR_INVALID_ARG;
-    const pa::KGeom g = kgeom(geom);
-    // TMA coordinates are int32: pool rows (32 per page) and q rows must fit.
-    if (g.nblocks * 32 >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
-    return cuda_status(pa::launch_prefill(g, q, pool, block_table, layer, batch, cu_seqlens,
+    bool no_work = false;
+    const pa_status st = prefill_args(geom, q, pool, block_table, layer, batch, cu_seqlens, slots, max_seqlen,
+                                      total_tokens, scale, o, err_flag, &no_work);
+    if (st != PA_OK || no_work) return st;
+    return cuda_status(pa::launch_prefill(kgeom(geom), q, pool, block_table, layer, batch, cu_seqlens,
                                           prefix_lens, slots, max_seqlen, total_tokens, scale, o,
                                           lse, err_flag, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+PA_API pa_status pa_prefill_rope(const pa_geom* geom, const void* q, const void* pool,
+                                 const int32_t* block_table, int32_t layer, int32_t batch,
+                                 const int32_t* cu_seqlens, const int32_t* prefix_lens,
+                                 const int32_t* slots, int32_t max_seqlen, int32_t total_tokens,
+                                 float scale, const float* cos_table, const float* sin_table,
+                                 int32_t max_pos, void* o, float* lse, int32_t* err_flag,
+                                 pa_stream_t stream) {
+    if (max_pos < 0) return PA_ERR_INVALID_ARG;
+    bool no_work = false;
+    const pa_status st = prefill_args(geom, q, pool, block_table, layer, batch, cu_seqlens, slots, max_seqlen,
+                                      total_tokens, scale, o, err_flag, &no_work);
+    if (st != PA_OK || no_work) return st;
+    if (!cos_table || !sin_table || !aligned16(cos_table) || !aligned16(sin_table)) return PA_ERR_INVALID_ARG;
+    return cuda_status(pa::launch_prefill(kgeom(geom), q, pool, block_table, layer, batch, cu_seqlens,
+                                          prefix_lens, slots, max_seqlen, total_tokens, scale, o, lse, err_flag,
+                                          reinterpret_cast<cudaStream_t>(stream), cos_table, sin_table, max_pos));
 }
 
 PA_API pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool,

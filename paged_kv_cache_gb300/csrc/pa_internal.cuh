@@ -522,6 +522,38 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
+// RoPE of 8 pairs (tiny-vllm part 3, "RoPE: a rotation that references a
+// table"): element e of `lo` and element e of `hi` (bf16, the halves i and
+// i + d/2 of one head) turn by the angle whose cos / sin are c[e] / s[e]:
+//   x1' = x1 c - x2 s,   x2' = x1 s + x2 c,
+// each product and sum rounded on its own (no FMA contraction), then to bf16
+// nearest even.  Shared by the K scatter and the prefill's query prologue, so
+// that Q and K turn bit for bit alike.
+__device__ __forceinline__ void rope8(uint4& lo, uint4& hi, const float4 c0, const float4 c1, const float4 s0,
+                                      const float4 s1) {
+    const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t ra = 0, rb = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int e = 2 * w + h;
+            const float x1 = __uint_as_float((a[w] >> (16 * h)) << 16);
+            const float x2 = __uint_as_float((b[w] >> (16 * h)) << 16);
+            const float y1 = __fsub_rn(__fmul_rn(x1, cs[e]), __fmul_rn(x2, sn[e]));
+            const float y2 = __fadd_rn(__fmul_rn(x1, sn[e]), __fmul_rn(x2, cs[e]));
+            ra |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(y1))) << (16 * h);
+            rb |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(y2))) << (16 * h);
+        }
+        a[w] = ra;
+        b[w] = rb;
+    }
+    lo = make_uint4(a[0], a[1], a[2], a[3]);
+    hi = make_uint4(b[0], b[1], b[2], b[3]);
+}
+
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLog2e = 1.442695040888963407f;
 
@@ -555,7 +587,8 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool,
                            const int32_t* block_table, int layer, int batch,
                            const int32_t* cu_seqlens, const int32_t* prefix_lens,
                            const int32_t* slots, int max_seqlen, int total_tokens, float scale,
-                           void* o, float* lse, int32_t* err, cudaStream_t stream);
+                           void* o, float* lse, int32_t* err, cudaStream_t stream,
+                           const float* cos_tab = nullptr, const float* sin_tab = nullptr, int max_pos = 0);
 
 size_t decode_workspace_bytes(const KGeom& g, int batch, int max_seq_len);
 pa_status decode_args(const pa_geom* geom, const void* q, const void* pool, const int32_t* block_table,

@@ -42,6 +42,12 @@
 //    holds its P in its first 16 columns), then O.
 //  * A partial last page has its V rows past the sequence end zeroed in shared
 //    memory before the PV products (masked P is exactly 0, but 0 x NaN is not).
+//  * RoPE on the queries (pa_prefill_rope; tiny-vllm part 3, "RoPE: a rotation
+//    that references a table": Q turns with the tables K turned with): once
+//    the query tiles have landed, each softmax thread turns its own row of its
+//    tile in shared memory, following the 128-byte swizzle, with the angle
+//    row of the query's position (loaded before the tiles arrive), and the
+//    first QK product waits for every row to be turned.
 #include <math_constants.h>
 
 #include "pa_internal.cuh"
@@ -74,6 +80,7 @@ struct Cfg {
     static constexpr uint32_t TMEM_COLS = T * TILE_COLS <= 128 ? 128u : T * TILE_COLS <= 256 ? 256u : 512u;
     static_assert(T * TILE_COLS <= 512, "tensor memory holds S and O of every tile");
     static_assert(NST >= 2, "two K/V stages at least");
+    static_assert(1 + 2 * NST + 3 * T + MMA_WARPS + 1 <= 64, "barriers fit below the TMEM slot");
     static __device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(TILE_COLS * t); }
     static __device__ __forceinline__ uint32_t o_col(int t) { return static_cast<uint32_t>(TILE_COLS * t + BN); }
     // P columns of key step ks (16 keys) of tile t: the 32 keys of each half of
@@ -100,6 +107,9 @@ struct PrefillParams {
     bool o_32b;           // o is 32-byte aligned: rows go out in whole 32-byte sectors
     float* lse;
     int32_t* err;
+    const float* cos_tab;  // RoPE-Q: angle tables [max_pos][d/2] (null without RoPE)
+    const float* sin_tab;
+    int max_pos;
 };
 
 // P = 2^(s * sc + nm) of 32 scores, packed to bf16 pairs; adds the fp32 P to ls.
@@ -129,6 +139,52 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], float m) {
 #pragma unroll
     for (int e = 0; e < 32; e += 2) mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
     return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// RoPE of row r of one query tile in shared memory (the tile's 64-dim chunks
+// are 128 rows of 128 bytes, 16-byte pieces swizzled by row % 8): pair (e,
+// e + D/2) of every 8-element group turns by the angle row of position pos.
+// The angle rows are requested before the tile is waited for.  Returns false
+// if the wait for the tile gave up.
+template <int D>
+__device__ __forceinline__ bool rope_q_row(uint8_t* tile, int r, bool turn, long long pos, uint64_t* q_full,
+                                           volatile int* abort_flag, const PrefillParams& p) {
+    constexpr int NG = D / 16;             // groups of 8 pairs
+    constexpr int GB = NG < 4 ? NG : 4;    // groups whose angles are in registers at once
+    float4 cs[GB][4];
+    auto load = [&](int g0) {
+#pragma unroll
+        for (int gg = 0; gg < GB; ++gg) {
+            const long long a = pos * (D / 2) + 8 * (g0 + gg);
+            const float4* ct = reinterpret_cast<const float4*>(p.cos_tab + a);
+            const float4* st = reinterpret_cast<const float4*>(p.sin_tab + a);
+            cs[gg][0] = __ldg(ct);
+            cs[gg][1] = __ldg(ct + 1);
+            cs[gg][2] = __ldg(st);
+            cs[gg][3] = __ldg(st + 1);
+        }
+    };
+    if (turn) load(0);
+    if (!__all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, p.err))) return false;
+    auto piece = [&](int e) -> uint4* {  // the 16 bytes holding elements e .. e + 7 of row r
+        return reinterpret_cast<uint4*>(tile + (e / 64) * kQChunkBytes + r * 128 + ((((e % 64) / 8) ^ (r & 7)) * 16));
+    };
+    if (turn) {
+#pragma unroll
+        for (int g0 = 0; g0 < NG; g0 += GB) {
+            if (g0 > 0) load(g0);
+#pragma unroll
+            for (int gg = 0; gg < GB; ++gg) {
+                const int e = 8 * (g0 + gg);
+                uint4 lo = *piece(e), hi = *piece(e + D / 2);
+                rope8(lo, hi, cs[gg][0], cs[gg][1], cs[gg][2], cs[gg][3]);
+                *piece(e) = lo;
+                *piece(e + D / 2) = hi;
+            }
+        }
+        fence_proxy_async_smem();  // the turned rows before the tensor core reads them
+    }
+    return true;
 }
 
 // Softmax of query tile t: the warp's thread owns row r (TMEM lane r).
@@ -263,7 +319,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
     }
 }
 
-template <int D, int T>
+template <int D, int T, bool ROPE>
 __global__ void __launch_bounds__(Cfg<D, T>::THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
                const PrefillParams p) {
@@ -282,6 +338,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint64_t* p_full = s_full + T;                // [T] P of a tile in TMEM
     uint64_t* o_done = s_full + 2 * T;            // [T] the last PV product of a tile done
     uint64_t* mma_done = s_full + 3 * T;          // [MMA_WARPS]
+    uint64_t* q_ready = mma_done + C::MMA_WARPS;  // RoPE-Q: every query row turned
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 65);
 
@@ -329,6 +386,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&o_done[t], 1);
         }
         for (int m = 0; m < C::MMA_WARPS; ++m) mbar_init(&mma_done[m], 1);
+        if (ROPE) mbar_init(q_ready, 4 * T);  // one arrive per softmax warp
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -434,14 +492,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                   umma_sdesc_sw128(sV + c * kKChunkBytes + ks * 2048, 1024, 1024), idesc_pv,
                                   (acc || ks > 0) ? 1u : 0u);
         };
-        bool ok = wait_all(q_full, 0) && wait_all(&kv_full[0], 0);
+        bool ok = wait_all(ROPE ? q_ready : q_full, 0) && wait_all(&kv_full[0], 0);
         if (ok) {
             tc_fence_after_sync();
 #pragma unroll
             for (int t = 0; t < T; ++t)
                 if (t % C::MMA_WARPS == mw) qk(t, 0);
         }
-        for (int j = 0; ok && j < nkv; ++j) {
+        for (int j = 0; j < nkv; ++j) {
             const int st = j % C::NST;
             const int st1 = (j + 1) % C::NST;
             const bool more = j + 1 < nkv;
@@ -476,9 +534,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // ------------------------------------------------------------ softmax
         const int t = warp >> 2;
         const int r = (warp & 3) * 32 + lane;  // query row = TMEM lane
-        softmax_role<D, T>(t, r, tmem + tmem_lane_base(warp), i, nkv, n, pre + BM * i, kv_len, cu0, hq0 + t, sKV,
-                           &s_full[t], &p_full[t],
-                           &o_done[t], kv_full, abort_flag, p);
+        bool ok = true;
+        if constexpr (ROPE) {
+            const long long pos = static_cast<long long>(pre) + BM * i + r;
+            const bool in_chunk = BM * i + r < n;
+            const bool turn = in_chunk && pos < p.max_pos;
+            if (in_chunk && !turn) set_error(p.err, PA_ERR_BAD_BLOCK);
+            ok = rope_q_row<D>(sQ + t * C::Q_BYTES, r, turn, pos, q_full, abort_flag, p);
+            __syncwarp();
+            if (ok) mbar_arrive_elect(q_ready);
+        }
+        if (ok)
+            softmax_role<D, T>(t, r, tmem + tmem_lane_base(warp), i, nkv, n, pre + BM * i, kv_len, cu0, hq0 + t, sKV,
+                               &s_full[t], &p_full[t], &o_done[t], kv_full, abort_flag, p);
     }
 
     tc_fence_before_sync();
@@ -507,7 +575,7 @@ bool encode_2d(CUtensorMap* map, const void* base, unsigned long long cols, unsi
 template <int D, int T>
 cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, const PrefillParams& p, cudaStream_t stream) {
     using C = Cfg<D, T>;
-    auto kern = prefill_kernel<D, T>;
+    auto kern = p.cos_tab ? prefill_kernel<D, T, true> : prefill_kernel<D, T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const long long grid = static_cast<long long>(p.n_row_tiles) * p.batch * (p.g.hq / T);
@@ -521,7 +589,7 @@ cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, const Pref
 cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, const int32_t* block_table, int layer,
                            int batch, const int32_t* cu_seqlens, const int32_t* prefix_lens, const int32_t* slots,
                            int max_seqlen, int total_tokens, float scale, void* o, float* lse, int32_t* err,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const float* cos_tab, const float* sin_tab, int max_pos) {
     CUtensorMap qmap, kvmap;
     if (!encode_2d(&qmap, q, static_cast<unsigned long long>(g.hq) * g.d, static_cast<unsigned long long>(total_tokens),
                    static_cast<unsigned long long>(g.hq) * g.d * 2, BM))
@@ -550,6 +618,9 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, cons
     p.o_32b = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
     p.lse = lse;
     p.err = err;
+    p.cos_tab = cos_tab;
+    p.sin_tab = sin_tab;
+    p.max_pos = max_pos;
     if (g.d == 64) {
         if (p.heads_per_cta == 4) return launch<64, 4>(qmap, kvmap, p, stream);
         if (p.heads_per_cta == 2) return launch<64, 2>(qmap, kvmap, p, stream);

@@ -66,44 +66,7 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
     }
 }
 
-// The same scatter with K rotated by RoPE on the way (jaehun.me tiny-vllm part
-// 3, "RoPE: a rotation that references a table"): in each kv head, element i
-// and element i + d/2 form a pair turned by the angle of the row's position,
-//   x1' = x1 c - x2 s,   x2' = x1 s + x2 c,
-// with c, s from caller tables [max_pos][d/2] fp32.  Each product and sum is
-// rounded on its own (no FMA contraction), then to bf16 nearest-even.
-// Threads work on groups of kRopeRows rows: the group's K threads first (8
-// pairs, 16 bytes of each half, in each of KPT heads Hkv/KPT apart, which
-// share one angle row), then its V threads (VPT 16-byte chunks each, a row's
-// V threads taking consecutive chunks in each pass), so that a warp runs
-// either the rotation or the copy.
-// Every thread reads its row's data, then the position, then the page entry
-// and (K) the angle rows together, so that the latencies overlap.
-__device__ __forceinline__ void rope8(uint4& lo, uint4& hi, const float4 c0, const float4 c1, const float4 s0,
-                                      const float4 s1) {
-    const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-    uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        uint32_t ra = 0, rb = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int e = 2 * w + h;
-            const float x1 = __uint_as_float((a[w] >> (16 * h)) << 16);
-            const float x2 = __uint_as_float((b[w] >> (16 * h)) << 16);
-            const float y1 = __fsub_rn(__fmul_rn(x1, cs[e]), __fmul_rn(x2, sn[e]));
-            const float y2 = __fadd_rn(__fmul_rn(x1, sn[e]), __fmul_rn(x2, cs[e]));
-            ra |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(y1))) << (16 * h);
-            rb |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(y2))) << (16 * h);
-        }
-        a[w] = ra;
-        b[w] = rb;
-    }
-    lo = make_uint4(a[0], a[1], a[2], a[3]);
-    hi = make_uint4(b[0], b[1], b[2], b[3]);
-}
-
+// Streaming 16-byte load (read once: not kept in L1).
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -111,6 +74,20 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
                  : "l"(p));
     return v;
 }
+
+// The same scatter with K rotated by RoPE on the way (jaehun.me tiny-vllm part
+// 3, "RoPE: a rotation that references a table"): in each kv head, element i
+// and element i + d/2 form a pair turned by the angle of the row's position,
+//   x1' = x1 c - x2 s,   x2' = x1 s + x2 c,
+// with c, s from caller tables [max_pos][d/2] fp32.  Each product and sum is
+// rounded on its own (no FMA contraction), then to bf16 nearest-even (rope8).
+// Threads work on groups of kRopeRows rows: the group's K threads first (8
+// pairs, 16 bytes of each half, in each of KPT heads Hkv/KPT apart, which
+// share one angle row), then its V threads (VPT 16-byte chunks each, a row's
+// V threads taking consecutive chunks in each pass), so that a warp runs
+// either the rotation or the copy.
+// Every thread reads its row's data, then the position, then the page entry
+// and (K) the angle rows together, so that the latencies overlap.
 
 constexpr int kRopeRows = 8;  // rows per thread group of the RoPE scatter
 
