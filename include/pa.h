@@ -12,7 +12,8 @@
  *   pa_alloc_pages, pa_release_slots   page allocation on the device, table in place,
  *   pa_prefill_backward  gradients of the prefill (tcgen05 / TMEM),
  *   pa_decode_noalloc  pa_decode with the library's fixed scratch instead of a workspace,
- *   pa_page_bytes, pa_decode_workspace_size, pa_status_string   sizes and messages.
+ *   pa_page_bytes, pa_decode_workspace_size, pa_status_string   sizes and messages,
+ *   pa_debug_hold_first_copy  diagnostic that makes a kernel's bounded wait run out (tests).
  *
  * The problem statement follows these web pages (cited by title and section):
  *  - jaehun.me, "6. KV cache 를 16토큰 블록으로 쪼개기 -- block table 로 비연속 블록을
@@ -365,6 +366,23 @@ pa_status pa_alloc_pages(const pa_geom* geom, int32_t* block_table, int32_t batc
 pa_status pa_release_slots(const pa_geom* geom, int32_t* block_table, int32_t n,
                            const int32_t* slots, int32_t* free_pages, int32_t* free_count,
                            int32_t* err_flag, pa_stream_t stream);
+
+/*
+ * pa_debug_hold_first_copy -- diagnostic for the bounded waits inside the
+ * kernels (tests only; the pages have no counterpart).  While enabled, the
+ * first CTA of every later pa_prefill / pa_prefill_cached / pa_prefill_rope /
+ * pa_decode launch arms the barrier of its first tensor copy (the query tiles
+ * of the prefill, the first page of the decode) without issuing the copy, so
+ * that barrier's phase never completes and the roles waiting on it give up
+ * after the kernels' wait limit of about 2 seconds.  That CTA then records
+ * PA_ERR_TIMEOUT in *err_flag, tells its other roles to stop, lets every copy
+ * it did issue land, frees its tensor memory and returns; no kernel traps and
+ * the context stays usable.  The outputs of that call are unspecified; other
+ * CTAs run normally.  Process-wide, not to be changed while a call is being
+ * enqueued on another thread.  enable = 0 restores normal operation (the
+ * default).  Returns PA_OK.
+ */
+pa_status pa_debug_hold_first_copy(int32_t enable);
 
 /* Static, NUL-terminated description of a status code. */
 const char* pa_status_string(pa_status status);

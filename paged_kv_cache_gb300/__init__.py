@@ -19,6 +19,7 @@ Calls (same names as the C ABI):
 * ``pa_alloc_pages(geom, block_table, slots, seq_lens, free_pages, free_count, err_flag, old_lens=None)``
 * ``pa_release_slots(geom, block_table, slots, free_pages, free_count, err_flag)``
 * ``pa_decode_workspace_size(geom, batch, max_seq_len)``, ``pa_page_bytes(geom)``, ``pa_status_string(code)``
+* ``pa_debug_hold_first_copy(enable)`` (diagnostic for the tests of the kernels' bounded waits)
 
 Tensors are torch CUDA tensors (bf16 data may be given as bfloat16 or int16
 views); ``err_flag`` is a one-element int32 CUDA tensor the caller zeroes.
@@ -39,7 +40,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libpa.so")
 EXPORTED = ("pa_page_bytes", "pa_write_kv", "pa_write_kv_rope", "pa_prefill", "pa_prefill_cached", "pa_prefill_rope",
             "pa_prefill_backward", "pa_decode_workspace_size", "pa_decode",
-            "pa_decode_noalloc", "pa_alloc_pages", "pa_release_slots", "pa_status_string")
+            "pa_decode_noalloc", "pa_alloc_pages", "pa_release_slots", "pa_debug_hold_first_copy",
+            "pa_status_string")
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 PA_PAGES_MAX_SLOTS = 65536
 
@@ -108,6 +110,8 @@ def load_library(path: str = None):
     L.pa_alloc_pages.argtypes = [C.POINTER(PaGeom), _P, C.c_int32, _P, _P, _P, _P, _P, _P, _P]
     L.pa_release_slots.restype = C.c_int
     L.pa_release_slots.argtypes = [C.POINTER(PaGeom), _P, C.c_int32, _P, _P, _P, _P, _P]
+    L.pa_debug_hold_first_copy.restype = C.c_int
+    L.pa_debug_hold_first_copy.argtypes = [C.c_int32]
     L.pa_status_string.restype = C.c_char_p
     L.pa_status_string.argtypes = [C.c_int]
     if path == LIB_PATH:
@@ -144,6 +148,13 @@ def _stream(stream):
 def _check(call, code):
     if code != PA_OK:
         raise PaError(call, code)
+
+
+def pa_debug_hold_first_copy(enable: bool) -> None:
+    """Diagnostic (tests only): while enabled, the first CTA of each later
+    prefill or decode launch arms its first tensor copy without issuing it, so
+    its bounded waits run out and the call reports PA_ERR_TIMEOUT."""
+    _check("pa_debug_hold_first_copy", lib().pa_debug_hold_first_copy(1 if enable else 0))
 
 
 def pa_status_string(code: int) -> str:

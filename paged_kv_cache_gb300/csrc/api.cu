@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libpa.so (declared in include/pa.h): argument
 // validation, then one asynchronous launch sequence per call.  No memory is
 // allocated and no state is kept between calls.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -9,6 +10,11 @@
 #define PA_API extern "C" __attribute__((visibility("default")))
 
 namespace pa {
+namespace {
+std::atomic<int> g_hold_first_copy{0};
+}
+int debug_hold_first_copy() { return g_hold_first_copy.load(std::memory_order_relaxed); }
+
 EncodeTiledFn tensor_map_encoder() {
     static EncodeTiledFn fn = nullptr;
     if (!fn) {
@@ -281,6 +287,11 @@ PA_API pa_status pa_release_slots(const pa_geom* geom, int32_t* block_table, int
     if (n == 0) return PA_OK;
     return cuda_status(pa::launch_release_slots(kgeom(geom), block_table, n, slots, free_pages, free_count,
                                                 err_flag, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+PA_API pa_status pa_debug_hold_first_copy(int32_t enable) {
+    pa::g_hold_first_copy.store(enable ? 1 : 0, std::memory_order_relaxed);
+    return PA_OK;
 }
 
 PA_API const char* pa_status_string(pa_status status) {

@@ -91,6 +91,7 @@ struct DecodeParams {
     int q_bytes;          // hq * d * 2
     int qslot_bytes;      // q row + stage header, 64-byte multiple
     int stages_off;       // offset of the (1024-aligned) page stages in shared memory
+    int hold_first_copy;  // diagnostic: CTA 0 arms its first page copy without issuing it
 };
 
 __host__ __device__ inline long long align_up(long long x, long long a) { return (x + a - 1) / a * a; }
@@ -260,9 +261,9 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
             nxt_b = bb;
         };
         if (sp + pages_b < p_end) preload(b + 1);  // the range goes past this sequence
+        const bool hold = p.hold_first_copy && c == 0;
         bool whole = false;
         long long k = 0;
-        bool stop = false;
         for (long long pg = p_begin; pg < p_end; ++pg, ++k) {
             if (pg >= sp + pages_b) {
                 while (pg >= sp + pages_b) {  // next sequence with pages
@@ -296,11 +297,8 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
             if (first) whole = (lp == 0) && (sp + pages_b <= p_end);
             const int ntok = (lp == pages_b - 1) ? len_b - static_cast<int>(lp) * kBlockTokens : kBlockTokens;
             const int st = static_cast<int>(k % p.nst);
-            if (k >= p.nst &&
-                !mbar_wait(&empty[st], static_cast<uint32_t>((k / p.nst - 1) & 1), abort_flag, p.err)) {
-                stop = true;
-                break;
-            }
+            if (k >= p.nst && !mbar_wait(&empty[st], static_cast<uint32_t>((k / p.nst - 1) & 1), abort_flag, p.err))
+                break;  // a consumer stopped the CTA, or the wait ran out
             if (lane == 0) {
                 uint8_t* stage = stages + static_cast<long long>(st) * p.kv_stage_bytes;
                 uint8_t* qslot = qslots + st * p.qslot_bytes;
@@ -312,7 +310,8 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
                 hdr->slot_idx = static_cast<int>(b + c);
                 const uint32_t kv_bytes = bad ? 0u : static_cast<uint32_t>(p.kv_stage_bytes);
                 mbar_arrive_expect_tx(&full[st], kv_bytes + (first ? static_cast<uint32_t>(p.q_bytes) : 0u));
-                if (!bad) {  // whole K half and whole V half (a partial page's tail is not used)
+                // the diagnostic hold: the first page's copy is armed, not issued
+                if (!bad && !(hold && k == 0)) {  // whole K half and whole V half (a partial page's tail is not used)
                     tma_load_3d(stage, &kvmap, 0, entry * 32, 0, &full[st]);
                     tma_load_3d(stage + p.kv_stage_bytes / 2, &kvmap, 0, entry * 32 + 16, 0, &full[st]);
                 }
@@ -322,11 +321,12 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
             }
             __syncwarp();
         }
-        // Drain: the copies of the last stages must land before the CTA exits.
-        if (stop && lane == 0) {
+        // Drain: the copies of the last stages land before the CTA exits,
+        // whichever role stopped it (phases already complete return at once).
+        if (lane == 0) {
             const long long k0 = k > p.nst ? k - p.nst : 0;
             for (long long i = k0; i < k; ++i)
-                mbar_drain(&full[i % p.nst], static_cast<uint32_t>((i / p.nst) & 1));
+                if (!(hold && i == 0)) mbar_drain(&full[i % p.nst], static_cast<uint32_t>((i / p.nst) & 1));
         }
         return;
     }
@@ -819,6 +819,7 @@ cudaError_t launch_decode(const KGeom& g, const void* q, const void* pool, const
     p.q_bytes = s.q_bytes;
     p.qslot_bytes = s.qslot_bytes;
     p.stages_off = s.stages_off;
+    p.hold_first_copy = debug_hold_first_copy();
     CUtensorMap map;
     if (!encode_pool_map(&map, g, pool)) return cudaErrorInvalidValue;
 

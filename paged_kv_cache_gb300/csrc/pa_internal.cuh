@@ -568,6 +568,9 @@ EncodeTiledFn tensor_map_encoder();
 
 // ------------------------------------------------------------ host entry
 
+// The diagnostic switch of pa_debug_hold_first_copy (0 unless a test set it).
+int debug_hold_first_copy();
+
 // Kernel launchers (one per translation unit); return a cudaError_t.
 cudaError_t launch_write_kv(const KGeom& g, void* pool, const int32_t* block_table, int layer,
                             int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,

@@ -110,6 +110,7 @@ struct PrefillParams {
     const float* cos_tab;  // RoPE-Q: angle tables [max_pos][d/2] (null without RoPE)
     const float* sin_tab;
     int max_pos;
+    int hold_first_copy;   // diagnostic: CTA 0 arms its query copy without issuing it
 };
 
 // P = 2^(s * sc + nm) of 32 scores, packed to bf16 pairs; adds the fp32 P to ls.
@@ -398,30 +399,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    int producer_issued = 0;       // K/V tiles the producer issued (its lane 0 drains them on an abort)
+    bool producer_held_q = false;  // the diagnostic hold kept the query copy back
 
     if (warp == C::PRODUCER_WARP) {
         // ------------------------------------------------------------ TMA producer
+        // the diagnostic hold: the query tiles' barrier is armed but no copy is
+        // issued, so its phase never completes and the waits on it run out
+        const bool hold_q = p.hold_first_copy && blockIdx.x == 0;
         if (lane == 0) {
             prefetch_tensor_map(&qmap);
             prefetch_tensor_map(&kvmap);
             mbar_arrive_expect_tx(q_full, T * C::Q_BYTES);
+            if (!hold_q) {
 #pragma unroll
-            for (int t = 0; t < T; ++t)
+                for (int t = 0; t < T; ++t)
 #pragma unroll
-                for (int c = 0; c < C::KCH; ++c)
-                    tma_load_2d(sQ + t * C::Q_BYTES + c * kQChunkBytes, &qmap, (hq0 + t) * D + 64 * c, cu0 + i * BM,
-                                q_full);
+                    for (int c = 0; c < C::KCH; ++c)
+                        tma_load_2d(sQ + t * C::Q_BYTES + c * kQChunkBytes, &qmap, (hq0 + t) * D + 64 * c,
+                                    cu0 + i * BM, q_full);
+            }
         }
         const int oob_row = static_cast<int>(g.nblocks * 32);  // first row past the pool: zero fill
         int issued = 0;
-        bool stop = false;
         for (int j = 0; j < nkv; ++j) {
             const int st = j % C::NST;
             if (j >= C::NST &&
-                !__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((j / C::NST) - 1) & 1, abort_flag, p.err))) {
-                stop = true;
-                break;
-            }
+                !__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((j / C::NST) - 1) & 1, abort_flag, p.err)))
+                break;  // another role stopped the CTA, or the wait ran out (then *abort_flag is set)
             // lanes 0..3 fetch the tile's page ids
             const int lp = j * kPagesPerTile + lane;
             int row = -1;
@@ -449,11 +454,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
             ++issued;
         }
-        if (stop && lane == 0) {  // let every copy in flight land before leaving
-            mbar_drain(q_full, 0);
-            for (int jj = issued > C::NST ? issued - C::NST : 0; jj < issued; ++jj)
-                mbar_drain(&kv_full[jj % C::NST], (jj / C::NST) & 1);
-        }
+        producer_issued = issued;
+        producer_held_q = hold_q;
     } else if (warp >= C::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuers
         // Per key tile j, for each of this warp's query tiles in turn: once its
@@ -555,6 +557,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         tc_fence_after_sync();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
+    // Without an abort every copy issued was waited for by the role that uses
+    // it.  After one, the copies still in flight land before the CTA leaves
+    // (phases already complete return at once).
+    if (warp == C::PRODUCER_WARP && lane == 0 && *abort_flag) {
+        if (!producer_held_q) mbar_drain(q_full, 0);
+        for (int jj = producer_issued > C::NST ? producer_issued - C::NST : 0; jj < producer_issued; ++jj)
+            mbar_drain(&kv_full[jj % C::NST], (jj / C::NST) & 1);
+    }
 }
 
 // 2D bf16 tensor [rows][cols] with row pitch `pitch_bytes`, box {64, box_rows},
@@ -621,6 +631,7 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, cons
     p.cos_tab = cos_tab;
     p.sin_tab = sin_tab;
     p.max_pos = max_pos;
+    p.hold_first_copy = debug_hold_first_copy();
     if (g.d == 64) {
         if (p.heads_per_cta == 4) return launch<64, 4>(qmap, kvmap, p, stream);
         if (p.heads_per_cta == 2) return launch<64, 2>(qmap, kvmap, p, stream);
