@@ -111,6 +111,8 @@ struct PrefillParams {
     const float* sin_tab;
     int max_pos;
     int hold_first_copy;   // diagnostic: CTA 0 arms its query copy without issuing it
+    int item_base;         // work item of this launch's CTA 0
+    int tail;              // launched as a programmatic dependent of the launch before it
 };
 
 // P = 2^(s * sc + nm) of 32 scores, packed to bf16 pairs; adds the fp32 P to ls.
@@ -345,12 +347,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const KGeom& g = p.g;
+    // A launch of the tail items may be scheduled once every CTA of this one
+    // has started: it then fills the SMs this launch's last wave leaves idle.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // The tail launch reads nothing the launch before it writes; its CTAs only
+    // wait for that launch to finish before they leave (tail_wait at every
+    // exit), so that the call is complete, in stream order, when the tail
+    // launch is.
+    auto tail_wait = [&p]() {
+        if (p.tail) asm volatile("griddepcontrol.wait;" ::: "memory");
+    };
 
     // ---- work item: row tile (heaviest first), sequence, kv head, group of T q heads
     const int qgroups = g.group / T;
     const int units = g.hkv * qgroups;
     const int per_tile = p.batch * units;
-    const int item = blockIdx.x;
+    const int item = blockIdx.x + p.item_base;
     const int i = p.n_row_tiles - 1 - item / per_tile;
     const int rem = item % per_tile;
     const int b = rem / units;
@@ -363,8 +375,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const bool bad_len = cu0 < 0 || n < 0 || cu1 > p.total_tokens || n > p.max_seqlen || pre < 0 ||
                          static_cast<long long>(pre) + n > static_cast<long long>(g.maxb) * kBlockTokens;
     if (i == 0 && u == 0 && tid == 0 && bad_len) set_error(p.err, PA_ERR_BAD_BLOCK);
-    if (bad_len || n <= 0) return;
-    if (i * BM >= n) return;
+    if (bad_len || n <= 0 || i * BM >= n) {
+        tail_wait();
+        return;
+    }
     const int slot = p.slots[b];
     const bool slot_ok = slot >= 0 && slot < g.num_slots;
     if (!slot_ok && tid == 0) set_error(p.err, PA_ERR_BAD_BLOCK);
@@ -565,6 +579,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (int jj = producer_issued > C::NST ? producer_issued - C::NST : 0; jj < producer_issued; ++jj)
             mbar_drain(&kv_full[jj % C::NST], (jj / C::NST) & 1);
     }
+    tail_wait();
 }
 
 // 2D bf16 tensor [rows][cols] with row pitch `pitch_bytes`, box {64, box_rows},
@@ -582,16 +597,54 @@ bool encode_2d(CUtensorMap* map, const void* base, unsigned long long cols, unsi
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Work items [first, first + count) of the T-heads-per-CTA numbering; `tail`
+// launches them as a programmatic dependent of the launch before.
 template <int D, int T>
-cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, const PrefillParams& p, cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, PrefillParams p, long long first,
+                   long long count, bool tail, cudaStream_t stream) {
     using C = Cfg<D, T>;
     auto kern = p.cos_tab ? prefill_kernel<D, T, true> : prefill_kernel<D, T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    const long long grid = static_cast<long long>(p.n_row_tiles) * p.batch * (p.g.hq / T);
-    if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
-    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(qmap, kvmap, p);
-    return cudaGetLastError();
+    if (count <= 0) return cudaSuccess;
+    if (first + count > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    p.heads_per_cta = T;
+    p.item_base = static_cast<int>(first);
+    p.tail = tail ? 1 : 0;
+    if (!tail) {
+        kern<<<static_cast<unsigned>(count), C::THREADS, C::SMEM, stream>>>(qmap, kvmap, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(count), 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, qmap, kvmap, p);
+}
+
+// The call's work items with T q heads per CTA, heaviest first.  When they
+// make only a few waves over the SMs and the last one is partial, the items of
+// that last wave run instead with T/2 heads per CTA (each item is exactly two
+// of those, the same rows and kv head), as twice as many half-size CTAs in a
+// second launch that starts while the first one's last wave runs.
+template <int D, int T>
+cudaError_t launch_items(const CUtensorMap& qmap, const CUtensorMap& kvmap, const PrefillParams& p, int sms,
+                         cudaStream_t stream) {
+    const long long n = static_cast<long long>(p.n_row_tiles) * p.batch * (p.g.hq / T);
+    constexpr int kFewWaves = 8;
+    if (T == 1 || sms <= 0 || n % sms == 0 || n >= static_cast<long long>(kFewWaves) * sms)
+        return launch<D, T>(qmap, kvmap, p, 0, n, false, stream);
+    constexpr int TH = T > 1 ? T / 2 : 1;
+    const long long full = n / sms * sms;  // items of the whole waves
+    cudaError_t e = launch<D, T>(qmap, kvmap, p, 0, full, false, stream);
+    if (e != cudaSuccess) return e;
+    return launch<D, TH>(qmap, kvmap, p, 2 * full, 2 * (n - full), full > 0, stream);
 }
 
 }  // namespace
@@ -632,13 +685,20 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, cons
     p.sin_tab = sin_tab;
     p.max_pos = max_pos;
     p.hold_first_copy = debug_hold_first_copy();
+    p.item_base = 0;
+    p.tail = 0;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     if (g.d == 64) {
-        if (p.heads_per_cta == 4) return launch<64, 4>(qmap, kvmap, p, stream);
-        if (p.heads_per_cta == 2) return launch<64, 2>(qmap, kvmap, p, stream);
-        return launch<64, 1>(qmap, kvmap, p, stream);
+        if (p.heads_per_cta == 4) return launch_items<64, 4>(qmap, kvmap, p, sms, stream);
+        if (p.heads_per_cta == 2) return launch_items<64, 2>(qmap, kvmap, p, sms, stream);
+        return launch_items<64, 1>(qmap, kvmap, p, sms, stream);
     }
-    if (p.heads_per_cta == 2) return launch<128, 2>(qmap, kvmap, p, stream);
-    return launch<128, 1>(qmap, kvmap, p, stream);
+    if (p.heads_per_cta == 2) return launch_items<128, 2>(qmap, kvmap, p, sms, stream);
+    return launch_items<128, 1>(qmap, kvmap, p, sms, stream);
 }
 
 }  // namespace pa

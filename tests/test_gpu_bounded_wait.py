@@ -48,7 +48,7 @@ def test_prefill_wait_runs_out_and_the_next_call_is_right(rope):
         torch = H.torch_mod()
 
         def run():
-            o = torch.empty((case.total_tokens, 8, 64), dtype=torch.int16, device="cuda")
+            o = torch.zeros((case.total_tokens, 8, 64), dtype=torch.int16, device="cuda")
             lse = torch.empty((case.total_tokens, 8), dtype=torch.float32, device="cuda")
             err = torch.zeros(1, dtype=torch.int32, device="cuda")
             pa.pa_prefill_rope(H.pa_geom(case), H.to_dev(case.q), pool, bt, 0, H.to_dev(case.cu_seqlens), None,
@@ -56,8 +56,9 @@ def test_prefill_wait_runs_out_and_the_next_call_is_right(rope):
             torch.cuda.synchronize()
             return H.f32(o.cpu().numpy().view(np.uint16)), lse.cpu().numpy().astype(np.float64), int(err.item())
     else:
-        def run():
-            return H.gpu_prefill(case, pool, bt)
+        def run():  # zeroed outputs: the held CTA's rows stay unwritten
+            return H.gpu_prefill(case, pool, bt, o=H.torch_mod().zeros((case.total_tokens, 8, 64),
+                                                                         dtype=H.torch_mod().int16, device="cuda"))
     (o, l, err), secs = _held(run)
     assert err == pa.PA_ERR_TIMEOUT, pa.pa_status_string(err)
     assert secs >= 0.9 * WAIT_LIMIT_S
