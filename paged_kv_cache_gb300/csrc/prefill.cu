@@ -113,6 +113,7 @@ struct PrefillParams {
     int hold_first_copy;   // diagnostic: CTA 0 arms its query copy without issuing it
     int item_base;         // work item of this launch's CTA 0
     int tail;              // launched as a programmatic dependent of the launch before it
+    int has_tail;          // a tail launch follows this one
 };
 
 // P = 2^(s * sc + nm) of 32 scores, packed to bf16 pairs; adds the fp32 P to ls.
@@ -349,7 +350,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const KGeom& g = p.g;
     // A launch of the tail items may be scheduled once every CTA of this one
     // has started: it then fills the SMs this launch's last wave leaves idle.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (p.has_tail) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // The tail launch reads nothing the launch before it writes; its CTAs only
     // wait for that launch to finish before they leave (tail_wait at every
     // exit), so that the call is complete, in stream order, when the tail
@@ -601,7 +602,7 @@ bool encode_2d(CUtensorMap* map, const void* base, unsigned long long cols, unsi
 // launches them as a programmatic dependent of the launch before.
 template <int D, int T>
 cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, PrefillParams p, long long first,
-                   long long count, bool tail, cudaStream_t stream) {
+                   long long count, bool tail, bool has_tail, cudaStream_t stream) {
     using C = Cfg<D, T>;
     auto kern = p.cos_tab ? prefill_kernel<D, T, true> : prefill_kernel<D, T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -611,6 +612,7 @@ cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, PrefillPar
     p.heads_per_cta = T;
     p.item_base = static_cast<int>(first);
     p.tail = tail ? 1 : 0;
+    p.has_tail = has_tail ? 1 : 0;
     if (!tail) {
         kern<<<static_cast<unsigned>(count), C::THREADS, C::SMEM, stream>>>(qmap, kvmap, p);
         return cudaGetLastError();
@@ -639,12 +641,12 @@ cudaError_t launch_items(const CUtensorMap& qmap, const CUtensorMap& kvmap, cons
     const long long n = static_cast<long long>(p.n_row_tiles) * p.batch * (p.g.hq / T);
     constexpr int kFewWaves = 8;
     if (T == 1 || sms <= 0 || n % sms == 0 || n >= static_cast<long long>(kFewWaves) * sms)
-        return launch<D, T>(qmap, kvmap, p, 0, n, false, stream);
+        return launch<D, T>(qmap, kvmap, p, 0, n, false, false, stream);
     constexpr int TH = T > 1 ? T / 2 : 1;
     const long long full = n / sms * sms;  // items of the whole waves
-    cudaError_t e = launch<D, T>(qmap, kvmap, p, 0, full, false, stream);
+    cudaError_t e = launch<D, T>(qmap, kvmap, p, 0, full, false, true, stream);
     if (e != cudaSuccess) return e;
-    return launch<D, TH>(qmap, kvmap, p, 2 * full, 2 * (n - full), full > 0, stream);
+    return launch<D, TH>(qmap, kvmap, p, 2 * full, 2 * (n - full), full > 0, false, stream);
 }
 
 }  // namespace
@@ -687,6 +689,7 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, cons
     p.hold_first_copy = debug_hold_first_copy();
     p.item_base = 0;
     p.tail = 0;
+    p.has_tail = 0;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
