@@ -45,6 +45,25 @@
 
 #include "pa_internal.cuh"
 
+// Profiling build only (PA_DECODE_TRACE, libpa_trace.so): globaltimer marks of
+// every attend CTA (start, first page in shared memory, end, SM) and every
+// merge CTA (past the grid dependency, end), read back by
+// paged_kv_cache_gb300/decode_trace.py.  The product library has none of it.
+#ifndef PA_DECODE_TRACE
+#define PA_DECODE_TRACE 0
+#endif
+#if PA_DECODE_TRACE
+namespace pa {
+constexpr int kTraceAttend = 1024, kTraceMerge = 8192;
+__device__ unsigned long long g_trace[kTraceAttend * 4 + kTraceMerge * 2];
+__device__ __forceinline__ void trace_set(int i, unsigned long long v) { g_trace[i] = v; }
+__device__ __forceinline__ void trace_max(int i, unsigned long long v) { atomicMax(&g_trace[i], v); }
+}  // namespace pa
+#define PA_TRACE(stmt) stmt
+#else
+#define PA_TRACE(stmt)
+#endif
+
 namespace pa {
 namespace {
 
@@ -180,6 +199,12 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
     // The merge grid may be scheduled now: its CTAs wait (griddepcontrol.wait)
     // until this grid has finished and its writes are visible.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    PA_TRACE(if (tid == 0 && blockIdx.x < kTraceAttend) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        trace_set(blockIdx.x * 4 + 0, global_timer_ns());
+        trace_set(blockIdx.x * 4 + 3, smid);
+    })
 
     if (tid == 0) {
         for (int s = 0; s < p.nst; ++s) {
@@ -357,6 +382,8 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
     for (long long k = 0; k < n_pages; ++k) {
         const int st = static_cast<int>(k % p.nst);
         if (!mbar_wait(&full[st], static_cast<uint32_t>((k / p.nst) & 1), abort_flag, p.err)) break;
+        PA_TRACE(if (k == 0 && warp == 1 && lane == 0 && blockIdx.x < kTraceAttend)
+                     trace_set(blockIdx.x * 4 + 1, global_timer_ns());)
         uint8_t* stage = stages + static_cast<long long>(st) * p.kv_stage_bytes;
         const uint8_t* qslot = qslots + st * p.qslot_bytes;
         const StageHeader hdr = *reinterpret_cast<const StageHeader*>(qslot + p.q_bytes);
@@ -463,6 +490,7 @@ decode_attend_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodePara
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
     }
+    PA_TRACE(if (lane == 0 && blockIdx.x < kTraceAttend) trace_max(blockIdx.x * 4 + 2, global_timer_ns());)
 }
 
 // The CTAs of the attend grid that hold sequence b, from the lengths and the
@@ -528,6 +556,16 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     const long long G = p.attend_grid;
     const SeqSpan sp = seq_span(p, b, G, red);
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    PA_TRACE(const int trace_id = blockIdx.y * gridDim.x + blockIdx.x;
+             if (threadIdx.x == 0 && trace_id < kTraceMerge)
+                 trace_set(kTraceAttend * 4 + trace_id * 2, global_timer_ns());
+             struct TraceEnd {
+                 int id;
+                 __device__ ~TraceEnd() {
+                     if ((threadIdx.x & 31) == 0 && id < kTraceMerge)
+                         trace_max(kTraceAttend * 4 + id * 2 + 1, global_timer_ns());
+                 }
+             } trace_end{trace_id};)
     if (hq >= g.hq) return;
     const long long row = static_cast<long long>(b) * g.hq + hq;
     if (sp.len <= 0) {
@@ -625,6 +663,16 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_split_kernel(const
     const long long G = p.attend_grid;
     const SeqSpan sp = seq_span(p, b, G, red);
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    PA_TRACE(const int trace_id = blockIdx.y * gridDim.x + blockIdx.x;
+             if (threadIdx.x == 0 && trace_id < kTraceMerge)
+                 trace_set(kTraceAttend * 4 + trace_id * 2, global_timer_ns());
+             struct TraceEnd {
+                 int id;
+                 __device__ ~TraceEnd() {
+                     if ((threadIdx.x & 31) == 0 && id < kTraceMerge)
+                         trace_max(kTraceAttend * 4 + id * 2 + 1, global_timer_ns());
+                 }
+             } trace_end{trace_id};)
     const long long row = static_cast<long long>(b) * g.hq + hq;
     if (sp.len <= 0) {
         if (warp == 0) {
@@ -882,6 +930,18 @@ cudaError_t static_scratch(void** out) {
 
 }  // namespace
 }  // namespace pa
+
+#if PA_DECODE_TRACE
+// Profiling build only: clear the marks / copy them to host memory.
+extern "C" __attribute__((visibility("default"))) int pa_trace_decode_reset(void) {
+    static unsigned long long zero[pa::kTraceAttend * 4 + pa::kTraceMerge * 2];
+    return cudaMemcpyToSymbol(pa::g_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
+}
+extern "C" __attribute__((visibility("default"))) int pa_trace_decode_read(void* host, size_t bytes) {
+    if (bytes < sizeof(pa::g_trace)) return 1;
+    return cudaMemcpyFromSymbol(host, pa::g_trace, sizeof(pa::g_trace)) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 extern "C" __attribute__((visibility("default"))) pa_status pa_decode_noalloc(
     const pa_geom* geom, const void* q, const void* pool, const int32_t* block_table, int32_t layer,
