@@ -125,3 +125,34 @@ def test_bad_prefix_reports_and_recovers():
     assert err == 0
     ro, rl = H.oracle_prefill_cached(case, H.oracle_pool(case))
     H.assert_close(o, l, ro, rl, H.max_abs_v(case), "after bad prefixes")
+
+
+def test_chunked_bench_size_tail_launch():
+    """The chunked bench workload (4 x 2048 queries after 6144 cached tokens,
+    32 q / 8 kv heads, d 64): 512 four-head work items on the GPU's SMs make
+    more than three waves, so the last wave's items (row tiles 0 and 1 of every
+    sequence) run as two-head CTAs in a second, dependent launch.  Sampled rows
+    of every sequence, most of them in those row tiles, against the oracle."""
+    import oracle
+    prefix, chunk = 6144, 2048
+    pages = (prefix + chunk) // 16
+    geom = W.Geometry(32, 8, 64, 1, 4, pages, 4 * pages + 64)
+    case = W.make_chunked_case("tail", geom, [prefix] * 4, [chunk] * 4, seed=1006)
+    pool, bt, werr = H.gpu_setup(case)
+    assert werr == 0
+    o, l, err = H.gpu_prefill_cached(case, pool, bt)
+    assert err == 0
+    vmax = H.max_abs_v(case)
+    assert np.all(np.isfinite(o)) and np.max(np.abs(o)) <= vmax * (1 + 2 ** -7)
+    rng = np.random.default_rng(23)
+    cu, Hq = case.cu_seqlens, geom.num_q_heads
+    rows, heads = [], []
+    for b in range(case.batch):
+        for r in list(rng.integers(0, 256, 24)) + [0, 127, 128, 255, 1024, chunk - 1]:
+            rows.append(cu[b] + r)
+            heads.append(int(rng.integers(Hq)))
+    rows += [cu[1]] * Hq  # every head of one row of the tail
+    heads += list(range(Hq))
+    rows, heads = np.array(rows, np.int64), np.array(heads, np.int32)
+    ro, rl = H.oracle_prefill_cached(case, H.oracle_pool(case), rows=rows, heads=heads)
+    H.assert_close(o[rows, heads], l[rows, heads], ro, rl, vmax, "chunked bench size")
