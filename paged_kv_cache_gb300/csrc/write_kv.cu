@@ -19,7 +19,10 @@ namespace {
 // CPT 16-byte chunks of one K or V row per thread, a row's chunks/CPT threads
 // apart (CPT divides the row's chunk count).  The row's data is read before its page is looked up,
 // so the two global latencies overlap instead of adding up.
-template <int CPT>
+// V_ONLY: the V rows alone, for the RoPE scatter, which turns K in a kernel of
+// its own (rows at a position >= max_pos are skipped there too); this launch
+// lets that one start at once (it reads nothing this one writes).
+template <int CPT, bool V_ONLY>
 __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restrict__ pool,
                                                        const int32_t* __restrict__ block_table,
                                                        int layer, int n_tokens,
@@ -27,18 +30,20 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
                                                        const int32_t* __restrict__ tok_pos,
                                                        const uint4* __restrict__ k_new,
                                                        const uint4* __restrict__ v_new,
-                                                       int32_t* err) {
+                                                       int max_pos, int32_t* err) {
+    if (V_ONLY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int chunks = g.kv_dim / 8;  // 16-byte chunks per K (or V) row
     const int groups = chunks / CPT;  // threads per K (or V) row
-    const long long total = static_cast<long long>(n_tokens) * 2 * groups;
+    const int per_row = V_ONLY ? groups : 2 * groups;
+    const long long total = static_cast<long long>(n_tokens) * per_row;
     const long long half_page = g.page_bytes / 2;  // V_OFFSET
     const long long row_bytes = static_cast<long long>(g.kv_dim) * 2;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long row = idx / (2 * groups);
-        const int rem = static_cast<int>(idx - row * 2 * groups);
-        const int is_v = rem >= groups;
-        const int c = is_v ? rem - groups : rem;  // chunks c, c + groups, c + 2 groups, ...
+        const long long row = idx / per_row;
+        const int rem = static_cast<int>(idx - row * per_row);
+        const int is_v = V_ONLY || rem >= groups;
+        const int c = V_ONLY ? rem : is_v ? rem - groups : rem;  // chunks c, c + groups, c + 2 groups, ...
         const uint4* src = (is_v ? v_new : k_new) + row * chunks + c;
         uint4 val[CPT];
 #pragma unroll
@@ -49,7 +54,7 @@ __global__ void __launch_bounds__(256) write_kv_kernel(KGeom g, uint8_t* __restr
         const int slot = __ldg(tok_slot + row);
         const int pos = __ldg(tok_pos + row);
         long long blk = -1;
-        if (slot >= 0 && slot < g.num_slots && pos >= 0 && pos / kBlockTokens < g.maxb) {
+        if (slot >= 0 && slot < g.num_slots && pos >= 0 && pos / kBlockTokens < g.maxb && (!V_ONLY || pos < max_pos)) {
             const long long tidx =
                 (static_cast<long long>(slot) * g.n_layers + layer) * g.maxb + pos / kBlockTokens;
             const int e = __ldg(block_table + tidx);
@@ -91,7 +96,7 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 
 constexpr int kRopeRows = 8;  // rows per thread group of the RoPE scatter
 
-template <int KPT, int VPT>
+template <int KPT, int VPT, bool K_ONLY>
 __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __restrict__ pool,
                                                             const int32_t* __restrict__ block_table, int layer,
                                                             int n_tokens, const int32_t* __restrict__ tok_slot,
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __
     const int vc = g.kv_dim / 8;        // 16-byte V chunks per row
     const int vt = vc / VPT;            // V threads per row
     const int k_threads = kRopeRows * kt;
-    const int per_group = k_threads + kRopeRows * vt;
+    const int per_group = k_threads + (K_ONLY ? 0 : kRopeRows * vt);
     const long long total = static_cast<long long>((n_tokens + kRopeRows - 1) / kRopeRows) * per_group;
     const long long half_page = g.page_bytes / 2;  // V_OFFSET
     const long long row_bytes = static_cast<long long>(g.kv_dim) * 2;
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const long long grp = idx / per_group;
         const int rem = static_cast<int>(idx - grp * per_group);
-        const bool is_k = rem < k_threads;
+        const bool is_k = K_ONLY || rem < k_threads;
         const int local = is_k ? rem / kt : (rem - k_threads) / vt;
         const int c = is_k ? rem % kt : (rem - k_threads) % vt;  // K: (first head, pair chunk); V: first chunk
         const int c8 = 8 * (c % hc);                             // K: first pair element within the head
@@ -173,6 +178,9 @@ __global__ void __launch_bounds__(256) write_kv_rope_kernel(KGeom g, uint8_t* __
             for (int x = 0; x < VPT; ++x) dv[x * vt] = vv[x];
         }
     }
+    // K_ONLY runs as a programmatic dependent of the V copy: it leaves only once
+    // that launch is complete, so the call is, in stream order, when this is.
+    if (K_ONLY) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
@@ -181,21 +189,44 @@ cudaError_t launch_write_kv_rope(const KGeom& g, void* pool, const int32_t* bloc
                                  int n_tokens, const int32_t* tok_slot, const int32_t* tok_pos,
                                  const void* k_new, const void* v_new, const float* cos_tab,
                                  const float* sin_tab, int max_pos, int32_t* err, cudaStream_t stream) {
-    // KPT heads' pairs and 2 KPT V chunks per thread: KPT divides the kv head
-    // count, and d a multiple of 16 makes the V chunk count (2 Hkv d/16) a
-    // multiple of 2 KPT
+    // V rows by the plain scatter (few registers, many bytes in flight), then
+    // K turned by the RoPE kernel in a launch that runs beside it; KPT heads'
+    // pairs per thread, KPT dividing the kv head count
+    const int threads = 256;
+    {
+        const int chunks = g.kv_dim / 8;
+        const int cpt = chunks % 8 == 0 ? 8 : chunks % 4 == 0 ? 4 : 1;
+        const long long total = static_cast<long long>(n_tokens) * (chunks / cpt);
+        long long blocks = (total + threads - 1) / threads;
+        if (blocks > (1ll << 30)) blocks = 1ll << 30;  // grid-stride covers the rest
+        auto kern = cpt == 8 ? write_kv_kernel<8, true> : cpt == 4 ? write_kv_kernel<4, true> : write_kv_kernel<1, true>;
+        kern<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+            g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
+            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), max_pos, err);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const int kpt = g.hkv % 4 == 0 ? 4 : g.hkv % 2 == 0 ? 2 : 1;
     const int hc = g.d / 16;
-    const int per_group = kRopeRows * (g.hkv / kpt * hc + g.kv_dim / 8 / (2 * kpt));
+    const int per_group = kRopeRows * (g.hkv / kpt * hc);
     const long long total = static_cast<long long>((n_tokens + kRopeRows - 1) / kRopeRows) * per_group;
-    const int threads = 256;
     long long blocks = (total + threads - 1) / threads;
-    if (blocks > (1ll << 30)) blocks = 1ll << 30;  // grid-stride covers the rest
-    auto kern = kpt == 4 ? write_kv_rope_kernel<4, 8> : kpt == 2 ? write_kv_rope_kernel<2, 4> : write_kv_rope_kernel<1, 2>;
-    kern<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), cos_tab, sin_tab, max_pos, err);
-    return cudaGetLastError();
+    if (blocks > (1ll << 30)) blocks = 1ll << 30;
+    auto kern = kpt == 4 ? write_kv_rope_kernel<4, 8, true>
+                         : kpt == 2 ? write_kv_rope_kernel<2, 4, true> : write_kv_rope_kernel<1, 2, true>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot,
+                              tok_pos, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), cos_tab,
+                              sin_tab, max_pos, err);
 }
 
 cudaError_t launch_write_kv(const KGeom& g, void* pool, const int32_t* block_table, int layer,
@@ -209,17 +240,17 @@ cudaError_t launch_write_kv(const KGeom& g, void* pool, const int32_t* block_tab
     long long blocks = (total + threads - 1) / threads;
     if (blocks > (1ll << 30)) blocks = 1ll << 30;  // grid-stride covers the rest
     if (cpt == 8)
-        write_kv_kernel<8><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        write_kv_kernel<8, false><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
             g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
-            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), err);
+            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), 0, err);
     else if (cpt == 4)
-        write_kv_kernel<4><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        write_kv_kernel<4, false><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
             g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
-            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), err);
+            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), 0, err);
     else
-        write_kv_kernel<1><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        write_kv_kernel<1, false><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
             g, static_cast<uint8_t*>(pool), block_table, layer, n_tokens, tok_slot, tok_pos,
-            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), err);
+            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), 0, err);
     return cudaGetLastError();
 }
 
