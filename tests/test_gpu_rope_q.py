@@ -115,11 +115,13 @@ def test_positions_past_the_table_are_reported():
     H.assert_close(o[:n0], l[:n0], ro[:n0], rl[:n0], H.max_abs_v(case), "rope-q rows inside the table")
 
 
-def test_rope_q_long_prefill_sampled():
-    """The 4 x 8192 bench workload with K and Q turned, on sampled rows of
-    every sequence (both ends of each, every head of the last row)."""
-    case = W.long_prefill_case("d64")
-    cos_t, sin_t = W.rope_tables(8192, 64)
+@pytest.mark.parametrize("variant", ["d64", "d128"])
+def test_rope_q_long_prefill_sampled(variant):
+    """The 4 x 8192 bench workload with K and Q turned (32 q / 8 kv heads at
+    d 64, 16 / 4 at d 128), on sampled rows of every sequence (both ends of
+    each, every head of the last row)."""
+    case = W.long_prefill_case(variant)
+    cos_t, sin_t = W.rope_tables(8192, case.geom.head_dim)
     pool, bt, ref = _write_rope(case, cos_t, sin_t)
     o, l, err = _gpu_rope(case, pool, bt, cos_t, sin_t, None)
     assert err == 0
