@@ -16,15 +16,17 @@ std::atomic<int> g_hold_first_copy{0};
 int debug_hold_first_copy() { return g_hold_first_copy.load(std::memory_order_relaxed); }
 
 EncodeTiledFn tensor_map_encoder() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    // looked up once, by the first call from any thread (a function-local
+    // static is initialised exactly once, so concurrent first calls do not race)
+    static const EncodeTiledFn fn = [] {
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
+            return reinterpret_cast<EncodeTiledFn>(ptr);
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
     return fn;
 }
 }  // namespace pa

@@ -395,3 +395,27 @@ rescale factor for l and O is tiny (it may flush to zero)."""
     ref = H.oracle_prefill if kind == "prefill" else H.oracle_decode
     ro, rl = ref(case, H.oracle_pool(case))
     H.assert_close(o, l, ro, rl, H.max_abs_v(case), "jump " + kind)
+
+
+def test_decode_layer_and_slot_indirection():
+    """A three-layer table, the decode reading layer 2 of slots that are not the
+    batch index (a permutation of some of six slots), beside a chunked prefill
+    reading the same layer: the table index is ((slot L) + layer) MAXB + page."""
+    geom = W.Geometry(32, 8, 64, 3, 6, 40, 200)
+    lens = [600, 17, 1, 300]
+    slots = [5, 0, 3, 1]
+    case = W.make_decode_case("layer2", geom, lens, seed=44, layer=2, slots=slots, pool_fill="nan")
+    pool, bt, werr = H.gpu_setup(case)
+    assert werr == 0
+    o, l, err = H.gpu_decode(case, pool, bt)
+    assert err == 0
+    ro, rl = H.oracle_decode(case, H.oracle_pool(case))
+    H.assert_close(o, l, ro, rl, H.max_abs_v(case), "decode at layer 2, slots %s" % slots)
+    ccase = W.make_chunked_case("layer2c", geom, [100, 0, 33], [77, 130, 1], seed=45, layer=2, slots=[4, 2, 5],
+                                pool_fill="nan")
+    pool, bt, werr = H.gpu_setup(ccase)
+    assert werr == 0
+    o, l, err = H.gpu_prefill_cached(ccase, pool, bt)
+    assert err == 0
+    ro, rl = H.oracle_prefill_cached(ccase, H.oracle_pool(ccase))
+    H.assert_close(o, l, ro, rl, H.max_abs_v(ccase), "chunked prefill at layer 2")
