@@ -216,52 +216,95 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
             break;
         }
         tc_fence_after_sync();
-        // the row max of the 64 scores; the second half stays in registers
         const int rel = BN * j - pos0;  // first key of the tile relative to the first row's position
         const bool diag = rel > -BN;      // the tile crosses the diagonal
-        uint32_t vb[32];
-        float m_tile;
-        {
-            uint32_t va[32];
-            tmem_ld_x32(tS, va);
-            if (diag) mask_chunk(va, rel, r);
-            m_tile = chunk_max(va, -CUDART_INF_F);
-        }
-        tmem_ld_x32(tS + 32, vb);
-        if (diag) mask_chunk(vb, rel + 32, r);
-        m_tile = sc * chunk_max(vb, m_tile);
         float f = 1.f;  // factor for l and this row of O when the reference moves
-        if (m_tile > m_o + kMoveAbove) {
-            f = ex2_approx(m_o - m_tile);  // 0 from -inf
-            l *= f;
-            m_o = m_tile;
-        }
-        const float nm = m_o == -CUDART_INF_F ? 0.f : -m_o;
-        // P of the second half from registers, over its own first 16 columns;
-        // then the first half read again
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        {
-            uint32_t pk[16];
-            p_chunk(vb, sc, nm, ls, pk);
-            tmem_st_x16_nowait(tS + 32, pk);
-        }
-        if (j > 0 && __any_sync(0xffffffffu, f != 1.f)) {
-            // this row of O follows the reference (no PV product is in flight)
+        // this row of O follows the reference (no PV product is in flight)
+        auto rescale_o = [&]() {
+            if (j > 0 && __any_sync(0xffffffffu, f != 1.f)) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t ov[32];
-                tmem_ld_x32(tO + 32 * c, ov);
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld_x32(tO + 32 * c, ov);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-                tmem_st_x32(tO + 32 * c, ov);
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+                    tmem_st_x32(tO + 32 * c, ov);
+                }
             }
-        }
-        {
-            uint32_t va[32], pk[16];
-            tmem_ld_x32(tS, va);
-            if (diag) mask_chunk(va, rel, r);
-            p_chunk(va, sc, nm, ls, pk);
-            tmem_st_x16_nowait(tS, pk);
+        };
+        if constexpr (D == 64) {
+            // one read of each 32-key half: the first half's max may move the
+            // reference and its P waits in registers; should the second half
+            // move it again (by more than 2^8, rare past the first tile), that
+            // P and the partial sums follow the new reference in registers
+            uint32_t pa[16];
+            {
+                uint32_t va[32];
+                tmem_ld_x32(tS, va);
+                if (diag) mask_chunk(va, rel, r);
+                const float m_a = sc * chunk_max(va, -CUDART_INF_F);
+                if (m_a > m_o + kMoveAbove) {
+                    f = ex2_approx(m_o - m_a);  // 0 from -inf
+                    l *= f;
+                    m_o = m_a;
+                }
+                p_chunk(va, sc, m_o == -CUDART_INF_F ? 0.f : -m_o, ls, pa);
+            }
+            {
+                uint32_t vb[32], pk[16];
+                tmem_ld_x32(tS + 32, vb);
+                if (diag) mask_chunk(vb, rel + 32, r);
+                const float m_b = sc * chunk_max(vb, -CUDART_INF_F);
+                if (m_b > m_o + kMoveAbove) {
+                    const float f2 = ex2_approx(m_o - m_b);
+                    f *= f2;
+                    l *= f2;
+                    m_o = m_b;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ls[e] *= f2;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pa[e] = pack_bf16x2(bf16lo(pa[e]) * f2, bf16hi(pa[e]) * f2);
+                }
+                p_chunk(vb, sc, m_o == -CUDART_INF_F ? 0.f : -m_o, ls, pk);
+                tmem_st_x16_nowait(tS + 32, pk);
+            }
+            tmem_st_x16_nowait(tS, pa);
+            rescale_o();
+        } else {
+            // the row max of the 64 scores first (the second half stays in
+            // registers), then P of the second half, then the first half read
+            // again: P overwrites S, so no P is formed before the max is known
+            uint32_t vb[32];
+            float m_tile;
+            {
+                uint32_t va[32];
+                tmem_ld_x32(tS, va);
+                if (diag) mask_chunk(va, rel, r);
+                m_tile = chunk_max(va, -CUDART_INF_F);
+            }
+            tmem_ld_x32(tS + 32, vb);
+            if (diag) mask_chunk(vb, rel + 32, r);
+            m_tile = sc * chunk_max(vb, m_tile);
+            if (m_tile > m_o + kMoveAbove) {
+                f = ex2_approx(m_o - m_tile);  // 0 from -inf
+                l *= f;
+                m_o = m_tile;
+            }
+            const float nm = m_o == -CUDART_INF_F ? 0.f : -m_o;
+            {
+                uint32_t pk[16];
+                p_chunk(vb, sc, nm, ls, pk);
+                tmem_st_x16_nowait(tS + 32, pk);
+            }
+            rescale_o();
+            {
+                uint32_t va[32], pk[16];
+                tmem_ld_x32(tS, va);
+                if (diag) mask_chunk(va, rel, r);
+                p_chunk(va, sc, nm, ls, pk);
+                tmem_st_x16_nowait(tS, pk);
+            }
         }
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         if (j == j_tail) {
