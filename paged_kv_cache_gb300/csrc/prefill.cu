@@ -192,7 +192,10 @@ __device__ __forceinline__ bool rope_q_row(uint8_t* tile, int r, bool turn, long
 }
 
 // Softmax of query tile t: the warp's thread owns row r (TMEM lane r).
-template <int D, int T>
+// ONE_PASS: each 32-key half of the scores is read from tensor memory once
+// (measured faster at d 64 without the query rotation; the max-first order
+// is faster at d 128 and with the rotation prologue)
+template <int D, int T, bool ONE_PASS>
 __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, int i, int nkv, int n, int pos0,
                                              int kv_len, int cu0, int hq,
                                              uint8_t* sKV, uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
@@ -233,7 +236,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
                 }
             }
         };
-        if constexpr (D == 64) {
+        if constexpr (ONE_PASS) {
             // one read of each 32-key half: the first half's max may move the
             // reference and its P waits in registers; should the second half
             // move it again (by more than 2^8, rare past the first tile), that
@@ -605,7 +608,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             if (ok) mbar_arrive_elect(q_ready);
         }
         if (ok)
-            softmax_role<D, T>(t, r, tmem + tmem_lane_base(warp), i, nkv, n, pre + BM * i, kv_len, cu0, hq0 + t, sKV,
+            softmax_role<D, T, D == 64 && !ROPE>(t, r, tmem + tmem_lane_base(warp), i, nkv, n, pre + BM * i, kv_len, cu0, hq0 + t, sKV,
                                &s_full[t], &p_full[t], &o_done[t], kv_full, abort_flag, p);
     }
 

@@ -377,6 +377,56 @@ def test_growing_scores_move_the_reference_max(kind):
     H.assert_close(o, l, ro, rl, H.max_abs_v(case), "ramp " + kind)
 
 
+def _second_half_moves(case):
+    """How many (row, q head, key tile) steps of a d-64 prefill move the
+    reference max in the tile's second 32-key half, by more than 2^8 past a
+    reference the first half may already have moved (host arithmetic on the
+    bf16 inputs, independent of the kernel)."""
+    g, w, cu = case.geom, case.writes[0], case.cu_seqlens
+    grp = g.num_q_heads // g.num_kv_heads
+    K = W.bf16_to_f32(w.k).astype(np.float64).reshape(-1, g.num_kv_heads, g.head_dim)
+    q = W.bf16_to_f32(case.q).astype(np.float64)
+    c = case.scale * np.log2(np.e)
+    count = 0
+    for b, n in enumerate(case.lens):
+        n = int(n)
+        sel = np.where(w.tok_slot == case.slots[b])[0]
+        sel = sel[np.argsort(w.tok_pos[sel])]
+        for h in range(g.num_q_heads):
+            s = q[cu[b]:cu[b] + n, h] @ K[sel, h // grp].T * c
+            s[np.triu_indices(n, 1)] = -np.inf
+            m = np.full(n, -np.inf)
+            for j in range((n + 63) // 64):
+                live = np.arange(n) >= 64 * j
+                halves = [s[:, 64 * j + 32 * k:64 * j + 32 * k + 32] for k in (0, 1)]
+                mx = [x.max(axis=1) if x.shape[1] else np.full(n, -np.inf) for x in halves]
+                m = np.where(live & (mx[0] > m + 8), mx[0], m)
+                moves = live & (mx[1] > m + 8)
+                count += int(moves.sum())
+                m = np.where(moves, mx[1], m)
+    return count
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_second_half_moves_the_reference(d):
+    """Key magnitudes that step up every 32 keys: in thousands of key tiles the
+    second 32-key half exceeds the reference max by more than 2^8 after the
+    first half has formed its P, which must then follow the new reference
+    (with the partial sums and l).  At d 128 the same inputs take the
+    max-first order."""
+    geom = W.Geometry(8, 2, d, 1, 3, 64, 120)
+    case = W.make_prefill_case("halfstep", geom, [700, 300, 129], seed=93, pool_fill="nan")
+    _scale_keys(case, lambda pos: (0.25 + 0.9 * (pos // 32)).astype(np.float32))
+    if d == 64:
+        assert _second_half_moves(case) > 1000
+    pool, bt, werr = H.gpu_setup(case)
+    assert werr == 0
+    o, l, err = H.gpu_prefill(case, pool, bt)
+    assert err == 0
+    ro, rl = H.oracle_prefill(case, H.oracle_pool(case))
+    H.assert_close(o, l, ro, rl, H.max_abs_v(case), "half-step keys d%d" % d)
+
+
 @pytest.mark.parametrize("kind", ["prefill", "decode"])
 def test_large_score_jump(kind):
     """Keys from position 300 on are 40x larger: the tile max jumps by far more
