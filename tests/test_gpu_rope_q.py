@@ -7,8 +7,8 @@ the queries with orc_rope_q and attends with orc_prefill_cached.  Covered:
 every q-heads-per-CTA variant of the kernel (4, 2, 1 at d 64; 2, 1 at d 128),
 prefixes that are and are not multiples of the page and of the tiles, a
 NaN-filled pool, the Llama-3.2-1B-shaped prompts, the 4 x 8192 bench
-workload on sampled rows, the identity table (bit for bit the plain
-prefill) and positions past the table.
+workload on sampled rows, the identity table (the plain prefill: bit for bit
+at d 128, within the bar at d 64) and positions past the table.
 """
 import numpy as np
 import pytest
@@ -86,17 +86,25 @@ def test_rope_q_llama_prompts():
     _check(case, None, cos_t, sin_t, "rope-q Llama prompts")
 
 
-def test_identity_table_is_the_plain_prefill_bit_for_bit():
-    geom = W.Geometry(32, 8, 64, 1, 3, 32, 100)
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 64), (16, 4, 128)])
+def test_identity_table_is_the_plain_prefill(hq, hkv, d):
+    """cos 1, sin 0 leaves Q and K as they are: the RoPE-Q prefill equals the
+    plain one.  Bit for bit at d 128, where both take the same softmax order;
+    at d 64 the plain kernel reads each score half once and the RoPE-Q one
+    takes the max first, so the two agree within the parity bar."""
+    geom = W.Geometry(hq, hkv, d, 1, 3, 32, 100)
     case = W.make_chunked_case("rq_id", geom, [0, 23, 64], [300, 77, 5], seed=4)
     n = 400
-    one, zero = np.ones((n, 32), np.float32), np.zeros((n, 32), np.float32)
+    one, zero = np.ones((n, d // 2), np.float32), np.zeros((n, d // 2), np.float32)
     pool, bt, _ = _write_rope(case, one, zero)
     o1, l1, e1 = _gpu_rope(case, pool, bt, one, zero, case.extra["prefix"])
     o2, l2, e2 = H.gpu_prefill_cached(case, pool, bt)
     assert e1 == 0 and e2 == 0
-    np.testing.assert_array_equal(o1, o2)
-    np.testing.assert_array_equal(l1, l2)
+    if d == 128:
+        np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(l1, l2)
+    else:
+        H.assert_close(o1, l1, o2, l2, H.max_abs_v(case), "identity table d64")
 
 
 def test_positions_past_the_table_are_reported():
