@@ -189,6 +189,13 @@ pa_status pa_prefill(const pa_geom* geom, const void* q, const void* pool,
  * each >= 0 with prefix_lens[b] + n_b <= 16 * max_blocks_per_seq (larger or
  * negative values set PA_ERR_BAD_BLOCK and leave that sequence's output
  * unspecified).  max_seqlen bounds the chunk lengths n_b only.
+ * With a prefix array, work items that would leave the GPU's last wave
+ * partly idle run as two halves of their key range whose fp32 partials are
+ * combined by the LSE rule (part 3, "causalMask and online softmax"): the
+ * result is deterministic and agrees with the NULL-prefix call to rounding,
+ * not bit for bit.  Those halves take a few MB of scratch from a stream-
+ * ordered memory pool of the library's own, allocated and freed on `stream`
+ * (kept for the process); if it cannot be had, the call runs without it.
  */
 pa_status pa_prefill_cached(const pa_geom* geom, const void* q, const void* pool,
                             const int32_t* block_table, int32_t layer, int32_t batch,

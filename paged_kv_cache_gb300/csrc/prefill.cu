@@ -50,6 +50,8 @@
 //    first QK product waits for every row to be turned.
 #include <math_constants.h>
 
+#include <mutex>
+
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -114,7 +116,21 @@ struct PrefillParams {
     int item_base;         // work item of this launch's CTA 0
     int tail;              // launched as a programmatic dependent of the launch before it
     int has_tail;          // a tail launch follows this one
+    // Key split (a tail launch only): CTA 2k + h takes half h of the key tiles
+    // of item item_base + k and leaves its partial (O not yet divided by l,
+    // with its m and l) in ws_o / ws_ml; the second of the two to finish, as
+    // counted in ws_cnt[k], combines both.
+    int ksplit;
+    float* ws_o;    // [items][2][T][BM][D]
+    float2* ws_ml;  // [items][2][T][BM]: (m in scaled log2 units, l)
+    int* ws_cnt;    // [items], zero before the launch
 };
+
+// Barrier among the first `threads` threads of the CTA (the softmax warps) on
+// hardware barrier 1; barrier 0 is the CTA-wide one.
+__device__ __forceinline__ void softmax_barrier(int threads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+}
 
 // P = 2^(s * sc + nm) of 32 scores, packed to bf16 pairs; adds the fp32 P to ls.
 __device__ __forceinline__ void p_chunk(const uint32_t (&v)[32], float sc, float nm, float (&ls)[8],
@@ -195,11 +211,13 @@ __device__ __forceinline__ bool rope_q_row(uint8_t* tile, int r, bool turn, long
 // ONE_PASS: each 32-key half of the scores is read from tensor memory once
 // (measured faster at d 64 without the query rotation; the max-first order
 // is faster at d 128 and with the rotation prologue)
-template <int D, int T, bool ONE_PASS>
-__device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, int i, int nkv, int n, int pos0,
-                                             int kv_len, int cu0, int hq,
+// SPLIT: the instance may run as one half of a key split (not the RoPE-Q one).
+template <int D, int T, bool ONE_PASS, bool SPLIT>
+__device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, int i, int j0, int j1, int n,
+                                             int pos0, int kv_len, int cu0, int hq,
                                              uint8_t* sKV, uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
-                                             uint64_t* kv_full, volatile int* abort_flag, const PrefillParams& p) {
+                                             uint64_t* kv_full, volatile int* abort_flag, int* split_flag,
+                                             bool ok, const PrefillParams& p) {
     using C = Cfg<D, T>;
     const KGeom& g = p.g;
     const float sc = p.scale_log2;
@@ -212,9 +230,10 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
     // tiles' PV products are issued by different warps in no fixed order
     const int j_tail = tail_valid < kBlockTokens ? last_lp / kPagesPerTile : -1;
     float m_o = -CUDART_INF_F, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, p.err))) {
+    if constexpr (!SPLIT) ok = true;  // outside a key split the role is entered only when ok
+    for (int j = j0; (!SPLIT || ok) && j < j1; ++j) {
+        const int jj = j - j0;  // key tiles of this CTA so far: barrier phases and stages count from j0
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full, jj & 1, abort_flag, p.err))) {
             ok = false;
             break;
         }
@@ -225,7 +244,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         // this row of O follows the reference (no PV product is in flight)
         auto rescale_o = [&]() {
-            if (j > 0 && __any_sync(0xffffffffu, f != 1.f)) {
+            if (jj > 0 && __any_sync(0xffffffffu, f != 1.f)) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
@@ -312,8 +331,8 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         if (j == j_tail) {
             // V rows past the sequence end in the last page: zero (0 x NaN is NaN)
-            const int st = j % C::NST;
-            if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[st], (j / C::NST) & 1, abort_flag, p.err))) {
+            const int st = jj % C::NST;
+            if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[st], (jj / C::NST) & 1, abort_flag, p.err))) {
                 ok = false;
                 break;
             }
@@ -333,16 +352,84 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
         tc_fence_before_sync();
         mbar_arrive(p_full);
     }
-    if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, 0, abort_flag, p.err))) {
+    const bool empty = SPLIT && j1 <= j0;  // a key-split half with no key tile: O = 0, l = 0
+    // `have`: this warp's O and l are complete.  In a key split every softmax
+    // warp goes on from here whatever it says (the split's barriers count on it).
+    const bool have = ok && (empty || __all_sync(0xffffffffu, mbar_wait(o_done, 0, abort_flag, p.err)));
+    if (SPLIT || have) {
         tc_fence_after_sync();
         const bool store = row < n;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
         const long long orow = static_cast<long long>(cu0 + row) * g.hq + hq;
+        // this row of O, not yet divided by l: from TMEM, or 0 for an empty half
+        auto load_o = [&](int c, uint32_t (&ov)[32]) {
+            if (empty) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ov[e] = 0u;
+            } else {
+                tmem_ld_x32(tO + 32 * c, ov);
+            }
+        };
+        float m_fin = m_o, l_fin = l;       // the row's reference max and sum
+        float a_own = 1.f, a_other = 0.f;  // weights of this half's O and of the other half's
+        const float* o_other = nullptr;
+        if constexpr (SPLIT) {
+            // leave this half's partial; the second half to finish combines both
+            const int k = static_cast<int>(blockIdx.x >> 1), h = static_cast<int>(blockIdx.x & 1);
+            const long long prow = ((static_cast<long long>(k) * 2 + h) * T + t) * BM + r;
+            const long long qrow = ((static_cast<long long>(k) * 2 + (h ^ 1)) * T + t) * BM + r;
+            if (have) {
+                float4* wo = reinterpret_cast<float4*>(p.ws_o + prow * D);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    load_o(c, ov);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        wo[8 * c + e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                                    __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
+                }
+                p.ws_ml[prow] = make_float2(m_o, l);
+                __threadfence();
+            }
+            // the CTA's softmax warps, all of them: every partial of this half is out
+            softmax_barrier(4 * T * 32);
+            if (t == 0 && r == 0) *split_flag = atomicAdd(p.ws_cnt + k, 1);
+            softmax_barrier(4 * T * 32);
+            if (*split_flag != 1 || !have) return;  // the other half combines (or this one stopped)
+            __threadfence();
+            const float2 mlq = __ldcg(p.ws_ml + qrow);
+            // the same expression whichever half combines: half 0's terms first
+            const float m0 = h == 0 ? m_o : mlq.x, l0 = h == 0 ? l : mlq.y;
+            const float m1 = h == 0 ? mlq.x : m_o, l1 = h == 0 ? mlq.y : l;
+            m_fin = fmaxf(m0, m1);
+            const float a0 = m0 == -CUDART_INF_F ? 0.f : ex2_approx(m0 - m_fin);
+            const float a1 = m1 == -CUDART_INF_F ? 0.f : ex2_approx(m1 - m_fin);
+            l_fin = __fadd_rn(__fmul_rn(l0, a0), __fmul_rn(l1, a1));
+            a_own = h == 0 ? a0 : a1;
+            a_other = h == 0 ? a1 : a0;
+            o_other = p.ws_o + qrow * D;
+            if (t == 0 && r == 0) p.ws_cnt[k] = 0;  // ready for the next call
+        }
+        const float inv = l_fin > 0.f ? 1.f / l_fin : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
-            tmem_ld_x32(tO + 32 * c, ov);
+            load_o(c, ov);
+            if (SPLIT && o_other) {
+                // two rounded products and their sum, never fused: the same
+                // bits whichever half adds them
+                const float4* oq = reinterpret_cast<const float4*>(o_other) + 8 * c;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 w = __ldcg(oq + e);
+                    const float x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        ov[4 * e + q] = __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(ov[4 * e + q]), a_own),
+                                                                  __fmul_rn(x[q], a_other)));
+                }
+            }
             if (store && p.o_32b) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
@@ -365,11 +452,13 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
                 }
             }
         }
-        if (store && p.lse) p.lse[orow] = l > 0.f ? (m_o + lg2_approx(l)) * kLn2 : -CUDART_INF_F;
+        if (store && p.lse) p.lse[orow] = l_fin > 0.f ? (m_fin + lg2_approx(l_fin)) * kLn2 : -CUDART_INF_F;
     }
 }
 
-template <int D, int T, bool ROPE>
+// SPLIT: the instance that runs the halves of a key split (never with ROPE);
+// the other instances compile without any of its steps.
+template <int D, int T, bool ROPE, bool SPLIT>
 __global__ void __launch_bounds__(Cfg<D, T>::THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
                const PrefillParams p) {
@@ -391,6 +480,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint64_t* q_ready = mma_done + C::MMA_WARPS;  // RoPE-Q: every query row turned
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 65);
+    int* split_flag = reinterpret_cast<int*>(bars + 66);  // key split: this half finished second
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const KGeom& g = p.g;
@@ -409,7 +499,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int qgroups = g.group / T;
     const int units = g.hkv * qgroups;
     const int per_tile = p.batch * units;
-    const int item = blockIdx.x + p.item_base;
+    const int item = (SPLIT ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x)) + p.item_base;
     const int i = p.n_row_tiles - 1 - item / per_tile;
     const int rem = item % per_tile;
     const int b = rem / units;
@@ -433,6 +523,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // and none past the cached sequence
     const int kv_len = pre + n;
     const int nkv = min((pre + BM * (i + 1) + BN - 1) / BN, (kv_len + BN - 1) / BN);
+    // this CTA's key tiles [j0, j1): all of them, or one half of a key split
+    // (the second half holds the diagonal and the sequence's last page)
+    const int j0 = SPLIT && (blockIdx.x & 1) ? nkv / 2 : 0;
+    const int j1 = SPLIT && !(blockIdx.x & 1) ? nkv / 2 : nkv;
+    const int nk = j1 - j0;
     const int pages_b = (kv_len + kBlockTokens - 1) / kBlockTokens;
     const long long tbase = (static_cast<long long>(slot_ok ? slot : 0) * g.n_layers + p.layer) * g.maxb;
 
@@ -467,7 +562,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // ------------------------------------------------------------ TMA producer
         // the diagnostic hold: the query tiles' barrier is armed but no copy is
         // issued, so its phase never completes and the waits on it run out
-        const bool hold_q = p.hold_first_copy && blockIdx.x == 0;
+        // (an empty half of a key split copies nothing)
+        const bool hold_q = (p.hold_first_copy && blockIdx.x == 0) || (SPLIT && nk == 0);
         if (lane == 0) {
             prefetch_tensor_map(&qmap);
             prefetch_tensor_map(&kvmap);
@@ -483,10 +579,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
         const int oob_row = static_cast<int>(g.nblocks * 32);  // first row past the pool: zero fill
         int issued = 0;
-        for (int j = 0; j < nkv; ++j) {
-            const int st = j % C::NST;
-            if (j >= C::NST &&
-                !__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((j / C::NST) - 1) & 1, abort_flag, p.err)))
+        for (int j = j0; j < j1; ++j) {
+            const int jj = j - j0;
+            const int st = jj % C::NST;
+            if (jj >= C::NST &&
+                !__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((jj / C::NST) - 1) & 1, abort_flag, p.err)))
                 break;  // another role stopped the CTA, or the wait ran out (then *abort_flag is set)
             // lanes 0..3 fetch the tile's page ids
             const int lp = j * kPagesPerTile + lane;
@@ -555,30 +652,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                   umma_sdesc_sw128(sV + c * kKChunkBytes + ks * 2048, 1024, 1024), idesc_pv,
                                   (acc || ks > 0) ? 1u : 0u);
         };
-        bool ok = wait_all(ROPE ? q_ready : q_full, 0) && wait_all(&kv_full[0], 0);
+        bool ok = (!SPLIT || nk > 0) && wait_all(ROPE ? q_ready : q_full, 0) && wait_all(&kv_full[0], 0);
         if (ok) {
             tc_fence_after_sync();
 #pragma unroll
             for (int t = 0; t < T; ++t)
                 if (t % C::MMA_WARPS == mw) qk(t, 0);
         }
-        for (int j = 0; j < nkv; ++j) {
-            const int st = j % C::NST;
-            const int st1 = (j + 1) % C::NST;
-            const bool more = j + 1 < nkv;
+        for (int jj = 0; (!SPLIT || ok) && jj < nk; ++jj) {
+            const int st = jj % C::NST;
+            const int st1 = (jj + 1) % C::NST;
+            const bool more = jj + 1 < nk;
 #pragma unroll
             for (int t = 0; t < T; ++t) {
                 if (t % C::MMA_WARPS != mw) continue;
-                if (!wait_all(&p_full[t], j & 1)) {
+                if (!wait_all(&p_full[t], jj & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                pv(t, st, j > 0);
+                pv(t, st, jj > 0);
                 if (t + C::MMA_WARPS >= T) umma_commit_elect(&kv_empty[st]);  // this warp's last tile
                 if (more) {
                     if (t < C::MMA_WARPS) {  // this warp's first tile
-                        if (!wait_all(&kv_full[st1], ((j + 1) / C::NST) & 1)) {
+                        if (!wait_all(&kv_full[st1], ((jj + 1) / C::NST) & 1)) {
                             ok = false;
                             break;
                         }
@@ -607,9 +704,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             __syncwarp();
             if (ok) mbar_arrive_elect(q_ready);
         }
-        if (ok)
-            softmax_role<D, T, D == 64 && !ROPE>(t, r, tmem + tmem_lane_base(warp), i, nkv, n, pre + BM * i, kv_len, cu0, hq0 + t, sKV,
-                               &s_full[t], &p_full[t], &o_done[t], kv_full, abort_flag, p);
+        // in a key split every softmax warp enters, whatever `ok` says: the
+        // split's barriers count on it
+        if (SPLIT || ok)
+            softmax_role<D, T, D == 64 && !ROPE, SPLIT>(t, r, tmem + tmem_lane_base(warp), i, j0, j1, n, pre + BM * i, kv_len,
+                                             cu0, hq0 + t, sKV, &s_full[t], &p_full[t], &o_done[t], kv_full,
+                                             abort_flag, split_flag, ok, p);
     }
 
     tc_fence_before_sync();
@@ -650,7 +750,8 @@ template <int D, int T>
 cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, PrefillParams p, long long first,
                    long long count, bool tail, bool has_tail, cudaStream_t stream) {
     using C = Cfg<D, T>;
-    auto kern = p.cos_tab ? prefill_kernel<D, T, true> : prefill_kernel<D, T, false>;
+    auto kern = p.cos_tab ? prefill_kernel<D, T, true, false>
+                          : (p.ksplit ? prefill_kernel<D, T, false, true> : prefill_kernel<D, T, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     if (count <= 0) return cudaSuccess;
@@ -659,12 +760,13 @@ cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, PrefillPar
     p.item_base = static_cast<int>(first);
     p.tail = tail ? 1 : 0;
     p.has_tail = has_tail ? 1 : 0;
+    const unsigned grid = static_cast<unsigned>(p.ksplit ? 2 * count : count);  // key split: two CTAs an item
     if (!tail) {
-        kern<<<static_cast<unsigned>(count), C::THREADS, C::SMEM, stream>>>(qmap, kvmap, p);
+        kern<<<grid, C::THREADS, C::SMEM, stream>>>(qmap, kvmap, p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(count), 1, 1);
+    cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
@@ -676,11 +778,43 @@ cudaError_t launch(const CUtensorMap& qmap, const CUtensorMap& kvmap, PrefillPar
     return cudaLaunchKernelEx(&cfg, kern, qmap, kvmap, p);
 }
 
+// Scratch of a key-split launch, from a memory pool of the library's own per
+// device (kept for the process, never released to the system, so that a call
+// allocates and frees in stream order at the cost of a pool lookup).
+cudaError_t split_scratch(size_t bytes, cudaStream_t stream, void** out) {
+    static std::mutex mu;
+    static cudaMemPool_t pools[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!pools[dev]) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            e = cudaMemPoolCreate(&pools[dev], &props);
+            if (e != cudaSuccess) return e;
+            uint64_t keep = ~0ull;
+            e = cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+            if (e != cudaSuccess) return e;
+        }
+        pool = pools[dev];
+    }
+    return cudaMallocFromPoolAsync(out, bytes, pool, stream);
+}
+
 // The call's work items with T q heads per CTA, heaviest first.  When they
 // make only a few waves over the SMs and the last one is partial, the items of
-// that last wave run instead with T/2 heads per CTA (each item is exactly two
-// of those, the same rows and kv head), as twice as many half-size CTAs in a
-// second launch that starts while the first one's last wave runs.
+// that last wave run in a second launch that starts while the first one's last
+// wave runs:
+// - with a cached prefix (long key ranges) each item as two CTAs of T heads,
+//   one per half of its key tiles, whose partials the later one combines;
+// - otherwise (or if its scratch cannot be had) with T/2 heads per CTA (each
+//   item is exactly two of those, the same rows and kv head).
 template <int D, int T>
 cudaError_t launch_items(const CUtensorMap& qmap, const CUtensorMap& kvmap, const PrefillParams& p, int sms,
                          cudaStream_t stream) {
@@ -690,9 +824,36 @@ cudaError_t launch_items(const CUtensorMap& qmap, const CUtensorMap& kvmap, cons
         return launch<D, T>(qmap, kvmap, p, 0, n, false, false, stream);
     constexpr int TH = T > 1 ? T / 2 : 1;
     const long long full = n / sms * sms;  // items of the whole waves
+    const long long rest = n - full;
+    void* ws = nullptr;
+    PrefillParams ps = p;
+    if (p.prefix && !p.cos_tab) {
+        const size_t o_bytes = static_cast<size_t>(rest) * 2 * T * BM * D * sizeof(float);
+        const size_t ml_bytes = static_cast<size_t>(rest) * 2 * T * BM * sizeof(float2);
+        if (split_scratch(o_bytes + ml_bytes + static_cast<size_t>(rest) * sizeof(int), stream, &ws) == cudaSuccess) {
+            ps.ksplit = 1;
+            ps.ws_o = static_cast<float*>(ws);
+            ps.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + o_bytes);
+            ps.ws_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + o_bytes + ml_bytes);
+            cudaError_t e = cudaMemsetAsync(ps.ws_cnt, 0, static_cast<size_t>(rest) * sizeof(int), stream);
+            if (e != cudaSuccess) {
+                cudaFreeAsync(ws, stream);
+                return e;
+            }
+        } else {
+            (void)cudaGetLastError();  // no scratch: the head split needs none
+            ws = nullptr;
+        }
+    }
     cudaError_t e = launch<D, T>(qmap, kvmap, p, 0, full, false, true, stream);
-    if (e != cudaSuccess) return e;
-    return launch<D, TH>(qmap, kvmap, p, 2 * full, 2 * (n - full), full > 0, false, stream);
+    if (e == cudaSuccess)
+        e = ws ? launch<D, T>(qmap, kvmap, ps, full, rest, full > 0, false, stream)
+               : launch<D, TH>(qmap, kvmap, p, 2 * full, 2 * rest, full > 0, false, stream);
+    if (ws) {
+        const cudaError_t f = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess) e = f;
+    }
+    return e;
 }
 
 }  // namespace
@@ -736,6 +897,10 @@ cudaError_t launch_prefill(const KGeom& g, const void* q, const void* pool, cons
     p.item_base = 0;
     p.tail = 0;
     p.has_tail = 0;
+    p.ksplit = 0;
+    p.ws_o = nullptr;
+    p.ws_ml = nullptr;
+    p.ws_cnt = nullptr;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

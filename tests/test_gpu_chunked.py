@@ -52,6 +52,11 @@ def test_chunked_prefix_offsets(pre):
 
 
 def test_null_prefix_is_prefill_bit_for_bit():
+    """A null prefix array is the plain prefill, bit for bit.  Zero prefixes
+    passed as an array give the same attention, but a call with a prefix
+    array runs items as key halves when they leave the last wave partial
+    (here: fewer items than SMs), so it agrees to rounding, and with the
+    oracle."""
     geom = W.Geometry(32, 8, 64, 1, 2, 32, 80)
     case = W.make_chunked_case("null", geom, [0, 0], [300, 77], seed=2)
     pool, bt, werr = H.gpu_setup(case)
@@ -60,9 +65,12 @@ def test_null_prefix_is_prefill_bit_for_bit():
     o2, l2, e2 = H.gpu_prefill_cached(case, pool, bt, prefix=[0, 0])
     o3, l3, e3 = H.gpu_prefill(case, pool, bt)
     assert e1 == e2 == e3 == 0
-    np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(o1, o3)
     np.testing.assert_array_equal(l1, l3)
+    vmax = H.max_abs_v(case)
+    H.assert_close(o2, l2, o1, l1, vmax, "zero prefixes against the null prefix")
+    ro, rl = H.oracle_prefill_cached(case, H.oracle_pool(case))
+    H.assert_close(o2, l2, ro, rl, vmax, "zero prefixes against the oracle")
 
 
 def test_chunk_of_one_matches_decode_kernel():
@@ -131,8 +139,10 @@ def test_chunked_bench_size_tail_launch():
     """The chunked bench workload (4 x 2048 queries after 6144 cached tokens,
     32 q / 8 kv heads, d 64): 512 four-head work items on the GPU's SMs make
     more than three waves, so the last wave's items (row tiles 0 and 1 of every
-    sequence) run as two-head CTAs in a second, dependent launch.  Sampled rows
-    of every sequence, most of them in those row tiles, against the oracle."""
+    sequence) run in a second, dependent launch as two CTAs each, one per half
+    of the item's key tiles, the later of which combines both partials.
+    Sampled rows of every sequence, most of them in those row tiles, against
+    the oracle."""
     import oracle
     prefix, chunk = 6144, 2048
     pages = (prefix + chunk) // 16
@@ -156,3 +166,37 @@ def test_chunked_bench_size_tail_launch():
     rows, heads = np.array(rows, np.int64), np.array(heads, np.int32)
     ro, rl = H.oracle_prefill_cached(case, H.oracle_pool(case), rows=rows, heads=heads)
     H.assert_close(o[rows, heads], l[rows, heads], ro, rl, vmax, "chunked bench size")
+
+
+def test_key_split_is_deterministic_and_permutation_invariant():
+    """Items that run as two key halves (a batch of fewer items than SMs, each
+    item split; one-tile items leave the first half empty): whichever half
+    finishes second combines the same fp32 partials with the same arithmetic,
+    so repeated calls and a permuted page layout give the same bits; and the
+    result matches the oracle."""
+    pre = [0, 17, 500, 1000, 64]
+    lens = [300, 40, 129, 1, 256]
+    nb = sum((p + n + 15) // 16 for p, n in zip(pre, lens)) + 16
+    geom = W.Geometry(32, 8, 64, 1, 5, 128, nb)
+    case = W.make_chunked_case("ksplit", geom, pre, lens, seed=77, pool_fill="nan")
+    pool, bt, werr = H.gpu_setup(case)
+    assert werr == 0
+    runs = [H.gpu_prefill_cached(case, pool, bt) for _ in range(4)]
+    for o, l, err in runs:
+        assert err == 0
+        np.testing.assert_array_equal(o, runs[0][0])
+        np.testing.assert_array_equal(l, runs[0][1])
+    ro, rl = H.oracle_prefill_cached(case, H.oracle_pool(case))
+    H.assert_close(runs[0][0], runs[0][1], ro, rl, H.max_abs_v(case), "key-split chunked")
+    # the same logical cache on other physical pages
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(nb).astype(np.int32)
+    moved = W.Case(case.name, case.geom, case.scale, case.layer, case.slots, case.lens,
+                   np.where(case.block_table >= 0, perm[np.maximum(case.block_table, 0)], -1).astype(np.int32),
+                   case.writes, case.q, case.kind, case.pool_fill, case.seed, dict(case.extra))
+    pool2, bt2, werr2 = H.gpu_setup(moved)
+    assert werr2 == 0
+    o2, l2, err2 = H.gpu_prefill_cached(moved, pool2, bt2)
+    assert err2 == 0
+    np.testing.assert_array_equal(o2, runs[0][0])
+    np.testing.assert_array_equal(l2, runs[0][1])

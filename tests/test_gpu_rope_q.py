@@ -7,8 +7,9 @@ the queries with orc_rope_q and attends with orc_prefill_cached.  Covered:
 every q-heads-per-CTA variant of the kernel (4, 2, 1 at d 64; 2, 1 at d 128),
 prefixes that are and are not multiples of the page and of the tiles, a
 NaN-filled pool, the Llama-3.2-1B-shaped prompts, the 4 x 8192 bench
-workload on sampled rows, the identity table (the plain prefill: bit for bit
-at d 128, within the bar at d 64) and positions past the table.
+workload on sampled rows, the identity table (the plain prefill of fresh
+prompts: bit for bit at d 128, within the bar at d 64) and positions past
+the table.
 """
 import numpy as np
 import pytest
@@ -88,17 +89,18 @@ def test_rope_q_llama_prompts():
 
 @pytest.mark.parametrize("hq,hkv,d", [(32, 8, 64), (16, 4, 128)])
 def test_identity_table_is_the_plain_prefill(hq, hkv, d):
-    """cos 1, sin 0 leaves Q and K as they are: the RoPE-Q prefill equals the
-    plain one.  Bit for bit at d 128, where both take the same softmax order;
-    at d 64 the plain kernel reads each score half once and the RoPE-Q one
-    takes the max first, so the two agree within the parity bar."""
+    """cos 1, sin 0 leaves Q and K as they are: the RoPE-Q prefill of fresh
+    prompts equals the plain prefill.  Bit for bit at d 128, where both take
+    the same softmax order and work split; at d 64 the plain kernel reads each
+    score half once and the RoPE-Q one takes the max first, so the two agree
+    within the parity bar."""
     geom = W.Geometry(hq, hkv, d, 1, 3, 32, 100)
-    case = W.make_chunked_case("rq_id", geom, [0, 23, 64], [300, 77, 5], seed=4)
+    case = W.make_chunked_case("rq_id", geom, [0, 0, 0], [300, 77, 5], seed=4)
     n = 400
     one, zero = np.ones((n, d // 2), np.float32), np.zeros((n, d // 2), np.float32)
     pool, bt, _ = _write_rope(case, one, zero)
-    o1, l1, e1 = _gpu_rope(case, pool, bt, one, zero, case.extra["prefix"])
-    o2, l2, e2 = H.gpu_prefill_cached(case, pool, bt)
+    o1, l1, e1 = _gpu_rope(case, pool, bt, one, zero, None)
+    o2, l2, e2 = H.gpu_prefill(case, pool, bt)
     assert e1 == 0 and e2 == 0
     if d == 128:
         np.testing.assert_array_equal(o1, o2)
