@@ -85,3 +85,41 @@ def test_decode_wait_runs_out_and_the_next_call_is_right():
     assert err2 == 0
     ro, rl = H.oracle_decode(case, H.oracle_pool(case))
     H.assert_close(o2, l2, ro, rl, H.max_abs_v(case), "decode after the timeout")
+
+
+def test_key_split_wait_runs_out_and_the_next_call_is_right():
+    """A chunked call of fewer items than SMs runs every item as two halves of
+    its key range, the later half combining both.  CTA 0 (the first half of
+    the heaviest item) has its wait run out: its softmax warps still pass the
+    split's barriers, its partial is not written, and nothing waits on it;
+    the item's rows are then unspecified (the call reports PA_ERR_TIMEOUT),
+    the other items are right, and so is the next call."""
+    torch = H.torch_mod()
+    geom = W.Geometry(8, 2, 64, 1, 2, 72, 160)
+    case = W.make_chunked_case("held_split", geom, [300, 200], [700, 300], seed=33, pool_fill="nan")
+    pool, bt, werr = H.gpu_setup(case)
+    assert werr == 0
+    ro, rl = H.oracle_prefill_cached(case, H.oracle_pool(case))
+    vmax = H.max_abs_v(case)
+
+    def run():
+        o = torch.zeros((case.total_tokens, 8, 64), dtype=torch.int16, device="cuda")
+        lse = torch.empty((case.total_tokens, 8), dtype=torch.float32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pa.pa_prefill_cached(H.pa_geom(case), H.to_dev(case.q), pool, bt, 0, H.to_dev(case.cu_seqlens),
+                             H.to_dev(case.extra["prefix"]), H.to_dev(case.slots), case.max_len, case.scale,
+                             o, lse, err)
+        torch.cuda.synchronize()
+        return H.f32(o.cpu().numpy().view(np.uint16)), lse.cpu().numpy().astype(np.float64), int(err.item())
+
+    (o, l, err), secs = _held(run)
+    assert err == pa.PA_ERR_TIMEOUT, pa.pa_status_string(err)
+    assert secs >= 0.9 * WAIT_LIMIT_S
+    # item 0: the last 128-row tile of sequence 0 (rows 640..699), q heads 0..3
+    held = np.zeros((case.total_tokens, 8), bool)
+    held[640:700, 0:4] = True
+    ok = ~held
+    H.assert_close(o[ok], l[ok], ro[ok], rl[ok], vmax, "rows of the other items")
+    o2, l2, err2 = run()
+    assert err2 == 0
+    H.assert_close(o2, l2, ro, rl, vmax, "the call after the timeout")
