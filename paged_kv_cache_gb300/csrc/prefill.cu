@@ -234,6 +234,13 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
     const int j_tail = tail_valid < kBlockTokens ? last_lp / kPagesPerTile : -1;
     float m_o = -CUDART_INF_F, l = 0.f;
     float nm_reg = 0.f;  // -m_o, or 0 while m_o is -inf (NEG_REG)
+    // ONE_PASS: the move test in raw score units (scale > 0): a half whose raw
+    // max exceeds thr_raw = (m_o + 2^8) / sc moves the reference.  One multiply
+    // and one add fewer between a half's max and its exp2: 1077 -> 1092
+    // TFLOP/s at d 64, the same bits (the max-first order at d 128 measured
+    // 0.4 % slower with it).
+    const float move_raw = kMoveAbove / sc;
+    float thr_raw = -CUDART_INF_F;
     auto neg_ref = [&]() { return NEG_REG ? nm_reg : (m_o == -CUDART_INF_F ? 0.f : -m_o); };
     if constexpr (!SPLIT) ok = true;  // outside a key split the role is entered only when ok
     for (int j = j0; (!SPLIT || ok) && j < j1; ++j) {
@@ -246,10 +253,11 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
         const int rel = BN * j - pos0;  // first key of the tile relative to the first row's position
         const bool diag = rel > -BN;      // the tile crosses the diagonal
         float f = 1.f;  // factor for l and this row of O when the reference moves
+        bool moved = false;  // (ONE_PASS) the reference moved in this tile
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         // this row of O follows the reference (no PV product is in flight)
         auto rescale_o = [&]() {
-            if (jj > 0 && __any_sync(0xffffffffu, f != 1.f)) {
+            if (jj > 0 && __any_sync(0xffffffffu, ONE_PASS ? moved : f != 1.f)) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
@@ -270,8 +278,11 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
                 uint32_t va[32];
                 tmem_ld_x32(tS, va);
                 if (diag) mask_chunk(va, rel, r);
-                const float m_a = sc * chunk_max(va, -CUDART_INF_F);
-                if (m_a > m_o + kMoveAbove) {
+                const float ma_raw = chunk_max(va, -CUDART_INF_F);
+                if (ma_raw > thr_raw) {
+                    const float m_a = sc * ma_raw;
+                    thr_raw = ma_raw + move_raw;
+                    moved = true;
                     f = ex2_approx(m_o - m_a);  // 0 from -inf
                     l *= f;
                     m_o = m_a;
@@ -283,8 +294,11 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
                 uint32_t vb[32], pk[16];
                 tmem_ld_x32(tS + 32, vb);
                 if (diag) mask_chunk(vb, rel + 32, r);
-                const float m_b = sc * chunk_max(vb, -CUDART_INF_F);
-                if (m_b > m_o + kMoveAbove) {
+                const float mb_raw = chunk_max(vb, -CUDART_INF_F);
+                if (mb_raw > thr_raw) {
+                    const float m_b = sc * mb_raw;
+                    thr_raw = mb_raw + move_raw;
+                    moved = true;
                     const float f2 = ex2_approx(m_o - m_b);
                     f *= f2;
                     l *= f2;
