@@ -132,15 +132,33 @@ __device__ __forceinline__ void softmax_barrier(int threads) {
     asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
 }
 
+// One float twice, as the 64-bit pair operand of the packed fp32 ops.
+__device__ __forceinline__ uint64_t pair2(float a) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(a));
+    return r;
+}
+
 // P = 2^(s * sc + nm) of 32 scores, packed to bf16 pairs; adds the fp32 P to
 // ls (FIRST: the first half of the tile, whose first four pairs start ls).
-template <bool FIRST>
+// PAIRS: sc and nm enter the packed FMAs as pairs formed once per call.
+template <bool FIRST, bool PAIRS>
 __device__ __forceinline__ void p_chunk(const uint32_t (&v)[32], float sc, float nm, float (&ls)[8],
                                         uint32_t (&pk)[16]) {
+    const uint64_t sc2 = pair2(sc), nm2 = pair2(nm);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
         float x0, x1;
-        ffma2(x0, x1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), sc, sc, nm, nm);
+        if constexpr (PAIRS) {
+            asm("{\n\t.reg .b64 a2, d2;\n\t"
+                "mov.b64 a2, {%2, %3};\n\t"
+                "fma.rn.f32x2 d2, a2, %4, %5;\n\t"
+                "mov.b64 {%0, %1}, d2;\n\t}"
+                : "=f"(x0), "=f"(x1)
+                : "f"(__uint_as_float(v[2 * e])), "f"(__uint_as_float(v[2 * e + 1])), "l"(sc2), "l"(nm2));
+        } else {
+            ffma2(x0, x1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), sc, sc, nm, nm);
+        }
         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
         const int a = 2 * (e & 3);
         if (FIRST && e < 4) {
@@ -159,6 +177,22 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&v)[32], int c0, int r) {
 #pragma unroll
     for (int e = 0; e < 32; ++e)
         if (c0 + e > r) v[e] = __float_as_uint(-CUDART_INF_F);
+}
+
+// Max of 32 scores in 16 three-input max operations: four chains over
+// seven scores each, then their results with the four left over.
+__device__ __forceinline__ float chunk_max16(const uint32_t (&v)[32]) {
+    auto x = [&](int e) { return __uint_as_float(v[e]); };
+    float c[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        c[k] = fmax3(x(8 * k), x(8 * k + 1), x(8 * k + 2));
+        c[k] = fmax3(c[k], x(8 * k + 3), x(8 * k + 4));
+        c[k] = fmax3(c[k], x(8 * k + 5), x(8 * k + 6));
+    }
+    const float a = fmax3(c[0], c[1], x(7));
+    const float b = fmax3(c[2], c[3], x(15));
+    return fmaxf(fmax3(a, x(23), x(31)), b);
 }
 
 __device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], float m) {
@@ -293,7 +327,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
                 uint32_t va[32];
                 tmem_ld_x32(tS, va);
                 if (diag) mask_chunk(va, rel, r);
-                const float ma_raw = chunk_max(va, -CUDART_INF_F);
+                const float ma_raw = chunk_max16(va);
                 if (ma_raw > thr_raw) {
                     const float m_a = sc * ma_raw;
                     thr_raw = ma_raw + move_raw;
@@ -303,13 +337,13 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
                     m_o = m_a;
                     nm_reg = -m_o;
                 }
-                p_chunk<true>(va, sc, neg_ref(), ls, pa);
+                p_chunk<true, true>(va, sc, neg_ref(), ls, pa);
             }
             {
                 uint32_t vb[32], pk[16];
                 tmem_ld_x32(tS + 32, vb);
                 if (diag) mask_chunk(vb, rel + 32, r);
-                const float mb_raw = chunk_max(vb, -CUDART_INF_F);
+                const float mb_raw = chunk_max16(vb);
                 if (mb_raw > thr_raw) {
                     const float m_b = sc * mb_raw;
                     thr_raw = mb_raw + move_raw;
@@ -324,7 +358,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
 #pragma unroll
                     for (int e = 0; e < 16; ++e) pa[e] = pack_bf16x2(bf16lo(pa[e]) * f2, bf16hi(pa[e]) * f2);
                 }
-                p_chunk<false>(vb, sc, neg_ref(), ls, pk);
+                p_chunk<false, true>(vb, sc, neg_ref(), ls, pk);
                 tmem_st_x16_nowait(tS + 32, pk);
             }
             tmem_st_x16_nowait(tS, pa);
@@ -353,7 +387,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
             const float nm = neg_ref();
             {
                 uint32_t pk[16];
-                p_chunk<false>(vb, sc, nm, ls, pk);
+                p_chunk<false, false>(vb, sc, nm, ls, pk);
                 tmem_st_x16_nowait(tS + 32, pk);
             }
             rescale_o();
@@ -361,7 +395,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
                 uint32_t va[32], pk[16];
                 tmem_ld_x32(tS, va);
                 if (diag) mask_chunk(va, rel, r);
-                p_chunk<false>(va, sc, nm, ls, pk);
+                p_chunk<false, false>(va, sc, nm, ls, pk);
                 tmem_st_x16_nowait(tS, pk);
             }
         }
