@@ -250,13 +250,10 @@ __device__ __forceinline__ bool rope_q_row(uint8_t* tile, int r, bool turn, long
 
 // Softmax of query tile t: the warp's thread owns row r (TMEM lane r).
 // ONE_PASS: each 32-key half of the scores is read from tensor memory once
-// (measured faster at d 64 without the query rotation; the max-first order
-// is faster at d 128 and with the rotation prologue)
+// (measured faster at d 64, with and without the query rotation; the
+// max-first order is faster at d 128)
 // SPLIT: the instance may run as one half of a key split (not the RoPE-Q one).
-// NEG_REG: -m is kept in a register, updated when the reference moves
-// (0.8 % faster at d 64, 0.6 % at d 128; it makes the RoPE-Q instance spill,
-// which forms it from m at each use instead).
-template <int D, int T, bool ONE_PASS, bool SPLIT, bool NEG_REG>
+template <int D, int T, bool ONE_PASS, bool SPLIT>
 __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, int i, int j0, int j1, int n,
                                              int pos0, int kv_len, int cu0, int hq,
                                              uint8_t* sKV, uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
@@ -274,7 +271,10 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
     // tiles' PV products are issued by different warps in no fixed order
     const int j_tail = tail_valid < kBlockTokens ? last_lp / kPagesPerTile : -1;
     float m_o = -CUDART_INF_F, l = 0.f;
-    float nm_reg = 0.f;  // -m_o, or 0 while m_o is -inf (NEG_REG)
+    // -m_o (0 while m_o is -inf), kept in a register and set when the
+    // reference moves: 0.8 % faster at d 64, 0.6 % at d 128 than forming it
+    // from m_o before each use
+    float nm_reg = 0.f;
     // ONE_PASS: the move test in raw score units (scale > 0): a half whose raw
     // max exceeds thr_raw = (m_o + 2^8) / sc moves the reference.  One multiply
     // and one add fewer between a half's max and its exp2: 1077 -> 1092
@@ -282,7 +282,6 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
     // 0.4 % slower with it).
     const float move_raw = kMoveAbove / sc;
     float thr_raw = -CUDART_INF_F;
-    auto neg_ref = [&]() { return NEG_REG ? nm_reg : (m_o == -CUDART_INF_F ? 0.f : -m_o); };
     if constexpr (!SPLIT) ok = true;  // outside a key split the role is entered only when ok
     for (int j = j0; (!SPLIT || ok) && j < j1; ++j) {
         const int jj = j - j0;  // key tiles of this CTA so far: barrier phases and stages count from j0
@@ -337,7 +336,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
                     m_o = m_a;
                     nm_reg = -m_o;
                 }
-                p_chunk<true, true>(va, sc, neg_ref(), ls, pa);
+                p_chunk<true, true>(va, sc, nm_reg, ls, pa);
             }
             {
                 uint32_t vb[32], pk[16];
@@ -358,7 +357,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
 #pragma unroll
                     for (int e = 0; e < 16; ++e) pa[e] = pack_bf16x2(bf16lo(pa[e]) * f2, bf16hi(pa[e]) * f2);
                 }
-                p_chunk<false, true>(vb, sc, neg_ref(), ls, pk);
+                p_chunk<false, true>(vb, sc, nm_reg, ls, pk);
                 tmem_st_x16_nowait(tS + 32, pk);
             }
             tmem_st_x16_nowait(tS, pa);
@@ -384,7 +383,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
                 m_o = m_tile;
                 nm_reg = -m_o;
             }
-            const float nm = neg_ref();
+            const float nm = nm_reg;
             {
                 uint32_t pk[16];
                 p_chunk<false, false>(vb, sc, nm, ls, pk);
@@ -778,7 +777,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // in a key split every softmax warp enters, whatever `ok` says: the
         // split's barriers count on it
         if (SPLIT || ok)
-            softmax_role<D, T, D == 64 && !ROPE, SPLIT, !ROPE>(t, r, tmem + tmem_lane_base(warp), i, j0, j1, n, pre + BM * i, kv_len,
+            softmax_role<D, T, D == 64, SPLIT>(t, r, tmem + tmem_lane_base(warp), i, j0, j1, n, pre + BM * i, kv_len,
                                              cu0, hq0 + t, sKV, &s_full[t], &p_full[t], &o_done[t], kv_full,
                                              abort_flag, split_flag, ok, p);
     }
