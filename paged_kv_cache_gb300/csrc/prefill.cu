@@ -25,21 +25,26 @@
 //    K-major (Q, K) / MN-major (V) operand layouts of the tensor core.  Pages
 //    past the sequence end are read at an out-of-range row, which the copy
 //    engine fills with zeros.
-//  * Warps 4T+1 (and 4T+2 when T = 4) issue the MMAs; the whole warp runs the
-//    loop and one elected lane issues.  S_t = Q_t K^T (M 128, N 64, K 16
+//  * Warps 4T+1 (and 4T+2 when T >= 2) issue the MMAs; the whole warp runs
+//    the loop and one elected lane issues.  S_t = Q_t K^T (M 128, N 64, K 16
 //    steps) into TMEM; after tile t's softmax hands back P_t, O_t += P_t V (M
 //    128, N 64 per 64-dim chunk, K 16, P read from TMEM), then the next S_t.
 //    The tiles take turns, so the tensor core works on the others while one
 //    tile's softmax runs; with two issuing warps, tile t belongs to warp t % 2.
+//    Where tensor memory holds two score buffers per tile (T <= 2: d 128, and
+//    the two-head launches at d 64) S of key tile j + 1 is computed while the
+//    softmax works on tile j, and P of tile j is followed in its buffer by S
+//    of tile j + 2.
 //  * Warps 4t..4t+3 (softmax of tile t): thread r owns query row r, i.e. TMEM
 //    lane r, and all 64 scores of the key tile.  It takes the row max first,
 //    moves the reference max if the tile max exceeds it by more than 2^8 (l at
-//    once, its O row in TMEM in place -- no PV product is in flight then), and
+//    once, its O row in TMEM in place -- with one score buffer no PV product
+//    is in flight then; with two it first waits for the last one), and
 //    forms P = 2^(s*scale*log2e - m) with packed fp32 FMAs and the SFU exp2,
 //    packed to bf16.  The epilogue divides by l, writes o (bf16) and
 //    L = ln2 (m + log2 l).  Exact: o = O / l uses the one reference.
-//  * TMEM: tile t owns 64 + d columns from t (64 + d): S (each 32-key half
-//    holds its P in its first 16 columns), then O.
+//  * TMEM: tile t owns NB 64 + d columns from t (NB 64 + d): NB score buffers
+//    S (each 32-key half holds its P in its first 16 columns), then O.
 //  * A partial last page has its V rows past the sequence end zeroed in shared
 //    memory before the PV products (masked P is exactly 0, but 0 x NaN is not).
 //  * RoPE on the queries (pa_prefill_rope; tiny-vllm part 3, "RoPE: a rotation
@@ -68,7 +73,7 @@ template <int D, int T>
 struct Cfg {
     static constexpr int KCH = D / 64;
     static constexpr int PRODUCER_WARP = 4 * T;
-    static constexpr int MMA_WARPS = T >= 4 ? 2 : 1;  // tile t is issued by MMA warp t % MMA_WARPS
+    static constexpr int MMA_WARPS = T >= 2 ? 2 : 1;  // tile t is issued by MMA warp t % MMA_WARPS
     static constexpr int MMA_WARP = 4 * T + 1;        // the first one; it also owns the TMEM allocation
     static constexpr int THREADS = 32 * (4 * T + 1 + MMA_WARPS);
     static constexpr int Q_BYTES = KCH * kQChunkBytes;  // one query tile
@@ -78,17 +83,24 @@ struct Cfg {
     static constexpr int NST_FIT = (220 * 1024 - T * Q_BYTES - CTL_BYTES - 1024) / STAGE_BYTES;
     static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
     static constexpr int SMEM = 1024 + T * Q_BYTES + NST * STAGE_BYTES + CTL_BYTES;
-    static constexpr int TILE_COLS = BN + D;
+    // score buffers per tile: two where tensor memory holds them (S of key
+    // tile j + 1 is then computed while the softmax works on S of tile j)
+    static constexpr int NB = T * (2 * BN + D) <= 512 ? 2 : 1;
+    static constexpr int TILE_COLS = NB * BN + D;
     static constexpr uint32_t TMEM_COLS = T * TILE_COLS <= 128 ? 128u : T * TILE_COLS <= 256 ? 256u : 512u;
     static_assert(T * TILE_COLS <= 512, "tensor memory holds S and O of every tile");
     static_assert(NST >= 2, "two K/V stages at least");
-    static_assert(1 + 2 * NST + 3 * T + MMA_WARPS + 1 <= 64, "barriers fit below the TMEM slot");
-    static __device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(TILE_COLS * t); }
-    static __device__ __forceinline__ uint32_t o_col(int t) { return static_cast<uint32_t>(TILE_COLS * t + BN); }
-    // P columns of key step ks (16 keys) of tile t: the 32 keys of each half of
-    // the tile put their P over the first 16 of their own score columns
-    static __device__ __forceinline__ uint32_t p_col(int t, int ks) {
-        return s_col(t) + 32u * (ks >> 1) + 8u * (ks & 1);
+    static_assert(NB == 1 || NST >= 3, "a K/V stage for each score buffer in flight and one more");
+    static_assert(1 + 2 * NST + 2 * NB * T + 2 * T + MMA_WARPS + 1 <= 64, "barriers fit below the TMEM slot");
+    static __device__ __forceinline__ uint32_t s_col(int t, int b) {
+        return static_cast<uint32_t>(TILE_COLS * t + BN * b);
+    }
+    static __device__ __forceinline__ uint32_t o_col(int t) { return static_cast<uint32_t>(TILE_COLS * t + NB * BN); }
+    // P columns of key step ks (16 keys) in score buffer b of tile t: the 32
+    // keys of each half of the tile put their P over the first 16 of their
+    // own score columns
+    static __device__ __forceinline__ uint32_t p_col(int t, int b, int ks) {
+        return s_col(t, b) + 32u * (ks >> 1) + 8u * (ks & 1);
     }
 };
 
@@ -257,12 +269,12 @@ template <int D, int T, bool ONE_PASS, bool SPLIT>
 __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, int i, int j0, int j1, int n,
                                              int pos0, int kv_len, int cu0, int hq,
                                              uint8_t* sKV, uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
-                                             uint64_t* kv_full, volatile int* abort_flag, int* split_flag,
+                                             uint64_t* pv_done, uint64_t* kv_full, volatile int* abort_flag,
+                                             int* split_flag,
                                              bool ok, const PrefillParams& p) {
     using C = Cfg<D, T>;
     const KGeom& g = p.g;
     const float sc = p.scale_log2;
-    const uint32_t tS = tmem_lane + C::s_col(t);
     const uint32_t tO = tmem_lane + C::o_col(t);
     const int row = i * BM + r;  // query row within the chunk; its position is pos0 + r
     const int last_lp = (kv_len + kBlockTokens - 1) / kBlockTokens - 1;
@@ -285,7 +297,9 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
     if constexpr (!SPLIT) ok = true;  // outside a key split the role is entered only when ok
     for (int j = j0; (!SPLIT || ok) && j < j1; ++j) {
         const int jj = j - j0;  // key tiles of this CTA so far: barrier phases and stages count from j0
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full, jj & 1, abort_flag, p.err))) {
+        const int sb = jj % C::NB;  // this key tile's score buffer
+        const uint32_t tS = tmem_lane + C::s_col(t, sb);
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (jj / C::NB) & 1, abort_flag, p.err))) {
             ok = false;
             break;
         }
@@ -303,9 +317,15 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
 #pragma unroll
             for (int e = 0; e < 8; ++e) ls[e] = 0.f;
         }
-        // this row of O follows the reference (no PV product is in flight)
+        // this row of O follows the reference (with one score buffer no PV
+        // product is in flight here)
         auto rescale_o = [&]() {
             if (jj > 0 && __any_sync(0xffffffffu, ONE_PASS ? moved : f != 1.f)) {
+                // with two score buffers the PV product of key tile jj - 1 may
+                // still be adding into O: wait for it (bounded)
+                if constexpr (C::NB == 2) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (jj - 1) & 1, abort_flag, p.err))) return;
+                }
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
@@ -420,7 +440,7 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
         }
         tmem_wait_st();
         tc_fence_before_sync();
-        mbar_arrive(p_full);
+        mbar_arrive(&p_full[sb]);
     }
     const bool empty = SPLIT && j1 <= j0;  // a key-split half with no key tile: O = 0, l = 0
     // `have`: this warp's O and l are complete.  In a key split every softmax
@@ -543,11 +563,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;                 // [NST]
     uint64_t* kv_empty = bars + 1 + C::NST;       // [NST]
-    uint64_t* s_full = bars + 1 + 2 * C::NST;     // [T] scores of a tile in TMEM
-    uint64_t* p_full = s_full + T;                // [T] P of a tile in TMEM
-    uint64_t* o_done = s_full + 2 * T;            // [T] the last PV product of a tile done
-    uint64_t* mma_done = s_full + 3 * T;          // [MMA_WARPS]
+    uint64_t* s_full = bars + 1 + 2 * C::NST;     // [T][NB] scores of a tile in a TMEM buffer
+    uint64_t* p_full = s_full + C::NB * T;        // [T][NB] P of a tile in that buffer
+    uint64_t* o_done = s_full + 2 * C::NB * T;    // [T] the last PV product of a tile done
+    uint64_t* mma_done = o_done + T;              // [MMA_WARPS]
     uint64_t* q_ready = mma_done + C::MMA_WARPS;  // RoPE-Q: every query row turned
+    uint64_t* pv_done = q_ready + 1;              // [T] (NB = 2) each PV product of a tile done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 65);
     int* split_flag = reinterpret_cast<int*>(bars + 66);  // key split: this half finished second
@@ -608,9 +629,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&kv_empty[s], C::MMA_WARPS);
         }
         for (int t = 0; t < T; ++t) {
-            mbar_init(&s_full[t], 1);
-            mbar_init(&p_full[t], BM);
+            for (int b = 0; b < C::NB; ++b) {
+                mbar_init(&s_full[C::NB * t + b], 1);
+                mbar_init(&p_full[C::NB * t + b], BM);
+            }
             mbar_init(&o_done[t], 1);
+            if (C::NB == 2) mbar_init(&pv_done[t], 1);
         }
         for (int m = 0; m < C::MMA_WARPS; ++m) mbar_init(&mma_done[m], 1);
         if (ROPE) mbar_init(q_ready, 4 * T);  // one arrive per softmax warp
@@ -693,7 +717,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // softmax, the products of the other tiles keep the tensor core busy.
         // Two warps share the tiles so that the issue of one warp's products
         // overlaps the other warp's waits; a K/V stage is released once both
-        // have committed their last product on it.
+        // have committed their last product on it.  (At T = 2, one warp issuing
+        // both tiles' products spent ~44 cycles an instruction, about 1400 of
+        // the ~2400 cycles of a key step at d 128.)
         const int mw = warp - C::MMA_WARP;
         constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
         constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
@@ -701,24 +727,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err));
         };
-        auto qk = [&](int t, int st) {
+        auto qk = [&](int t, int st, int b) {
             const uint32_t sK = smem_u32(sKV + st * C::STAGE_BYTES);
             const uint32_t sqt = sq + t * C::Q_BYTES;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-                umma_ss_elect(tmem + C::s_col(t),
+                umma_ss_elect(tmem + C::s_col(t, b),
                               umma_sdesc_sw128(sqt + (ks / 4) * kQChunkBytes + (ks % 4) * 32, 16, 1024),
                               umma_sdesc_sw128(sK + (ks / 4) * kKChunkBytes + (ks % 4) * 32, 16, 1024), idesc_qk,
                               ks > 0 ? 1u : 0u);
-            umma_commit_elect(&s_full[t]);
+            umma_commit_elect(&s_full[C::NB * t + b]);
         };
-        auto pv = [&](int t, int st, bool acc) {
+        auto pv = [&](int t, int st, int b, bool acc) {
             const uint32_t sV = smem_u32(sKV + st * C::STAGE_BYTES) + C::K_BYTES;
 #pragma unroll
             for (int ks = 0; ks < BN / 16; ++ks)
 #pragma unroll
                 for (int c = 0; c < C::KCH; ++c)
-                    umma_ts_elect(tmem + C::o_col(t) + 64 * c, tmem + C::p_col(t, ks),
+                    umma_ts_elect(tmem + C::o_col(t) + 64 * c, tmem + C::p_col(t, b, ks),
                                   umma_sdesc_sw128(sV + c * kKChunkBytes + ks * 2048, 1024, 1024), idesc_pv,
                                   (acc || ks > 0) ? 1u : 0u);
         };
@@ -727,32 +753,48 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             tc_fence_after_sync();
 #pragma unroll
             for (int t = 0; t < T; ++t)
-                if (t % C::MMA_WARPS == mw) qk(t, 0);
+                if (t % C::MMA_WARPS == mw) qk(t, 0, 0);
         }
-        for (int jj = 0; (!SPLIT || ok) && jj < nk; ++jj) {
+        if constexpr (C::NB == 2) {
+            // the second buffer: scores of key tile 1 before any P is back
+            if (ok && nk > 1) {
+                ok = wait_all(&kv_full[1], 0);
+                if (ok) {
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int t = 0; t < T; ++t)
+                        if (t % C::MMA_WARPS == mw) qk(t, 1, 1);
+                }
+            }
+        }
+        for (int jj = 0; (!SPLIT || C::NB == 2 || ok) && jj < nk; ++jj) {
+            if (C::NB == 2 && !ok) break;
             const int st = jj % C::NST;
-            const int st1 = (jj + 1) % C::NST;
-            const bool more = jj + 1 < nk;
+            const int b = jj % C::NB;  // the buffer holding P of key tile jj
+            const int jn = jj + C::NB;  // the key tile whose scores go into that buffer next
+            const int stn = jn % C::NST;
+            const bool more = jn < nk;
 #pragma unroll
             for (int t = 0; t < T; ++t) {
                 if (t % C::MMA_WARPS != mw) continue;
-                if (!wait_all(&p_full[t], jj & 1)) {
+                if (!wait_all(&p_full[C::NB * t + b], (jj / C::NB) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                pv(t, st, jj > 0);
+                pv(t, st, b, jj > 0);
+                if constexpr (C::NB == 2) umma_commit_elect(&pv_done[t]);  // O may be rescaled once it is done
                 if (t + C::MMA_WARPS >= T) umma_commit_elect(&kv_empty[st]);  // this warp's last tile
                 if (more) {
                     if (t < C::MMA_WARPS) {  // this warp's first tile
-                        if (!wait_all(&kv_full[st1], ((jj + 1) / C::NST) & 1)) {
+                        if (!wait_all(&kv_full[stn], (jn / C::NST) & 1)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after_sync();
                     }
-                    qk(t, st1);
-                } else {
+                    qk(t, stn, b);
+                } else if (C::NB == 1 || jj == nk - 1) {
                     umma_commit_elect(&o_done[t]);
                 }
             }
@@ -778,7 +820,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // split's barriers count on it
         if (SPLIT || ok)
             softmax_role<D, T, D == 64, SPLIT>(t, r, tmem + tmem_lane_base(warp), i, j0, j1, n, pre + BM * i, kv_len,
-                                             cu0, hq0 + t, sKV, &s_full[t], &p_full[t], &o_done[t], kv_full,
+                                             cu0, hq0 + t, sKV, &s_full[C::NB * t], &p_full[C::NB * t], &o_done[t],
+                                             &pv_done[t], kv_full,
                                              abort_flag, split_flag, ok, p);
     }
 
