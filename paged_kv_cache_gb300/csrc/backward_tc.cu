@@ -27,7 +27,10 @@
 //    is issued before dV / dK of this one, so the tensor core works while the
 //    elementwise warps run; at d 128, whose dV, dK and dQ take 384 columns,
 //    there is one S^T / dP^T buffer and one dQ buffer, and the next S^T
-//    follows dV / dK.
+//    follows dV / dK.  At d 64 a second issuing warp (warp 22) takes dV, dK
+//    and dQ, so that S^T / dP^T of the next block need not wait behind them
+//    in one warp's issue order; the first issuer refills a buffer once the
+//    dV / dK products that read it are done (a barrier per buffer).
 //  * warps 2..17 (elementwise): thread = key (TMEM lane), four warps per lane
 //    quarter, 16 query rows each.  Mask j <= i < n, P^T, dS^T; P^T and dS^T to
 //    TMEM, dS^T also to shared memory (key rows of 64 query rows, 128-byte
@@ -54,7 +57,7 @@ constexpr int kMmaWarp = 1;
 constexpr int kEwWarp0 = 2;       // 16 elementwise warps
 constexpr int kEwWarps = 16;
 constexpr int kEpiWarp0 = kEwWarp0 + kEwWarps;  // 4 dQ epilogue warps
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+constexpr int kMmaWarp2 = kEpiWarp0 + 4;         // two issuers: dV, dK and dQ (kMmaWarp: S^T, dP^T)
 constexpr int kDsHalf = kKeys * 128;    // dS^T of 64 query rows for 128 keys
 constexpr int kDsBuf = 2 * kDsHalf;     // one pair of query blocks
 constexpr int kDqBox = 128 * 128;       // 128 rows x 32 fp32
@@ -66,6 +69,13 @@ struct TcCfg {
     static constexpr int NBUF = D == 64 ? 2 : 1;    // S^T / dP^T buffers in TMEM
     static constexpr int NDQ = D == 64 ? 2 : 1;     // dQ buffers in TMEM
     static constexpr int NST = D == 64 ? 5 : 2;     // Q / dO / L / D stages
+    // Two issuing warps where there are two S^T / dP^T buffers: S^T / dP^T of
+    // the next block go out while the other warp issues this block's dV, dK
+    // and dQ (d 64: 755 -> 771 TFLOP/s).  With one buffer the next S^T must
+    // wait for dV / dK to complete instead of merely following them in one
+    // thread's issue order (d 128: 863 -> 791), so d 128 keeps one issuer.
+    static constexpr bool TWO_ISSUERS = NBUF == 2;
+    static constexpr int THREADS = (kEpiWarp0 + 4 + (TWO_ISSUERS ? 1 : 0)) * 32;
     static constexpr int DQ_BOXES = D == 64 ? 2 : 1;  // 32-column fp32 staging boxes
     static constexpr int KV_CHUNK = kKeys * 128;    // one chunk of the K (or V) tile
     static constexpr int TILE_KV = KCH * KV_CHUNK;
@@ -162,7 +172,7 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int r0, int r1, int t, 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap domap,
               const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap dqmap,
               const BwdTcParams p) {
@@ -190,6 +200,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
     uint64_t* mma_done = kv_done + 1;      // 1: every product done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_done + 2);
+    uint64_t* buf_free = mma_done + 3;     // [2] (two issuers): dV / dK of the buffer's block done
+    uint64_t* mma_done2 = mma_done + 5;    // 1 (two issuers): every product of the second issuer done
     float* sLD = reinterpret_cast<float*>(smem + OFF_LD);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -216,7 +228,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
         mbar_init(kv_full, 1);
         for (int s = 0; s < kNst; ++s) {
             mbar_init(&q_full[s], 1 + 32);  // expect_tx arrival + one cp.async arrival per producer lane
-            mbar_init(&q_empty[s], 1);
+            mbar_init(&q_empty[s], C::TWO_ISSUERS ? 2 : 1);  // (two issuers: S^T / dP^T and dV / dK read it)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
@@ -227,6 +239,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
         }
         mbar_init(kv_done, 1);
         mbar_init(mma_done, 1);
+        mbar_init(mma_done2, 1);
+        for (int x = 0; x < 2; ++x) mbar_init(&buf_free[x], 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -334,27 +348,99 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
                               ks > 0 ? 1u : 0u);
             umma_commit_elect(&s_full[x]);
         };
-        bool ok = wait_all(kv_full, 0) && wait_all(&q_full[0], 0);
-        if (ok) {
-            tc_fence_after_sync();
-            issue_sdp(0);
+        if constexpr (C::TWO_ISSUERS) {
+            // S^T / dP^T of block it into buffer it % NBUF once the dV / dK
+            // products of the block before in that buffer are done
+            bool ok = wait_all(kv_full, 0);
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int s = it % kNst, x = it % C::NBUF;
+                if (it >= C::NBUF && !wait_all(&buf_free[x], ((it - C::NBUF) / C::NBUF) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (!wait_all(&q_full[s], (it / kNst) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                issue_sdp(it);
+                umma_commit_elect(&q_empty[s]);
+            }
+        } else {
+            bool ok = wait_all(kv_full, 0) && wait_all(&q_full[0], 0);
+            if (ok) {
+                tc_fence_after_sync();
+                issue_sdp(0);
+            }
+            // the next block's S^T / dP^T: into the other buffer before this block's dV / dK
+            // (two buffers), or after them, over the P^T / dS^T they read (one buffer)
+            auto next_sdp = [&](int it) {
+                if (it + 1 >= n_it) return true;
+                if (!wait_all(&q_full[(it + 1) % kNst], ((it + 1) / kNst) & 1)) return false;
+                tc_fence_after_sync();
+                issue_sdp(it + 1);
+                return true;
+            };
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int s = it % kNst, x = it % C::NBUF;
+                if (C::NBUF == 2 && !next_sdp(it)) {
+                    ok = false;
+                    break;
+                }
+                if (!wait_all(&p_ready[x], (it / C::NBUF) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sQ = sb + OFF_Q + s * kTileQ, sO = sb + OFF_DO + s * kTileQ;
+    #pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_ts_elect(tmem + COL_DV, tmem + COL_S + 64 * x + packed_col(ks),
+                                  umma_sdesc_sw128(sO + ks * 2048, C::Q_CHUNK, 1024), idesc_kv,
+                                  (it > 0 || ks > 0) ? 1u : 0u);
+    #pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_ts_elect(tmem + COL_DK, tmem + COL_DP + 64 * x + packed_col(ks),
+                                  umma_sdesc_sw128(sQ + ks * 2048, C::Q_CHUNK, 1024), idesc_kv,
+                                  (it > 0 || ks > 0) ? 1u : 0u);
+                umma_commit_elect(&q_empty[s]);
+                if (it + 1 == n_it) umma_commit_elect(kv_done);
+                if (C::NBUF == 1 && !next_sdp(it)) {
+                    ok = false;
+                    break;
+                }
+                if (it & 1) {
+                    const int pp = it >> 1, y = pp % C::NDQ, dsb = pp & 1;
+                    if (pp >= C::NDQ && !wait_all(&dq_empty[y], ((pp / C::NDQ) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sD = sb + OFF_DS + dsb * kDsBuf;
+    #pragma unroll
+                    for (int ks = 0; ks < kKeys / 16; ++ks)
+                        umma_ss_elect(tmem + COL_DQ + D * y, umma_sdesc_sw128(sD + ks * 2048, kDsHalf, 1024),
+                                      umma_sdesc_sw128(sK + ks * 2048, C::KV_CHUNK, 1024), idesc_q, ks > 0 ? 1u : 0u);
+                    umma_commit_elect(&dq_full[y]);
+                    umma_commit_elect(&ds_empty[dsb]);
+                }
+            }
         }
-        // the next block's S^T / dP^T: into the other buffer before this block's dV / dK
-        // (two buffers), or after them, over the P^T / dS^T they read (one buffer)
-        auto next_sdp = [&](int it) {
-            if (it + 1 >= n_it) return true;
-            if (!wait_all(&q_full[(it + 1) % kNst], ((it + 1) / kNst) & 1)) return false;
-            tc_fence_after_sync();
-            issue_sdp(it + 1);
-            return true;
+        umma_commit_elect(mma_done);
+        mbar_drain(mma_done, 0);
+        __syncwarp();
+    } else if (C::TWO_ISSUERS && warp == kMmaWarp2) {
+        // ------------------------------------------------------------ dV, dK, dQ issue (two issuers)
+        constexpr uint32_t idesc_kv = umma_idesc_bf16(128, D, true);         // dV, dK (A from TMEM)
+        constexpr uint32_t idesc_q = umma_idesc_bf16(128, D, true, true);    // dQ
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err));
         };
+        const uint32_t sK = sb + OFF_K;
+        bool ok = wait_all(kv_full, 0);
         for (int it = 0; ok && it < n_it; ++it) {
             const int s = it % kNst, x = it % C::NBUF;
-            if (C::NBUF == 2 && !next_sdp(it)) {
-                ok = false;
-                break;
-            }
-            if (!wait_all(&p_ready[x], (it / C::NBUF) & 1)) {
+            if (!wait_all(&q_full[s], (it / kNst) & 1) || !wait_all(&p_ready[x], (it / C::NBUF) & 1)) {
                 ok = false;
                 break;
             }
@@ -371,11 +457,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
                               umma_sdesc_sw128(sQ + ks * 2048, C::Q_CHUNK, 1024), idesc_kv,
                               (it > 0 || ks > 0) ? 1u : 0u);
             umma_commit_elect(&q_empty[s]);
+            umma_commit_elect(&buf_free[x]);  // S^T / dP^T of block it + NBUF may overwrite this buffer
             if (it + 1 == n_it) umma_commit_elect(kv_done);
-            if (C::NBUF == 1 && !next_sdp(it)) {
-                ok = false;
-                break;
-            }
             if (it & 1) {
                 const int pp = it >> 1, y = pp % C::NDQ, dsb = pp & 1;
                 if (pp >= C::NDQ && !wait_all(&dq_empty[y], ((pp / C::NDQ) - 1) & 1)) {
@@ -392,8 +475,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
                 umma_commit_elect(&ds_empty[dsb]);
             }
         }
-        umma_commit_elect(mma_done);
-        mbar_drain(mma_done, 0);
+        umma_commit_elect(mma_done2);
+        mbar_drain(mma_done2, 0);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------------ elementwise
@@ -598,7 +681,7 @@ cudaError_t launch_tc(const CUtensorMap& qmap, const CUtensorMap& domap, const C
     cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(batch * p.g.hkv), static_cast<unsigned>((max_seqlen + kKeys - 1) / kKeys));
-    bwd_tc_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(qmap, domap, kvmap, dqmap, p);
+    bwd_tc_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(qmap, domap, kvmap, dqmap, p);
     return cudaGetLastError();
 }
 
