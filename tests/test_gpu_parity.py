@@ -407,17 +407,19 @@ def _second_half_moves(case):
     return count
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_second_half_moves_the_reference(d):
+@pytest.mark.parametrize("hq,hkv,d", [(8, 2, 64), (6, 1, 64), (3, 3, 64), (8, 2, 128), (4, 4, 128)])
+def test_second_half_moves_the_reference(hq, hkv, d):
     """Key magnitudes that step up every 32 keys: in thousands of key tiles the
     second 32-key half exceeds the reference max by more than 2^8 after the
     first half has formed its P, which must then follow the new reference
     (with the partial sums and l).  At d 128 the same inputs take the
-    max-first order."""
-    geom = W.Geometry(8, 2, d, 1, 3, 64, 120)
+    max-first order.  Every move also rescales O; with two score buffers per
+    tile (two or one q heads per CTA: 6 / 1 and 3 / 3 at d 64, every d-128
+    case) that waits for the PV product of the key tile before."""
+    geom = W.Geometry(hq, hkv, d, 1, 3, 64, 120)
     case = W.make_prefill_case("halfstep", geom, [700, 300, 129], seed=93, pool_fill="nan")
     _scale_keys(case, lambda pos: (0.25 + 0.9 * (pos // 32)).astype(np.float32))
-    if d == 64:
+    if d == 64 and hq == 8:
         assert _second_half_moves(case) > 1000
     pool, bt, werr = H.gpu_setup(case)
     assert werr == 0
