@@ -36,11 +36,12 @@
 //    softmax works on tile j, and P of tile j is followed in its buffer by S
 //    of tile j + 2.
 //  * Warps 4t..4t+3 (softmax of tile t): thread r owns query row r, i.e. TMEM
-//    lane r, and all 64 scores of the key tile.  It takes the row max first,
-//    moves the reference max if the tile max exceeds it by more than 2^8 (l at
-//    once, its O row in TMEM in place -- with one score buffer no PV product
-//    is in flight then; with two it first waits for the last one), and
-//    forms P = 2^(s*scale*log2e - m) with packed fp32 FMAs and the SFU exp2,
+//    lane r, and all 64 scores of the key tile, read as two 32-key halves.  A
+//    half whose max exceeds the reference max by more than 2^8 moves it (l
+//    at once, the first half's P and partial sums in registers if the second
+//    half moves it, its O row in TMEM in place -- with one score buffer no PV
+//    product is in flight then; with two it first waits for the last one).
+//    P = 2^(s*scale*log2e - m) comes from packed fp32 FMAs and the SFU exp2,
 //    packed to bf16.  The epilogue divides by l, writes o (bf16) and
 //    L = ln2 (m + log2 l).  Exact: o = O / l uses the one reference.
 //  * TMEM: tile t owns NB 64 + d columns from t (NB 64 + d): NB score buffers
@@ -153,24 +154,20 @@ __device__ __forceinline__ uint64_t pair2(float a) {
 
 // P = 2^(s * sc + nm) of 32 scores, packed to bf16 pairs; adds the fp32 P to
 // ls (FIRST: the first half of the tile, whose first four pairs start ls).
-// PAIRS: sc and nm enter the packed FMAs as pairs formed once per call.
-template <bool FIRST, bool PAIRS>
+// sc and nm enter the packed FMAs as pairs formed once per call.
+template <bool FIRST>
 __device__ __forceinline__ void p_chunk(const uint32_t (&v)[32], float sc, float nm, float (&ls)[8],
                                         uint32_t (&pk)[16]) {
     const uint64_t sc2 = pair2(sc), nm2 = pair2(nm);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
         float x0, x1;
-        if constexpr (PAIRS) {
-            asm("{\n\t.reg .b64 a2, d2;\n\t"
-                "mov.b64 a2, {%2, %3};\n\t"
-                "fma.rn.f32x2 d2, a2, %4, %5;\n\t"
-                "mov.b64 {%0, %1}, d2;\n\t}"
-                : "=f"(x0), "=f"(x1)
-                : "f"(__uint_as_float(v[2 * e])), "f"(__uint_as_float(v[2 * e + 1])), "l"(sc2), "l"(nm2));
-        } else {
-            ffma2(x0, x1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), sc, sc, nm, nm);
-        }
+        asm("{\n\t.reg .b64 a2, d2;\n\t"
+            "mov.b64 a2, {%2, %3};\n\t"
+            "fma.rn.f32x2 d2, a2, %4, %5;\n\t"
+            "mov.b64 {%0, %1}, d2;\n\t}"
+            : "=f"(x0), "=f"(x1)
+            : "f"(__uint_as_float(v[2 * e])), "f"(__uint_as_float(v[2 * e + 1])), "l"(sc2), "l"(nm2));
         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
         const int a = 2 * (e & 3);
         if (FIRST && e < 4) {
@@ -205,13 +202,6 @@ __device__ __forceinline__ float chunk_max16(const uint32_t (&v)[32]) {
     const float a = fmax3(c[0], c[1], x(7));
     const float b = fmax3(c[2], c[3], x(15));
     return fmaxf(fmax3(a, x(23), x(31)), b);
-}
-
-__device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], float m) {
-    float mx[4] = {m, m, m, m};
-#pragma unroll
-    for (int e = 0; e < 32; e += 2) mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
 }
 
 // RoPE of row r of one query tile in shared memory (the tile's 64-dim chunks
@@ -260,12 +250,10 @@ __device__ __forceinline__ bool rope_q_row(uint8_t* tile, int r, bool turn, long
     return true;
 }
 
-// Softmax of query tile t: the warp's thread owns row r (TMEM lane r).
-// ONE_PASS: each 32-key half of the scores is read from tensor memory once
-// (measured faster at d 64, with and without the query rotation; the
-// max-first order is faster at d 128)
+// Softmax of query tile t: the warp's thread owns row r (TMEM lane r) and
+// reads each 32-key half of a key tile's scores from tensor memory once.
 // SPLIT: the instance may run as one half of a key split (not the RoPE-Q one).
-template <int D, int T, bool ONE_PASS, bool SPLIT>
+template <int D, int T, bool SPLIT>
 __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, int i, int j0, int j1, int n,
                                              int pos0, int kv_len, int cu0, int hq,
                                              uint8_t* sKV, uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
@@ -287,11 +275,10 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
     // reference moves: 0.8 % faster at d 64, 0.6 % at d 128 than forming it
     // from m_o before each use
     float nm_reg = 0.f;
-    // ONE_PASS: the move test in raw score units (scale > 0): a half whose raw
-    // max exceeds thr_raw = (m_o + 2^8) / sc moves the reference.  One multiply
+    // the move test in raw score units (scale > 0): a half whose raw max
+    // exceeds thr_raw = (m_o + 2^8) / sc moves the reference.  One multiply
     // and one add fewer between a half's max and its exp2: 1077 -> 1092
-    // TFLOP/s at d 64, the same bits (the max-first order at d 128 measured
-    // 0.4 % slower with it).
+    // TFLOP/s at d 64, the same bits.
     const float move_raw = kMoveAbove / sc;
     float thr_raw = -CUDART_INF_F;
     if constexpr (!SPLIT) ok = true;  // outside a key split the role is entered only when ok
@@ -307,20 +294,14 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
         const int rel = BN * j - pos0;  // first key of the tile relative to the first row's position
         const bool diag = rel > -BN;      // the tile crosses the diagonal
         float f = 1.f;  // factor for l and this row of O when the reference moves
-        bool moved = false;  // (ONE_PASS) the reference moved in this tile
-        // this tile's sums of P; the one-pass body starts them with its first
-        // half's values instead of adding those to zeros (d 64 1090 -> 1094
-        // TFLOP/s, the same bits; the max-first body at d 128 measured 0.8 %
-        // slower with it)
+        bool moved = false;  // the reference moved in this tile
+        // this tile's sums of P, started with its first half's values instead
+        // of adding those to zeros (d 64 1090 -> 1094 TFLOP/s, the same bits)
         float ls[8];
-        if constexpr (!ONE_PASS) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ls[e] = 0.f;
-        }
         // this row of O follows the reference (with one score buffer no PV
         // product is in flight here)
         auto rescale_o = [&]() {
-            if (jj > 0 && __any_sync(0xffffffffu, ONE_PASS ? moved : f != 1.f)) {
+            if (jj > 0 && __any_sync(0xffffffffu, moved)) {
                 // with two score buffers the PV product of key tile jj - 1 may
                 // still be adding into O: wait for it (bounded)
                 if constexpr (C::NB == 2) {
@@ -336,88 +317,51 @@ __device__ __forceinline__ void softmax_role(int t, int r, uint32_t tmem_lane, i
                 }
             }
         };
-        if constexpr (ONE_PASS) {
-            // one read of each 32-key half: the first half's max may move the
-            // reference and its P waits in registers; should the second half
-            // move it again (by more than 2^8, rare past the first tile), that
-            // P and the partial sums follow the new reference in registers
-            uint32_t pa[16];
-            {
-                uint32_t va[32];
-                tmem_ld_x32(tS, va);
-                if (diag) mask_chunk(va, rel, r);
-                const float ma_raw = chunk_max16(va);
-                if (ma_raw > thr_raw) {
-                    const float m_a = sc * ma_raw;
-                    thr_raw = ma_raw + move_raw;
-                    moved = true;
-                    f = ex2_approx(m_o - m_a);  // 0 from -inf
-                    l *= f;
-                    m_o = m_a;
-                    nm_reg = -m_o;
-                }
-                p_chunk<true, true>(va, sc, nm_reg, ls, pa);
-            }
-            {
-                uint32_t vb[32], pk[16];
-                tmem_ld_x32(tS + 32, vb);
-                if (diag) mask_chunk(vb, rel + 32, r);
-                const float mb_raw = chunk_max16(vb);
-                if (mb_raw > thr_raw) {
-                    const float m_b = sc * mb_raw;
-                    thr_raw = mb_raw + move_raw;
-                    moved = true;
-                    const float f2 = ex2_approx(m_o - m_b);
-                    f *= f2;
-                    l *= f2;
-                    m_o = m_b;
-                    nm_reg = -m_o;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ls[e] *= f2;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) pa[e] = pack_bf16x2(bf16lo(pa[e]) * f2, bf16hi(pa[e]) * f2);
-                }
-                p_chunk<false, true>(vb, sc, nm_reg, ls, pk);
-                tmem_st_x16_nowait(tS + 32, pk);
-            }
-            tmem_st_x16_nowait(tS, pa);
-            rescale_o();
-        } else {
-            // the row max of the 64 scores first (the second half stays in
-            // registers), then P of the second half, then the first half read
-            // again: P overwrites S, so no P is formed before the max is known
-            uint32_t vb[32];
-            float m_tile;
-            {
-                uint32_t va[32];
-                tmem_ld_x32(tS, va);
-                if (diag) mask_chunk(va, rel, r);
-                m_tile = chunk_max(va, -CUDART_INF_F);
-            }
-            tmem_ld_x32(tS + 32, vb);
-            if (diag) mask_chunk(vb, rel + 32, r);
-            m_tile = sc * chunk_max(vb, m_tile);
-            if (m_tile > m_o + kMoveAbove) {
-                f = ex2_approx(m_o - m_tile);  // 0 from -inf
+        // one read of each 32-key half: the first half's max may move the
+        // reference and its P waits in registers; should the second half
+        // move it again (by more than 2^8, rare past the first tile), that
+        // P and the partial sums follow the new reference in registers
+        uint32_t pa[16];
+        {
+            uint32_t va[32];
+            tmem_ld_x32(tS, va);
+            if (diag) mask_chunk(va, rel, r);
+            const float ma_raw = chunk_max16(va);
+            if (ma_raw > thr_raw) {
+                const float m_a = sc * ma_raw;
+                thr_raw = ma_raw + move_raw;
+                moved = true;
+                f = ex2_approx(m_o - m_a);  // 0 from -inf
                 l *= f;
-                m_o = m_tile;
+                m_o = m_a;
                 nm_reg = -m_o;
             }
-            const float nm = nm_reg;
-            {
-                uint32_t pk[16];
-                p_chunk<false, false>(vb, sc, nm, ls, pk);
-                tmem_st_x16_nowait(tS + 32, pk);
-            }
-            rescale_o();
-            {
-                uint32_t va[32], pk[16];
-                tmem_ld_x32(tS, va);
-                if (diag) mask_chunk(va, rel, r);
-                p_chunk<false, false>(va, sc, nm, ls, pk);
-                tmem_st_x16_nowait(tS, pk);
-            }
+            p_chunk<true>(va, sc, nm_reg, ls, pa);
         }
+        {
+            uint32_t vb[32], pk[16];
+            tmem_ld_x32(tS + 32, vb);
+            if (diag) mask_chunk(vb, rel + 32, r);
+            const float mb_raw = chunk_max16(vb);
+            if (mb_raw > thr_raw) {
+                const float m_b = sc * mb_raw;
+                thr_raw = mb_raw + move_raw;
+                moved = true;
+                const float f2 = ex2_approx(m_o - m_b);
+                f *= f2;
+                l *= f2;
+                m_o = m_b;
+                nm_reg = -m_o;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ls[e] *= f2;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pa[e] = pack_bf16x2(bf16lo(pa[e]) * f2, bf16hi(pa[e]) * f2);
+            }
+            p_chunk<false>(vb, sc, nm_reg, ls, pk);
+            tmem_st_x16_nowait(tS + 32, pk);
+        }
+        tmem_st_x16_nowait(tS, pa);
+        rescale_o();
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         if (j == j_tail) {
             // V rows past the sequence end in the last page: zero (0 x NaN is NaN)
@@ -819,7 +763,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // in a key split every softmax warp enters, whatever `ok` says: the
         // split's barriers count on it
         if (SPLIT || ok)
-            softmax_role<D, T, D == 64, SPLIT>(t, r, tmem + tmem_lane_base(warp), i, j0, j1, n, pre + BM * i, kv_len,
+            softmax_role<D, T, SPLIT>(t, r, tmem + tmem_lane_base(warp), i, j0, j1, n, pre + BM * i, kv_len,
                                              cu0, hq0 + t, sKV, &s_full[C::NB * t], &p_full[C::NB * t], &o_done[t],
                                              &pv_done[t], kv_full,
                                              abort_flag, split_flag, ok, p);
