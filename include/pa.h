@@ -43,9 +43,11 @@
  *   GQA: q head h reads kv head h / (Hq / Hkv).
  *
  * Ownership: the caller allocates and owns every buffer (device memory unless
- * stated).  The library allocates no memory and keeps no state between calls
- * (pa_decode_noalloc's fixed scratch, described at that call, is the one
- * exception to the second point).
+ * stated).  The library keeps no state between calls and allocates no memory,
+ * with two exceptions described at their calls: pa_decode_noalloc's fixed
+ * scratch, and the few MB of scratch pa_prefill_cached takes for a
+ * key-split last wave from a stream-ordered memory pool of the library's
+ * own.
  * All calls are asynchronous on `stream`; they return after validating the
  * arguments and enqueueing the kernels.
  *
