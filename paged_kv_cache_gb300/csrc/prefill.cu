@@ -68,7 +68,7 @@ constexpr int BN = 64;                  // keys per K/V tile
 constexpr int kPagesPerTile = BN / kBlockTokens;
 constexpr int kQChunkBytes = BM * 128;  // 128 rows x 128 bytes: one 64-dim chunk of a query tile
 constexpr int kKChunkBytes = BN * 128;  // 64 keys x 128 bytes: one 64-dim chunk of a K or V tile
-constexpr float kMoveAbove = 8.f;       // the reference max moves when a tile max exceeds it by 2^8
+constexpr float kMoveAbove = 8.f;       // the reference max moves when a 32-key half exceeds it by 2^8
 
 template <int D, int T>
 struct Cfg {
